@@ -1,0 +1,80 @@
+"""Oracle K/V pool: slot writes, block copies and contiguous gathers.
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Layout, from "PagedAttention 的块表与碎片控制" §06::
+
+    K_cache, V_cache : [N_layers, N_blocks, B, H_kv, D_h]
+    block_table      : [N_sequences, max_blocks_per_sequence]
+    context_lens     : [N_sequences]
+
+A token at logical position ``t`` of a sequence lives in physical block
+``block_table[seq, t // B]`` at slot ``t % B`` (§03, §06).  A flattened slot
+number is ``p * B + o``.
+
+Element storage: ``"f32"`` pools hold float32 values; ``"bf16"`` pools hold
+the raw 16-bit patterns (uint16).  A bf16 pattern ``h`` stands for the
+float32 whose bits are ``h << 16``; ``to_f64`` widens that exactly.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+STORAGE = {"f32": np.float32, "bf16": np.uint16}
+
+
+def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of stored elements to float64."""
+    if dtype == "f32":
+        return np.asarray(x, dtype=np.float32).astype(np.float64)
+    if dtype == "bf16":
+        bits = np.asarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+class KVStore:
+    def __init__(self, n_layers, n_blocks, block_size, n_kv_heads, head_dim, dtype="f32"):
+        self.L, self.N, self.B = n_layers, n_blocks, block_size
+        self.H, self.D, self.dtype = n_kv_heads, head_dim, dtype
+        shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
+        self.K = np.zeros(shape, dtype=STORAGE[dtype])
+        self.V = np.zeros(shape, dtype=STORAGE[dtype])
+
+    def write_slot(self, layer: int, slot: int, k_row, v_row) -> None:
+        p, o = divmod(int(slot), self.B)
+        self.K[layer, p, o] = k_row
+        self.V[layer, p, o] = v_row
+
+    def reshape_and_cache(self, layer: int, k_new, v_new, slots) -> None:
+        """Token ``i``'s rows ``[H_kv, D_h]`` go to slot ``slots[i]``; a
+        negative slot means "no write" for that token."""
+        for i, s in enumerate(slots):
+            if s < 0:
+                continue
+            self.write_slot(layer, s, k_new[i], v_new[i])
+
+    def copy_block(self, src: int, dst: int) -> None:
+        """Copy-on-write copy: every slot of block ``src`` in every layer,
+        K and V, into block ``dst``."""
+        self.K[:, dst] = self.K[:, src]
+        self.V[:, dst] = self.V[:, src]
+
+    def gather_raw(self, layer: int, table, ctx: int):
+        """Positions ``0..ctx-1`` of one sequence, in logical order, as
+        stored elements ``[ctx, H_kv, D_h]``."""
+        ks, vs = [], []
+        for t in range(ctx):
+            p = table[t // self.B]
+            o = t % self.B
+            ks.append(self.K[layer, p, o])
+            vs.append(self.V[layer, p, o])
+        shape = (0, self.H, self.D)
+        k = np.stack(ks) if ks else np.zeros(shape, dtype=self.K.dtype)
+        v = np.stack(vs) if vs else np.zeros(shape, dtype=self.V.dtype)
+        return k, v
+
+    def gather(self, layer: int, table, ctx: int):
+        """Same as ``gather_raw`` but widened to contiguous float64."""
+        k, v = self.gather_raw(layer, table, ctx)
+        return to_f64(k, self.dtype), to_f64(v, self.dtype)
