@@ -1,0 +1,510 @@
+"""Benchmark: paged decode attention KV GB/s (and decode tokens/s) on GB300.
+
+One step = the whole hot path over one decode batch: the host block manager
+reserves one slot per sequence (copy-on-write pairs included), then on the
+device the copy-on-write block copy, the slot write of the new token's K/V
+in every layer, and per layer the split-K decode pass and its merge.
+
+* ``value``: unique K/V bytes the step's attention must read from HBM per
+  second of device time (inputs resident in HBM; host reservations for all
+  steps made before timing, per-step metadata uploaded beforehand; L2
+  flushed between steps with a 256 MiB write outside the timed windows).
+* ``e2e``: the same metric through the C-ABI call ``kv_decode_step_host``
+  with pinned host buffers: host reservation, H2D of q / new K,V / slots /
+  pairs / tables / lengths, kernels, D2H of the float32 outputs, synchronise.
+* ``roofline``: the split pass (dominant kernel), its algorithmic bytes per
+  launch over its CUDA-event duration, against MEASURED_PEAKS.json.
+* ``cpu_baseline``: the CPU oracle (fp64, one thread) on a bounded sample of
+  the same workload, in a subprocess.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): replicas only -- each rank runs its own pool and batch
+(weak scaling); the value is the sum over ranks over the max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and decode tokens/s"
+DEFAULT_WORKLOAD = "qwen_2k"
+
+# Per-launch DRAM traffic of the split pass from an ncu capture, keyed by
+# workload, valid only for the kernel source it was taken on.
+TRAFFIC = {}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "ptx.cuh", "device.cu"):
+        with open(os.path.join(ROOT, "paged_kv_cache_65_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, local, ws
+
+
+def aggregate(local_bytes: float, local_seconds: float, world: int, device=None):
+    """Whole-job bytes and max-over-ranks seconds (barrier included)."""
+    if world <= 1:
+        return local_bytes, local_seconds
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([local_bytes, local_seconds], dtype=torch.float64, device=device)
+    b = t[:1].clone()
+    s = t[1:].clone()
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(b.item()), float(s.item())
+
+
+# -------------------------------------------------------------- workload
+def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device"):
+    """Build the workload's pool on the device.  ``fill="device"`` fills the
+    whole pool with seeded N(0,1) values generated on the GPU by torch and
+    skips history writes (the history values are whatever the pool holds);
+    ``fill="host"`` writes the recipe's CPU-generated values slot by slot."""
+    import torch
+
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    wl = synth.workload(name, **({"block_size": block_size} if name == "pool36" else {}))
+    cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
+                         wl.dtype, free_order=wl.free_order, device=device)
+    if fill == "device":
+        g = torch.Generator(device=device)
+        g.manual_seed(synth.torch_seed((wl.seed, 5)))
+        for t in (cache.k, cache.v):
+            flat = t.view(-1)
+            step = 1 << 28
+            for i in range(0, flat.numel(), step):
+                seg = flat[i:i + step]
+                seg.copy_(torch.randn(seg.numel(), generator=g, device=device, dtype=torch.float32))
+    run = DeviceRun(cache, wl.n_q_heads)
+    values = None if fill == "device" else wl.append_values
+    for op in wl.build_ops:
+        if op[0] == "append" and values is None:
+            slots, pairs = cache.seq_append_tokens(op[1], op[2])
+            if len(pairs):
+                d = torch.from_numpy(np.ascontiguousarray(pairs)).to(device)
+                cache.cow_copy(d, len(pairs))
+            run.lengths[op[1]] = run.lengths.get(op[1], 0) + op[2]
+        else:
+            run.apply(op, values)
+    torch.cuda.synchronize()
+    return wl, cache, run
+
+
+def unique_kv_bytes(cache, seq_ids, lengths, esize):
+    """Distinct (block, valid rows) the step's attention reads, all layers."""
+    B = cache.B
+    table, lens = cache.seq_block_table(seq_ids, max(1, max(-(-lengths[s] // B) for s in seq_ids)))
+    rows = {}
+    for i in range(len(seq_ids)):
+        n = int(lens[i])
+        for j in range(-(-n // B)):
+            r = min(B, n - j * B)
+            p = int(table[i, j])
+            rows[p] = max(rows.get(p, 0), r)
+    per_row = 2 * cache.H * cache.D * esize * cache.L
+    return sum(rows.values()) * per_row, int(lens.sum()) * per_row
+
+
+# ----------------------------------------------------------------- ours
+def bench_ours(args):
+    import torch
+
+    rank, local, world = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl, cache, run = setup(args.workload, args.block_size, dev)
+    esize = wl.elem_bytes
+    seqs = wl.decode_seqs
+    n = len(seqs)
+    L = wl.n_layers
+    stream = torch.cuda.current_stream()
+    n_steps = args.warmup + args.steps
+
+    # host part of every step first (reservations + tables), then upload
+    plans = []
+    max_blocks = 1
+    for i in range(n_steps):
+        slots, pairs = run.reserve(seqs)
+        table, lens = cache.seq_block_table(seqs, run.max_blocks(seqs))
+        ub, lb = unique_kv_bytes(cache, seqs, run.lengths, esize)
+        plans.append((slots, pairs, table, lens, ub, lb))
+        max_blocks = max(max_blocks, table.shape[1])
+    dplans = []
+    for slots, pairs, table, lens, ub, lb in plans:
+        tpad = np.full((n, max_blocks), -1, dtype=np.int32)
+        tpad[:, :table.shape[1]] = table
+        dplans.append(dict(
+            slots=torch.from_numpy(slots).to(dev),
+            pairs=torch.from_numpy(np.ascontiguousarray(pairs)).to(dev) if len(pairs) else None,
+            npairs=len(pairs), table=torch.from_numpy(tpad).to(dev),
+            lens=torch.from_numpy(lens).to(dev), ub=ub, lb=lb, ctx=int(lens.sum())))
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.torch_seed((wl.seed, 6)))
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    q = torch.randn((L, n, wl.n_q_heads, wl.head_dim), generator=g, device=dev).to(tdt)
+    kn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
+    vn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
+    out = torch.empty((L, n, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    ws = run.workspace(n)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_steps)]
+    ev_layer = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(L)] for _ in range(n_steps)]
+    launches = 0
+
+    def one_step(i, record=True):
+        nonlocal launches
+        p = dplans[i]
+        flush.fill_(i & 0xFF)  # evict L2 outside the timed windows
+        e = ev[i]
+        e[0].record(stream)
+        cnt = 0
+        if p["npairs"]:
+            cache.cow_copy(p["pairs"], p["npairs"], stream)
+            cnt += 1
+        cache.reshape_and_cache(-1, kn, vn, p["slots"], n, stream)
+        cnt += 1
+        e[1].record(stream)
+        for layer in range(L):
+            a, b = ev_layer[i][layer]
+            a.record(stream)
+            cache.paged_decode_partials(layer, q[layer], wl.n_q_heads, p["table"], max_blocks,
+                                        p["lens"], n, ws, 0.0, stream)
+            b.record(stream)
+            cache.paged_decode_merge(wl.n_q_heads, p["lens"], n, out[layer], ws, stream)
+            cnt += 2
+        e[2].record(stream)
+        if record:
+            launches += cnt
+
+    for i in range(args.warmup):
+        one_step(i, record=False)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.warmup, n_steps):
+        one_step(i)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.warmup, n_steps)]
+    split_ms = [ev_layer[i][l][0].elapsed_time(ev_layer[i][l][1])
+                for i in range(args.warmup, n_steps) for l in range(L)]
+    dev_s = sum(step_ms) / 1e3
+    ub = sum(dplans[i]["ub"] for i in range(args.warmup, n_steps))
+    lb = sum(dplans[i]["lb"] for i in range(args.warmup, n_steps))
+    tot_b, max_s = aggregate(float(ub), dev_s, world, dev)
+    value = tot_b / max_s / 1e9
+    ms_per_step = max_s / args.steps * 1e3
+    toks = world * n * args.steps / max_s
+
+    # roofline of the split pass: algorithmic bytes per launch / mean duration
+    per_launch_alg = []
+    for i in range(args.warmup, n_steps):
+        p = dplans[i]
+        kv = p["ub"] / L
+        qb = n * wl.n_q_heads * wl.head_dim * esize
+        per_launch_alg.append(kv + qb)
+    alg = float(np.mean(per_launch_alg))
+    split_s = float(np.mean(split_ms)) / 1e3
+    peak, peak_kind = read_peaks()
+    achieved = alg / split_s / 1e9
+    traffic = TRAFFIC.get(args.workload)
+    traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha() else None
+
+    # e2e through the public C-ABI call with pinned host buffers
+    e2e = bench_e2e(args, wl, cache, run, dev, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
+            "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
+                       "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
+                       "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
+                       "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "pct_of_8tbs_nominal": round(100 * value / 8000.0, 2),
+            "logical_kv_gbs": round(lb / dev_s / 1e9, 2),
+            "decode_tokens_per_s": round(toks, 1),
+            "decode_tokens_per_s_36_layers": round(toks * L / 36.0, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
+                         "kernel": "decode_split_kernel", "peak_source": peak_kind,
+                         "alg_bytes_per_launch": int(alg),
+                         "mean_launch_us": round(split_s * 1e6, 2)},
+            "gpu_launches": launches * world,
+            "e2e": e2e,
+            "clocks": clk,
+            "wall_s_timed": round(t_wall, 4),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def bench_e2e(args, wl, cache, run, dev, world):
+    import torch
+
+    seqs = wl.decode_seqs
+    n = len(seqs)
+    L = wl.n_layers
+    steps = max(1, args.steps)
+    max_blocks = run.max_blocks(seqs) + (steps + args.warmup) // wl.block_size + 2
+    staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
+                          dtype=torch.uint8, device=dev)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    g = torch.Generator()
+    g.manual_seed(synth.torch_seed((wl.seed, 7)))
+    hq = torch.randn((L, n, wl.n_q_heads, wl.head_dim), generator=g).to(tdt).pin_memory()
+    hk = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g).to(tdt).pin_memory()
+    hv = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g).to(tdt).pin_memory()
+    ho = torch.empty((L, n, wl.n_q_heads, wl.head_dim), dtype=torch.float32).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    esize = wl.elem_bytes
+    total_s, total_b = 0.0, 0
+    h2d = d2h = 0
+    for i in range(args.warmup + steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        cache.kv_decode_step_host(seqs, wl.n_q_heads, max_blocks, hq, hk, hv, ho, staging)
+        dt = time.perf_counter() - t0
+        for s in seqs:
+            run.lengths[s] += 1
+        if i >= args.warmup:
+            total_s += dt
+            ub, _ = unique_kv_bytes(cache, seqs, run.lengths, esize)
+            total_b += ub
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * esize + n * 8 + n * 8 + n * max_blocks * 4 + n * 4
+    d2h = ho.numel() * 4
+    tot_b, max_s = aggregate(float(total_b), total_s, world, dev)
+    return {"value": round(tot_b / max_s / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(max_s / steps * 1e3, 4), "api": "kv_decode_step_host"}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(workload: str):
+    """Build the oracle's pool for the workload and make one decode step's
+    host reservation and writes (setup, untimed)."""
+    from oracle.runner import OracleRun
+
+    wl = synth.workload(workload)
+    orc = OracleRun(wl)
+    slots, cows = orc.reserve_step()
+    q = orc.write_step(0, slots, cows)
+    return wl, orc, q
+
+
+def oracle_attend(wl, orc, q, seconds: float, max_seqs: int | None = None, start: int = 0):
+    """The oracle as it stands: layer-0 attention sequence by sequence until
+    ``seconds`` have passed.  Returns (bytes of K/V read, seconds, count)."""
+    per_tok = 2 * wl.n_kv_heads * wl.head_dim * wl.elem_bytes
+    done, nbytes = 0, 0
+    n = len(wl.decode_seqs)
+    t0 = time.perf_counter()
+    while True:
+        i = (start + done) % n
+        orc.attend(0, q, seq_index=[i])
+        done += 1
+        nbytes += orc.bm.lengths[wl.decode_seqs[i]] * per_tok
+        if time.perf_counter() - t0 > seconds or (max_seqs and done >= max_seqs):
+            break
+    return nbytes, time.perf_counter() - t0, done
+
+
+def cpu_leg(workload: str, seconds: float):
+    wl, orc, q = oracle_sample(workload)
+    nbytes, dt, done = oracle_attend(wl, orc, q, seconds)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{workload}: layer-0 decode attention of {done} of {len(wl.decode_seqs)} "
+                      f"sequences (paged gather + fp64 softmax, one thread), {dt:.1f} s",
+            "seconds": round(dt, 3), "sequences": done, "bytes": int(nbytes)}
+
+
+def cpu_baseline(workload: str, seconds: float):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", workload,
+                        "--cpu-seconds", str(seconds)], capture_output=True, text=True, env=env,
+                       timeout=600)
+    for ln in r.stdout.splitlines()[::-1]:
+        if ln.startswith("{"):
+            return json.loads(ln)
+    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "failed: " + r.stderr[-200:]}
+
+
+def bench_reference(args):
+    """The reference arm: the CPU oracle as it stands, each step a bounded
+    sample (two sequences' layer-0 attention) of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(k, "1")
+    wl, orc, q = oracle_sample(args.workload)
+    secs, nbytes = [], []
+    for i in range(args.warmup + args.steps):
+        b, dt, _ = oracle_attend(wl, orc, q, 1e9, max_seqs=2, start=2 * i)
+        if i >= args.warmup:
+            secs.append(dt)
+            nbytes.append(b)
+    value = round(sum(nbytes) / sum(secs) / 1e9, 4)
+    sample = (f"{args.workload}: per step, layer-0 decode attention of 2 of "
+              f"{len(wl.decode_seqs)} sequences (paged gather + fp64 softmax, one thread)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(secs)), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-leg", default=None)
+    args = ap.parse_args()
+    if args.cpu_leg:
+        print(json.dumps(cpu_leg(args.cpu_leg, args.cpu_seconds)), flush=True)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * pagedkv.h -- C ABI of a GB300 (sm_103a) paged KV cache: block manager,
+ * slot write, copy-on-write block copy and split-K decode attention.
+ *
+ * Pages followed (cited by title and section):
+ *   [BT] "KV Cache 还有空间为何新请求却进不来？PagedAttention 的块表与碎片控制"
+ *        (zwjcode.cn), sections 03-13.
+ *   [KC] "KV 缓存管理" (gptbert.com, mlsys vol. 3), sections "PagedAttention
+ *        虚拟内存模型" and "通过写时复制分支实现零复制审慎推理", and the
+ *        chunked-prefill section (online-softmax merge).
+ *   [IO] "第 8 章 推理优化" (bojieli.github.io), sections 8.3.1-8.3.2.
+ *
+ * Layout ([BT] §06):
+ *   K_cache, V_cache : [N_layers][N_blocks][B][H_kv][D_h], row-major, dtype
+ *                      float32 or bfloat16, owned by the caller (device).
+ *   block_table      : int32 [N_seq][max_blocks], -1 past ceil(ctx / B).
+ *   context_lens     : int32 [N_seq].
+ *   slot             : int64 p * B + o for physical block p, offset o.
+ * Token t of a sequence lives at (block_table[seq][t / B], t % B) ([BT] §03).
+ *
+ * Conventions
+ *   - Every function returns a kvStatus.  Arguments are checked before any
+ *     state changes: a call that fails changes nothing ([BT] §10).
+ *   - Host functions (block_*, seq_*, kv_pool_stats/check) never touch the
+ *     device and are synchronous.  A pool is not thread safe.
+ *   - Device functions enqueue work on the given stream (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream) and return after the
+ *     launch; they report launch errors only.  Bad block ids or slots met on
+ *     the device are skipped and recorded in the pool's device status word;
+ *     kv_pool_device_status() reads it.
+ *   - The library allocates no device memory.  Device buffers (pools, the
+ *     status word, decode workspaces) come from the caller.
+ *   - A freed block may be handed out again by the next allocation; device
+ *     readers stay safe because later writers are ordered after them on the
+ *     same stream ([IO] §8.3.2: free only once the accelerator is done).
+ *     Callers that use several streams must order them themselves.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kvStatus;
+enum {
+  KV_OK = 0,
+  KV_ERR_NO_FREE_BLOCK = 1, /* free list empty ([BT] §05 "no free KV block") */
+  KV_ERR_INVALID_ARG = 2,   /* bad shape, id, size or unknown sequence      */
+  KV_ERR_REFCOUNT = 3,      /* handle not held, double free, broken counts   */
+  KV_ERR_CUDA = 4,          /* a CUDA runtime call failed                   */
+  KV_ERR_DEVICE_CHECK = 5,  /* a kernel recorded a bad id / slot / timeout  */
+  KV_ERR_UNSUPPORTED = 6    /* shape outside the compiled kernel set        */
+};
+
+enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1 };
+
+/* bits of the device status word */
+enum {
+  KV_DEV_BAD_BLOCK_ID = 1, /* block_table entry outside [0, N_blocks)  */
+  KV_DEV_BAD_SLOT = 2,     /* slot_mapping entry >= N_blocks * B       */
+  KV_DEV_BAD_COW_PAIR = 4, /* copy pair id outside [0, N_blocks)       */
+  KV_DEV_WAIT_TIMEOUT = 8, /* a pipeline wait gave up (never expected) */
+  KV_DEV_BAD_CONTEXT = 16  /* context_lens entry < 0 or > max_blocks * B */
+};
+
+typedef struct kvPool kvPool;
+
+const char* kv_status_string(kvStatus s);
+
+/* ---------------------------------------------------------------- pool -- */
+
+/* Create a pool over caller-owned device caches.
+ *   k_cache, v_cache: device pointers, layout above, 16-byte aligned; may be
+ *     NULL for a host-only manager (device functions then fail with
+ *     KV_ERR_INVALID_ARG).
+ *   d_status: device int32 the kernels OR error bits into; may be NULL.
+ *   free_order: host array of n_blocks ids, a permutation of 0..n_blocks-1
+ *     giving the initial FIFO free list ([BT] §05); NULL means 0..n_blocks-1.
+ * Supported: block_size 1..256, head_dim 64 or 128, dtype F32 or BF16. */
+kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_heads,
+                        int head_dim, int dtype, void* k_cache, void* v_cache,
+                        int32_t* d_status, const int32_t* free_order, kvPool** out);
+void kv_pool_destroy(kvPool* pool);
+
+/* Free / allocated / shared (count > 1) block counts; [KC] Eq. 8 U_KV is
+ * n_allocated / (n_free + n_allocated). */
+kvStatus kv_pool_stats(const kvPool* pool, int* n_free, int* n_allocated, int* n_shared);
+
+/* Conservation checks of [BT] §13: N_free + N_alloc = N_total, the set of
+ * blocks with a positive count is exactly the allocated set, each count
+ * equals the table entries naming the block plus the caller-held handles,
+ * and every table holds ceil(len / B) entries.  KV_ERR_REFCOUNT if broken. */
+kvStatus kv_pool_check(const kvPool* pool);
+
+/* Reference count of one block (debugging aid). */
+kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
+
+/* Synchronise `stream`, copy the device status word to *out_bits and clear
+ * it.  Returns KV_ERR_DEVICE_CHECK when any bit was set. */
+kvStatus kv_pool_device_status(kvPool* pool, void* stream, int* out_bits);
+
+/* ---------------------------------------------------------- block level --
+ * Caller-held handles on blocks, sharing the pool's free list and counts
+ * ([KC] zero-copy branching section).                                     */
+
+/* Pop n ids from the head of the free list (all or nothing), count 1 each. */
+kvStatus block_alloc(kvPool* pool, int n, int32_t* out_ids);
+/* Drop one handle per listed id; a count reaching 0 returns the block to the
+ * tail of the free list.  KV_ERR_REFCOUNT if a handle is not held. */
+kvStatus block_free(kvPool* pool, const int32_t* ids, int n);
+/* Add one handle per listed id (share).  KV_ERR_REFCOUNT if a block is free. */
+kvStatus block_fork(kvPool* pool, const int32_t* ids, int n);
+/* Copy-on-write for a held handle on `id`: if the block is shared, take a new
+ * block from the free list, move the handle to it and return it in *out_id
+ * (the caller then copies id -> *out_id with cow_copy); otherwise return id. */
+kvStatus block_cow(kvPool* pool, int32_t id, int32_t* out_id);
+
+/* ------------------------------------------------------- sequence level --
+ * The teaching BlockManager of [BT] §05 with the counts, fork and CoW of
+ * [KC].  A sequence is created by its first append.                       */
+
+/* One slot for each listed sequence, in the listed order, all or nothing
+ * ([BT] §10).  For sequence i, out_slots[i] = p * B + o where (p, o) is the
+ * new token's position ([BT] §03-§04).  When a token lands in a shared,
+ * partly filled tail block, a fresh block replaces it in that sequence's
+ * table and the pair (old, new) is appended to out_cow_pairs (capacity
+ * n_seq pairs, int32 [n][2]); *out_n_cow gets the number of pairs.  The
+ * first sharer to write copies; the last one writes in place.  A sequence
+ * listed twice is KV_ERR_INVALID_ARG. */
+kvStatus seq_append_slots(kvPool* pool, const int32_t* seq_ids, int n_seq, int64_t* out_slots,
+                          int32_t* out_cow_pairs, int* out_n_cow);
+/* n_tokens consecutive slots for one sequence (a prefill chunk), all or
+ * nothing; at most one copy pair (capacity 1 pair). */
+kvStatus seq_append_tokens(kvPool* pool, int32_t seq, int n_tokens, int64_t* out_slots,
+                           int32_t* out_cow_pair, int* out_n_cow);
+/* Child gets a copy of the parent's table, one more count on each block and
+ * the parent's length ([KC] fork steps 1-3).  No device work. */
+kvStatus seq_fork(kvPool* pool, int32_t parent, int32_t child);
+/* Drop one count per table entry, in table order; blocks reaching 0 go to the
+ * free-list tail ([KC] release_sequence_blocks).  No device work. */
+kvStatus seq_release(kvPool* pool, int32_t seq);
+kvStatus seq_length(const kvPool* pool, int32_t seq, int* out_len);
+/* Rows of the listed sequences' tables, padded with -1 to max_blocks, and
+ * their context lengths.  KV_ERR_INVALID_ARG if a table is wider. */
+kvStatus seq_block_table(const kvPool* pool, const int32_t* seq_ids, int n_seq, int max_blocks,
+                         int32_t* out_table, int32_t* out_context_lens);
+
+/* ------------------------------------------------------------- device --
+ * All pointers below are device pointers.                                */
+
+/* Copy-on-write copy ([KC] CoW paragraph; [IO] §8.3.2): for each pair
+ * d_pairs[i] = (src, dst) copy every slot of block src into block dst, K and
+ * V, in every layer.  No dst may be another pair's src in the same call. */
+kvStatus cow_copy(kvPool* pool, const int32_t* d_pairs, int n_pairs, void* stream);
+
+/* Slot write ("reshape_and_cache"; [KC] paging section, [BT] §04): token i's
+ * K and V rows [H_kv][D_h] go to slot d_slot_mapping[i] of `layer`; a
+ * negative slot skips the token.  layer == -1 writes every layer at once,
+ * with k_new / v_new laid out [N_layers][n_tokens][H_kv][D_h]. */
+kvStatus reshape_and_cache(kvPool* pool, int layer, const void* d_k_new, const void* d_v_new,
+                           const int64_t* d_slot_mapping, int n_tokens, void* stream);
+
+/* Bytes of decode workspace for n_seq sequences with n_q_heads query heads.
+ * Independent of the context lengths. */
+size_t paged_decode_workspace_bytes(const kvPool* pool, int n_seq, int n_q_heads);
+
+/* Split-K partial pass of decode attention ([BT] §07; [KC] online softmax).
+ * q: [n_seq][n_q_heads][D_h] in the pool dtype.  Query head h reads K/V head
+ * h / (n_q_heads / H_kv).  The work (all sequences x K/V heads x blocks) is
+ * cut into equal contiguous block ranges, one per CTA; each CTA writes the
+ * running max m, normaliser l and unnormalised output O of every range it
+ * covers into the workspace.  scale <= 0 means 1 / sqrt(D_h). */
+kvStatus paged_decode_partials(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                               const int32_t* d_block_table, int max_blocks,
+                               const int32_t* d_context_lens, int n_seq, float scale,
+                               void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* Merge pass: m = max m_i, l = sum l_i e^(m_i - m), out = sum O_i e^(m_i - m)
+ * / l per (sequence, query head); out [n_seq][n_q_heads][D_h] as float32
+ * (out_dtype F32) or bfloat16 (BF16).  A sequence with context 0 gets zeros.
+ * Must follow paged_decode_partials on the same stream with the same
+ * arguments. */
+kvStatus paged_decode_merge(kvPool* pool, int n_q_heads, const int32_t* d_context_lens,
+                            int n_seq, void* d_out, int out_dtype, const void* d_workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Both passes: decode attention of one layer for every listed sequence. */
+kvStatus paged_decode_attention(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                const int32_t* d_block_table, int max_blocks,
+                                const int32_t* d_context_lens, int n_seq, float scale,
+                                void* d_out, int out_dtype, void* d_workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------- whole decode step --
+ * One decode step through host buffers ([BT] §10 order): reserve a slot per
+ * listed sequence on the host, copy q / new K,V / slots / copy pairs /
+ * tables / lengths to the device, run cow_copy, then per layer
+ * reshape_and_cache and paged_decode_attention, copy the float32 outputs
+ * back and synchronise the stream.
+ *   h_q     : [N_layers][n_seq][n_q_heads][D_h]  (pool dtype)
+ *   h_k_new : [N_layers][n_seq][H_kv][D_h]        (pool dtype), same h_v_new
+ *   h_out   : [N_layers][n_seq][n_q_heads][D_h]  float32
+ *   d_staging: caller device buffer of kv_decode_step_staging_bytes() bytes.
+ * max_blocks bounds every listed table after the step. */
+size_t kv_decode_step_staging_bytes(const kvPool* pool, int n_seq, int n_q_heads, int max_blocks);
+kvStatus kv_decode_step_host(kvPool* pool, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                             int max_blocks, const void* h_q, const void* h_k_new,
+                             const void* h_v_new, float scale, float* h_out, void* d_staging,
+                             size_t staging_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

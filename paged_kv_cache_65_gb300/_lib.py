@@ -1,0 +1,124 @@
+"""ctypes binding of ``libpagedkv.so`` (C ABI in ``include/pagedkv.h``).
+
+Argument marshalling only: every step of the hot path runs in the library.
+Functions keep the C names; device pointers are passed as integers (for
+example ``tensor.data_ptr()``), host arrays as NumPy arrays, streams as the
+integer handle of a CUDA stream (``torch.cuda.current_stream().cuda_stream``)
+or 0 for the legacy default stream.
+
+Importing this module raises ``ImportError`` when the library has not been
+built: there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpagedkv.so")
+
+KV_OK = 0
+KV_ERR_NO_FREE_BLOCK = 1
+KV_ERR_INVALID_ARG = 2
+KV_ERR_REFCOUNT = 3
+KV_ERR_CUDA = 4
+KV_ERR_DEVICE_CHECK = 5
+KV_ERR_UNSUPPORTED = 6
+KV_DTYPE_F32 = 0
+KV_DTYPE_BF16 = 1
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing; build it with `python -m paged_kv_cache_65_gb300.build` "
+        "(or __graft_entry__.build())")
+
+lib = C.CDLL(LIB_PATH)
+
+_i32p = C.POINTER(C.c_int32)
+_i64p = C.POINTER(C.c_int64)
+_ip = C.POINTER(C.c_int)
+_vp = C.c_void_p
+_f32p = C.POINTER(C.c_float)
+
+# (name, restype, argtypes): every symbol declared in include/pagedkv.h
+SIGNATURES = [
+    ("kv_status_string", C.c_char_p, [C.c_int]),
+    ("kv_pool_create", C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _vp, _vp,
+                                 _vp, _i32p, C.POINTER(_vp)]),
+    ("kv_pool_destroy", None, [_vp]),
+    ("kv_pool_stats", C.c_int, [_vp, _ip, _ip, _ip]),
+    ("kv_pool_check", C.c_int, [_vp]),
+    ("kv_block_refcount", C.c_int, [_vp, C.c_int32, _ip]),
+    ("kv_pool_device_status", C.c_int, [_vp, _vp, _ip]),
+    ("block_alloc", C.c_int, [_vp, C.c_int, _i32p]),
+    ("block_free", C.c_int, [_vp, _i32p, C.c_int]),
+    ("block_fork", C.c_int, [_vp, _i32p, C.c_int]),
+    ("block_cow", C.c_int, [_vp, C.c_int32, _i32p]),
+    ("seq_append_slots", C.c_int, [_vp, _i32p, C.c_int, _i64p, _i32p, _ip]),
+    ("seq_append_tokens", C.c_int, [_vp, C.c_int32, C.c_int, _i64p, _i32p, _ip]),
+    ("seq_fork", C.c_int, [_vp, C.c_int32, C.c_int32]),
+    ("seq_release", C.c_int, [_vp, C.c_int32]),
+    ("seq_length", C.c_int, [_vp, C.c_int32, _ip]),
+    ("seq_block_table", C.c_int, [_vp, _i32p, C.c_int, C.c_int, _i32p, _i32p]),
+    ("cow_copy", C.c_int, [_vp, _vp, C.c_int, _vp]),
+    ("reshape_and_cache", C.c_int, [_vp, C.c_int, _vp, _vp, _vp, C.c_int, _vp]),
+    ("paged_decode_workspace_bytes", C.c_size_t, [_vp, C.c_int, C.c_int]),
+    ("paged_decode_partials", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, C.c_int,
+                                        C.c_float, _vp, C.c_size_t, _vp]),
+    ("paged_decode_merge", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, C.c_size_t,
+                                     _vp]),
+    ("paged_decode_attention", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, C.c_int,
+                                         C.c_float, _vp, C.c_int, _vp, C.c_size_t, _vp]),
+    ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
+    ("kv_decode_step_host", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
+                                      C.c_float, _f32p, _vp, C.c_size_t, _vp]),
+]
+
+for _name, _res, _args in SIGNATURES:
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = lib.kv_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})" if where else msg)
+
+
+def check(status: int, where: str = "") -> None:
+    if status != KV_OK:
+        raise KVError(status, where)
+
+
+def i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def ptr_i32(a: np.ndarray):
+    return a.ctypes.data_as(_i32p)
+
+
+def ptr_i64(a: np.ndarray):
+    return a.ctypes.data_as(_i64p)
+
+
+def ptr_f32(a: np.ndarray):
+    return a.ctypes.data_as(_f32p)
+
+
+def vp(x) -> _vp:
+    """A device/host address from an int, a torch tensor or a NumPy array."""
+    if x is None:
+        return _vp(0)
+    if isinstance(x, int):
+        return _vp(x)
+    if hasattr(x, "data_ptr"):
+        return _vp(x.data_ptr())
+    if isinstance(x, np.ndarray):
+        return _vp(x.ctypes.data)
+    raise TypeError(type(x))

@@ -1,0 +1,215 @@
+"""Python face of the C ABI: one object per pool.
+
+``PagedKVCache`` owns the device tensors (allocated with torch: K and V pools
+``[N_layers, N_blocks, B, H_kv, D_h]`` and a status word) and the library's
+pool handle.  Each method forwards to the C function of the same name;
+nothing here computes any part of the method.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from . import _lib
+from ._lib import check, i32, lib, ptr_f32, ptr_i32, ptr_i64, vp
+
+DTYPES = {"f32": _lib.KV_DTYPE_F32, "bf16": _lib.KV_DTYPE_BF16}
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        except Exception:  # pragma: no cover - torch always present here
+            pass
+        return C.c_void_p(0)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+class PagedKVCache:
+    def __init__(self, n_layers, n_blocks, block_size, n_kv_heads, head_dim, dtype="bf16",
+                 device="cuda", free_order=None, allocate=True, k_cache=None, v_cache=None):
+        self.L, self.N, self.B = n_layers, n_blocks, block_size
+        self.H, self.D, self.dtype = n_kv_heads, head_dim, dtype
+        self.k = k_cache
+        self.v = v_cache
+        self.status = None
+        if allocate and k_cache is None:
+            import torch
+
+            tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+            shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
+            self.k = torch.empty(shape, dtype=tdt, device=device)
+            self.v = torch.empty(shape, dtype=tdt, device=device)
+        if self.k is not None:
+            import torch
+
+            self.status = torch.zeros(1, dtype=torch.int32, device=self.k.device)
+        order = None if free_order is None else i32(free_order)
+        h = C.c_void_p()
+        check(lib.kv_pool_create(n_layers, n_blocks, block_size, n_kv_heads, head_dim,
+                                 DTYPES[dtype], vp(self.k), vp(self.v), vp(self.status),
+                                 ptr_i32(order) if order is not None else None, C.byref(h)),
+              "kv_pool_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ host
+    def kv_pool_stats(self):
+        f, a, s = C.c_int(), C.c_int(), C.c_int()
+        check(lib.kv_pool_stats(self.handle, C.byref(f), C.byref(a), C.byref(s)), "kv_pool_stats")
+        return f.value, a.value, s.value
+
+    def kv_pool_check(self):
+        check(lib.kv_pool_check(self.handle), "kv_pool_check")
+
+    def kv_block_refcount(self, block_id):
+        out = C.c_int()
+        check(lib.kv_block_refcount(self.handle, int(block_id), C.byref(out)), "kv_block_refcount")
+        return out.value
+
+    def block_alloc(self, n):
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib.block_alloc(self.handle, n, ptr_i32(out)), "block_alloc")
+        return out[:n]
+
+    def block_free(self, ids):
+        a = i32(ids)
+        check(lib.block_free(self.handle, ptr_i32(a), a.size), "block_free")
+
+    def block_fork(self, ids):
+        a = i32(ids)
+        check(lib.block_fork(self.handle, ptr_i32(a), a.size), "block_fork")
+
+    def block_cow(self, block_id):
+        out = C.c_int32()
+        check(lib.block_cow(self.handle, int(block_id), C.byref(out)), "block_cow")
+        return out.value
+
+    def seq_append_slots(self, seq_ids):
+        ids = i32(seq_ids)
+        n = ids.size
+        slots = np.zeros(max(n, 1), dtype=np.int64)
+        pairs = np.zeros((max(n, 1), 2), dtype=np.int32)
+        ncow = C.c_int()
+        check(lib.seq_append_slots(self.handle, ptr_i32(ids), n, ptr_i64(slots), ptr_i32(pairs),
+                                   C.byref(ncow)), "seq_append_slots")
+        return slots[:n], pairs[:ncow.value]
+
+    def seq_append_tokens(self, seq, n_tokens):
+        slots = np.zeros(max(n_tokens, 1), dtype=np.int64)
+        pair = np.zeros(2, dtype=np.int32)
+        ncow = C.c_int()
+        check(lib.seq_append_tokens(self.handle, int(seq), int(n_tokens), ptr_i64(slots),
+                                    ptr_i32(pair), C.byref(ncow)), "seq_append_tokens")
+        return slots[:n_tokens], pair.reshape(1, 2)[:ncow.value]
+
+    def seq_fork(self, parent, child):
+        check(lib.seq_fork(self.handle, int(parent), int(child)), "seq_fork")
+
+    def seq_release(self, seq):
+        check(lib.seq_release(self.handle, int(seq)), "seq_release")
+
+    def seq_length(self, seq):
+        out = C.c_int()
+        check(lib.seq_length(self.handle, int(seq), C.byref(out)), "seq_length")
+        return out.value
+
+    def seq_block_table(self, seq_ids, max_blocks):
+        ids = i32(seq_ids)
+        n = ids.size
+        table = np.zeros((max(n, 1), max(max_blocks, 1)), dtype=np.int32)
+        lens = np.zeros(max(n, 1), dtype=np.int32)
+        check(lib.seq_block_table(self.handle, ptr_i32(ids), n, max_blocks, ptr_i32(table),
+                                  ptr_i32(lens)), "seq_block_table")
+        return table[:n, :max_blocks], lens[:n]
+
+    # ---------------------------------------------------------- device
+    def kv_pool_device_status(self, stream=None):
+        bits = C.c_int()
+        st = lib.kv_pool_device_status(self.handle, _stream(stream), C.byref(bits))
+        if st not in (_lib.KV_OK, _lib.KV_ERR_DEVICE_CHECK):
+            check(st, "kv_pool_device_status")
+        return bits.value
+
+    def cow_copy(self, d_pairs, n_pairs, stream=None):
+        check(lib.cow_copy(self.handle, vp(d_pairs), int(n_pairs), _stream(stream)), "cow_copy")
+
+    def reshape_and_cache(self, layer, k_new, v_new, d_slots, n_tokens, stream=None):
+        check(lib.reshape_and_cache(self.handle, int(layer), vp(k_new), vp(v_new), vp(d_slots),
+                                    int(n_tokens), _stream(stream)), "reshape_and_cache")
+
+    def paged_decode_workspace_bytes(self, n_seq, n_q_heads):
+        return int(lib.paged_decode_workspace_bytes(self.handle, int(n_seq), int(n_q_heads)))
+
+    def paged_decode_partials(self, layer, q, n_q_heads, d_table, max_blocks, d_lens, n_seq,
+                              workspace, scale=0.0, stream=None):
+        check(lib.paged_decode_partials(self.handle, int(layer), vp(q), int(n_q_heads), vp(d_table),
+                                        int(max_blocks), vp(d_lens), int(n_seq), float(scale),
+                                        vp(workspace), _nbytes(workspace), _stream(stream)),
+              "paged_decode_partials")
+
+    def paged_decode_merge(self, n_q_heads, d_lens, n_seq, out, workspace, stream=None):
+        check(lib.paged_decode_merge(self.handle, int(n_q_heads), vp(d_lens), int(n_seq), vp(out),
+                                     _out_dtype(out), vp(workspace), _nbytes(workspace),
+                                     _stream(stream)), "paged_decode_merge")
+
+    def paged_decode_attention(self, layer, q, n_q_heads, d_table, max_blocks, d_lens, n_seq, out,
+                               workspace, scale=0.0, stream=None):
+        check(lib.paged_decode_attention(self.handle, int(layer), vp(q), int(n_q_heads),
+                                         vp(d_table), int(max_blocks), vp(d_lens), int(n_seq),
+                                         float(scale), vp(out), _out_dtype(out), vp(workspace),
+                                         _nbytes(workspace), _stream(stream)),
+              "paged_decode_attention")
+
+    def kv_decode_step_staging_bytes(self, n_seq, n_q_heads, max_blocks):
+        return int(lib.kv_decode_step_staging_bytes(self.handle, int(n_seq), int(n_q_heads),
+                                                    int(max_blocks)))
+
+    def kv_decode_step_host(self, seq_ids, n_q_heads, max_blocks, h_q, h_k_new, h_v_new, h_out,
+                            staging, scale=0.0, stream=None):
+        ids = i32(seq_ids)
+        check(lib.kv_decode_step_host(self.handle, ptr_i32(ids), ids.size, int(n_q_heads),
+                                      int(max_blocks), vp(h_q), vp(h_k_new), vp(h_v_new),
+                                      float(scale), C.cast(C.c_void_p(_addr(h_out)), _lib._f32p),
+                                      vp(staging), _nbytes(staging), _stream(stream)),
+              "kv_decode_step_host")
+
+
+def _addr(x) -> int:
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data
+
+
+def _nbytes(t) -> int:
+    if hasattr(t, "numel"):
+        return t.numel() * t.element_size()
+    return t.nbytes
+
+
+def _out_dtype(out) -> int:
+    import torch
+
+    if out.dtype == torch.float32:
+        return _lib.KV_DTYPE_F32
+    if out.dtype == torch.bfloat16:
+        return _lib.KV_DTYPE_BF16
+    raise TypeError(out.dtype)

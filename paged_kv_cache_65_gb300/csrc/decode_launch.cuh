@@ -1,0 +1,41 @@
+// Launch helper for one instantiation of the split pass.
+#pragma once
+
+#include "decode.cuh"
+
+namespace pkv {
+
+// Launches decode_split_kernel<ESIZE, D, G>.  On the first call for a pool
+// (*grid_io <= 0) it raises the kernel's dynamic shared-memory limit and sizes
+// the persistent grid as (resident CTAs per SM) x (SM count), capped at
+// max_grid; later calls reuse *grid_io.
+template <int ESIZE, int D, int G>
+cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
+                         int max_grid, int* grid_io, cudaStream_t st) {
+  constexpr int smem = decode_smem_bytes<ESIZE, D, G>();
+  auto kern = decode_split_kernel<ESIZE, D, G>;
+  if (*grid_io <= 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    int g = occ * sm_count;
+    *grid_io = g > max_grid ? max_grid : g;
+  }
+  a.grid = *grid_io;
+  kern<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+// Dispatch over (D, G) for one element size; *supported = false when the
+// shape has no compiled instantiation.
+cudaError_t launch_split_e2(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
+                            cudaStream_t st, bool* supported);
+cudaError_t launch_split_e4(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
+                            cudaStream_t st, bool* supported);
+
+}  // namespace pkv

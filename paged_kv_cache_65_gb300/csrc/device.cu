@@ -1,0 +1,473 @@
+// Device entry points of the C ABI: TMA descriptors, slot write
+// (reshape_and_cache), copy-on-write block copy, the merge pass of split-K
+// decode attention, and the whole-step driver over host buffers.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "decode_launch.cuh"
+#include "pool.h"
+#include "ptx.cuh"
+
+using pkv::record_status;
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int ilog2_small(int g) { return g == 1 ? 0 : g == 2 ? 1 : g == 4 ? 2 : g == 8 ? 3 : -1; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Encode a 2-D view of one cache: inner dimension H_kv * D_h elements (one
+// token row of every head), outer dimension N_layers * N_blocks * B rows; a
+// box is D_h elements of one head by `rows` token rows.
+kvStatus encode_cache_map(kvPool* p, void* base, int rows, CUtensorMap* out) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return KV_ERR_CUDA;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->H) * p->D,
+                              static_cast<cuuint64_t>(p->L) * p->N * p->B};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->H) * p->D * p->esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(p->D), static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      p->dtype == KV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(out, dt, 2, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
+}
+
+// First device use of a pool: device, SM count, TMA descriptors.
+kvStatus ensure_device(kvPool* p) {
+  if (p->dev_ready) return KV_OK;
+  if (!p->k || !p->v) return KV_ERR_INVALID_ARG;
+  if (cudaGetDevice(&p->device) != cudaSuccess) return KV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
+      cudaSuccess)
+    return KV_ERR_CUDA;
+  if (p->D == 64 || p->D == 128) {
+    const int ts = pkv::stage_tokens(p->esize, p->D);
+    if (p->B > ts && p->B % ts != 0) return KV_ERR_UNSUPPORTED;
+    const int rows = p->B < ts ? p->B : ts;
+    kvStatus s = encode_cache_map(p, p->k, rows, reinterpret_cast<CUtensorMap*>(p->tmap[0]));
+    if (s != KV_OK) return s;
+    s = encode_cache_map(p, p->v, rows, reinterpret_cast<CUtensorMap*>(p->tmap[1]));
+    if (s != KV_OK) return s;
+  }
+  p->dev_ready = true;
+  return KV_OK;
+}
+
+// ------------------------------------------------------------- kernels
+
+// Slot write: one CTA per (token, layer); 16-byte copies of the token's row
+// [H_kv][D_h] into K_cache[layer][slot / B][slot % B] and the same for V.
+__global__ void slot_write_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                  const int64_t* __restrict__ slots, int n_tok, uint4* kc,
+                                  uint4* vc, int layer, long long slots_per_layer, int row_vecs,
+                                  int32_t* status) {
+  const int i = blockIdx.x;
+  const int ly = layer >= 0 ? layer : blockIdx.y;
+  const int64_t slot = slots[i];
+  if (slot < 0) return;
+  if (slot >= slots_per_layer) {
+    if (threadIdx.x == 0) record_status(status, KV_DEV_BAD_SLOT);
+    return;
+  }
+  const long long src = ((layer >= 0 ? 0LL : (long long)blockIdx.y * n_tok) + i) * row_vecs;
+  const long long dst = ((long long)ly * slots_per_layer + slot) * row_vecs;
+  for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
+    kc[dst + v] = k_new[src + v];
+    vc[dst + v] = v_new[src + v];
+  }
+}
+
+// Copy-on-write copy: CTA (pair, layer, part) copies a slice of block src
+// into block dst in K and V.
+__global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, uint4* vc,
+                                int n_blocks, long long block_vecs, int32_t* status) {
+  const int i = blockIdx.x;
+  const int ly = blockIdx.y;
+  const int src = pairs[2 * i], dst = pairs[2 * i + 1];
+  if (src < 0 || src >= n_blocks || dst < 0 || dst >= n_blocks) {
+    if (threadIdx.x == 0 && ly == 0 && blockIdx.z == 0) record_status(status, KV_DEV_BAD_COW_PAIR);
+    return;
+  }
+  if (src == dst) return;
+  const long long s0 = ((long long)ly * n_blocks + src) * block_vecs;
+  const long long d0 = ((long long)ly * n_blocks + dst) * block_vecs;
+  const long long per = (block_vecs + gridDim.z - 1) / gridDim.z;
+  const long long b = (long long)blockIdx.z * per;
+  const long long e = b + per < block_vecs ? b + per : block_vecs;
+  for (long long v = b + threadIdx.x; v < e; v += blockDim.x) {
+    kc[d0 + v] = kc[s0 + v];
+    vc[d0 + v] = vc[s0 + v];
+  }
+}
+
+// Merge pass: per (sequence, query head) combine the partials of every piece
+// of its segment: M = max m_i, L = sum l_i 2^(m_i - M),
+// out = sum O_i 2^(m_i - M) / L.  A warp per head; the max over pieces is a
+// shuffle reduction.
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict__ pre,
+                                                    const float* __restrict__ ws_ml,
+                                                    const float* __restrict__ ws_o, int n_seq,
+                                                    int H, int Hq, int grid, float* out_f32,
+                                                    __nv_bfloat16* out_bf16) {
+  constexpr int DL = D / 32;
+  const int s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = Hq / H;
+  // blocks of this sequence, as the split pass counted them
+  const int nb = static_cast<int>((pre[s + 1] - pre[s]) / H);
+  const long long W = pre[n_seq];
+  long long chunk = (W + grid - 1) / grid;
+  if (chunk == 0) chunk = 1;
+  for (int hq = warp; hq < Hq; hq += 4) {
+    float o[DL];
+#pragma unroll
+    for (int d = 0; d < DL; ++d) o[d] = 0.f;
+    if (nb > 0) {
+      const int h = hq / G, g = hq - h * G;
+      const long long a0 = pre[s] + (long long)h * nb;
+      const long long c0 = a0 / chunk, c1 = (a0 + nb - 1) / chunk;
+      const long long seg = (long long)s * H + h;
+      const int np = static_cast<int>(c1 - c0 + 1);
+      float M = -INFINITY;
+      for (int i = lane; i < np; i += 32) M = fmaxf(M, ws_ml[((c0 + i + seg) * G + g) * 2]);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float L = 0.f;
+      for (int i = 0; i < np; ++i) {
+        const long long slot = (c0 + i + seg) * G + g;
+        const float f = pkv::exp2_approx(ws_ml[slot * 2] - M);
+        L += f * ws_ml[slot * 2 + 1];
+        const float* src = ws_o + slot * D + lane * DL;
+        if constexpr (DL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          o[0] += f * v.x;
+          o[1] += f * v.y;
+          o[2] += f * v.z;
+          o[3] += f * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          o[0] += f * v.x;
+          o[1] += f * v.y;
+        }
+      }
+      const float inv = 1.f / L;
+#pragma unroll
+      for (int d = 0; d < DL; ++d) o[d] *= inv;
+    }
+    const long long ob = ((long long)s * Hq + hq) * D + lane * DL;
+    if (out_f32) {
+#pragma unroll
+      for (int d = 0; d < DL; ++d) out_f32[ob + d] = o[d];
+    } else {
+#pragma unroll
+      for (int d = 0; d < DL; ++d) out_bf16[ob + d] = __float2bfloat16_rn(o[d]);
+    }
+  }
+}
+
+struct WsLayout {
+  size_t pre, ml, o, total;
+};
+
+WsLayout ws_layout(const kvPool* p, int n_seq, int G) {
+  const size_t n_slots = static_cast<size_t>(kMaxDecodeCtas) + static_cast<size_t>(n_seq) * p->H;
+  WsLayout w;
+  w.pre = 0;
+  w.ml = align256(sizeof(long long) * (static_cast<size_t>(n_seq) + 1));
+  w.o = w.ml + align256(n_slots * G * 2 * sizeof(float));
+  w.total = w.o + n_slots * G * p->D * sizeof(float);
+  return w;
+}
+
+bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
+
+kvStatus check_decode_args(const kvPool* p, int layer, const void* q, int n_q_heads,
+                           const int32_t* table, int max_blocks, const int32_t* ctx, int n_seq,
+                           const void* ws, size_t ws_bytes) {
+  if (!p || !p->k) return KV_ERR_INVALID_ARG;
+  if (n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= p->L) return KV_ERR_INVALID_ARG;
+  const int G = n_q_heads / p->H;
+  if (ilog2_small(G) < 0 || (p->D != 64 && p->D != 128)) return KV_ERR_UNSUPPORTED;
+  if (n_seq == 0) return KV_OK;
+  if (!q || !table || !ctx || !ws || max_blocks <= 0) return KV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(ws)) return KV_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(p, n_seq, G).total) return KV_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_blocks) * p->B >= (1LL << 31)) return KV_ERR_INVALID_ARG;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvStatus kv_pool_device_status(kvPool* p, void* stream, int* out_bits) {
+  if (!p || !out_bits) return KV_ERR_INVALID_ARG;
+  *out_bits = 0;
+  if (!p->d_status) return KV_OK;
+  cudaStream_t st = as_stream(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, p->d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KV_ERR_CUDA;
+  if (v && cudaMemset(p->d_status, 0, sizeof(int32_t)) != cudaSuccess) return KV_ERR_CUDA;
+  *out_bits = v;
+  return v ? KV_ERR_DEVICE_CHECK : KV_OK;
+}
+
+kvStatus cow_copy(kvPool* p, const int32_t* d_pairs, int n_pairs, void* stream) {
+  if (!p || n_pairs < 0 || (n_pairs > 0 && !d_pairs)) return KV_ERR_INVALID_ARG;
+  if (n_pairs == 0) return KV_OK;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  const long long block_vecs = static_cast<long long>(p->B) * p->H * p->D * p->esize / 16;
+  const int parts = block_vecs >= 4096 ? 4 : 1;
+  dim3 grid(n_pairs, p->L, parts);
+  cow_copy_kernel<<<grid, 256, 0, as_stream(stream)>>>(
+      d_pairs, reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v), p->N, block_vecs,
+      p->d_status);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kvStatus reshape_and_cache(kvPool* p, int layer, const void* d_k_new, const void* d_v_new,
+                           const int64_t* d_slot_mapping, int n_tokens, void* stream) {
+  if (!p || n_tokens < 0 || layer < -1 || layer >= p->L) return KV_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KV_OK;
+  if (!d_k_new || !d_v_new || !d_slot_mapping) return KV_ERR_INVALID_ARG;
+  if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KV_ERR_INVALID_ARG;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  const int row_vecs = p->H * p->D * p->esize / 16;
+  dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
+  const int threads = row_vecs >= 128 ? 128 : (row_vecs >= 64 ? 64 : 32);
+  slot_write_kernel<<<grid, threads, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint4*>(d_k_new), reinterpret_cast<const uint4*>(d_v_new),
+      d_slot_mapping, n_tokens, reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v),
+      layer, static_cast<long long>(p->N) * p->B, row_vecs, p->d_status);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+size_t paged_decode_workspace_bytes(const kvPool* p, int n_seq, int n_q_heads) {
+  if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return 0;
+  return ws_layout(p, n_seq, n_q_heads / p->H).total;
+}
+
+kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                               const int32_t* d_block_table, int max_blocks,
+                               const int32_t* d_context_lens, int n_seq, float scale,
+                               void* d_workspace, size_t workspace_bytes, void* stream) {
+  kvStatus s = check_decode_args(p, layer, d_q, n_q_heads, d_block_table, max_blocks,
+                                 d_context_lens, n_seq, d_workspace, workspace_bytes);
+  if (s != KV_OK || n_seq == 0) return s;
+  s = ensure_device(p);
+  if (s != KV_OK) return s;
+  const int G = n_q_heads / p->H;
+  const WsLayout w = ws_layout(p, n_seq, G);
+  unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
+  pkv::DecodeArgs a;
+  a.q = d_q;
+  a.table = d_block_table;
+  a.ctx = d_context_lens;
+  a.ws_pre = reinterpret_cast<long long*>(ws + w.pre);
+  a.ws_ml = reinterpret_cast<float*>(ws + w.ml);
+  a.ws_o = reinterpret_cast<float*>(ws + w.o);
+  a.status = p->d_status;
+  a.n_seq = n_seq;
+  a.max_blocks = max_blocks;
+  a.layer = layer;
+  a.n_blocks = p->N;
+  a.block_size = p->B;
+  a.n_kv_heads = p->H;
+  a.n_q_heads = n_q_heads;
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
+  a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.grid = 0;
+  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[0]);
+  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[1]);
+  int* grid_io = &p->grid_by_g[ilog2_small(G)];
+  bool supported = false;
+  cudaError_t e = p->esize == 2 ? pkv::launch_split_e2(p->D, G, tk, tv, a, p->sm_count,
+                                                        kMaxDecodeCtas, grid_io,
+                                                        as_stream(stream), &supported)
+                                : pkv::launch_split_e4(p->D, G, tk, tv, a, p->sm_count,
+                                                        kMaxDecodeCtas, grid_io,
+                                                        as_stream(stream), &supported);
+  if (!supported) return KV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kvStatus paged_decode_merge(kvPool* p, int n_q_heads, const int32_t* d_context_lens, int n_seq,
+                            void* d_out, int out_dtype, const void* d_workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  const int G = n_q_heads / p->H;
+  if (ilog2_small(G) < 0 || (p->D != 64 && p->D != 128)) return KV_ERR_UNSUPPORTED;
+  if (n_seq == 0) return KV_OK;
+  if (!d_context_lens || !d_out || !d_workspace) return KV_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(p, n_seq, G);
+  if (workspace_bytes < w.total || !aligned16(d_workspace)) return KV_ERR_INVALID_ARG;
+  const int grid = p->grid_by_g[ilog2_small(G)];
+  if (grid <= 0) return KV_ERR_INVALID_ARG;  // no split pass has run on this pool
+  const unsigned char* ws = reinterpret_cast<const unsigned char*>(d_workspace);
+  const long long* pre = reinterpret_cast<const long long*>(ws + w.pre);
+  const float* ml = reinterpret_cast<const float*>(ws + w.ml);
+  const float* o = reinterpret_cast<const float*>(ws + w.o);
+  float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
+  __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
+  if (p->D == 128)
+    merge_kernel<128><<<n_seq, 128, 0, as_stream(stream)>>>(pre, ml, o, n_seq, p->H, n_q_heads,
+                                                            grid, of, ob);
+  else
+    merge_kernel<64><<<n_seq, 128, 0, as_stream(stream)>>>(pre, ml, o, n_seq, p->H, n_q_heads,
+                                                           grid, of, ob);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kvStatus paged_decode_attention(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                const int32_t* d_block_table, int max_blocks,
+                                const int32_t* d_context_lens, int n_seq, float scale,
+                                void* d_out, int out_dtype, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (n_seq > 0 && !d_out) return KV_ERR_INVALID_ARG;
+  kvStatus s = paged_decode_partials(p, layer, d_q, n_q_heads, d_block_table, max_blocks,
+                                     d_context_lens, n_seq, scale, d_workspace, workspace_bytes,
+                                     stream);
+  if (s != KV_OK || n_seq == 0) return s;
+  return paged_decode_merge(p, n_q_heads, d_context_lens, n_seq, d_out, out_dtype, d_workspace,
+                            workspace_bytes, stream);
+}
+
+// ------------------------------------------------------ whole decode step
+
+namespace {
+struct StepLayout {
+  size_t q, k, v, slots, pairs, table, lens, out, ws, total;
+};
+
+StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks) {
+  StepLayout l;
+  const size_t L = p->L, n = n_seq;
+  size_t off = 0;
+  l.q = off;
+  off += align256(L * n * n_q_heads * p->D * p->esize);
+  l.k = off;
+  off += align256(L * n * p->H * p->D * p->esize);
+  l.v = off;
+  off += align256(L * n * p->H * p->D * p->esize);
+  l.slots = off;
+  off += align256(n * sizeof(int64_t));
+  l.pairs = off;
+  off += align256(n * 2 * sizeof(int32_t));
+  l.table = off;
+  off += align256(n * static_cast<size_t>(max_blocks) * sizeof(int32_t));
+  l.lens = off;
+  off += align256(n * sizeof(int32_t));
+  l.out = off;
+  off += align256(L * n * n_q_heads * p->D * sizeof(float));
+  l.ws = off;
+  off += align256(ws_layout(p, n_seq, n_q_heads / p->H).total);
+  l.total = off;
+  return l;
+}
+}  // namespace
+
+size_t kv_decode_step_staging_bytes(const kvPool* p, int n_seq, int n_q_heads, int max_blocks) {
+  if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0 || max_blocks <= 0) return 0;
+  return step_layout(p, n_seq, n_q_heads, max_blocks).total;
+}
+
+kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                             int max_blocks, const void* h_q, const void* h_k_new,
+                             const void* h_v_new, float scale, float* h_out, void* d_staging,
+                             size_t staging_bytes, void* stream) {
+  if (!p || !p->k || n_seq <= 0 || !seq_ids || !h_q || !h_k_new || !h_v_new || !h_out ||
+      !d_staging || max_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
+  const StepLayout l = step_layout(p, n_seq, n_q_heads, max_blocks);
+  if (staging_bytes < l.total || !aligned16(d_staging)) return KV_ERR_INVALID_ARG;
+  // every table must fit max_blocks after the step
+  for (int i = 0; i < n_seq; ++i) {
+    auto it = p->seqs.find(seq_ids[i]);
+    const long long len = it == p->seqs.end() ? 0 : it->second.len;
+    if ((len + 1 + p->B - 1) / p->B > max_blocks) return KV_ERR_INVALID_ARG;
+  }
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  // host: reserve (all or nothing)
+  p->h_slots.resize(n_seq);
+  p->h_pairs.resize(2 * static_cast<size_t>(n_seq));
+  int n_cow = 0;
+  s = seq_append_slots(p, seq_ids, n_seq, p->h_slots.data(), p->h_pairs.data(), &n_cow);
+  if (s != KV_OK) return s;
+  p->h_table.resize(static_cast<size_t>(n_seq) * max_blocks);
+  p->h_lens.resize(n_seq);
+  s = seq_block_table(p, seq_ids, n_seq, max_blocks, p->h_table.data(), p->h_lens.data());
+  if (s != KV_OK) return s;
+  // host -> device
+  cudaStream_t st = as_stream(stream);
+  unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
+  const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->esize;
+  const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->esize;
+  const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
+  bool ok = true;
+  ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.slots, p->h_slots.data(), n_seq * sizeof(int64_t),
+                        cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (n_cow)
+    ok &= cudaMemcpyAsync(d + l.pairs, p->h_pairs.data(), 2 * n_cow * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.table, p->h_table.data(), p->h_table.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.lens, p->h_lens.data(), n_seq * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (!ok) return KV_ERR_CUDA;
+  // device: copy shared tails, write the new token in every layer, attend
+  s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
+  if (s != KV_OK) return s;
+  s = reshape_and_cache(p, -1, d + l.k, d + l.v, reinterpret_cast<const int64_t*>(d + l.slots),
+                        n_seq, stream);
+  if (s != KV_OK) return s;
+  const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
+  for (int layer = 0; layer < p->L; ++layer) {
+    s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
+                               reinterpret_cast<const int32_t*>(d + l.table), max_blocks,
+                               reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale,
+                               d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
+                               d + l.ws, staging_bytes - l.ws, stream);
+    if (s != KV_OK) return s;
+  }
+  if (cudaMemcpyAsync(h_out, d + l.out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
+  return KV_OK;
+}
+
+}  // extern "C"

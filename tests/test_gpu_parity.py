@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the
+same seeded inputs.
+
+Integer work (slots, copy pairs, tables, pool bytes after slot writes and
+copy-on-write) must be bit-exact; attention outputs must be within 1e-5
+max-abs for float32 K/V and 2e-3 for bfloat16 K/V (float32 accumulation).
+"""
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.attention import decode_attention
+from oracle.kv_store import to_f64
+from oracle.runner import OracleRun
+
+torch = pytest.importorskip("torch")
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+TOL = {"f32": 1e-5, "bf16": 2e-3}
+
+
+def make(wl, zero=True):
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
+                         wl.dtype, free_order=wl.free_order)
+    if zero:
+        cache.k.zero_()
+        cache.v.zero_()
+    run = DeviceRun(cache, wl.n_q_heads)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    return cache, run
+
+
+def host_bits(t):
+    from paged_kv_cache_65_gb300.driver import to_host_bits
+
+    return to_host_bits(t)
+
+
+def check_status(cache):
+    assert cache.kv_pool_device_status() == 0
+
+
+def max_err(gpu, ref):
+    return float(np.max(np.abs(gpu.astype(np.float64) - ref))) if ref.size else 0.0
+
+
+@pytest.mark.parametrize("steps", [2])
+def test_tiny_full_parity(steps):
+    wl = synth.workload("tiny")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+    assert np.array_equal(host_bits(cache.v), orc.st.V)
+    for step in range(steps):
+        so, co, q, outs = orc.step(step)
+        _, k, v = wl.step_values(step)
+        sg, pg, og = run.step(wl.decode_seqs, q, k, v)
+        assert list(sg) == so and [tuple(p) for p in pg] == co
+        assert np.array_equal(host_bits(cache.k), orc.st.K)
+        assert np.array_equal(host_bits(cache.v), orc.st.V)
+        err = max_err(og.cpu().numpy()[0], outs[0])
+        assert err <= TOL["f32"], err
+    check_status(cache)
+
+
+def test_qwen_2k_full_parity():
+    wl = synth.workload("qwen_2k")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    for step in range(2):
+        so, co, q, outs = orc.step(step)
+        _, k, v = wl.step_values(step)
+        sg, pg, og = run.step(wl.decode_seqs, q, k, v)
+        assert list(sg) == so and len(pg) == 0
+        err = max_err(og.cpu().numpy()[0], outs[0])
+        assert err <= TOL["bf16"], err
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+    assert np.array_equal(host_bits(cache.v), orc.st.V)
+    check_status(cache)
+
+
+def test_shared_8k_sampled_parity():
+    wl = synth.workload("shared_8k")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+    assert list(sg) == so and len(pg) == 0
+    sample = [0, 7, 15]
+    ref = orc.attend(0, qh, seq_index=sample)
+    got = og.cpu().numpy()[0]
+    for i in sample:
+        assert max_err(got[i], ref[i]) <= TOL["bf16"]
+    # the 384 shared prefix blocks are read by all 16 sequences: bit-identical pools
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+    check_status(cache)
+
+
+def test_gqa70b_32k_cow_and_sampled_parity():
+    wl = synth.workload("gqa70b_32k")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    sample = [0, 5, 26, 47]
+    for step in range(2):
+        so, co = orc.reserve_step()
+        qh = orc.write_step(step, so, co)
+        _, k, v = wl.step_values(step)
+        sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+        assert list(sg) == so
+        assert [tuple(p) for p in pg] == co
+        assert len(co) == (48 if step == 0 else 0)
+        if step == 0:
+            kd = host_bits(cache.k)
+            for src, dst in co:
+                assert np.array_equal(kd[:, dst], orc.st.K[:, dst])
+                # the copy kept the shared tokens and the new token went to the copy
+                assert np.array_equal(kd[:, dst, :3], kd[:, src, :3])
+        ref = orc.attend(0, qh, seq_index=sample)
+        got = og.cpu().numpy()[0]
+        for i in sample:
+            assert max_err(got[i], ref[i]) <= TOL["bf16"]
+    check_status(cache)
+
+
+def ragged_workload(dtype, D, G, B, lens, H_kv=2, seed=0, n_blocks=None):
+    """Independent sequences of the given lengths after one decode step."""
+    n_blocks = n_blocks or sum(-(-l // B) for l in lens) + len(lens) + 3
+    ops = [("append", s, l - 1, s) for s, l in enumerate(lens) if l > 1]
+    return synth.Workload("ragged", 1, n_blocks, B, H_kv * G, H_kv, D, dtype, seed,
+                          synth.permutation((seed, 9), n_blocks), ops, list(range(len(lens))))
+
+
+SHAPES = [
+    ("f32", 64, 4, 4), ("f32", 64, 1, 2), ("f32", 128, 8, 16), ("f32", 128, 2, 1),
+    ("bf16", 128, 4, 16), ("bf16", 128, 8, 16), ("bf16", 128, 1, 8), ("bf16", 128, 2, 32),
+    ("bf16", 64, 4, 16), ("bf16", 64, 8, 64), ("bf16", 128, 4, 3), ("bf16", 128, 4, 64),
+    ("f32", 64, 8, 5),
+]
+
+
+@pytest.mark.parametrize("dtype,D,G,B", SHAPES)
+def test_ragged_shapes(dtype, D, G, B):
+    lens = [1, 2, B - 1 if B > 1 else 3, B, B + 1, 3 * B + 2, 97, 700]
+    lens = [max(1, l) for l in lens]
+    wl = ragged_workload(dtype, D, G, B, lens, seed=D + G + B)
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+    assert list(sg) == so
+    ref = orc.attend(0, qh)
+    assert max_err(og.cpu().numpy()[0], ref) <= TOL[dtype]
+    check_status(cache)
+
+
+def test_block_size_two_lengths_one_to_five():
+    # "PagedAttention 的块表与碎片控制" §13: block size 2 with lengths 1..5
+    wl = ragged_workload("f32", 64, 4, 2, [1, 2, 3, 4, 5], seed=5)
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, qh, k, v)
+    assert max_err(og.cpu().numpy()[0], orc.attend(0, qh)) <= 1e-5
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+
+
+def test_single_token_context_returns_value_exactly():
+    wl = ragged_workload("f32", 64, 4, 4, [1, 1, 1])
+    cache, run = make(wl)
+    q, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, q, k, v)
+    got = og.cpu().numpy()[0]
+    for s in range(3):
+        for h in range(8):
+            assert np.array_equal(got[s, h], v[0, s, h // 4])
+
+
+def test_empty_context_gives_zeros_and_others_unchanged():
+    wl = ragged_workload("bf16", 128, 4, 16, [40, 17, 300])
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    run.write(*run.reserve(wl.decode_seqs), k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    d_lens[1] = 0
+    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
+    out = run.attend(0, qd, d_table, mb, d_lens, 3)
+    got = out.cpu().numpy()
+    ref = orc.attend(0, qh)
+    assert not got[1].any()
+    assert max_err(got[[0, 2]], ref[[0, 2]]) <= TOL["bf16"]
+
+
+def test_placement_invariance_and_determinism():
+    outs = []
+    for order_seed in (1, 2):
+        wl = ragged_workload("bf16", 128, 4, 16, [33, 1000, 2049, 5], seed=3)
+        wl.free_order = synth.permutation((order_seed, 77), wl.n_blocks)
+        cache, run = make(wl)
+        q, k, v = wl.step_values(0)
+        _, _, og = run.step(wl.decode_seqs, q, k, v)
+        d_table, d_lens, mb = run.tables(wl.decode_seqs)
+        qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+        again = run.attend(0, qd, d_table, mb, d_lens, 4)
+        assert torch.equal(again, og[0])
+        outs.append(og.cpu())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_split_and_merge_calls_equal_one_call():
+    wl = ragged_workload("bf16", 128, 8, 16, [5000, 3, 800], seed=4)
+    cache, run = make(wl)
+    q, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, q, k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+    ws = run.workspace(3)
+    out = torch.empty_like(og[0])
+    cache.paged_decode_partials(0, qd, 64, d_table, mb, d_lens, 3, ws)
+    cache.paged_decode_merge(64, d_lens, 3, out, ws)
+    assert torch.equal(out, og[0])
+
+
+def test_bf16_output():
+    wl = ragged_workload("bf16", 128, 4, 16, [100, 2000], seed=6)
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    run.write(*run.reserve(wl.decode_seqs), k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
+    out = run.attend(0, qd, d_table, mb, d_lens, 2, out_dtype=torch.bfloat16)
+    got = out.float().cpu().numpy()
+    ref = orc.attend(0, qh)
+    assert np.all(np.abs(got - ref) <= 2e-3 + np.abs(ref) * 2.0 ** -8)
+
+
+def test_multilayer_decode_step_host_buffers():
+    # the whole-step C entry point with host buffers, 3 layers, shared prefix
+    L, B, H, G, D = 3, 8, 2, 4, 128
+    # sequences 0 and 1 share a prefix whose tail block holds 3 of 8 slots:
+    # step 0 makes 0 copy it and lets 1 write in place
+    ops = [("append", 100, 43, 0), ("fork", 100, 0), ("fork", 100, 1), ("release", 100),
+           ("append", 2, 77, 2)]
+    wl = synth.Workload("multi", L, 64, B, H * G, H, D, "bf16", 8,
+                        synth.permutation((8, 1), 64), ops, [0, 1, 2])
+    orc = OracleRun(wl)
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(L, 64, B, H, D, "bf16", free_order=wl.free_order)
+    cache.k.zero_()
+    cache.v.zero_()
+    run = DeviceRun(cache, H * G)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    max_blocks = 16
+    staging = torch.empty(cache.kv_decode_step_staging_bytes(3, H * G, max_blocks),
+                          dtype=torch.uint8, device="cuda")
+    for step in range(3):
+        so, co = orc.reserve_step()
+        assert len(co) == (1 if step == 0 else 0)
+        q = orc.write_step(step, so, co)
+        qL = np.ascontiguousarray(np.broadcast_to(q, (L,) + q.shape))
+        _, k, v = wl.step_values(step)
+        out = np.zeros((L, 3, H * G, D), dtype=np.float32)
+        cache.kv_decode_step_host([0, 1, 2], H * G, max_blocks, qL, k, v, out, staging)
+        for layer in range(L):
+            ref = orc.attend(layer, q)
+            assert max_err(out[layer], ref) <= TOL["bf16"]
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+    assert np.array_equal(host_bits(cache.v), orc.st.V)
+    check_status(cache)
+
+
+def test_device_checks_flag_bad_ids_without_faulting():
+    wl = ragged_workload("bf16", 128, 4, 16, [40, 50])
+    cache, run = make(wl)
+    q, k, v = wl.step_values(0)
+    run.step(wl.decode_seqs, q, k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    d_table[0, 0] = wl.n_blocks + 5  # out of range: the kernel substitutes block 0
+    qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+    run.attend(0, qd, d_table, mb, d_lens, 2)
+    assert cache.kv_pool_device_status() & 1
+    bad = torch.tensor([wl.n_blocks * 16 + 3], dtype=torch.int64, device="cuda")
+    kk = torch.zeros((1, 1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    cache.reshape_and_cache(0, kk, kk, bad, 1)
+    assert cache.kv_pool_device_status() & 2
+    assert cache.kv_pool_device_status() == 0
