@@ -32,7 +32,7 @@ KV_DTYPE_BF16 = 1
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing; build it with `python -m paged_kv_cache_65_gb300.build` "
+        f"{LIB_PATH} is missing; build it with `python paged_kv_cache_65_gb300/build.py` "
         "(or __graft_entry__.build())")
 
 lib = C.CDLL(LIB_PATH)

@@ -7,7 +7,7 @@ linked statically; the driver API is reached through the runtime's entry
 point query, so the library loads on machines without a GPU driver (host-only
 calls work there, device calls fail with KV_ERR_CUDA).
 
-Usage: ``python -m paged_kv_cache_65_gb300.build [-v]``
+Usage: ``python paged_kv_cache_65_gb300/build.py [-v] [-f] [--ptxas]``
 """
 
 from __future__ import annotations
@@ -53,6 +53,15 @@ def _newer(target: str, deps) -> bool:
 def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    # objects from another host architecture are never reused
+    import platform
+
+    stamp = os.path.join(BUILD, "machine")
+    prev = open(stamp).read().strip() if os.path.exists(stamp) else ""
+    if prev != platform.machine():
+        force = True
+        with open(stamp, "w") as f:
+            f.write(platform.machine())
     cu, cpp = _sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "pagedkv.h"))
@@ -83,7 +92,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
                 sys.stderr.write(" ".join(cmd[-3:]) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"compile failed: {' '.join(cmd)}")
-    if jobs or not os.path.exists(LIB):
+    if jobs or force or not os.path.exists(LIB):
         cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs + ["-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if verbose or r.returncode != 0:
