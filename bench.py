@@ -68,6 +68,9 @@ def read_peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms with arrival times; the
+    summary keeps the samples inside the timed window (widened by 0.3 s on
+    each side so that a short window still has a sample next to it)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -81,20 +84,24 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 5.0:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self):
+    def stop(self, t_begin: float, t_end: float):
         if self.proc is None:
             return None
+        time.sleep(0.35)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -102,7 +109,9 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if not (t_begin - 0.3 <= t <= t_end + 0.3):
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -215,11 +224,14 @@ def bench_ours(args):
     L = wl.n_layers
     stream = torch.cuda.current_stream()
     n_steps = args.warmup + args.steps
+    # host part of the steps first (reservations + tables), then upload; the
+    # timed loop cycles over n_plans distinct steps so that contexts grow by
+    # at most n_plans tokens however many steps are timed
+    n_plans = min(n_steps, args.plans)
 
-    # host part of every step first (reservations + tables), then upload
     plans = []
     max_blocks = 1
-    for i in range(n_steps):
+    for i in range(n_plans):
         slots, pairs = run.reserve(seqs)
         table, lens = cache.seq_block_table(seqs, run.max_blocks(seqs))
         ub, lb = unique_kv_bytes(cache, seqs, run.lengths, esize)
@@ -251,7 +263,7 @@ def bench_ours(args):
 
     def one_step(i, record=True):
         nonlocal launches
-        p = dplans[i]
+        p = dplans[i % n_plans]
         flush.fill_(i & 0xFF)  # evict L2 outside the timed windows
         e = ev[i]
         e[0].record(stream)
@@ -288,14 +300,15 @@ def bench_ours(args):
     for i in range(args.warmup, n_steps):
         one_step(i)
     torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
+    clk = clocks.stop(t_wall0, t_wall1)
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.warmup, n_steps)]
     split_ms = [ev_layer[i][l][0].elapsed_time(ev_layer[i][l][1])
                 for i in range(args.warmup, n_steps) for l in range(L)]
     dev_s = sum(step_ms) / 1e3
-    ub = sum(dplans[i]["ub"] for i in range(args.warmup, n_steps))
-    lb = sum(dplans[i]["lb"] for i in range(args.warmup, n_steps))
+    ub = sum(dplans[i % n_plans]["ub"] for i in range(args.warmup, n_steps))
+    lb = sum(dplans[i % n_plans]["lb"] for i in range(args.warmup, n_steps))
     tot_b, max_s = aggregate(float(ub), dev_s, world, dev)
     value = tot_b / max_s / 1e9
     ms_per_step = max_s / args.steps * 1e3
@@ -304,7 +317,7 @@ def bench_ours(args):
     # roofline of the split pass: algorithmic bytes per launch / mean duration
     per_launch_alg = []
     for i in range(args.warmup, n_steps):
-        p = dplans[i]
+        p = dplans[i % n_plans]
         kv = p["ub"] / L
         qb = n * wl.n_q_heads * wl.head_dim * esize
         per_launch_alg.append(kv + qb)
@@ -364,7 +377,8 @@ def bench_e2e(args, wl, cache, run, dev, world):
     seqs = wl.decode_seqs
     n = len(seqs)
     L = wl.n_layers
-    steps = max(1, args.steps)
+    # each e2e step advances the host state by one token per sequence
+    steps = max(1, min(args.steps, args.plans))
     max_blocks = run.max_blocks(seqs) + (steps + args.warmup) // wl.block_size + 2
     staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
                           dtype=torch.uint8, device=dev)
@@ -486,7 +500,9 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--plans", type=int, default=32,
+                    help="distinct decode steps the timed loop cycles over")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))

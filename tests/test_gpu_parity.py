@@ -232,8 +232,8 @@ def test_split_and_merge_calls_equal_one_call():
     qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
     ws = run.workspace(3)
     out = torch.empty_like(og[0])
-    cache.paged_decode_partials(0, qd, 64, d_table, mb, d_lens, 3, ws)
-    cache.paged_decode_merge(64, d_lens, 3, out, ws)
+    cache.paged_decode_partials(0, qd, wl.n_q_heads, d_table, mb, d_lens, 3, ws)
+    cache.paged_decode_merge(wl.n_q_heads, d_lens, 3, out, ws)
     assert torch.equal(out, og[0])
 
 
