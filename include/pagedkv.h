@@ -99,6 +99,12 @@ kvStatus kv_pool_check(const kvPool* pool);
 /* Reference count of one block (debugging aid). */
 kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
 
+/* Pool options.  KV_OPT_DECODE_PATH: 0 = automatic (tensor-core split pass
+ * for bfloat16 pools whose block size is a multiple of 8, CUDA-core pass
+ * otherwise), 1 = always the CUDA-core pass. */
+enum { KV_OPT_DECODE_PATH = 1 };
+kvStatus kv_pool_set_option(kvPool* pool, int option, int value);
+
 /* Synchronise `stream`, copy the device status word to *out_bits and clear
  * it.  Returns KV_ERR_DEVICE_CHECK when any bit was set. */
 kvStatus kv_pool_device_status(kvPool* pool, void* stream, int* out_bits);

@@ -27,6 +27,7 @@ KV_ERR_REFCOUNT = 3
 KV_ERR_CUDA = 4
 KV_ERR_DEVICE_CHECK = 5
 KV_ERR_UNSUPPORTED = 6
+KV_OPT_DECODE_PATH = 1
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
 
@@ -52,6 +53,7 @@ SIGNATURES = [
     ("kv_pool_stats", C.c_int, [_vp, _ip, _ip, _ip]),
     ("kv_pool_check", C.c_int, [_vp]),
     ("kv_block_refcount", C.c_int, [_vp, C.c_int32, _ip]),
+    ("kv_pool_set_option", C.c_int, [_vp, C.c_int, C.c_int]),
     ("kv_pool_device_status", C.c_int, [_vp, _vp, _ip]),
     ("block_alloc", C.c_int, [_vp, C.c_int, _i32p]),
     ("block_free", C.c_int, [_vp, _i32p, C.c_int]),

@@ -80,6 +80,9 @@ class PagedKVCache:
     def kv_pool_check(self):
         check(lib.kv_pool_check(self.handle), "kv_pool_check")
 
+    def kv_pool_set_option(self, option, value):
+        check(lib.kv_pool_set_option(self.handle, int(option), int(value)), "kv_pool_set_option")
+
     def kv_block_refcount(self, block_id):
         out = C.c_int()
         check(lib.kv_block_refcount(self.handle, int(block_id), C.byref(out)), "kv_block_refcount")

@@ -185,6 +185,16 @@ kvStatus kv_pool_check(const kvPool* p) {
   return KV_OK;
 }
 
+kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  if (option == KV_OPT_DECODE_PATH && (value == 0 || value == 1)) {
+    p->force_cuda_cores = value == 1;
+    for (int& g : p->grid_by_g) g = 0;  // grid sizes depend on the kernel
+    return KV_OK;
+  }
+  return KV_ERR_INVALID_ARG;
+}
+
 kvStatus kv_block_refcount(const kvPool* p, int32_t id, int* out) {
   if (!p || !out || !valid_id(p, id)) return KV_ERR_INVALID_ARG;
   *out = p->ref[id];

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "decode.cuh"
+#include "decode_mma.cuh"
 
 namespace pkv {
 
@@ -28,6 +29,31 @@ cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArg
   kern<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
   return cudaGetLastError();
 }
+
+template <int D, int G>
+cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
+                       int max_grid, int* grid_io, cudaStream_t st) {
+  constexpr int smem = decode_mma_smem_bytes<D, G>();
+  auto kern = decode_mma_kernel<D, G>;
+  if (*grid_io <= 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    int g = occ * sm_count;
+    *grid_io = g > max_grid ? max_grid : g;
+  }
+  a.grid = *grid_io;
+  kern<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+// Tensor-core variant for bfloat16 (swizzled TMA maps, B a multiple of 8).
+cudaError_t launch_mma_bf16(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
+                            cudaStream_t st, bool* supported);
 
 // Dispatch over (D, G) for one element size; *supported = false when the
 // shape has no compiled instantiation.

@@ -30,7 +30,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 // Encode a 2-D view of one cache: inner dimension H_kv * D_h elements (one
 // token row of every head), outer dimension N_layers * N_blocks * B rows; a
 // box is D_h elements of one head by `rows` token rows.
-kvStatus encode_cache_map(kvPool* p, void* base, int rows, CUtensorMap* out) {
+kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizzle128,
+                          CUtensorMap* out) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
@@ -44,13 +45,13 @@ kvStatus encode_cache_map(kvPool* p, void* base, int rows, CUtensorMap* out) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->H) * p->D,
                               static_cast<cuuint64_t>(p->L) * p->N * p->B};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->H) * p->D * p->esize};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(p->D), static_cast<cuuint32_t>(rows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows)};
   const cuuint32_t estride[2] = {1, 1};
   const CUtensorMapDataType dt =
       p->dtype == KV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUresult r = fn(out, dt, 2, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -66,10 +67,20 @@ kvStatus ensure_device(kvPool* p) {
     const int ts = pkv::stage_tokens(p->esize, p->D);
     if (p->B > ts && p->B % ts != 0) return KV_ERR_UNSUPPORTED;
     const int rows = p->B < ts ? p->B : ts;
-    kvStatus s = encode_cache_map(p, p->k, rows, reinterpret_cast<CUtensorMap*>(p->tmap[0]));
+    kvStatus s = encode_cache_map(p, p->k, p->D, rows, false,
+                                  reinterpret_cast<CUtensorMap*>(p->tmap[0]));
     if (s != KV_OK) return s;
-    s = encode_cache_map(p, p->v, rows, reinterpret_cast<CUtensorMap*>(p->tmap[1]));
+    s = encode_cache_map(p, p->v, p->D, rows, false, reinterpret_cast<CUtensorMap*>(p->tmap[1]));
     if (s != KV_OK) return s;
+    // tensor-core path: rows of 64 bf16 (128 bytes) with the 128-byte swizzle;
+    // each box must start on a 1 KiB boundary, hence B a multiple of 8
+    if (p->dtype == KV_DTYPE_BF16 && p->B % 8 == 0) {
+      s = encode_cache_map(p, p->k, 64, rows, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
+      if (s != KV_OK) return s;
+      s = encode_cache_map(p, p->v, 64, rows, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));
+      if (s != KV_OK) return s;
+      p->mma_ok = true;
+    }
   }
   p->dev_ready = true;
   return KV_OK;
@@ -124,8 +135,8 @@ __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, ui
 
 // Merge pass: per (sequence, query head) combine the partials of every piece
 // of its segment: M = max m_i, L = sum l_i 2^(m_i - M),
-// out = sum O_i 2^(m_i - M) / L.  A warp per head; the max over pieces is a
-// shuffle reduction.
+// out = sum O_i 2^(m_i - M) / L.  One warp per (sequence, query head), four
+// heads per CTA; the max over pieces is a shuffle reduction.
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict__ pre,
                                                     const float* __restrict__ ws_ml,
@@ -141,7 +152,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
   const long long W = pre[n_seq];
   long long chunk = (W + grid - 1) / grid;
   if (chunk == 0) chunk = 1;
-  for (int hq = warp; hq < Hq; hq += 4) {
+  {
+    const int hq = blockIdx.y * 4 + warp;
+    if (hq >= Hq) return;
     float o[DL];
 #pragma unroll
     for (int d = 0; d < DL; ++d) o[d] = 0.f;
@@ -305,16 +318,22 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
   a.grid = 0;
-  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[0]);
-  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[1]);
   int* grid_io = &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
-  cudaError_t e = p->esize == 2 ? pkv::launch_split_e2(p->D, G, tk, tv, a, p->sm_count,
-                                                        kMaxDecodeCtas, grid_io,
-                                                        as_stream(stream), &supported)
-                                : pkv::launch_split_e4(p->D, G, tk, tv, a, p->sm_count,
-                                                        kMaxDecodeCtas, grid_io,
-                                                        as_stream(stream), &supported);
+  cudaError_t e;
+  if (p->mma_ok && !p->force_cuda_cores) {
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+    e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
+                             as_stream(stream), &supported);
+  } else {
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[0]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[1]);
+    e = p->esize == 2 ? pkv::launch_split_e2(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                             grid_io, as_stream(stream), &supported)
+                      : pkv::launch_split_e4(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                             grid_io, as_stream(stream), &supported);
+  }
   if (!supported) return KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
@@ -339,11 +358,11 @@ kvStatus paged_decode_merge(kvPool* p, int n_q_heads, const int32_t* d_context_l
   float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
   __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
   if (p->D == 128)
-    merge_kernel<128><<<n_seq, 128, 0, as_stream(stream)>>>(pre, ml, o, n_seq, p->H, n_q_heads,
-                                                            grid, of, ob);
+    merge_kernel<128><<<dim3(n_seq, (n_q_heads + 3) / 4), 128, 0, as_stream(stream)>>>(
+        pre, ml, o, n_seq, p->H, n_q_heads, grid, of, ob);
   else
-    merge_kernel<64><<<n_seq, 128, 0, as_stream(stream)>>>(pre, ml, o, n_seq, p->H, n_q_heads,
-                                                           grid, of, ob);
+    merge_kernel<64><<<dim3(n_seq, (n_q_heads + 3) / 4), 128, 0, as_stream(stream)>>>(
+        pre, ml, o, n_seq, p->H, n_q_heads, grid, of, ob);
   return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 

@@ -33,7 +33,9 @@ struct kvPool {
   int device = -1;
   int sm_count = 0;
   int grid_by_g[4] = {0, 0, 0, 0};  // split-pass CTAs per log2(H_q / H_kv)
-  alignas(64) unsigned char tmap[2][128];  // TMA descriptors of K and V
+  alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
+  bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
+  bool force_cuda_cores = false;            // decode on CUDA cores even when mma_ok
 
   // host staging reused by kv_decode_step_host
   std::vector<int64_t> h_slots;

@@ -23,13 +23,18 @@ pytestmark = [
 TOL = {"f32": 1e-5, "bf16": 2e-3}
 
 
-def make(wl, zero=True):
+def make(wl, zero=True, path=0, fill_nan=False):
     from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300 import _lib
     from paged_kv_cache_65_gb300.driver import DeviceRun
 
     cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
                          wl.dtype, free_order=wl.free_order)
-    if zero:
+    cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, path)
+    if fill_nan:
+        cache.k.fill_(float("nan"))
+        cache.v.fill_(float("nan"))
+    elif zero:
         cache.k.zero_()
         cache.v.zero_()
     run = DeviceRun(cache, wl.n_q_heads)
@@ -148,13 +153,17 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype,D,G,B", SHAPES)
-def test_ragged_shapes(dtype, D, G, B):
+CASES = [s + (0,) for s in SHAPES] + [s + (1,) for s in SHAPES if s[0] == "bf16" and s[3] % 8 == 0]
+
+
+@pytest.mark.parametrize("dtype,D,G,B,path", CASES)
+def test_ragged_shapes(dtype, D, G, B, path):
+    # path 0: automatic (tensor cores for bf16 with B % 8 == 0); 1: CUDA cores
     lens = [1, 2, B - 1 if B > 1 else 3, B, B + 1, 3 * B + 2, 97, 700]
     lens = [max(1, l) for l in lens]
     wl = ragged_workload(dtype, D, G, B, lens, seed=D + G + B)
     orc = OracleRun(wl)
-    cache, run = make(wl)
+    cache, run = make(wl, path=path)
     so, co = orc.reserve_step()
     qh = orc.write_step(0, so, co)
     _, k, v = wl.step_values(0)
@@ -306,3 +315,36 @@ def test_device_checks_flag_bad_ids_without_faulting():
     cache.reshape_and_cache(0, kk, kk, bad, 1)
     assert cache.kv_pool_device_status() & 2
     assert cache.kv_pool_device_status() == 0
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_unused_slots_holding_nan_do_not_leak(path):
+    # the pool starts as NaN bit patterns: slots past each context in the last
+    # block are loaded with the block but must not reach any output
+    wl = ragged_workload("bf16", 128, 4, 16, [1, 5, 17, 33, 250, 1000], seed=12)
+    orc = OracleRun(wl)
+    cache, run = make(wl, fill_nan=True, path=path)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, qh, k, v)
+    got = og.cpu().numpy()[0]
+    assert np.isfinite(got).all()
+    assert max_err(got, orc.attend(0, qh)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["qwen_2k", "gqa70b_32k"])
+def test_tensor_core_and_cuda_core_paths_agree(name):
+    wl = synth.workload(name)
+    if name == "gqa70b_32k":
+        wl.build_ops = wl.build_ops[:10]  # two parents, eight branches: keeps the test short
+        wl.decode_seqs = wl.decode_seqs[:8]
+    outs = []
+    for path in (0, 1):
+        cache, run = make(wl, zero=False, path=path)
+        q, k, v = wl.step_values(0)
+        _, _, og = run.step(wl.decode_seqs, q, k, v)
+        outs.append(og.cpu().numpy())
+        del cache, run
+        torch.cuda.empty_cache()
+    assert float(np.max(np.abs(outs[0] - outs[1]))) <= 2e-3
