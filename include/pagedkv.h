@@ -64,7 +64,8 @@ enum {
   KV_DEV_BAD_SLOT = 2,     /* slot_mapping entry >= N_blocks * B       */
   KV_DEV_BAD_COW_PAIR = 4, /* copy pair id outside [0, N_blocks)       */
   KV_DEV_WAIT_TIMEOUT = 8, /* a pipeline wait gave up (never expected) */
-  KV_DEV_BAD_CONTEXT = 16  /* context_lens entry < 0 or > max_blocks * B */
+  KV_DEV_BAD_CONTEXT = 16, /* context_lens entry < 0 or > max_blocks * B */
+  KV_DEV_SMEM_ALIGN = 32   /* shared staging not 1 KiB aligned: pass skipped */
 };
 
 typedef struct kvPool kvPool;

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
   using C = DecodeCfg<ESIZE, D, G>;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   unsigned char* k_st = smem;
@@ -413,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
         alive = false;
         if (lane == 0) record_status(a.status, 8);
       }
+      alive = __all_sync(0xffffffffu, alive);  // reconverge after the poll loop
       const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
       const unsigned char* ks = k_st + slot * C::STAGE_BYTES;
       const unsigned char* vs = v_st + slot * C::STAGE_BYTES;

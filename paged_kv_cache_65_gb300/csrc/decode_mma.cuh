@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
   using C = MmaCfg<D, G>;
   constexpr int NST = C::NST;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the declared alignment stays at 16 so that the explicit round-up to the
+  // 1 KiB the 128-byte swizzle needs is never folded away
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
@@ -115,6 +117,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int STG = SB * UR;                   // tokens per stage
   const uint32_t unit_bytes = (uint32_t)UR * D * 2;  // K (or V) bytes of one box row set
 
+  // self-check: swizzled TMA destinations must sit on 1 KiB boundaries
+  if ((smem_u32(k_st) & 1023u) != 0u) {
+    if (threadIdx.x == 0) record_status(a.status, 32);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
@@ -230,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         alive = false;
         if (lane == 0) record_status(a.status, 8);
       }
+      alive = __all_sync(0xffffffffu, alive);  // reconverge before ldmatrix / mma.sync
       const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
       const uint32_t kb = k_base + slot * C::STAGE_BYTES;
       const uint32_t vb = v_base + slot * C::STAGE_BYTES;

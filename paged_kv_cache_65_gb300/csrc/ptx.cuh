@@ -57,7 +57,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// `limit_ns` of wall-clock time and returns false.
+// `limit_ns` of wall-clock time and returns false.  Lanes leave the poll loop
+// independently: callers reconverge (__syncwarp) before warp-collective
+// .aligned instructions.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -84,9 +86,10 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// Barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
+// Barrier over a subset of warps (ids 1..15; 0 is __syncthreads).  The
+// non-.aligned form: threads of a warp may arrive from divergent paths.
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ float exp2_approx(float x) {
