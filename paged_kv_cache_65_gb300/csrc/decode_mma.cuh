@@ -15,7 +15,7 @@
 // the weights keep ~16 mantissa bits.  Query heads beyond G are zero padding.
 //
 // Shared memory: each stage holds TS token rows of K and of V for one K/V
-// head, written by TMA with the 128-byte swizzle (rows of 64 elements, the
+// head (16 tokens at D = 128), written by TMA with the 128-byte swizzle (rows of 64 elements, the
 // 16-byte chunk c of row r stored at chunk c ^ (r mod 8)), so the 8 rows an
 // ldmatrix phase reads fall in 8 different bank groups.  Warp w consumes
 // stages w, w+4, w+8, ... with its own running softmax state; the four states
@@ -62,17 +62,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Tokens per stage of the tensor-core pass: 4 KiB of K (and of V).
+constexpr int mma_stage_tokens(int D) { return 8192 / (2 * D) / 2; }
+
 template <int D, int G>
 struct MmaCfg {
-  static constexpr int TS = stage_tokens(2, D);   // tokens per stage
-  static constexpr int TILES = TS / 16;           // 16-token tiles per stage
+  static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
   static constexpr int KS = D / 16;               // k-steps of Q.K and m-tiles of O^T
   static constexpr int HALVES = D / 64;           // 64-element swizzled row halves
   static constexpr int HALF_BYTES = TS * 128;     // one half of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * 2;  // K (or V) per stage
-  static constexpr int NST = G <= 4 ? 6 : 5;      // stages in the ring
+  // Stages in the ring.  Warp w consumes stages w, w+4, ...; with a multiple
+  // of 4 slots every slot is always consumed by the same warp, in order, so a
+  // warp's parity wait on a slot's barrier is never two phases behind.
+  static constexpr int NST = G <= 4 ? 12 : 8;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(G >= 1 && G <= 8, "group size");
+  static_assert(NST % kConsumerWarps == 0, "slot ownership");
+  static_assert(TS % 16 == 0, "whole tiles per stage");
 };
 
 template <int D, int G>

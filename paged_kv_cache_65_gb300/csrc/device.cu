@@ -73,11 +73,15 @@ kvStatus ensure_device(kvPool* p) {
     s = encode_cache_map(p, p->v, p->D, rows, false, reinterpret_cast<CUtensorMap*>(p->tmap[1]));
     if (s != KV_OK) return s;
     // tensor-core path: rows of 64 bf16 (128 bytes) with the 128-byte swizzle;
-    // each box must start on a 1 KiB boundary, hence B a multiple of 8
-    if (p->dtype == KV_DTYPE_BF16 && p->B % 8 == 0) {
-      s = encode_cache_map(p, p->k, 64, rows, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
+    // each box must start on a 1 KiB boundary, hence B a multiple of 8, and
+    // a stage must hold whole blocks or a block whole stages
+    const int tsm = pkv::mma_stage_tokens(p->D);
+    const bool fits = p->B <= tsm ? tsm % p->B == 0 : p->B % tsm == 0;
+    if (p->dtype == KV_DTYPE_BF16 && p->B % 8 == 0 && fits) {
+      const int rm = p->B < tsm ? p->B : tsm;
+      s = encode_cache_map(p, p->k, 64, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
       if (s != KV_OK) return s;
-      s = encode_cache_map(p, p->v, 64, rows, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));
+      s = encode_cache_map(p, p->v, 64, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));
       if (s != KV_OK) return s;
       p->mma_ok = true;
     }
