@@ -42,6 +42,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any real wait
+constexpr int kTableCache = 256;  // block-table entries cached by the producer
 
 struct DecodeArgs {
   const void* q;
@@ -89,6 +90,7 @@ constexpr int decode_smem_bytes() {
          + kConsumerWarps * G * D * 4                    // combine: O per warp
          + kConsumerWarps * G * 2 * 4                    // combine: m, l per warp
          + 2 * kStages * 8                               // mbarriers
+         + kTableCache * 4                               // producer table cache
          + 64 + 128;                                     // walk state + alignment
 }
 
@@ -228,6 +230,32 @@ __device__ inline void write_prefix(const int32_t* ctx, int n_seq, int B, int H,
   if (lane == 0) pre[n_seq] = run;
 }
 
+// Producer-side cache of block-table entries in shared memory: the producer
+// warp refills kTableCache consecutive entries of one sequence at a time
+// (kTableCache / 32 independent loads per lane, one round trip) instead of
+// paying a dependent global load before every TMA issue.
+
+struct TableCache {
+  int32_t* ent;  // shared, kTableCache entries
+  int seq = -1;
+  int base = 0;
+
+  // Make blocks [jf, jl] of `seq` available; whole warp calls.
+  __device__ void ensure(const int32_t* table, int max_blocks, int s, int jf, int jl, int lane) {
+    if (s == seq && jf >= base && jl < base + kTableCache) return;
+    __syncwarp();
+    seq = s;
+    base = jf;
+    const int32_t* row = table + (long long)s * max_blocks;
+#pragma unroll
+    for (int i = 0; i < kTableCache / 32; ++i) {
+      const int j = base + i * 32 + lane;
+      ent[i * 32 + lane] = j < max_blocks ? row[j] : 0;
+    }
+    __syncwarp();
+  }
+};
+
 // Iterates the pieces of [r0, r1) in segment order.
 struct PieceWalker {
   const int32_t* ctx;
@@ -284,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * G * 2);
   uint64_t* empty = full + kStages;
   long long* walk = reinterpret_cast<long long*>(empty + kStages);  // s, pre, W, chunk
+  int32_t* tcache = reinterpret_cast<int32_t*>(walk + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -333,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
     }
     bool alive = true;
     int stage = 0;
+    TableCache tc;
+    tc.ent = tcache;
     while (pw.next()) {
       const int tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
       for (int tok0 = pw.b0 * B; tok0 < tok_end; tok0 += STG) {
@@ -345,13 +376,14 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
         }
         const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
         const int nunits = (nvalid + UR - 1) / UR;
+        tc.ensure(a.table, a.max_blocks, pw.seq, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * box_bytes);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int t = tok0 + u * UR;
           const int j = t / B;
           const int row = t - j * B;
-          int pid = a.table[(long long)pw.seq * a.max_blocks + j];
+          int pid = tc.ent[j - tc.base];
           if (pid < 0 || pid >= a.n_blocks) {
             record_status(a.status, 1);
             pid = 0;  // stay in bounds; the result is flagged as invalid

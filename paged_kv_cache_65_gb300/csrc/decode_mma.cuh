@@ -89,6 +89,7 @@ constexpr int decode_mma_smem_bytes() {
          + kConsumerWarps * G * D * 4       // combine: O per warp
          + kConsumerWarps * G * 2 * 4       // combine: m, l per warp
          + 2 * C::NST * 8                   // mbarriers
+         + kTableCache * 4                  // producer table cache
          + 64 + 1024;                       // walk state + 1 KiB alignment
 }
 
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * G * 2);
   uint64_t* empty = full + NST;
   long long* walk = reinterpret_cast<long long*>(empty + NST);
+  int32_t* tcache = reinterpret_cast<int32_t*>(walk + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     bool alive = true;
     int stage = 0;
+    TableCache tc;
+    tc.ent = tcache;
     while (pw.next()) {
       const int tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
       for (int tok0 = pw.b0 * B; tok0 < tok_end; tok0 += STG) {
@@ -181,13 +185,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
         const int nunits = (nvalid + UR - 1) / UR;
+        tc.ensure(a.table, a.max_blocks, pw.seq, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * unit_bytes);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int t = tok0 + u * UR;
           const int j = t / B;
           const int row = t - j * B;
-          int pid = a.table[(long long)pw.seq * a.max_blocks + j];
+          int pid = tc.ent[j - tc.base];
           if (pid < 0 || pid >= a.n_blocks) {
             record_status(a.status, 1);
             pid = 0;  // stay in bounds; the result is flagged as invalid
