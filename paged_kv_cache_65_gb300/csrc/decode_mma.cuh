@@ -15,11 +15,12 @@
 // the weights keep ~16 mantissa bits.  Query heads beyond G are zero padding.
 //
 // Shared memory: each stage holds TS token rows of K and of V for one K/V
-// head (16 tokens at D = 128), written by TMA with the 128-byte swizzle (rows of 64 elements, the
-// 16-byte chunk c of row r stored at chunk c ^ (r mod 8)), so the 8 rows an
-// ldmatrix phase reads fall in 8 different bank groups.  Warp w consumes
-// stages w, w+4, w+8, ... with its own running softmax state; the four states
-// are merged through shared memory at the end of each piece.
+// head (64 tokens at D = 128), written by TMA with the 128-byte swizzle (rows
+// of 64 elements, the 16-byte chunk c of row r stored at chunk c ^ (r mod 8)),
+// so the 8 rows an ldmatrix phase reads fall in 8 different bank groups.  All
+// four consumer warps consume every stage, warp w taking its 16-token tile(s)
+// with its own running softmax state; the four states are merged through
+// shared memory at the end of each piece.
 #pragma once
 
 #include "decode.cuh"
@@ -62,31 +63,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Tokens per stage of the tensor-core pass: 4 KiB of K (and of V).
-constexpr int mma_stage_tokens(int D) { return 8192 / (2 * D) / 2; }
+// Tokens per stage of the tensor-core pass: one 16-token tile per consumer
+// warp (16 KiB of K and 16 KiB of V at D = 128).
+constexpr int mma_stage_tokens(int D) { return 16 * 4 * (D == 64 ? 2 : 1); }
 
 template <int D, int G>
 struct MmaCfg {
   static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
+  static constexpr int TPW = TS / 16 / kConsumerWarps;  // tiles per warp per stage
   static constexpr int KS = D / 16;               // k-steps of Q.K and m-tiles of O^T
   static constexpr int HALVES = D / 64;           // 64-element swizzled row halves
   static constexpr int HALF_BYTES = TS * 128;     // one half of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * 2;  // K (or V) per stage
-  // Stages in the ring.  Warp w consumes stages w, w+4, ...; with a multiple
-  // of 4 slots every slot is always consumed by the same warp, in order, so a
-  // warp's parity wait on a slot's barrier is never two phases behind.
-  static constexpr int NST = G <= 4 ? 12 : 8;
+  static constexpr int NST = 3;                   // stages in the ring
+  static constexpr int GC = G < 4 ? G : 4;        // heads per combine pass
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(G >= 1 && G <= 8, "group size");
-  static_assert(NST % kConsumerWarps == 0, "slot ownership");
-  static_assert(TS % 16 == 0, "whole tiles per stage");
+  static_assert(TS % (16 * kConsumerWarps) == 0, "whole tiles per warp");
 };
 
 template <int D, int G>
 constexpr int decode_mma_smem_bytes() {
   using C = MmaCfg<D, G>;
   return 2 * C::NST * C::STAGE_BYTES        // K and V stages
-         + kConsumerWarps * G * D * 4       // combine: O per warp
+         + kConsumerWarps * C::GC * D * 4   // combine: O per warp, GC heads at a time
          + kConsumerWarps * G * 2 * 4       // combine: m, l per warp
          + 2 * C::NST * 8                   // mbarriers
          + kTableCache * 4                  // producer table cache
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE_BYTES;
   float* cmb_o = reinterpret_cast<float*>(v_st + NST * C::STAGE_BYTES);
-  float* cmb_ml = cmb_o + kConsumerWarps * G * D;
+  float* cmb_ml = cmb_o + kConsumerWarps * C::GC * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * G * 2);
   uint64_t* empty = full + NST;
   long long* walk = reinterpret_cast<long long*>(empty + NST);
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
     }
     fence_barrier_init();
   }
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const int tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
     for (int tok0 = pw.b0 * B; tok0 < tok_end; tok0 += STG, ++stage) {
-      if ((stage & (kConsumerWarps - 1)) != warp) continue;
+      // every consumer warp waits on every stage and takes its own tiles of it
       const int slot = stage % NST;
       if (alive && !mbar_wait_bounded(&full[slot], (stage / NST) & 1, kWaitLimitNs)) {
         alive = false;
@@ -253,10 +253,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
       const uint32_t kb = k_base + slot * C::STAGE_BYTES;
       const uint32_t vb = v_base + slot * C::STAGE_BYTES;
-      const int ntiles = (nvalid + 15) >> 4;
-      for (int tt = 0; tt < ntiles; ++tt) {
-        // ---- S^T = K . Q^T
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int tw = 0; tw < C::TPW; ++tw) {
+        const int tt = tw * kConsumerWarps + warp;
+        if (tt * 16 >= nvalid) break;
+        // ---- S^T = K . Q^T (two independent accumulator chains)
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const int r = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
@@ -264,8 +266,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int d0 = ks * 16 + (lane >> 4) * 8;
             uint32_t a0, a1, a2, a3;
             ldsm_x4(swz(kb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
-            mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            if (ks & 1)
+              mma_bf16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+              mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[i] += s2[i];
         }
         // ---- scale, mask, tile max per head (heads 2t, 2t+1; tokens g, g+8)
         const int row0 = tt * 16 + g;
@@ -336,43 +343,53 @@ __global__ void __launch_bounds__(kThreads, 2)
       l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
       l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], off);
     }
+    if (g == 0) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int h = 2 * t + k;
-      if (h < G) {
-        if (g == 0) {
+      for (int k = 0; k < 2; ++k) {
+        const int h = 2 * t + k;
+        if (h < G) {
           cmb_ml[(warp * G + h) * 2] = m_run[k];
           cmb_ml[(warp * G + h) * 2 + 1] = l_run[k];
         }
+      }
+    }
+    const long long slot_id = (long long)blockIdx.x + (long long)pw.seq * a.n_kv_heads + pw.head;
 #pragma unroll
-        for (int mt = 0; mt < C::KS; ++mt) {
-          cmb_o[(warp * G + h) * D + mt * 16 + g] = o[mt][k];
-          cmb_o[(warp * G + h) * D + mt * 16 + g + 8] = o[mt][2 + k];
+    for (int h0 = 0; h0 < G; h0 += C::GC) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int h = 2 * t + k;
+        if (h >= h0 && h < h0 + C::GC) {
+#pragma unroll
+          for (int mt = 0; mt < C::KS; ++mt) {
+            cmb_o[(warp * C::GC + h - h0) * D + mt * 16 + g] = o[mt][k];
+            cmb_o[(warp * C::GC + h - h0) * D + mt * 16 + g + 8] = o[mt][2 + k];
+          }
         }
       }
-    }
-    named_bar_sync(1, kConsumerWarps * 32);
-    const long long slot_id = (long long)blockIdx.x + (long long)pw.seq * a.n_kv_heads + pw.head;
-    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-      const int h = idx / D, d = idx - h * D;
-      float M = -INFINITY;
+      named_bar_sync(1, kConsumerWarps * 32);
+      for (int idx = threadIdx.x; idx < C::GC * D; idx += kConsumerWarps * 32) {
+        const int hh = idx / D, d = idx - hh * D;
+        const int h = h0 + hh;
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cmb_ml[(w * G + h) * 2]);
-      float L = 0.f, O = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cmb_ml[(w * G + h) * 2]);
+        float L = 0.f, O = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = cmb_ml[(w * G + h) * 2];
-        const float f = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
-        L += f * cmb_ml[(w * G + h) * 2 + 1];
-        O += f * cmb_o[(w * G + h) * D + d];
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = cmb_ml[(w * G + h) * 2];
+          const float f = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
+          L += f * cmb_ml[(w * G + h) * 2 + 1];
+          O += f * cmb_o[(w * C::GC + hh) * D + d];
+        }
+        a.ws_o[(slot_id * G + h) * D + d] = O;
+        if (d == 0) {
+          a.ws_ml[(slot_id * G + h) * 2] = M;
+          a.ws_ml[(slot_id * G + h) * 2 + 1] = L;
+        }
       }
-      a.ws_o[(slot_id * G + h) * D + d] = O;
-      if (d == 0) {
-        a.ws_ml[(slot_id * G + h) * 2] = M;
-        a.ws_ml[(slot_id * G + h) * 2 + 1] = L;
-      }
+      named_bar_sync(1, kConsumerWarps * 32);
     }
-    named_bar_sync(1, kConsumerWarps * 32);
   }
 }
 
