@@ -53,7 +53,8 @@ enum {
   KV_ERR_REFCOUNT = 3,      /* handle not held, double free, broken counts   */
   KV_ERR_CUDA = 4,          /* a CUDA runtime call failed                   */
   KV_ERR_DEVICE_CHECK = 5,  /* a kernel recorded a bad id / slot / timeout  */
-  KV_ERR_UNSUPPORTED = 6    /* shape outside the compiled kernel set        */
+  KV_ERR_UNSUPPORTED = 6,   /* shape outside the compiled kernel set        */
+  KV_ERR_SCRATCH_TOO_SMALL = 7 /* request exceeds the static scratch array    */
 };
 
 enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1 };
@@ -201,6 +202,22 @@ kvStatus paged_decode_attention(kvPool* pool, int layer, const void* d_q, int n_
                                 const int32_t* d_context_lens, int n_seq, float scale,
                                 void* d_out, int out_dtype, void* d_workspace,
                                 size_t workspace_bytes, void* stream);
+
+/* Same as paged_decode_attention, without a caller workspace, for callers
+ * that cannot allocate device memory (inside a global-mode stream capture,
+ * where cudaMalloc is refused; under an allocator that has reserved all
+ * device memory; plain C hosts with no allocator).  The workspace is a
+ * 16 MiB array in the library's static device memory, one per GPU, held
+ * until the process exits.  Requests whose paged_decode_workspace_bytes()
+ * exceed 16 MiB (about 880 sequences at G = 4, D_h = 128, H_kv = 8) fail with
+ * KV_ERR_SCRATCH_TOO_SMALL before any device work.  The first call on a
+ * device looks up the array's device address; make it before any stream
+ * capture.  Calls on one GPU share the array: calls that overlap on the GPU
+ * race.  The pages have no counterpart of this call. */
+kvStatus paged_decode_attention_noalloc(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const int32_t* d_context_lens, int n_seq, float scale,
+                                        void* d_out, int out_dtype, void* stream);
 
 /* --------------------------------------------------- whole decode step --
  * One decode step through host buffers ([BT] §10 order): reserve a slot per

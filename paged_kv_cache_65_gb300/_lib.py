@@ -27,6 +27,7 @@ KV_ERR_REFCOUNT = 3
 KV_ERR_CUDA = 4
 KV_ERR_DEVICE_CHECK = 5
 KV_ERR_UNSUPPORTED = 6
+KV_ERR_SCRATCH_TOO_SMALL = 7
 KV_OPT_DECODE_PATH = 1
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
@@ -74,6 +75,8 @@ SIGNATURES = [
                                      _vp]),
     ("paged_decode_attention", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, C.c_int,
                                          C.c_float, _vp, C.c_int, _vp, C.c_size_t, _vp]),
+    ("paged_decode_attention_noalloc", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
+                                                 C.c_int, C.c_float, _vp, C.c_int, _vp]),
     ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
     ("kv_decode_step_host", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
                                       C.c_float, _f32p, _vp, C.c_size_t, _vp]),

@@ -182,6 +182,16 @@ class PagedKVCache:
                                          _nbytes(workspace), _stream(stream)),
               "paged_decode_attention")
 
+    def paged_decode_attention_noalloc(self, layer, q, n_q_heads, d_table, max_blocks, d_lens,
+                                       n_seq, out, scale=0.0, stream=None):
+        """Decode attention with the library's static scratch instead of a
+        caller workspace (for callers that cannot allocate device memory)."""
+        check(lib.paged_decode_attention_noalloc(self.handle, int(layer), vp(q), int(n_q_heads),
+                                                 vp(d_table), int(max_blocks), vp(d_lens),
+                                                 int(n_seq), float(scale), vp(out),
+                                                 _out_dtype(out), _stream(stream)),
+              "paged_decode_attention_noalloc")
+
     def kv_decode_step_staging_bytes(self, n_seq, n_q_heads, max_blocks):
         return int(lib.kv_decode_step_staging_bytes(self.handle, int(n_seq), int(n_q_heads),
                                                     int(max_blocks)))

@@ -100,6 +100,7 @@ const char* kv_status_string(kvStatus s) {
     case KV_ERR_CUDA: return "CUDA error";
     case KV_ERR_DEVICE_CHECK: return "device check failed";
     case KV_ERR_UNSUPPORTED: return "unsupported shape";
+    case KV_ERR_SCRATCH_TOO_SMALL: return "request exceeds the static scratch size";
     default: return "unknown status";
   }
 }
