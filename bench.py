@@ -52,7 +52,7 @@ TRAFFIC = {}
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "ptx.cuh", "device.cu"):
+    for f in ("decode.cuh", "decode_mma.cuh", "ptx.cuh", "device.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_65_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -219,6 +219,10 @@ def bench_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl, cache, run = setup(args.workload, args.block_size, dev)
+    if args.cuda_cores:
+        from paged_kv_cache_65_gb300 import _lib
+
+        cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, 1)
     esize = wl.elem_bytes
     seqs = wl.decode_seqs
     n = len(seqs)
@@ -390,6 +394,7 @@ def bench_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
             "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
+                       "decode_path": "cuda_cores" if args.cuda_cores else "auto",
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
                        "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
@@ -560,6 +565,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="decode on CUDA cores even where the tensor-core pass applies")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-leg", default=None)
     args = ap.parse_args()
