@@ -47,7 +47,13 @@ DEFAULT_WORKLOAD = "qwen_2k"
 
 # Per-launch DRAM traffic of the split pass from an ncu capture, keyed by
 # workload, valid only for the kernel source it was taken on.
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
+    # (profiles/decode_mma_qwen_2k.md, decode_mma_shared_8k.md, decode_mma_gqa70b_32k.md)
+    "qwen_2k": {"bytes": 331786000 + 3565000, "sha": "5d3f0bdbd949986c"},
+    "shared_8k": {"bytes": 177484000 + 3827000, "sha": "5d3f0bdbd949986c"},
+    "gqa70b_32k": {"bytes": 4869517000 + 4925000, "sha": "5d3f0bdbd949986c"},
+}
 
 
 def kernel_sha() -> str:
