@@ -203,6 +203,34 @@ kvStatus paged_decode_attention(kvPool* pool, int layer, const void* d_q, int n_
                                 void* d_out, int out_dtype, void* d_workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------- sharing-aware decode plan --
+ * Sequences that share physical blocks (after seq_fork, or a shared prompt;
+ * [KC] zero-copy branching, [IO] §8.3.2) can have each shared block read
+ * once for all of them.  paged_decode_plan builds, on the host, from the
+ * pool's tables, a work list for the listed sequences (in their current
+ * state, after the step's seq_append_slots): sequences whose tables start
+ * with the same run of full blocks (at least min_shared_tokens tokens; 0
+ * means 128) form groups of at most 32 / G members, whose shared prefix is one
+ * segment per K/V head carrying all members' query heads; the rest of each
+ * sequence is a segment of its own.  The plan is a flat byte buffer to copy
+ * to the device as-is.  *out_workspace_bytes gets the decode workspace size
+ * the plan needs. */
+size_t paged_decode_plan_bytes(const kvPool* pool, int n_seq, int n_q_heads);
+kvStatus paged_decode_plan(const kvPool* pool, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                           int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
+                           size_t* out_workspace_bytes);
+
+/* Decode attention of one layer following a plan: d_block_table and d_q hold
+ * the listed sequences' rows in plan order; d_plan is the device copy of
+ * h_plan (both are read: the host copy for sizes, the device copy by the
+ * kernels).  Tensor-core path only (bfloat16 pool, B a multiple of 8):
+ * KV_ERR_UNSUPPORTED otherwise.  Output as paged_decode_attention. */
+kvStatus paged_decode_attention_planned(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const void* d_plan, const void* h_plan, float scale,
+                                        void* d_out, int out_dtype, void* d_workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* Same as paged_decode_attention, without a caller workspace, for callers
  * that cannot allocate device memory (inside a global-mode stream capture,
  * where cudaMalloc is refused; under an allocator that has reserved all

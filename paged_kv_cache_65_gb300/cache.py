@@ -182,6 +182,26 @@ class PagedKVCache:
                                          _nbytes(workspace), _stream(stream)),
               "paged_decode_attention")
 
+    def paged_decode_plan(self, seq_ids, n_q_heads, max_blocks, min_shared_tokens=0):
+        """Host plan of a sharing-aware decode pass: (plan bytes, workspace bytes)."""
+        ids = i32(seq_ids)
+        cap = int(lib.paged_decode_plan_bytes(self.handle, ids.size, int(n_q_heads)))
+        buf = np.zeros(max(cap, 16), dtype=np.uint8)
+        ws = C.c_size_t()
+        check(lib.paged_decode_plan(self.handle, ptr_i32(ids), ids.size, int(n_q_heads),
+                                    int(max_blocks), int(min_shared_tokens), vp(buf), buf.nbytes,
+                                    C.byref(ws)), "paged_decode_plan")
+        return buf, int(ws.value)
+
+    def paged_decode_attention_planned(self, layer, q, n_q_heads, d_table, max_blocks, d_plan,
+                                       h_plan, out, workspace, scale=0.0, stream=None):
+        check(lib.paged_decode_attention_planned(self.handle, int(layer), vp(q), int(n_q_heads),
+                                                 vp(d_table), int(max_blocks), vp(d_plan),
+                                                 vp(h_plan), float(scale), vp(out),
+                                                 _out_dtype(out), vp(workspace),
+                                                 _nbytes(workspace), _stream(stream)),
+              "paged_decode_attention_planned")
+
     def paged_decode_attention_noalloc(self, layer, q, n_q_heads, d_table, max_blocks, d_lens,
                                        n_seq, out, scale=0.0, stream=None):
         """Decode attention with the library's static scratch instead of a
@@ -226,3 +246,25 @@ def _out_dtype(out) -> int:
     if out.dtype == torch.bfloat16:
         return _lib.KV_DTYPE_BF16
     raise TypeError(out.dtype)
+
+
+PLAN_SEG = np.dtype([("wpre", "<i8"), ("rep", "<i4"), ("b0", "<i4"), ("b1", "<i4"),
+                     ("tok_end", "<i4"), ("head", "<i4"), ("ncols", "<i4"), ("mem", "<i4"),
+                     ("pad", "<i4")])
+PLAN_ENTRY = np.dtype([("seg", "<i4"), ("col_base", "<i4")])
+
+
+def parse_plan(buf: np.ndarray) -> dict:
+    """Read a plan built by ``paged_decode_plan`` (layout of csrc/plan.h)."""
+    h = np.frombuffer(buf[:80].tobytes(), dtype=np.int32)
+    W = int(np.frombuffer(buf[:8].tobytes(), dtype=np.int64)[0])
+    (n_segs, n_members, n_entries, c_max, n_seq, n_kv_heads, group, block_size, seg_off,
+     mem_off, eoff_off, ent_off, n_shared) = (int(x) for x in h[2:15])
+    segs = np.frombuffer(buf[seg_off:seg_off + 40 * n_segs].tobytes(), dtype=PLAN_SEG)
+    members = np.frombuffer(buf[mem_off:mem_off + 4 * n_members].tobytes(), dtype=np.int32)
+    eoff = np.frombuffer(buf[eoff_off:eoff_off + 4 * (n_seq * n_kv_heads + 1)].tobytes(),
+                         dtype=np.int32)
+    ents = np.frombuffer(buf[ent_off:ent_off + 8 * n_entries].tobytes(), dtype=PLAN_ENTRY)
+    return dict(W=W, n_segs=n_segs, c_max=c_max, n_seq=n_seq, H=n_kv_heads, G=group,
+                B=block_size, n_shared_segs=n_shared, segs=segs, members=members, eoff=eoff,
+                ents=ents)

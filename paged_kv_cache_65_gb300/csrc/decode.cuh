@@ -34,6 +34,7 @@
 
 #include <cstdint>
 
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -49,12 +50,19 @@ struct DecodeArgs {
   const int32_t* table;
   const int32_t* ctx;
   long long* ws_pre;  // [n_seq + 1]: blocks (all heads) before each sequence
-  float* ws_ml;  // [n_slots][G][2]: (m in base-2 units, l)
-  float* ws_o;   // [n_slots][G][D]
+  float* ws_ml;  // [n_slots][columns][2]: (m in base-2 units, l)
+  float* ws_o;   // [n_slots][columns][D]
   int32_t* status;
   int n_seq, max_blocks, layer, n_blocks, block_size, n_kv_heads, n_q_heads;
   float qscale;  // scale * log2(e), folded into q
   int grid;
+  // sharing-aware plan (tensor-core pass only); segs == nullptr: one segment
+  // per (sequence, K/V head) taken from the context lengths
+  const PlanSeg* segs;
+  const int32_t* members;
+  int n_segs;
+  int c_max;
+  long long plan_W;
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }

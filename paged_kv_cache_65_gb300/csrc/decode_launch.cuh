@@ -34,19 +34,34 @@ template <int D, int G>
 cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
                        int max_grid, int* grid_io, cudaStream_t st) {
   constexpr int smem = decode_mma_smem_bytes<D, G>();
-  auto kern = decode_mma_kernel<D, G>;
-  if (*grid_io <= 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto k_plain = decode_mma_kernel<D, G, false>;
+  auto k_plan = decode_mma_kernel<D, G, true>;
+  // the dynamic shared-memory limit is a per-function, per-device attribute
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int v = a.segs ? 1 : 0;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[v][dev]) {
+    e = cudaFuncSetAttribute(v ? k_plan : k_plain, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
     if (e != cudaSuccess) return e;
+    attr_set[v][dev] = true;
+  }
+  if (*grid_io <= 0) {
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v ? k_plan : k_plain, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     int g = occ * sm_count;
     *grid_io = g > max_grid ? max_grid : g;
   }
   a.grid = *grid_io;
-  kern<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
+  if (v)
+    k_plan<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
+  else
+    k_plain<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
   return cudaGetLastError();
 }
 

@@ -1,26 +1,32 @@
 // Split-K paged decode attention, partial pass, bfloat16 K/V on tensor cores.
 //
 // Same contract, work split and workspace as decode.cuh (see there): per
-// (sequence, K/V head, block range) it emits the base-2 online-softmax
-// statistics m, l and the unnormalised O for the G query heads of the group.
+// piece of a segment (a block range of one table row and one K/V head) it
+// emits the base-2 online-softmax statistics m, l and the unnormalised O of
+// every query column of the segment.  Without a plan a segment is one
+// (sequence, K/V head) and its columns are that sequence's G query heads;
+// with a plan (plan.h) a segment of blocks shared by several sequences
+// carries all of their columns, so each shared block is read once.
 //
-// The two products of a 16-token tile are small MMAs over the query group
+// The products of a 16-token tile and an 8-column n-tile are MMAs
 // (m16n8k16, bf16 in, f32 accumulate):
-//     S^T [16 tokens x 8 heads] = K [16 x D] . Q^T [D x 8]       (D/16 MMAs)
-//     O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]     (2 x D/16)
+//     S^T [16 tokens x 8 cols] = K [16 x D] . Q^T [D x 8]        (D/16 MMAs)
+//     O^T [D x 8 cols]        += V^T [D x 16] . P^T [16 x 8]      (2 x D/16)
 // K and V^T come straight from shared memory with ldmatrix (V transposed on
 // load), Q^T lives in registers for the whole piece, and P^T is the S^T
 // accumulator turned into bf16 and transposed inside the warp with movmatrix.
 // P is split into a bf16 high part and a bf16 remainder (two MMAs) so that
-// the weights keep ~16 mantissa bits.  Query heads beyond G are zero padding.
+// the weights keep ~16 mantissa bits.  Columns past the segment's are zero.
 //
 // Shared memory: each stage holds TS token rows of K and of V for one K/V
 // head (64 tokens at D = 128), written by TMA with the 128-byte swizzle (rows
 // of 64 elements, the 16-byte chunk c of row r stored at chunk c ^ (r mod 8)),
 // so the 8 rows an ldmatrix phase reads fall in 8 different bank groups.  All
-// four consumer warps consume every stage, warp w taking its 16-token tile(s)
-// with its own running softmax state; the four states are merged through
-// shared memory at the end of each piece.
+// four consumer warps consume every stage.  A piece with NT n-tiles (1, 2 or
+// 4) gives warp w the n-tile w mod NT and the stage's tiles w / NT, w / NT +
+// 4 / NT, ...; each warp keeps its own running softmax state, and the states
+// of warps sharing an n-tile are merged through shared memory at the end of
+// the piece.
 #pragma once
 
 #include "decode.cuh"
@@ -63,31 +69,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Tokens per stage of the tensor-core pass: one 16-token tile per consumer
-// warp (16 KiB of K and 16 KiB of V at D = 128).
+// Tokens per stage of the tensor-core pass: 64 tokens (16 KiB of K and 16
+// KiB of V at D = 128).
 constexpr int mma_stage_tokens(int D) { return 16 * 4 * (D == 64 ? 2 : 1); }
 
 template <int D, int G>
 struct MmaCfg {
   static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
-  static constexpr int TPW = TS / 16 / kConsumerWarps;  // tiles per warp per stage
+  static constexpr int TILES = TS / 16;           // 16-token tiles per stage
   static constexpr int KS = D / 16;               // k-steps of Q.K and m-tiles of O^T
   static constexpr int HALVES = D / 64;           // 64-element swizzled row halves
   static constexpr int HALF_BYTES = TS * 128;     // one half of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * 2;  // K (or V) per stage
   static constexpr int NST = 3;                   // stages in the ring
-  static constexpr int GC = G < 4 ? G : 4;        // heads per combine pass
+  static constexpr int CC = 4;                    // columns per combine pass
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(G >= 1 && G <= 8, "group size");
-  static_assert(TS % (16 * kConsumerWarps) == 0, "whole tiles per warp");
+  static_assert(TILES % kConsumerWarps == 0, "whole tiles per warp");
 };
 
 template <int D, int G>
 constexpr int decode_mma_smem_bytes() {
   using C = MmaCfg<D, G>;
   return 2 * C::NST * C::STAGE_BYTES        // K and V stages
-         + kConsumerWarps * C::GC * D * 4   // combine: O per warp, GC heads at a time
-         + kConsumerWarps * G * 2 * 4       // combine: m, l per warp
+         + kConsumerWarps * C::CC * D * 4   // combine: O per warp, CC columns at a time
+         + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
          + kTableCache * 4                  // producer table cache
          + 64 + 1024;                       // walk state + 1 KiB alignment
@@ -98,7 +104,60 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int r, int c) {
   return half_base + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-template <int D, int G>
+// One piece of work: blocks [b0, b1) of table row `rep` for K/V head `head`,
+// tokens below tok_end, `ncols` query columns taken from members mem.. (or
+// from `rep` itself without a plan); `seg` numbers the segment.
+struct Piece {
+  int rep, head, b0, b1, tok_end, ncols, mem, seg;
+};
+
+// Walks the plan's segments over the block range [r, r1).
+struct PlanWalker {
+  const PlanSeg* segs;
+  int n_segs, B, s;
+  long long r, r1;
+
+  __device__ bool next(Piece& p) {
+    while (r < r1 && s < n_segs) {
+      const PlanSeg sg = segs[s];
+      const long long len = sg.b1 - sg.b0;
+      if (len <= 0 || r >= sg.wpre + len) {
+        ++s;
+        continue;
+      }
+      const long long end = r1 < sg.wpre + len ? r1 : sg.wpre + len;
+      p.rep = sg.rep;
+      p.head = sg.head;
+      p.b0 = sg.b0 + (int)(r - sg.wpre);
+      p.b1 = sg.b0 + (int)(end - sg.wpre);
+      p.tok_end = p.b1 * B < sg.tok_end ? p.b1 * B : sg.tok_end;
+      p.ncols = sg.ncols;
+      p.mem = sg.mem;
+      p.seg = s;
+      r = end;
+      return true;
+    }
+    return false;
+  }
+};
+
+// One warp: the segment whose block range holds r0 (segments sorted by wpre).
+__device__ inline int plan_find(const PlanSeg* segs, int n_segs, long long r0) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n_segs;  // wpre[lo] <= r0 holds throughout
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool ok = idx < hi && segs[idx].wpre <= r0;
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    const int L = 31 - __clz(m);
+    lo = lo + L * step;
+    hi = lo + step < hi ? lo + step : hi;
+  }
+  return lo;
+}
+
+template <int D, int G, bool PLAN>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
@@ -112,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE_BYTES;
   float* cmb_o = reinterpret_cast<float*>(v_st + NST * C::STAGE_BYTES);
-  float* cmb_ml = cmb_o + kConsumerWarps * C::GC * D;
-  uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * G * 2);
+  float* cmb_ml = cmb_o + kConsumerWarps * C::CC * D;
+  uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * 8 * 2);
   uint64_t* empty = full + NST;
   long long* walk = reinterpret_cast<long long*>(empty + NST);
   int32_t* tcache = reinterpret_cast<int32_t*>(walk + 4);
@@ -121,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int B = a.block_size;
+  const int H = a.n_kv_heads;
   const int UR = B < C::TS ? B : C::TS;      // rows per TMA box (a multiple of 8)
   const int SB = B < C::TS ? C::TS / B : 1;  // boxes per stage
   const int STG = SB * UR;                   // tokens per stage
@@ -139,29 +199,70 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_barrier_init();
   }
   if (warp == 0) {
-    WalkStart w = find_start(a.ctx, a.n_seq, B, a.n_kv_heads, a.max_blocks, a.grid, blockIdx.x,
-                             a.status);
-    if (blockIdx.x == 0) write_prefix(a.ctx, a.n_seq, B, a.n_kv_heads, a.max_blocks, a.ws_pre);
-    if (lane == 0) {
-      walk[0] = w.s;
-      walk[1] = w.pre;
-      walk[2] = w.W;
-      walk[3] = w.chunk;
+    if constexpr (PLAN) {
+      const long long W = a.plan_W;
+      long long chunk = (W + a.grid - 1) / a.grid;
+      if (chunk == 0) chunk = 1;
+      const long long r0 = (long long)blockIdx.x * chunk;
+      const int s0 = r0 < W ? plan_find(a.segs, a.n_segs, r0) : a.n_segs;
+      if (lane == 0) {
+        walk[0] = s0;
+        walk[1] = 0;
+        walk[2] = W;
+        walk[3] = chunk;
+      }
+    } else {
+      WalkStart w = find_start(a.ctx, a.n_seq, B, H, a.max_blocks, a.grid, blockIdx.x, a.status);
+      if (blockIdx.x == 0) write_prefix(a.ctx, a.n_seq, B, H, a.max_blocks, a.ws_pre);
+      if (lane == 0) {
+        walk[0] = w.s;
+        walk[1] = w.pre;
+        walk[2] = w.W;
+        walk[3] = w.chunk;
+      }
     }
   }
   __syncthreads();
 
   const long long W = walk[2], chunk = walk[3];
+  const long long r_begin = (long long)blockIdx.x * chunk;
+  const long long r_end = r_begin + chunk < W ? r_begin + chunk : W;
   PieceWalker pw;
-  pw.ctx = a.ctx;
-  pw.n_seq = a.n_seq;
-  pw.B = B;
-  pw.H = a.n_kv_heads;
-  pw.max_blocks = a.max_blocks;
-  pw.s = (int)walk[0];
-  pw.pre = walk[1];
-  pw.r = (long long)blockIdx.x * chunk;
-  pw.r1 = pw.r + chunk < W ? pw.r + chunk : W;
+  PlanWalker plw;
+  if constexpr (PLAN) {
+    plw.segs = a.segs;
+    plw.n_segs = a.n_segs;
+    plw.B = B;
+    plw.s = (int)walk[0];
+    plw.r = r_begin;
+    plw.r1 = r_end;
+  } else {
+    pw.ctx = a.ctx;
+    pw.n_seq = a.n_seq;
+    pw.B = B;
+    pw.H = H;
+    pw.max_blocks = a.max_blocks;
+    pw.s = (int)walk[0];
+    pw.pre = walk[1];
+    pw.r = r_begin;
+    pw.r1 = r_end;
+  }
+  auto next_piece = [&](Piece& p) -> bool {
+    if constexpr (PLAN) {
+      return plw.next(p);
+    } else {
+      if (!pw.next()) return false;
+      p.rep = pw.seq;
+      p.head = pw.head;
+      p.b0 = pw.b0;
+      p.b1 = pw.b1;
+      p.tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
+      p.ncols = G;
+      p.mem = -1;
+      p.seg = pw.seq * H + pw.head;
+      return true;
+    }
+  };
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -173,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     int stage = 0;
     TableCache tc;
     tc.ent = tcache;
-    while (pw.next()) {
-      const int tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
-      for (int tok0 = pw.b0 * B; tok0 < tok_end; tok0 += STG) {
+    Piece p;
+    while (next_piece(p)) {
+      for (int tok0 = p.b0 * B; tok0 < p.tok_end; tok0 += STG) {
         const int slot = stage % NST;
         if (stage >= NST && alive) {
           if (!mbar_wait_bounded(&empty[slot], ((stage / NST) & 1) ^ 1, kWaitLimitNs)) {
@@ -183,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) record_status(a.status, 8);
           }
         }
-        const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
+        const int nvalid = p.tok_end - tok0 < STG ? p.tok_end - tok0 : STG;
         const int nunits = (nvalid + UR - 1) / UR;
-        tc.ensure(a.table, a.max_blocks, pw.seq, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
+        tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * unit_bytes);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
@@ -200,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int y = (a.layer * a.n_blocks + pid) * B + row;
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h) {
-            const int x = pw.head * D + h * 64;
+            const int x = p.head * D + h * 64;
             const int off = slot * C::STAGE_BYTES + h * C::HALF_BYTES + u * UR * 128;
             tma_load_2d(k_st + off, &tmap_k, x, y, &full[slot]);
             tma_load_2d(v_st + off, &tmap_v, x, y, &full[slot]);
@@ -220,20 +321,33 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int t = lane & 3;   // thread in group
   const uint32_t k_base = smem_u32(k_st);
   const uint32_t v_base = smem_u32(v_st);
+  const int cstride = PLAN ? a.c_max : G;  // columns per workspace slot
   bool alive = true;
   int stage = 0;
+  Piece p;
 
-  while (pw.next()) {
-    // Q^T fragments: head g of the group, dims ks*16 + 2t (+1) and + 8
+  while (next_piece(p)) {
+    const int NT = p.ncols <= 8 ? 1 : (p.ncols <= 16 ? 2 : 4);  // n-tiles of the piece
+    const int WT = kConsumerWarps / NT;                           // warps per n-tile
+    const int wn = warp % NT, wt = warp / NT;
+    // Q^T fragments of column wn*8 + g: dims ks*16 + 2t (+1) and + 8
     uint32_t qf[C::KS][2];
     {
+      const int col = wn * 8 + g;
+      const bool colv = col < p.ncols;
+      int seqm = p.rep, gi = col;
+      if constexpr (PLAN) {
+        const int mi = col / G;
+        gi = col - mi * G;
+        seqm = colv ? a.members[p.mem + mi] : 0;
+      }
       const uint32_t* qw = reinterpret_cast<const uint32_t*>(
           reinterpret_cast<const unsigned char*>(a.q) +
-          ((long long)pw.seq * a.n_q_heads + (long long)pw.head * G + (g < G ? g : 0)) * D * 2);
+          ((long long)seqm * a.n_q_heads + (long long)p.head * G + (colv ? gi : 0)) * D * 2);
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        qf[ks][0] = g < G ? qw[(ks * 16 + 2 * t) / 2] : 0u;
-        qf[ks][1] = g < G ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
+        qf[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
+        qf[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
       }
     }
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -241,8 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int mt = 0; mt < C::KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    const int tok_end = pw.b1 * B < pw.ctx_len ? pw.b1 * B : pw.ctx_len;
-    for (int tok0 = pw.b0 * B; tok0 < tok_end; tok0 += STG, ++stage) {
+    for (int tok0 = p.b0 * B; tok0 < p.tok_end; tok0 += STG, ++stage) {
       // every consumer warp waits on every stage and takes its own tiles of it
       const int slot = stage % NST;
       if (alive && !mbar_wait_bounded(&full[slot], (stage / NST) & 1, kWaitLimitNs)) {
@@ -250,12 +363,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) record_status(a.status, 8);
       }
       alive = __all_sync(0xffffffffu, alive);  // reconverge before ldmatrix / mma.sync
-      const int nvalid = tok_end - tok0 < STG ? tok_end - tok0 : STG;
+      const int nvalid = p.tok_end - tok0 < STG ? p.tok_end - tok0 : STG;
       const uint32_t kb = k_base + slot * C::STAGE_BYTES;
       const uint32_t vb = v_base + slot * C::STAGE_BYTES;
 #pragma unroll 1
-      for (int tw = 0; tw < C::TPW; ++tw) {
-        const int tt = tw * kConsumerWarps + warp;
+      for (int tt = wt; tt < C::TILES; tt += WT) {
         if (tt * 16 >= nvalid) break;
         // ---- S^T = K . Q^T (two independent accumulator chains)
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -274,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int i = 0; i < 4; ++i) s[i] += s2[i];
         }
-        // ---- scale, mask, tile max per head (heads 2t, 2t+1; tokens g, g+8)
+        // ---- scale, mask, tile max per column (columns 2t, 2t+1; tokens g, g+8)
         const int row0 = tt * 16 + g;
         const bool v0 = row0 < nvalid, v1 = row0 + 8 < nvalid;
         s[0] = v0 ? s[0] * a.qscale : -INFINITY;
@@ -337,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
 
-    // ---- combine the 4 warps' states for this piece
+    // ---- combine the states of the warps that share an n-tile
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], off);
@@ -346,46 +458,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (g == 0) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int h = 2 * t + k;
-        if (h < G) {
-          cmb_ml[(warp * G + h) * 2] = m_run[k];
-          cmb_ml[(warp * G + h) * 2 + 1] = l_run[k];
-        }
+        cmb_ml[(warp * 8 + 2 * t + k) * 2] = m_run[k];
+        cmb_ml[(warp * 8 + 2 * t + k) * 2 + 1] = l_run[k];
       }
     }
-    const long long slot_id = (long long)blockIdx.x + (long long)pw.seq * a.n_kv_heads + pw.head;
-#pragma unroll
-    for (int h0 = 0; h0 < G; h0 += C::GC) {
+    const long long slot_id = (long long)blockIdx.x + p.seg;
+    for (int pc = 0; pc < 8; pc += C::CC) {
+      if (pc >= p.ncols) break;  // no column of any n-tile in this pass
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int h = 2 * t + k;
-        if (h >= h0 && h < h0 + C::GC) {
+        const int c8 = 2 * t + k;
+        if (c8 >= pc && c8 < pc + C::CC) {
 #pragma unroll
           for (int mt = 0; mt < C::KS; ++mt) {
-            cmb_o[(warp * C::GC + h - h0) * D + mt * 16 + g] = o[mt][k];
-            cmb_o[(warp * C::GC + h - h0) * D + mt * 16 + g + 8] = o[mt][2 + k];
+            cmb_o[(warp * C::CC + c8 - pc) * D + mt * 16 + g] = o[mt][k];
+            cmb_o[(warp * C::CC + c8 - pc) * D + mt * 16 + g + 8] = o[mt][2 + k];
           }
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);
-      for (int idx = threadIdx.x; idx < C::GC * D; idx += kConsumerWarps * 32) {
-        const int hh = idx / D, d = idx - hh * D;
-        const int h = h0 + hh;
+      for (int idx = threadIdx.x; idx < NT * C::CC * D; idx += kConsumerWarps * 32) {
+        const int wni = idx / (C::CC * D);
+        const int rem = idx - wni * C::CC * D;
+        const int cc = rem / D, d = rem - cc * D;
+        const int col = wni * 8 + pc + cc;
+        if (col >= p.ncols) continue;
         float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cmb_ml[(w * G + h) * 2]);
+        for (int j = 0; j < WT; ++j) M = fmaxf(M, cmb_ml[((wni + j * NT) * 8 + pc + cc) * 2]);
         float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = cmb_ml[(w * G + h) * 2];
+        for (int j = 0; j < WT; ++j) {
+          const int w = wni + j * NT;
+          const float mw = cmb_ml[(w * 8 + pc + cc) * 2];
           const float f = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
-          L += f * cmb_ml[(w * G + h) * 2 + 1];
-          O += f * cmb_o[(w * C::GC + hh) * D + d];
+          L += f * cmb_ml[(w * 8 + pc + cc) * 2 + 1];
+          O += f * cmb_o[(w * C::CC + cc) * D + d];
         }
-        a.ws_o[(slot_id * G + h) * D + d] = O;
+        a.ws_o[(slot_id * cstride + col) * D + d] = O;
         if (d == 0) {
-          a.ws_ml[(slot_id * G + h) * 2] = M;
-          a.ws_ml[(slot_id * G + h) * 2 + 1] = L;
+          a.ws_ml[(slot_id * cstride + col) * 2] = M;
+          a.ws_ml[(slot_id * cstride + col) * 2 + 1] = L;
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);

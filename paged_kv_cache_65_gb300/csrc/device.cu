@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "decode_launch.cuh"
+#include "plan.h"
 #include "pool.h"
 #include "ptx.cuh"
 
@@ -205,6 +206,72 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
   }
 }
 
+// Merge pass of a planned decode: per (sequence, query head) combine the
+// partials of every piece of every segment its merge entries name (shared
+// prefix and private rest), with the same rule as merge_kernel.
+template <int D>
+__global__ void __launch_bounds__(128) merge_plan_kernel(
+    const PlanSeg* __restrict__ segs, const int32_t* __restrict__ eoff,
+    const PlanEntry* __restrict__ ents, long long W, int grid, int c_max,
+    const float* __restrict__ ws_ml, const float* __restrict__ ws_o, int H, int Hq,
+    float* out_f32, __nv_bfloat16* out_bf16) {
+  constexpr int DL = D / 32;
+  const int s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = blockIdx.y * 4 + warp;
+  if (hq >= Hq) return;
+  const int G = Hq / H;
+  const int h = hq / G, g = hq - h * G;
+  long long chunk = (W + grid - 1) / grid;
+  if (chunk == 0) chunk = 1;
+  const int e0 = eoff[s * H + h], e1 = eoff[s * H + h + 1];
+  float M = -INFINITY;
+  for (int e = e0; e < e1; ++e) {
+    const PlanEntry en = ents[e];
+    const PlanSeg sg = segs[en.seg];
+    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + (sg.b1 - sg.b0) - 1) / chunk;
+    for (long long i = c0 + lane; i <= c1; i += 32)
+      M = fmaxf(M, ws_ml[((i + en.seg) * c_max + en.col_base + g) * 2]);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float o[DL];
+#pragma unroll
+  for (int d = 0; d < DL; ++d) o[d] = 0.f;
+  float L = 0.f;
+  for (int e = e0; e < e1; ++e) {
+    const PlanEntry en = ents[e];
+    const PlanSeg sg = segs[en.seg];
+    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + (sg.b1 - sg.b0) - 1) / chunk;
+    for (long long i = c0; i <= c1; ++i) {
+      const long long slot = (i + en.seg) * c_max + en.col_base + g;
+      const float f = pkv::exp2_approx(ws_ml[slot * 2] - M);
+      L += f * ws_ml[slot * 2 + 1];
+      const float* src = ws_o + slot * D + lane * DL;
+      if constexpr (DL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        o[0] += f * v.x;
+        o[1] += f * v.y;
+        o[2] += f * v.z;
+        o[3] += f * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        o[0] += f * v.x;
+        o[1] += f * v.y;
+      }
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const long long ob = ((long long)s * Hq + hq) * D + lane * DL;
+#pragma unroll
+  for (int d = 0; d < DL; ++d) {
+    if (out_f32)
+      out_f32[ob + d] = o[d] * inv;
+    else
+      out_bf16[ob + d] = __float2bfloat16_rn(o[d] * inv);
+  }
+}
+
 struct WsLayout {
   size_t pre, ml, o, total;
 };
@@ -322,6 +389,11 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
   a.grid = 0;
+  a.segs = nullptr;
+  a.members = nullptr;
+  a.n_segs = 0;
+  a.c_max = G;
+  a.plan_W = 0;
   int* grid_io = &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
@@ -385,11 +457,88 @@ kvStatus paged_decode_attention(kvPool* p, int layer, const void* d_q, int n_q_h
                             workspace_bytes, stream);
 }
 
+kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const void* d_plan, const void* h_plan, float scale,
+                                        void* d_out, int out_dtype, void* d_workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!p || !p->k || !h_plan || !d_plan) return KV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= p->L || n_q_heads <= 0 || n_q_heads % p->H != 0)
+    return KV_ERR_INVALID_ARG;
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  PlanHeader hd;
+  std::memcpy(&hd, h_plan, sizeof(hd));
+  const int G = n_q_heads / p->H;
+  if (hd.n_kv_heads != p->H || hd.group != G || hd.block_size != p->B || hd.n_seq < 0 ||
+      hd.c_max < G || hd.c_max > kPlanMaxCols)
+    return KV_ERR_INVALID_ARG;
+  if (hd.n_seq == 0) return KV_OK;
+  if (!d_q || !d_block_table || !d_out || !d_workspace || max_blocks <= 0) return KV_ERR_INVALID_ARG;
+  if (!aligned16(d_q) || !aligned16(d_workspace) || !aligned16(d_plan)) return KV_ERR_INVALID_ARG;
+  if (workspace_bytes < plan_workspace_bytes(hd.n_segs, hd.c_max, p->D)) return KV_ERR_INVALID_ARG;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  if (!p->mma_ok || p->force_cuda_cores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
+  const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
+  const size_t n_slots = static_cast<size_t>(kMaxDecodeCtas) + hd.n_segs;
+  const size_t ml_bytes = (n_slots * hd.c_max * 2 * sizeof(float) + 255) & ~size_t(255);
+  unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
+  pkv::DecodeArgs a;
+  a.q = d_q;
+  a.table = d_block_table;
+  a.ctx = nullptr;
+  a.ws_pre = nullptr;
+  a.ws_ml = reinterpret_cast<float*>(ws);
+  a.ws_o = reinterpret_cast<float*>(ws + ml_bytes);
+  a.status = p->d_status;
+  a.n_seq = hd.n_seq;
+  a.max_blocks = max_blocks;
+  a.layer = layer;
+  a.n_blocks = p->N;
+  a.block_size = p->B;
+  a.n_kv_heads = p->H;
+  a.n_q_heads = n_q_heads;
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
+  a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.grid = 0;
+  a.segs = reinterpret_cast<const PlanSeg*>(dp + hd.seg_off);
+  a.members = reinterpret_cast<const int32_t*>(dp + hd.mem_off);
+  a.n_segs = hd.n_segs;
+  a.c_max = hd.c_max;
+  a.plan_W = hd.W;
+  if (hd.W > 0) {
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+    bool supported = false;
+    const cudaError_t e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                               &p->grid_by_g[ilog2_small(G)], as_stream(stream),
+                                               &supported);
+    if (!supported) return KV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+  }
+  const int grid = p->grid_by_g[ilog2_small(G)] > 0 ? p->grid_by_g[ilog2_small(G)] : 1;
+  const PlanSeg* segs = reinterpret_cast<const PlanSeg*>(dp + hd.seg_off);
+  const int32_t* eoff = reinterpret_cast<const int32_t*>(dp + hd.eoff_off);
+  const PlanEntry* ents = reinterpret_cast<const PlanEntry*>(dp + hd.ent_off);
+  float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
+  __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
+  const dim3 mg(hd.n_seq, (n_q_heads + 3) / 4);
+  if (p->D == 128)
+    merge_plan_kernel<128><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, grid,
+                                                              hd.c_max, a.ws_ml, a.ws_o, p->H,
+                                                              n_q_heads, of, ob);
+  else
+    merge_plan_kernel<64><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, grid,
+                                                             hd.c_max, a.ws_ml, a.ws_o, p->H,
+                                                             n_q_heads, of, ob);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 // ------------------------------------------------------ whole decode step
 
 namespace {
 struct StepLayout {
-  size_t q, k, v, slots, pairs, table, lens, out, ws, total;
+  size_t q, k, v, slots, pairs, table, lens, out, plan, ws, total;
 };
 
 StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks) {
@@ -412,8 +561,12 @@ StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks
   off += align256(n * sizeof(int32_t));
   l.out = off;
   off += align256(L * n * n_q_heads * p->D * sizeof(float));
+  l.plan = off;
+  off += align256(paged_decode_plan_bytes(p, n_seq, n_q_heads));
   l.ws = off;
-  off += align256(ws_layout(p, n_seq, n_q_heads / p->H).total);
+  const size_t ws_plain = ws_layout(p, n_seq, n_q_heads / p->H).total;
+  const size_t ws_plan = plan_workspace_bytes(2 * n_seq * p->H, kPlanMaxCols, p->D);
+  off += align256(ws_plain > ws_plan ? ws_plain : ws_plan);
   l.total = off;
   return l;
 }
@@ -472,6 +625,20 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   ok &= cudaMemcpyAsync(d + l.lens, p->h_lens.data(), n_seq * sizeof(int32_t),
                         cudaMemcpyHostToDevice, st) == cudaSuccess;
   if (!ok) return KV_ERR_CUDA;
+  // sharing-aware plan on the tensor-core path (shared blocks read once)
+  const int G = n_q_heads / p->H;
+  const bool planned = p->mma_ok && !p->force_cuda_cores && ilog2_small(G) >= 0 &&
+                       (p->D == 64 || p->D == 128);
+  if (planned) {
+    p->h_plan.resize(paged_decode_plan_bytes(p, n_seq, n_q_heads));
+    size_t ws_need = 0;
+    s = paged_decode_plan(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, p->h_plan.data(),
+                          p->h_plan.size(), &ws_need);
+    if (s != KV_OK) return s;
+    if (cudaMemcpyAsync(d + l.plan, p->h_plan.data(), p->h_plan.size(), cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+      return KV_ERR_CUDA;
+  }
   // device: copy shared tails, write the new token in every layer, attend
   s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
   if (s != KV_OK) return s;
@@ -480,11 +647,18 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   if (s != KV_OK) return s;
   const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
   for (int layer = 0; layer < p->L; ++layer) {
-    s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
-                               reinterpret_cast<const int32_t*>(d + l.table), max_blocks,
-                               reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale,
-                               d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
-                               d + l.ws, staging_bytes - l.ws, stream);
+    if (planned)
+      s = paged_decode_attention_planned(
+          p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
+          reinterpret_cast<const int32_t*>(d + l.table), max_blocks, d + l.plan,
+          p->h_plan.data(), scale, d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
+          d + l.ws, staging_bytes - l.ws, stream);
+    else
+      s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
+                                 reinterpret_cast<const int32_t*>(d + l.table), max_blocks,
+                                 reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale,
+                                 d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
+                                 d + l.ws, staging_bytes - l.ws, stream);
     if (s != KV_OK) return s;
   }
   if (cudaMemcpyAsync(h_out, d + l.out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)

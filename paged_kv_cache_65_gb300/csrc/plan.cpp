@@ -1,0 +1,217 @@
+// Host builder of the sharing-aware decode plan (see plan.h).
+//
+// Prefix sharing comes from fork (one table copied into another, "KV 缓存管理",
+// zero-copy branching section) and from shared prompts ("第 8 章 推理优化"
+// §8.3.2): the blocks stay shared until a write into a partly filled tail
+// copies it.  Decode attention only reads, so every block that several
+// listed sequences' tables name at the same logical position, within all of
+// their contexts, can be read once for all of them.
+//
+// Grouping: listed sequences are grouped by the physical id of their first
+// block; a group's shared prefix is the longest run of leading blocks common
+// to all members, cut to whole blocks inside every member's context.  Groups
+// wider than kPlanMaxCols / G members are cut into sub-groups (each reads the
+// prefix once).  Prefixes shorter than `min_shared_tokens` are not shared.
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "plan.h"
+#include "pool.h"
+
+namespace {
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+struct Layout {
+  size_t seg, mem, eoff, ent, total;
+};
+
+Layout plan_layout(int n_seq, int H, int n_segs, int n_members, int n_entries) {
+  Layout l;
+  size_t off = align16(sizeof(PlanHeader));
+  l.seg = off;
+  off += align16(sizeof(PlanSeg) * static_cast<size_t>(n_segs));
+  l.mem = off;
+  off += align16(sizeof(int32_t) * static_cast<size_t>(n_members));
+  l.eoff = off;
+  off += align16(sizeof(int32_t) * (static_cast<size_t>(n_seq) * H + 1));
+  l.ent = off;
+  off += align16(sizeof(PlanEntry) * static_cast<size_t>(n_entries));
+  l.total = off;
+  return l;
+}
+
+}  // namespace
+
+size_t plan_workspace_bytes(int n_segs, int c_max, int D) {
+  const size_t n_slots = static_cast<size_t>(kMaxDecodeCtas) + static_cast<size_t>(n_segs);
+  const size_t ml = (n_slots * c_max * 2 * sizeof(float) + 255) & ~size_t(255);
+  return ml + n_slots * c_max * D * sizeof(float);
+}
+
+extern "C" {
+
+size_t paged_decode_plan_bytes(const kvPool* p, int n_seq, int n_q_heads) {
+  if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return 0;
+  // at most one private and one shared segment per (sequence, head), and
+  // two member slots and two entries per sequence (and head)
+  return plan_layout(n_seq, p->H, 2 * n_seq * p->H, 2 * n_seq, 2 * n_seq * p->H).total;
+}
+
+kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                           int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
+                           size_t* out_workspace_bytes) {
+  if (!p || n_seq < 0 || (n_seq > 0 && !seq_ids) || !h_plan || max_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
+  const int H = p->H, B = p->B, G = n_q_heads / H;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  if (plan_bytes < paged_decode_plan_bytes(p, n_seq, n_q_heads)) return KV_ERR_INVALID_ARG;
+  if (min_shared_tokens <= 0) min_shared_tokens = 128;
+  std::vector<const kvSeq*> seqs(n_seq);
+  {
+    std::vector<int32_t> sorted(seq_ids, seq_ids + n_seq);
+    std::sort(sorted.begin(), sorted.end());
+    if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return KV_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n_seq; ++i) {
+    auto it = p->seqs.find(seq_ids[i]);
+    if (it == p->seqs.end()) return KV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(it->second.table.size()) > max_blocks) return KV_ERR_INVALID_ARG;
+    if (it->second.len > static_cast<int64_t>(max_blocks) * B) return KV_ERR_INVALID_ARG;
+    seqs[i] = &it->second;
+  }
+  const int max_members = kPlanMaxCols / G;
+
+  // ---- groups: listed sequences with the same first physical block
+  std::vector<int> order;
+  for (int i = 0; i < n_seq; ++i)
+    if (!seqs[i]->table.empty()) order.push_back(i);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return seqs[a]->table[0] < seqs[b]->table[0]; });
+  std::vector<int> shared(n_seq, 0);     // shared prefix blocks per sequence
+  std::vector<int> pos_in(n_seq, -1);    // column group position in its shared segment
+  std::vector<std::vector<int>> chunks;  // sub-groups that read a prefix together
+  std::vector<int> chunk_p;              // their shared prefix length (blocks)
+  for (size_t a = 0; a < order.size();) {
+    size_t b = a + 1;
+    while (b < order.size() && seqs[order[b]]->table[0] == seqs[order[a]]->table[0]) ++b;
+    for (size_t c0 = a; b - a >= 2 && c0 < b; c0 += max_members) {
+      const size_t c1 = std::min(b, c0 + max_members);
+      if (c1 - c0 < 2) break;
+      std::vector<int> mem(order.begin() + c0, order.begin() + c1);
+      std::sort(mem.begin(), mem.end());
+      int P = static_cast<int>(seqs[mem[0]]->table.size());
+      for (int m : mem) {
+        const std::vector<int32_t>& t0 = seqs[mem[0]]->table;
+        const std::vector<int32_t>& t = seqs[m]->table;
+        int j = 0;
+        while (j < P && j < static_cast<int>(t.size()) && t[j] == t0[j]) ++j;
+        P = j;
+        P = std::min<int64_t>(P, seqs[m]->len / B);  // whole blocks inside every context
+      }
+      if (static_cast<int64_t>(P) * B < min_shared_tokens) continue;
+      for (size_t k = 0; k < mem.size(); ++k) {
+        shared[mem[k]] = P;
+        pos_in[mem[k]] = static_cast<int>(k);
+      }
+      chunks.push_back(mem);
+      chunk_p.push_back(P);
+    }
+    a = b;
+  }
+
+  // ---- segments, members, entries
+  std::vector<PlanSeg> segs;
+  std::vector<int32_t> members;
+  std::vector<std::vector<PlanEntry>> ents(static_cast<size_t>(n_seq) * H);
+  int c_max = G;
+  std::vector<int> chunk_of(n_seq, -1);
+  for (size_t c = 0; c < chunks.size(); ++c) {
+    const int mem0 = static_cast<int>(members.size());
+    for (int m : chunks[c]) {
+      members.push_back(m);
+      chunk_of[m] = static_cast<int>(c);
+    }
+    const int ncols = static_cast<int>(chunks[c].size()) * G;
+    c_max = std::max(c_max, ncols);
+    for (int h = 0; h < H; ++h) {
+      PlanSeg s{};
+      s.rep = chunks[c][0];
+      s.b0 = 0;
+      s.b1 = chunk_p[c];
+      s.tok_end = chunk_p[c] * B;
+      s.head = h;
+      s.ncols = ncols;
+      s.mem = mem0;
+      const int si = static_cast<int>(segs.size());
+      segs.push_back(s);
+      for (int m : chunks[c]) ents[static_cast<size_t>(m) * H + h].push_back({si, pos_in[m] * G});
+    }
+  }
+  for (int i = 0; i < n_seq; ++i) {
+    const int nb = static_cast<int>((seqs[i]->len + B - 1) / B);
+    if (nb <= shared[i]) continue;
+    const int mem0 = static_cast<int>(members.size());
+    members.push_back(i);
+    for (int h = 0; h < H; ++h) {
+      PlanSeg s{};
+      s.rep = i;
+      s.b0 = shared[i];
+      s.b1 = nb;
+      s.tok_end = static_cast<int32_t>(seqs[i]->len);
+      s.head = h;
+      s.ncols = G;
+      s.mem = mem0;
+      const int si = static_cast<int>(segs.size());
+      segs.push_back(s);
+      ents[static_cast<size_t>(i) * H + h].push_back({si, 0});
+    }
+  }
+  int64_t W = 0;
+  for (PlanSeg& s : segs) {
+    s.wpre = W;
+    W += s.b1 - s.b0;
+  }
+  int n_entries = 0;
+  for (const auto& e : ents) n_entries += static_cast<int>(e.size());
+
+  // ---- serialise
+  const Layout l = plan_layout(n_seq, H, static_cast<int>(segs.size()),
+                               static_cast<int>(members.size()), n_entries);
+  if (l.total > plan_bytes) return KV_ERR_INVALID_ARG;
+  unsigned char* out = static_cast<unsigned char*>(h_plan);
+  std::memset(out, 0, l.total);
+  PlanHeader hd{};
+  hd.W = W;
+  hd.n_segs = static_cast<int32_t>(segs.size());
+  hd.n_members = static_cast<int32_t>(members.size());
+  hd.n_entries = n_entries;
+  hd.c_max = c_max;
+  hd.n_seq = n_seq;
+  hd.n_kv_heads = H;
+  hd.group = G;
+  hd.block_size = B;
+  hd.seg_off = static_cast<int32_t>(l.seg);
+  hd.mem_off = static_cast<int32_t>(l.mem);
+  hd.eoff_off = static_cast<int32_t>(l.eoff);
+  hd.ent_off = static_cast<int32_t>(l.ent);
+  hd.n_shared_segs = static_cast<int32_t>(chunks.size()) * H;
+  std::memcpy(out, &hd, sizeof(hd));
+  if (!segs.empty()) std::memcpy(out + l.seg, segs.data(), sizeof(PlanSeg) * segs.size());
+  if (!members.empty()) std::memcpy(out + l.mem, members.data(), sizeof(int32_t) * members.size());
+  int32_t* eoff = reinterpret_cast<int32_t*>(out + l.eoff);
+  PlanEntry* ent = reinterpret_cast<PlanEntry*>(out + l.ent);
+  int k = 0;
+  for (size_t i = 0; i < ents.size(); ++i) {
+    eoff[i] = k;
+    for (const PlanEntry& e : ents[i]) ent[k++] = e;
+  }
+  eoff[ents.size()] = k;
+  if (out_workspace_bytes) *out_workspace_bytes = plan_workspace_bytes(hd.n_segs, c_max, p->D);
+  return KV_OK;
+}
+
+}  // extern "C"

@@ -40,7 +40,11 @@ struct kvPool {
   // host staging reused by kv_decode_step_host
   std::vector<int64_t> h_slots;
   std::vector<int32_t> h_pairs, h_table, h_lens;
+  std::vector<unsigned char> h_plan;
 };
 
 // Largest CTA count the split pass uses; sizes the decode workspace.
 constexpr int kMaxDecodeCtas = 1024;
+
+// Workspace bytes of a planned decode pass (plan.cpp).
+size_t plan_workspace_bytes(int n_segs, int c_max, int D);

@@ -110,7 +110,25 @@ class DeviceRun:
                                  out, self.workspace(n_seq), 0.0, self.stream)
         return out
 
-    def step(self, seq_ids, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray):
+    def plan(self, seq_ids, max_blocks, min_shared_tokens=0):
+        """Host plan of the sharing-aware pass and its device copy."""
+        buf, ws_bytes = self.c.paged_decode_plan(seq_ids, self.n_q_heads, max_blocks,
+                                                 min_shared_tokens)
+        return buf, torch.from_numpy(buf).to(self.dev), ws_bytes
+
+    def attend_planned(self, layer, q_dev, d_table, max_blocks, h_plan, d_plan, ws_bytes,
+                       out=None, out_dtype=torch.float32):
+        c = self.c
+        n_seq = int(q_dev.shape[0])
+        if out is None:
+            out = torch.empty((n_seq, self.n_q_heads, c.D), dtype=out_dtype, device=self.dev)
+        if self._ws is None or self._ws.numel() < ws_bytes:
+            self._ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.dev)
+        c.paged_decode_attention_planned(layer, q_dev, self.n_q_heads, d_table, max_blocks, d_plan,
+                                         h_plan, out, self._ws, 0.0, self.stream)
+        return out
+
+    def step(self, seq_ids, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, planned=False):
         """q ``[n_seq, H_q, D_h]`` (or ``[L, n_seq, H_q, D_h]``), new K/V
         ``[L, n_seq, H_kv, D_h]``.  Returns slots, pairs and float32 outputs
         ``[L, n_seq, H_q, D_h]`` on the device."""
@@ -120,7 +138,12 @@ class DeviceRun:
         L = self.c.L
         qd = to_device(q, self.c.dtype, self.dev)
         outs = []
+        if planned:
+            h_plan, d_plan, ws_bytes = self.plan(seq_ids, mb)
         for layer in range(L):
             ql = qd[layer] if qd.dim() == 4 else qd
-            outs.append(self.attend(layer, ql, d_table, mb, d_lens, len(seq_ids)))
+            if planned:
+                outs.append(self.attend_planned(layer, ql, d_table, mb, h_plan, d_plan, ws_bytes))
+            else:
+                outs.append(self.attend(layer, ql, d_table, mb, d_lens, len(seq_ids)))
         return slots, pairs, torch.stack(outs)

@@ -348,3 +348,126 @@ def test_tensor_core_and_cuda_core_paths_agree(name):
         del cache, run
         torch.cuda.empty_cache()
     assert float(np.max(np.abs(outs[0] - outs[1]))) <= 2e-3
+
+
+# ---------------------------------------------------------------- planned
+# The sharing-aware pass: shared prefix blocks are read once for all sharers.
+
+
+def test_planned_shared_8k_against_oracle_and_plain_pass():
+    wl = synth.workload("shared_8k")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    run.write(*run.reserve(wl.decode_seqs), k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
+    h_plan, d_plan, ws_bytes = run.plan(wl.decode_seqs, mb)
+    got = run.attend_planned(0, qd, d_table, mb, h_plan, d_plan, ws_bytes).cpu().numpy()
+    plain = run.attend(0, qd, d_table, mb, d_lens, len(wl.decode_seqs)).cpu().numpy()
+    assert float(np.max(np.abs(got - plain))) <= TOL["bf16"]
+    sample = [0, 7, 8, 15]
+    ref = orc.attend(0, qh, seq_index=sample)
+    for i in sample:
+        assert max_err(got[i], ref[i]) <= TOL["bf16"]
+    check_status(cache)
+
+
+def test_planned_gqa70b_32k_against_oracle():
+    wl = synth.workload("gqa70b_32k")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    sample = [0, 3, 21, 46]
+    for step in range(2):
+        so, co = orc.reserve_step()
+        qh = orc.write_step(step, so, co)
+        _, k, v = wl.step_values(step)
+        sg, pg, og = run.step(wl.decode_seqs, qh, k, v, planned=True)
+        assert list(sg) == so and [tuple(p) for p in pg] == co
+        ref = orc.attend(0, qh, seq_index=sample)
+        got = og.cpu().numpy()[0]
+        for i in sample:
+            assert max_err(got[i], ref[i]) <= TOL["bf16"]
+    check_status(cache)
+
+
+@pytest.mark.parametrize("seed,G,B", [(0, 1, 16), (1, 2, 8), (2, 4, 16), (3, 8, 16), (4, 4, 8),
+                                      (5, 8, 32)])
+def test_planned_random_fork_trees_against_oracle(seed, G, B):
+    rng = np.random.default_rng(seed)
+    H = 2
+    ops, live, nxt = [], [], 0
+    for _ in range(4):
+        ops.append(("append", nxt, int(rng.integers(100, 700)), nxt))
+        live.append(nxt)
+        nxt += 1
+    for _ in range(14):
+        p = int(rng.choice(live))
+        if rng.random() < 0.6:
+            ops.append(("fork", p, nxt))
+            live.append(nxt)
+            nxt += 1
+        else:
+            ops.append(("append", p, int(rng.integers(1, 200)), 1000 + nxt + len(ops)))
+    wl = synth.Workload("forks", 1, 2048, B, H * G, H, 128, "bf16", seed,
+                        synth.permutation((seed, 5), 2048), ops, live)
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v, planned=True)
+    assert list(sg) == so and [tuple(p) for p in pg] == co
+    h_plan, _, _ = run.plan(wl.decode_seqs, run.max_blocks(wl.decode_seqs))
+    from paged_kv_cache_65_gb300.cache import parse_plan
+
+    assert parse_plan(h_plan)["n_shared_segs"] > 0  # the trees do share prefixes
+    assert max_err(og.cpu().numpy()[0], orc.attend(0, qh)) <= TOL["bf16"]
+    check_status(cache)
+
+
+def test_planned_equals_plain_without_sharing():
+    wl = synth.workload("qwen_2k")
+    cache, run = make(wl, zero=False)
+    q, k, v = wl.step_values(0)
+    run.write(*run.reserve(wl.decode_seqs), k, v)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+    h_plan, d_plan, ws_bytes = run.plan(wl.decode_seqs, mb)
+    a = run.attend_planned(0, qd, d_table, mb, h_plan, d_plan, ws_bytes).clone()
+    b = run.attend(0, qd, d_table, mb, d_lens, len(wl.decode_seqs))
+    assert float((a - b).abs().max()) <= 1e-6
+
+
+def test_multilayer_host_step_with_long_shared_prefix():
+    # kv_decode_step_host plans the step: sequences 0-2 share 300 tokens
+    L, B, H, G, D = 2, 16, 2, 4, 128
+    ops = [("append", 100, 300, 0), ("fork", 100, 0), ("fork", 100, 1), ("fork", 100, 2),
+           ("release", 100), ("append", 1, 20, 1), ("append", 3, 77, 2)]
+    wl = synth.Workload("multi_shared", L, 128, B, H * G, H, D, "bf16", 9,
+                        synth.permutation((9, 1), 128), ops, [0, 1, 2, 3])
+    orc = OracleRun(wl)
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(L, 128, B, H, D, "bf16", free_order=wl.free_order)
+    cache.k.zero_()
+    cache.v.zero_()
+    run = DeviceRun(cache, H * G)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    max_blocks = 32
+    staging = torch.empty(cache.kv_decode_step_staging_bytes(4, H * G, max_blocks),
+                          dtype=torch.uint8, device="cuda")
+    for step in range(2):
+        so, co = orc.reserve_step()
+        q = orc.write_step(step, so, co)
+        qL = np.ascontiguousarray(np.broadcast_to(q, (L,) + q.shape))
+        _, k, v = wl.step_values(step)
+        out = np.zeros((L, 4, H * G, D), dtype=np.float32)
+        cache.kv_decode_step_host([0, 1, 2, 3], H * G, max_blocks, qL, k, v, out, staging)
+        for layer in range(L):
+            assert max_err(out[layer], orc.attend(layer, q)) <= TOL["bf16"]
+    check_status(cache)

@@ -1,0 +1,111 @@
+"""The sharing-aware decode plan (host, through the C ABI) against the
+oracle's block tables: every (sequence, K/V head) is covered by its merge
+entries exactly once over [0, context), every segment reads, for each member,
+the very physical blocks that member's own table names, and shared segments
+carry all their members' query heads."""
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.block_manager import BlockManager
+from paged_kv_cache_65_gb300 import PagedKVCache
+from paged_kv_cache_65_gb300.cache import parse_plan
+
+
+def build_both(wl):
+    bm = BlockManager(wl.n_blocks, wl.block_size, wl.free_order)
+    c = PagedKVCache(1, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim, wl.dtype,
+                     allocate=False, free_order=wl.free_order)
+    for op in wl.build_ops:
+        if op[0] == "append":
+            bm.append_tokens(op[1], op[2])
+            c.seq_append_tokens(op[1], op[2])
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2])
+            c.seq_fork(op[1], op[2])
+        else:
+            bm.release(op[1])
+            c.seq_release(op[1])
+    bm.append_slots(wl.decode_seqs)
+    c.seq_append_slots(wl.decode_seqs)
+    return bm, c
+
+
+def check_plan(bm, plan, seqs, G, min_tokens):
+    B, H = plan["B"], plan["H"]
+    segs, mem, eoff, ents = plan["segs"], plan["members"], plan["eoff"], plan["ents"]
+    assert plan["G"] == G and plan["n_seq"] == len(seqs)
+    assert plan["W"] == int(sum(int(s["b1"]) - int(s["b0"]) for s in segs))
+    assert list(segs["wpre"]) == list(np.cumsum([0] + [int(s["b1"] - s["b0"]) for s in segs])[:-1])
+    for si, s in enumerate(segs):
+        assert s["ncols"] % G == 0 and 0 < s["ncols"] <= 32
+        members = mem[s["mem"]:s["mem"] + s["ncols"] // G]
+        assert s["rep"] == members[0]
+        rep_table = bm.tables[seqs[s["rep"]]]
+        for m in members:
+            t = bm.tables[seqs[m]]
+            # the segment's blocks are this member's own blocks, inside its context
+            assert t[s["b0"]:s["b1"]] == rep_table[s["b0"]:s["b1"]]
+            assert s["tok_end"] <= bm.lengths[seqs[m]]
+        if len(members) > 1:
+            assert s["tok_end"] == s["b1"] * B and s["b1"] * B >= min_tokens
+    for i, sid in enumerate(seqs):
+        L = bm.lengths[sid]
+        for h in range(H):
+            covered = np.zeros(L, dtype=np.int64)
+            for e in ents[eoff[i * H + h]:eoff[i * H + h + 1]]:
+                s = segs[e["seg"]]
+                assert s["head"] == h
+                members = list(mem[s["mem"]:s["mem"] + s["ncols"] // G])
+                assert members.index(i) * G == e["col_base"]
+                covered[s["b0"] * B:min(s["b1"] * B, s["tok_end"])] += 1
+            assert (covered == 1).all(), (sid, h)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_2k", "shared_8k", "gqa70b_32k"])
+def test_plans_of_the_workloads(name):
+    wl = synth.workload(name)
+    bm, c = build_both(wl)
+    G = wl.n_q_heads // wl.n_kv_heads
+    mb = max(len(bm.tables[s]) for s in wl.decode_seqs)
+    buf, ws = c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)
+    plan = parse_plan(buf)
+    check_plan(bm, plan, wl.decode_seqs, G, 128)
+    assert ws > 0
+    shared = [s for s in plan["segs"] if s["ncols"] > G]
+    if name == "gqa70b_32k":
+        # 12 parents x 4 branches: one shared segment per parent and K/V head
+        assert len(shared) == 12 * 8 and all(s["ncols"] == 32 for s in shared)
+        assert all(s["b1"] == 2048 for s in shared)
+    elif name == "shared_8k":
+        # 16 sharers of 384 blocks at G = 4: two sub-groups of 8 per K/V head
+        assert len(shared) == 2 * 8 and all(s["b1"] == 384 for s in shared)
+    else:
+        assert not shared
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_plans_of_random_fork_trees(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.choice([8, 16]))
+    H, G = 2, int(rng.choice([1, 2, 4, 8]))
+    ops, live, nxt = [], [], 0
+    for _ in range(8):
+        ops.append(("append", nxt, int(rng.integers(1, 300)), nxt))
+        live.append(nxt)
+        nxt += 1
+    for _ in range(30):
+        p = int(rng.choice(live))
+        if rng.random() < 0.5:
+            ops.append(("fork", p, nxt))
+            live.append(nxt)
+            nxt += 1
+        else:
+            ops.append(("append", p, int(rng.integers(1, 40)), nxt))
+    wl = synth.Workload("forks", 1, 4096, B, H * G, H, 128, "bf16", seed, None, ops, live)
+    bm, c = build_both(wl)
+    mb = max(len(bm.tables[s]) for s in live)
+    for min_tokens in (16, 128, 0):
+        buf, _ = c.paged_decode_plan(live, H * G, mb, min_tokens)
+        check_plan(bm, parse_plan(buf), live, G, min_tokens or 128)
