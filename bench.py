@@ -240,7 +240,9 @@ def bench_ours(args):
     # at most n_plans tokens however many steps are timed
     n_plans = min(n_steps, args.plans)
 
-    plans = []
+    use_plan = not (args.plain or args.cuda_cores) and wl.dtype == "bf16" and \
+        wl.block_size % 8 == 0
+    plans, host_plans = [], []
     max_blocks = 1
     for i in range(n_plans):
         slots, pairs = run.reserve(seqs)
@@ -248,15 +250,23 @@ def bench_ours(args):
         ub, lb = unique_kv_bytes(cache, seqs, run.lengths, esize)
         plans.append((slots, pairs, table, lens, ub, lb))
         max_blocks = max(max_blocks, table.shape[1])
+        if use_plan:  # the sharing-aware plan of exactly this step's tables
+            host_plans.append(cache.paged_decode_plan(seqs, wl.n_q_heads, 1 << 24))
     dplans = []
-    for slots, pairs, table, lens, ub, lb in plans:
+    ws_bytes = cache.paged_decode_workspace_bytes(n, wl.n_q_heads)
+    for i, (slots, pairs, table, lens, ub, lb) in enumerate(plans):
         tpad = np.full((n, max_blocks), -1, dtype=np.int32)
         tpad[:, :table.shape[1]] = table
-        dplans.append(dict(
+        d = dict(
             slots=torch.from_numpy(slots).to(dev),
             pairs=torch.from_numpy(np.ascontiguousarray(pairs)).to(dev) if len(pairs) else None,
             npairs=len(pairs), table=torch.from_numpy(tpad).to(dev),
-            lens=torch.from_numpy(lens).to(dev), ub=ub, lb=lb, ctx=int(lens.sum())))
+            lens=torch.from_numpy(lens).to(dev), ub=ub, lb=lb, ctx=int(lens.sum()))
+        dplans.append(d)
+    for d, hp in zip(dplans, host_plans):
+        d["h_plan"], d["ws"] = hp
+        d["d_plan"] = torch.from_numpy(hp[0]).to(dev)
+        ws_bytes = max(ws_bytes, hp[1])
     g = torch.Generator(device=dev)
     g.manual_seed(synth.torch_seed((wl.seed, 6)))
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
@@ -264,7 +274,7 @@ def bench_ours(args):
     kn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
     vn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
     out = torch.empty((L, n, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
-    ws = run.workspace(n)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
 
@@ -287,11 +297,19 @@ def bench_ours(args):
         for layer in range(L):
             if ext is not None:
                 ext[layer][0].record()
-            cache.paged_decode_partials(layer, q[layer], wl.n_q_heads, p["table"], max_blocks,
-                                        p["lens"], n, ws, 0.0)
+            if use_plan:
+                cache.paged_decode_partials_planned(layer, q[layer], wl.n_q_heads, p["table"],
+                                                    max_blocks, p["d_plan"], p["h_plan"], ws)
+            else:
+                cache.paged_decode_partials(layer, q[layer], wl.n_q_heads, p["table"], max_blocks,
+                                            p["lens"], n, ws, 0.0)
             if ext is not None:
                 ext[layer][1].record()
-            cache.paged_decode_merge(wl.n_q_heads, p["lens"], n, out[layer], ws)
+            if use_plan:
+                cache.paged_decode_merge_planned(wl.n_q_heads, p["d_plan"], p["h_plan"],
+                                                 out[layer], ws)
+            else:
+                cache.paged_decode_merge(wl.n_q_heads, p["lens"], n, out[layer], ws)
             cnt += 2
         return cnt
 
@@ -316,9 +334,14 @@ def bench_ours(args):
                 gs = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gs, stream=cap):
                     for layer in range(L):
-                        cache.paged_decode_partials(layer, q[layer], wl.n_q_heads,
-                                                    dplans[pi]["table"], max_blocks,
-                                                    dplans[pi]["lens"], n, ws, 0.0)
+                        if use_plan:
+                            cache.paged_decode_partials_planned(
+                                layer, q[layer], wl.n_q_heads, dplans[pi]["table"], max_blocks,
+                                dplans[pi]["d_plan"], dplans[pi]["h_plan"], ws)
+                        else:
+                            cache.paged_decode_partials(layer, q[layer], wl.n_q_heads,
+                                                        dplans[pi]["table"], max_blocks,
+                                                        dplans[pi]["lens"], n, ws, 0.0)
                 split_graphs.append(gs)
     torch.cuda.current_stream().wait_stream(cap)
     torch.cuda.synchronize()
@@ -400,7 +423,8 @@ def bench_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
             "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
-                       "decode_path": "cuda_cores" if args.cuda_cores else "auto",
+                       "decode_path": ("cuda_cores" if args.cuda_cores else
+                                       "planned" if use_plan else "plain"),
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
                        "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
@@ -573,6 +597,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="decode on CUDA cores even where the tensor-core pass applies")
+    ap.add_argument("--plain", action="store_true",
+                    help="no sharing-aware plan: one segment per (sequence, K/V head)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-leg", default=None)
     args = ap.parse_args()

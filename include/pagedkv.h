@@ -220,6 +220,17 @@ kvStatus paged_decode_plan(const kvPool* pool, const int32_t* seq_ids, int n_seq
                            int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
                            size_t* out_workspace_bytes);
 
+/* The two passes of a planned decode, separately (same arguments as
+ * paged_decode_attention_planned; the merge must follow the partials on the
+ * same stream with the same plan and workspace). */
+kvStatus paged_decode_partials_planned(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                       const int32_t* d_block_table, int max_blocks,
+                                       const void* d_plan, const void* h_plan, float scale,
+                                       void* d_workspace, size_t workspace_bytes, void* stream);
+kvStatus paged_decode_merge_planned(kvPool* pool, int n_q_heads, const void* d_plan,
+                                    const void* h_plan, void* d_out, int out_dtype,
+                                    const void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* Decode attention of one layer following a plan: d_block_table and d_q hold
  * the listed sequences' rows in plan order; d_plan is the device copy of
  * h_plan (both are read: the host copy for sizes, the device copy by the

@@ -78,6 +78,10 @@ SIGNATURES = [
     ("paged_decode_plan_bytes", C.c_size_t, [_vp, C.c_int, C.c_int]),
     ("paged_decode_plan", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, C.c_int, _vp,
                                     C.c_size_t, C.POINTER(C.c_size_t)]),
+    ("paged_decode_partials_planned", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
+                                                _vp, C.c_float, _vp, C.c_size_t, _vp]),
+    ("paged_decode_merge_planned", C.c_int, [_vp, C.c_int, _vp, _vp, _vp, C.c_int, _vp,
+                                             C.c_size_t, _vp]),
     ("paged_decode_attention_planned", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
                                                  _vp, C.c_float, _vp, C.c_int, _vp, C.c_size_t,
                                                  _vp]),

@@ -193,6 +193,20 @@ class PagedKVCache:
                                     C.byref(ws)), "paged_decode_plan")
         return buf, int(ws.value)
 
+    def paged_decode_partials_planned(self, layer, q, n_q_heads, d_table, max_blocks, d_plan,
+                                      h_plan, workspace, scale=0.0, stream=None):
+        check(lib.paged_decode_partials_planned(self.handle, int(layer), vp(q), int(n_q_heads),
+                                                vp(d_table), int(max_blocks), vp(d_plan),
+                                                vp(h_plan), float(scale), vp(workspace),
+                                                _nbytes(workspace), _stream(stream)),
+              "paged_decode_partials_planned")
+
+    def paged_decode_merge_planned(self, n_q_heads, d_plan, h_plan, out, workspace, stream=None):
+        check(lib.paged_decode_merge_planned(self.handle, int(n_q_heads), vp(d_plan), vp(h_plan),
+                                             vp(out), _out_dtype(out), vp(workspace),
+                                             _nbytes(workspace), _stream(stream)),
+              "paged_decode_merge_planned")
+
     def paged_decode_attention_planned(self, layer, q, n_q_heads, d_table, max_blocks, d_plan,
                                        h_plan, out, workspace, scale=0.0, stream=None):
         check(lib.paged_decode_attention_planned(self.handle, int(layer), vp(q), int(n_q_heads),

@@ -457,31 +457,43 @@ kvStatus paged_decode_attention(kvPool* p, int layer, const void* d_q, int n_q_h
                             workspace_bytes, stream);
 }
 
-kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
-                                        const int32_t* d_block_table, int max_blocks,
-                                        const void* d_plan, const void* h_plan, float scale,
-                                        void* d_out, int out_dtype, void* d_workspace,
-                                        size_t workspace_bytes, void* stream) {
-  if (!p || !p->k || !h_plan || !d_plan) return KV_ERR_INVALID_ARG;
-  if (layer < 0 || layer >= p->L || n_q_heads <= 0 || n_q_heads % p->H != 0)
-    return KV_ERR_INVALID_ARG;
-  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
-  PlanHeader hd;
-  std::memcpy(&hd, h_plan, sizeof(hd));
+namespace {
+// Header of a host plan, checked against the pool and the call.
+kvStatus read_plan_header(const kvPool* p, int n_q_heads, const void* h_plan, PlanHeader* hd) {
+  if (!p || !p->k || !h_plan) return KV_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
+  std::memcpy(hd, h_plan, sizeof(*hd));
   const int G = n_q_heads / p->H;
-  if (hd.n_kv_heads != p->H || hd.group != G || hd.block_size != p->B || hd.n_seq < 0 ||
-      hd.c_max < G || hd.c_max > kPlanMaxCols)
+  if (hd->n_kv_heads != p->H || hd->group != G || hd->block_size != p->B || hd->n_seq < 0 ||
+      hd->c_max < G || hd->c_max > kPlanMaxCols || hd->n_segs < 0)
     return KV_ERR_INVALID_ARG;
-  if (hd.n_seq == 0) return KV_OK;
-  if (!d_q || !d_block_table || !d_out || !d_workspace || max_blocks <= 0) return KV_ERR_INVALID_ARG;
+  return KV_OK;
+}
+
+size_t plan_ml_bytes(const PlanHeader& hd) {
+  const size_t n_slots = static_cast<size_t>(kMaxDecodeCtas) + hd.n_segs;
+  return (n_slots * hd.c_max * 2 * sizeof(float) + 255) & ~size_t(255);
+}
+}  // namespace
+
+kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                       const int32_t* d_block_table, int max_blocks,
+                                       const void* d_plan, const void* h_plan, float scale,
+                                       void* d_workspace, size_t workspace_bytes, void* stream) {
+  PlanHeader hd;
+  kvStatus s = read_plan_header(p, n_q_heads, h_plan, &hd);
+  if (s != KV_OK) return s;
+  if (layer < 0 || layer >= p->L) return KV_ERR_INVALID_ARG;
+  if (hd.n_seq == 0 || hd.W == 0) return KV_OK;
+  if (!d_plan || !d_q || !d_block_table || !d_workspace || max_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
   if (!aligned16(d_q) || !aligned16(d_workspace) || !aligned16(d_plan)) return KV_ERR_INVALID_ARG;
   if (workspace_bytes < plan_workspace_bytes(hd.n_segs, hd.c_max, p->D)) return KV_ERR_INVALID_ARG;
-  kvStatus s = ensure_device(p);
+  s = ensure_device(p);
   if (s != KV_OK) return s;
+  const int G = n_q_heads / p->H;
   if (!p->mma_ok || p->force_cuda_cores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
   const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
-  const size_t n_slots = static_cast<size_t>(kMaxDecodeCtas) + hd.n_segs;
-  const size_t ml_bytes = (n_slots * hd.c_max * 2 * sizeof(float) + 255) & ~size_t(255);
   unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
   pkv::DecodeArgs a;
   a.q = d_q;
@@ -489,7 +501,7 @@ kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, i
   a.ctx = nullptr;
   a.ws_pre = nullptr;
   a.ws_ml = reinterpret_cast<float*>(ws);
-  a.ws_o = reinterpret_cast<float*>(ws + ml_bytes);
+  a.ws_o = reinterpret_cast<float*>(ws + plan_ml_bytes(hd));
   a.status = p->d_status;
   a.n_seq = hd.n_seq;
   a.max_blocks = max_blocks;
@@ -506,32 +518,64 @@ kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, i
   a.n_segs = hd.n_segs;
   a.c_max = hd.c_max;
   a.plan_W = hd.W;
-  if (hd.W > 0) {
-    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
-    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
-    bool supported = false;
-    const cudaError_t e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
-                                               &p->grid_by_g[ilog2_small(G)], as_stream(stream),
-                                               &supported);
-    if (!supported) return KV_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return KV_ERR_CUDA;
-  }
-  const int grid = p->grid_by_g[ilog2_small(G)] > 0 ? p->grid_by_g[ilog2_small(G)] : 1;
+  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+  bool supported = false;
+  const cudaError_t e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                             &p->grid_by_g[ilog2_small(G)], as_stream(stream),
+                                             &supported);
+  if (!supported) return KV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kvStatus paged_decode_merge_planned(kvPool* p, int n_q_heads, const void* d_plan,
+                                    const void* h_plan, void* d_out, int out_dtype,
+                                    const void* d_workspace, size_t workspace_bytes,
+                                    void* stream) {
+  PlanHeader hd;
+  kvStatus s = read_plan_header(p, n_q_heads, h_plan, &hd);
+  if (s != KV_OK) return s;
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  if (hd.n_seq == 0) return KV_OK;
+  if (!d_plan || !d_out || !d_workspace) return KV_ERR_INVALID_ARG;
+  if (workspace_bytes < plan_workspace_bytes(hd.n_segs, hd.c_max, p->D)) return KV_ERR_INVALID_ARG;
+  const int G = n_q_heads / p->H;
+  if (ilog2_small(G) < 0 || (p->D != 64 && p->D != 128)) return KV_ERR_UNSUPPORTED;
+  const int grid = p->grid_by_g[ilog2_small(G)];
+  if (hd.W > 0 && grid <= 0) return KV_ERR_INVALID_ARG;  // no split pass has run on this pool
+  const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
+  const unsigned char* ws = reinterpret_cast<const unsigned char*>(d_workspace);
+  const float* ml = reinterpret_cast<const float*>(ws);
+  const float* o = reinterpret_cast<const float*>(ws + plan_ml_bytes(hd));
   const PlanSeg* segs = reinterpret_cast<const PlanSeg*>(dp + hd.seg_off);
   const int32_t* eoff = reinterpret_cast<const int32_t*>(dp + hd.eoff_off);
   const PlanEntry* ents = reinterpret_cast<const PlanEntry*>(dp + hd.ent_off);
   float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
   __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
   const dim3 mg(hd.n_seq, (n_q_heads + 3) / 4);
+  const int gr = grid > 0 ? grid : 1;
   if (p->D == 128)
-    merge_plan_kernel<128><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, grid,
-                                                              hd.c_max, a.ws_ml, a.ws_o, p->H,
-                                                              n_q_heads, of, ob);
+    merge_plan_kernel<128><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, gr,
+                                                              hd.c_max, ml, o, p->H, n_q_heads,
+                                                              of, ob);
   else
-    merge_plan_kernel<64><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, grid,
-                                                             hd.c_max, a.ws_ml, a.ws_o, p->H,
-                                                             n_q_heads, of, ob);
+    merge_plan_kernel<64><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, gr, hd.c_max,
+                                                             ml, o, p->H, n_q_heads, of, ob);
   return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const void* d_plan, const void* h_plan, float scale,
+                                        void* d_out, int out_dtype, void* d_workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  kvStatus s = paged_decode_partials_planned(p, layer, d_q, n_q_heads, d_block_table, max_blocks,
+                                             d_plan, h_plan, scale, d_workspace, workspace_bytes,
+                                             stream);
+  if (s != KV_OK) return s;
+  return paged_decode_merge_planned(p, n_q_heads, d_plan, h_plan, d_out, out_dtype, d_workspace,
+                                    workspace_bytes, stream);
 }
 
 // ------------------------------------------------------ whole decode step
