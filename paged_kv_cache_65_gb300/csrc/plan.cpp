@@ -123,17 +123,44 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     a = b;
   }
 
-  // ---- segments, members, entries
+  // ---- segments, members, entries.  Order: per group and K/V head, the
+  // shared segment followed by the members' private rests, then the
+  // ungrouped sequences; tiny private rests are thus spread over the work
+  // list instead of piling up at its end (the split balances blocks, and
+  // every piece has a fixed cost).
   std::vector<PlanSeg> segs;
   std::vector<int32_t> members;
   std::vector<std::vector<PlanEntry>> ents(static_cast<size_t>(n_seq) * H);
   int c_max = G;
-  std::vector<int> chunk_of(n_seq, -1);
+  std::vector<int> priv_mem(n_seq, -1);  // member-list slot of a sequence's private rest
+  auto private_member = [&](int i) {
+    if (priv_mem[i] < 0) {
+      priv_mem[i] = static_cast<int>(members.size());
+      members.push_back(i);
+    }
+    return priv_mem[i];
+  };
+  auto push_private = [&](int i, int h) {
+    const int nb = static_cast<int>((seqs[i]->len + B - 1) / B);
+    if (nb <= shared[i]) return;
+    PlanSeg s{};
+    s.rep = i;
+    s.b0 = shared[i];
+    s.b1 = nb;
+    s.tok_end = static_cast<int32_t>(seqs[i]->len);
+    s.head = h;
+    s.ncols = G;
+    s.mem = private_member(i);
+    const int si = static_cast<int>(segs.size());
+    segs.push_back(s);
+    ents[static_cast<size_t>(i) * H + h].push_back({si, 0});
+  };
+  std::vector<char> grouped(n_seq, 0);
   for (size_t c = 0; c < chunks.size(); ++c) {
     const int mem0 = static_cast<int>(members.size());
     for (int m : chunks[c]) {
       members.push_back(m);
-      chunk_of[m] = static_cast<int>(c);
+      grouped[m] = 1;
     }
     const int ncols = static_cast<int>(chunks[c].size()) * G;
     c_max = std::max(c_max, ncols);
@@ -149,27 +176,12 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
       const int si = static_cast<int>(segs.size());
       segs.push_back(s);
       for (int m : chunks[c]) ents[static_cast<size_t>(m) * H + h].push_back({si, pos_in[m] * G});
+      for (int m : chunks[c]) push_private(m, h);
     }
   }
-  for (int i = 0; i < n_seq; ++i) {
-    const int nb = static_cast<int>((seqs[i]->len + B - 1) / B);
-    if (nb <= shared[i]) continue;
-    const int mem0 = static_cast<int>(members.size());
-    members.push_back(i);
-    for (int h = 0; h < H; ++h) {
-      PlanSeg s{};
-      s.rep = i;
-      s.b0 = shared[i];
-      s.b1 = nb;
-      s.tok_end = static_cast<int32_t>(seqs[i]->len);
-      s.head = h;
-      s.ncols = G;
-      s.mem = mem0;
-      const int si = static_cast<int>(segs.size());
-      segs.push_back(s);
-      ents[static_cast<size_t>(i) * H + h].push_back({si, 0});
-    }
-  }
+  for (int i = 0; i < n_seq; ++i)
+    if (!grouped[i])
+      for (int h = 0; h < H; ++h) push_private(i, h);
   int64_t W = 0;
   for (PlanSeg& s : segs) {
     s.wpre = W;
