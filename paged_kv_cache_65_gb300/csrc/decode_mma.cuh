@@ -419,20 +419,35 @@ __global__ void __launch_bounds__(kThreads, 2)
         // partial tile the rows past the context hold whatever the pool held
         // there (possibly NaN bit patterns): their V^T elements are zeroed,
         // since 0 * NaN would reach the sum even with P = 0.
-        const int nv = nvalid - tt * 16;
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (nv < 16) {
-          mlo = (2 * t < nv ? 0x0000ffffu : 0u) | (2 * t + 1 < nv ? 0xffff0000u : 0u);
-          mhi = (2 * t + 8 < nv ? 0x0000ffffu : 0u) | (2 * t + 9 < nv ? 0xffff0000u : 0u);
-        }
-        {
-          const int r = tt * 16 + (lane & 7) + (lane >> 4) * 8;
+        // The rescale is skipped when no running max of the warp moved (alpha
+        // is then exactly 1), which is the common case once the max settles.
+        if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
           for (int mt = 0; mt < C::KS; ++mt) {
             o[mt][0] *= al0;
             o[mt][1] *= al1;
             o[mt][2] *= al0;
             o[mt][3] *= al1;
+          }
+        }
+        const int nv = nvalid - tt * 16;
+        const int r = tt * 16 + (lane & 7) + (lane >> 4) * 8;
+        if (nv >= 16) {
+#pragma unroll
+          for (int mt = 0; mt < C::KS; ++mt) {
+            const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(swz(vb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
+            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+          }
+        } else {
+          const uint32_t mlo =
+              (2 * t < nv ? 0x0000ffffu : 0u) | (2 * t + 1 < nv ? 0xffff0000u : 0u);
+          const uint32_t mhi =
+              (2 * t + 8 < nv ? 0x0000ffffu : 0u) | (2 * t + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < C::KS; ++mt) {
             const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
             uint32_t a0, a1, a2, a3;
             ldsm_x4_t(swz(vb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
