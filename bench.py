@@ -225,10 +225,11 @@ def bench_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl, cache, run = setup(args.workload, args.block_size, dev)
-    if args.cuda_cores:
-        from paged_kv_cache_65_gb300 import _lib
+    from paged_kv_cache_65_gb300 import _lib
 
+    if args.cuda_cores:
         cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, 1)
+    cache.kv_pool_set_option(_lib.KV_OPT_PDL, 0 if args.no_pdl else 1)
     esize = wl.elem_bytes
     seqs = wl.decode_seqs
     n = len(seqs)
@@ -321,16 +322,21 @@ def bench_ours(args):
                        for _ in range(L)] for _ in range(n_plans)]
     except TypeError:
         ext_events = None
-    graphs, split_graphs = [], []
+    graphs, instr_graphs, split_graphs = [], [], []
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
         for pi in range(n_plans):
             g_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_, stream=cap):
-                per_step_launches = enqueue(dplans[pi], ext_events[pi] if ext_events else None)
+                per_step_launches = enqueue(dplans[pi])
             graphs.append(g_)
-            if ext_events is None:
+            gi = torch.cuda.CUDAGraph()
+            if ext_events is not None:
+                with torch.cuda.graph(gi, stream=cap):
+                    enqueue(dplans[pi], ext_events[pi])
+                instr_graphs.append(gi)
+            else:
                 gs = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gs, stream=cap):
                     for layer in range(L):
@@ -369,28 +375,35 @@ def bench_ours(args):
         graphs[pi].replay()
         ev[i][1].record(stream)
         launches += per_step_launches
-        if ext_events is not None:
-            ev[i][1].synchronize()
-            split_ms.extend(ext_events[pi][l][0].elapsed_time(ext_events[pi][l][1])
-                            for l in range(L))
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     t_wall = t_wall1 - t_wall0
     clk = clocks.stop(t_wall0, t_wall1)
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, n_steps)]
-    split_src = "event-record nodes around each split launch inside the step graphs"
-    if ext_events is None:
-        # separate timed loop over graphs that hold only the split launches
+    # the split pass alone: the same steps replayed from graphs that hold
+    # event-record nodes around each split launch (a second timed loop, so
+    # that the step timing above keeps the kernels' programmatic edges)
+    n_split = min(args.steps, 200)
+    if ext_events is not None:
+        split_src = "event-record nodes around each split launch in the step graphs"
+        for j in range(n_split):
+            pi = j % n_plans
+            flush_l2(j)
+            instr_graphs[pi].replay()
+            torch.cuda.synchronize()
+            split_ms.extend(ext_events[pi][l][0].elapsed_time(ext_events[pi][l][1])
+                            for l in range(L))
+    else:
+        split_src = "events around graphs holding only the split launches"
         e0s = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for j in range(args.steps):
+               for _ in range(n_split)]
+        for j in range(n_split):
             flush_l2(j)
             e0s[j][0].record(stream)
             split_graphs[j % n_plans].replay()
             e0s[j][1].record(stream)
         torch.cuda.synchronize()
         split_ms = [a.elapsed_time(b) / L for a, b in e0s]
-        split_src = "events around graphs holding only the split launches"
     dev_s = sum(step_ms) / 1e3
     ub = sum(dplans[i % n_plans]["ub"] for i in range(args.warmup, n_steps))
     lb = sum(dplans[i % n_plans]["lb"] for i in range(args.warmup, n_steps))
@@ -401,7 +414,7 @@ def bench_ours(args):
 
     # roofline of the split pass: algorithmic bytes per launch (2 * H_kv * D_h
     # * b bytes per distinct context token row of the layer) / mean duration
-    per_launch_alg = [dplans[i % n_plans]["ub"] / L for i in range(args.warmup, n_steps)]
+    per_launch_alg = [dplans[j % n_plans]["ub"] / L for j in range(n_split)]
     alg = float(np.mean(per_launch_alg))
     split_s = float(np.mean(split_ms)) / 1e3
     peak, peak_kind = read_peaks()
@@ -425,6 +438,7 @@ def bench_ours(args):
             "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
                        "decode_path": ("cuda_cores" if args.cuda_cores else
                                        "planned" if use_plan else "plain"),
+                       "pdl": not args.no_pdl,
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
                        "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
@@ -597,6 +611,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="decode on CUDA cores even where the tensor-core pass applies")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependencies between kernels")
     ap.add_argument("--plain", action="store_true",
                     help="no sharing-aware plan: one segment per (sequence, K/V head)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -103,8 +103,11 @@ kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
 
 /* Pool options.  KV_OPT_DECODE_PATH: 0 = automatic (tensor-core split pass
  * for bfloat16 pools whose block size is a multiple of 8, CUDA-core pass
- * otherwise), 1 = always the CUDA-core pass. */
-enum { KV_OPT_DECODE_PATH = 1 };
+ * otherwise), 1 = always the CUDA-core pass.  KV_OPT_PDL: 1 (default) =
+ * launch kernels with a programmatic dependency on the previous grid in the
+ * stream (each kernel waits for its predecessors before reading their
+ * results, but is scheduled while they finish), 0 = plain launches. */
+enum { KV_OPT_DECODE_PATH = 1, KV_OPT_PDL = 2 };
 kvStatus kv_pool_set_option(kvPool* pool, int option, int value);
 
 /* Synchronise `stream`, copy the device status word to *out_bits and clear

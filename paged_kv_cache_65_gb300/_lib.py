@@ -29,6 +29,7 @@ KV_ERR_DEVICE_CHECK = 5
 KV_ERR_UNSUPPORTED = 6
 KV_ERR_SCRATCH_TOO_SMALL = 7
 KV_OPT_DECODE_PATH = 1
+KV_OPT_PDL = 2
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
 

@@ -193,6 +193,10 @@ kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
     for (int& g : p->grid_by_g) g = 0;  // grid sizes depend on the kernel
     return KV_OK;
   }
+  if (option == KV_OPT_PDL && (value == 0 || value == 1)) {
+    p->pdl = value == 1;
+    return KV_OK;
+  }
   return KV_ERR_INVALID_ARG;
 }
 

@@ -337,6 +337,10 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 2))
     }
     fence_barrier_init();
   }
+  // everything above touches only shared memory; global inputs (pool, q,
+  // tables) may come from the previous grid in the stream
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 0) {
     WalkStart w = find_start(a.ctx, a.n_seq, B, a.n_kv_heads, a.max_blocks, a.grid, blockIdx.x,
                              a.status);

@@ -5,17 +5,17 @@ namespace pkv {
 
 cudaError_t launch_split_e4(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
-                            cudaStream_t st, bool* supported) {
+                            cudaStream_t st, bool pdl, bool* supported) {
   *supported = true;
   switch (D * 16 + G) {
-    case 64 * 16 + 1: return launch_split<4, 64, 1>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 64 * 16 + 2: return launch_split<4, 64, 2>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 64 * 16 + 4: return launch_split<4, 64, 4>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 64 * 16 + 8: return launch_split<4, 64, 8>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 128 * 16 + 1: return launch_split<4, 128, 1>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 128 * 16 + 2: return launch_split<4, 128, 2>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 128 * 16 + 4: return launch_split<4, 128, 4>(tk, tv, a, sm_count, max_grid, grid_io, st);
-    case 128 * 16 + 8: return launch_split<4, 128, 8>(tk, tv, a, sm_count, max_grid, grid_io, st);
+    case 64 * 16 + 1: return launch_split<4, 64, 1>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 64 * 16 + 2: return launch_split<4, 64, 2>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 64 * 16 + 4: return launch_split<4, 64, 4>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 64 * 16 + 8: return launch_split<4, 64, 8>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 128 * 16 + 1: return launch_split<4, 128, 1>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 128 * 16 + 2: return launch_split<4, 128, 2>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 128 * 16 + 4: return launch_split<4, 128, 4>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
+    case 128 * 16 + 8: return launch_split<4, 128, 8>(tk, tv, a, sm_count, max_grid, grid_io, st, pdl);
     default: break;
   }
   *supported = false;

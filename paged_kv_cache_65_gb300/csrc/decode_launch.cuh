@@ -3,6 +3,7 @@
 
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "launch.cuh"
 
 namespace pkv {
 
@@ -12,7 +13,7 @@ namespace pkv {
 // max_grid; later calls reuse *grid_io.
 template <int ESIZE, int D, int G>
 cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
-                         int max_grid, int* grid_io, cudaStream_t st) {
+                         int max_grid, int* grid_io, cudaStream_t st, bool pdl) {
   constexpr int smem = decode_smem_bytes<ESIZE, D, G>();
   auto kern = decode_split_kernel<ESIZE, D, G>;
   if (*grid_io <= 0) {
@@ -26,13 +27,12 @@ cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArg
     *grid_io = g > max_grid ? max_grid : g;
   }
   a.grid = *grid_io;
-  kern<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
-  return cudaGetLastError();
+  return launch_kernel(pdl, kern, dim3(a.grid), dim3(kThreads), smem, st, tk, tv, a);
 }
 
 template <int D, int G>
 cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
-                       int max_grid, int* grid_io, cudaStream_t st) {
+                       int max_grid, int* grid_io, cudaStream_t st, bool pdl) {
   constexpr int smem = decode_mma_smem_bytes<D, G>();
   auto k_plain = decode_mma_kernel<D, G, false>;
   auto k_plan = decode_mma_kernel<D, G, true>;
@@ -58,25 +58,22 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs 
     *grid_io = g > max_grid ? max_grid : g;
   }
   a.grid = *grid_io;
-  if (v)
-    k_plan<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
-  else
-    k_plain<<<a.grid, kThreads, smem, st>>>(tk, tv, a);
-  return cudaGetLastError();
+  return launch_kernel(pdl, v ? k_plan : k_plain, dim3(a.grid), dim3(kThreads), smem, st, tk, tv,
+                       a);
 }
 
 // Tensor-core variant for bfloat16 (swizzled TMA maps, B a multiple of 8).
 cudaError_t launch_mma_bf16(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
-                            cudaStream_t st, bool* supported);
+                            cudaStream_t st, bool pdl, bool* supported);
 
 // Dispatch over (D, G) for one element size; *supported = false when the
 // shape has no compiled instantiation.
 cudaError_t launch_split_e2(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
-                            cudaStream_t st, bool* supported);
+                            cudaStream_t st, bool pdl, bool* supported);
 cudaError_t launch_split_e4(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
-                            cudaStream_t st, bool* supported);
+                            cudaStream_t st, bool pdl, bool* supported);
 
 }  // namespace pkv

@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     fence_barrier_init();
   }
+  // everything above touches only shared memory; global inputs (pool, q,
+  // tables) may come from the previous grid in the stream
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 0) {
     if constexpr (PLAN) {
       const long long W = a.plan_W;

@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "decode_launch.cuh"
+#include "launch.cuh"
 #include "plan.h"
 #include "pool.h"
 #include "ptx.cuh"
@@ -99,6 +100,8 @@ __global__ void slot_write_kernel(const uint4* __restrict__ k_new, const uint4* 
                                   const int64_t* __restrict__ slots, int n_tok, uint4* kc,
                                   uint4* vc, int layer, long long slots_per_layer, int row_vecs,
                                   int32_t* status) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
   const int i = blockIdx.x;
   const int ly = layer >= 0 ? layer : blockIdx.y;
   const int64_t slot = slots[i];
@@ -119,6 +122,8 @@ __global__ void slot_write_kernel(const uint4* __restrict__ k_new, const uint4* 
 // into block dst in K and V.
 __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, uint4* vc,
                                 int n_blocks, long long block_vecs, int32_t* status) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
   const int i = blockIdx.x;
   const int ly = blockIdx.y;
   const int src = pairs[2 * i], dst = pairs[2 * i + 1];
@@ -148,6 +153,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
                                                     const float* __restrict__ ws_o, int n_seq,
                                                     int H, int Hq, int grid, float* out_f32,
                                                     __nv_bfloat16* out_bf16) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
   constexpr int DL = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,6 +222,8 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
     const PlanEntry* __restrict__ ents, long long W, int grid, int c_max,
     const float* __restrict__ ws_ml, const float* __restrict__ ws_o, int H, int Hq,
     float* out_f32, __nv_bfloat16* out_bf16) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
   constexpr int DL = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -330,10 +339,11 @@ kvStatus cow_copy(kvPool* p, const int32_t* d_pairs, int n_pairs, void* stream) 
   const long long block_vecs = static_cast<long long>(p->B) * p->H * p->D * p->esize / 16;
   const int parts = block_vecs >= 4096 ? 4 : 1;
   dim3 grid(n_pairs, p->L, parts);
-  cow_copy_kernel<<<grid, 256, 0, as_stream(stream)>>>(
-      d_pairs, reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v), p->N, block_vecs,
+  const cudaError_t e = pkv::launch_kernel(
+      p->pdl, cow_copy_kernel, grid, dim3(256), 0, as_stream(stream), d_pairs,
+      reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v), p->N, block_vecs,
       p->d_status);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 kvStatus reshape_and_cache(kvPool* p, int layer, const void* d_k_new, const void* d_v_new,
@@ -347,11 +357,12 @@ kvStatus reshape_and_cache(kvPool* p, int layer, const void* d_k_new, const void
   const int row_vecs = p->H * p->D * p->esize / 16;
   dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
   const int threads = row_vecs >= 128 ? 128 : (row_vecs >= 64 ? 64 : 32);
-  slot_write_kernel<<<grid, threads, 0, as_stream(stream)>>>(
+  const cudaError_t e = pkv::launch_kernel(
+      p->pdl, slot_write_kernel, grid, dim3(threads), 0, as_stream(stream),
       reinterpret_cast<const uint4*>(d_k_new), reinterpret_cast<const uint4*>(d_v_new),
       d_slot_mapping, n_tokens, reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v),
       layer, static_cast<long long>(p->N) * p->B, row_vecs, p->d_status);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 size_t paged_decode_workspace_bytes(const kvPool* p, int n_seq, int n_q_heads) {
@@ -401,14 +412,14 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
     e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
-                             as_stream(stream), &supported);
+                             as_stream(stream), p->pdl, &supported);
   } else {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[0]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[1]);
     e = p->esize == 2 ? pkv::launch_split_e2(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
-                                             grid_io, as_stream(stream), &supported)
+                                             grid_io, as_stream(stream), p->pdl, &supported)
                       : pkv::launch_split_e4(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
-                                             grid_io, as_stream(stream), &supported);
+                                             grid_io, as_stream(stream), p->pdl, &supported);
   }
   if (!supported) return KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
@@ -433,13 +444,15 @@ kvStatus paged_decode_merge(kvPool* p, int n_q_heads, const int32_t* d_context_l
   const float* o = reinterpret_cast<const float*>(ws + w.o);
   float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
   __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
-  if (p->D == 128)
-    merge_kernel<128><<<dim3(n_seq, (n_q_heads + 3) / 4), 128, 0, as_stream(stream)>>>(
-        pre, ml, o, n_seq, p->H, n_q_heads, grid, of, ob);
-  else
-    merge_kernel<64><<<dim3(n_seq, (n_q_heads + 3) / 4), 128, 0, as_stream(stream)>>>(
-        pre, ml, o, n_seq, p->H, n_q_heads, grid, of, ob);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  const dim3 mg(n_seq, (n_q_heads + 3) / 4);
+  const cudaError_t e =
+      p->D == 128 ? pkv::launch_kernel(p->pdl, merge_kernel<128>, mg, dim3(128), 0,
+                                       as_stream(stream), pre, ml, o, n_seq, p->H, n_q_heads,
+                                       grid, of, ob)
+                  : pkv::launch_kernel(p->pdl, merge_kernel<64>, mg, dim3(128), 0,
+                                       as_stream(stream), pre, ml, o, n_seq, p->H, n_q_heads,
+                                       grid, of, ob);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 kvStatus paged_decode_attention(kvPool* p, int layer, const void* d_q, int n_q_heads,
@@ -523,7 +536,7 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   bool supported = false;
   const cudaError_t e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
                                              &p->grid_by_g[ilog2_small(G)], as_stream(stream),
-                                             &supported);
+                                             p->pdl, &supported);
   if (!supported) return KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
@@ -554,14 +567,14 @@ kvStatus paged_decode_merge_planned(kvPool* p, int n_q_heads, const void* d_plan
   __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
   const dim3 mg(hd.n_seq, (n_q_heads + 3) / 4);
   const int gr = grid > 0 ? grid : 1;
-  if (p->D == 128)
-    merge_plan_kernel<128><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, gr,
-                                                              hd.c_max, ml, o, p->H, n_q_heads,
-                                                              of, ob);
-  else
-    merge_plan_kernel<64><<<mg, 128, 0, as_stream(stream)>>>(segs, eoff, ents, hd.W, gr, hd.c_max,
-                                                             ml, o, p->H, n_q_heads, of, ob);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  const cudaError_t e =
+      p->D == 128 ? pkv::launch_kernel(p->pdl, merge_plan_kernel<128>, mg, dim3(128), 0,
+                                       as_stream(stream), segs, eoff, ents, hd.W, gr, hd.c_max, ml,
+                                       o, p->H, n_q_heads, of, ob)
+                  : pkv::launch_kernel(p->pdl, merge_plan_kernel<64>, mg, dim3(128), 0,
+                                       as_stream(stream), segs, eoff, ents, hd.W, gr, hd.c_max, ml,
+                                       o, p->H, n_q_heads, of, ob);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,

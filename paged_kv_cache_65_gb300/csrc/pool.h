@@ -36,6 +36,7 @@ struct kvPool {
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
   bool force_cuda_cores = false;            // decode on CUDA cores even when mma_ok
+  bool pdl = true;                          // programmatic dependent launch
 
   // host staging reused by kv_decode_step_host
   std::vector<int64_t> h_slots;

@@ -92,6 +92,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Programmatic dependent launch.  wait: block until the grids this one
+// depends on have completed and their memory is visible (a no-op when the
+// grid was launched without a programmatic dependency).  launch_dependents:
+// allow the next grid in the stream to be scheduled now; it still waits in its
+// own griddep_wait before touching this grid's results.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -471,3 +471,19 @@ def test_multilayer_host_step_with_long_shared_prefix():
         for layer in range(L):
             assert max_err(out[layer], orc.attend(layer, q)) <= TOL["bf16"]
     check_status(cache)
+
+
+@pytest.mark.parametrize("planned", [False, True])
+def test_programmatic_launch_gives_identical_results(planned):
+    # the same step with and without programmatic dependent launches
+    from paged_kv_cache_65_gb300 import _lib
+
+    outs = []
+    for pdl in (1, 0):
+        wl = ragged_workload("bf16", 128, 4, 16, [33, 1000, 2049, 5, 700], seed=31)
+        cache, run = make(wl)
+        cache.kv_pool_set_option(_lib.KV_OPT_PDL, pdl)
+        q, k, v = wl.step_values(0)
+        _, _, og = run.step(wl.decode_seqs, q, k, v, planned=planned)
+        outs.append(og.cpu())
+    assert torch.equal(outs[0], outs[1])
