@@ -264,7 +264,7 @@ def _out_dtype(out) -> int:
 
 PLAN_SEG = np.dtype([("wpre", "<i8"), ("rep", "<i4"), ("b0", "<i4"), ("b1", "<i4"),
                      ("tok_end", "<i4"), ("head", "<i4"), ("ncols", "<i4"), ("mem", "<i4"),
-                     ("pad", "<i4")])
+                     ("w", "<i4")])
 PLAN_ENTRY = np.dtype([("seg", "<i4"), ("col_base", "<i4")])
 
 

@@ -117,19 +117,23 @@ struct PlanWalker {
   int n_segs, B, s;
   long long r, r1;
 
+  // A piece for every segment whose units meet [r, r1); its blocks are those
+  // whose first unit lies in the range, possibly none.
   __device__ bool next(Piece& p) {
     while (r < r1 && s < n_segs) {
       const PlanSeg sg = segs[s];
       const long long len = sg.b1 - sg.b0;
-      if (len <= 0 || r >= sg.wpre + len) {
+      const long long w = sg.w > 0 ? sg.w : 1;
+      if (len <= 0 || r >= sg.wpre + len * w) {
         ++s;
         continue;
       }
-      const long long end = r1 < sg.wpre + len ? r1 : sg.wpre + len;
+      const long long end = r1 < sg.wpre + len * w ? r1 : sg.wpre + len * w;
+      const long long jb = (r - sg.wpre + w - 1) / w, je = (end - sg.wpre + w - 1) / w;
       p.rep = sg.rep;
       p.head = sg.head;
-      p.b0 = sg.b0 + (int)(r - sg.wpre);
-      p.b1 = sg.b0 + (int)(end - sg.wpre);
+      p.b0 = sg.b0 + (int)jb;
+      p.b1 = sg.b0 + (int)je;
       p.tok_end = p.b1 * B < sg.tok_end ? p.b1 * B : sg.tok_end;
       p.ncols = sg.ncols;
       p.mem = sg.mem;

@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
   for (int e = e0; e < e1; ++e) {
     const PlanEntry en = ents[e];
     const PlanSeg sg = segs[en.seg];
-    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + (sg.b1 - sg.b0) - 1) / chunk;
+    const long long units = static_cast<long long>(sg.b1 - sg.b0) * (sg.w > 0 ? sg.w : 1);
+    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + units - 1) / chunk;
     for (long long i = c0 + lane; i <= c1; i += 32)
       M = fmaxf(M, ws_ml[((i + en.seg) * c_max + en.col_base + g) * 2]);
   }
@@ -251,10 +252,13 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
   for (int e = e0; e < e1; ++e) {
     const PlanEntry en = ents[e];
     const PlanSeg sg = segs[en.seg];
-    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + (sg.b1 - sg.b0) - 1) / chunk;
+    const long long units = static_cast<long long>(sg.b1 - sg.b0) * (sg.w > 0 ? sg.w : 1);
+    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + units - 1) / chunk;
     for (long long i = c0; i <= c1; ++i) {
       const long long slot = (i + en.seg) * c_max + en.col_base + g;
-      const float f = pkv::exp2_approx(ws_ml[slot * 2] - M);
+      const float mi = ws_ml[slot * 2];
+      if (mi == -INFINITY) continue;  // a CTA whose range held no block start of the segment
+      const float f = pkv::exp2_approx(mi - M);
       L += f * ws_ml[slot * 2 + 1];
       const float* src = ws_o + slot * D + lane * DL;
       if constexpr (DL == 4) {

@@ -184,8 +184,9 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
       for (int h = 0; h < H; ++h) push_private(i, h);
   int64_t W = 0;
   for (PlanSeg& s : segs) {
+    s.w = plan_block_weight(s.ncols);
     s.wpre = W;
-    W += s.b1 - s.b0;
+    W += static_cast<int64_t>(s.b1 - s.b0) * s.w;
   }
   int n_entries = 0;
   for (const auto& e : ents) n_entries += static_cast<int>(e.size());

@@ -8,12 +8,18 @@
 // columns) and one private segment per head for the rest; the merge entries
 // list, per (sequence, K/V head), the segments and column offsets whose
 // partials make up that sequence's softmax.
+//
+// Work units: block j of a segment occupies units [wpre + j*w, wpre + (j+1)*w);
+// the split pass gives CTA c the units [c*chunk, (c+1)*chunk) and with them
+// the blocks whose first unit falls in that range (possibly none: the CTA then
+// writes an empty partial, m = -inf, l = 0).  The CTAs holding pieces of a
+// segment are wpre / chunk .. (wpre + len*w - 1) / chunk.
 #pragma once
 
 #include <cstdint>
 
 struct PlanHeader {
-  int64_t W;          // total blocks over all segments
+  int64_t W;          // total work units over all segments
   int32_t n_segs;
   int32_t n_members;
   int32_t n_entries;
@@ -32,14 +38,14 @@ struct PlanHeader {
 static_assert(sizeof(PlanHeader) == 80, "plan header layout");
 
 struct PlanSeg {
-  int64_t wpre;     // blocks of all segments before this one
+  int64_t wpre;     // work units of all segments before this one
   int32_t rep;      // table row (listed sequence index) the blocks come from
   int32_t b0, b1;   // blocks [b0, b1) of that row
   int32_t tok_end;  // tokens at or past this position are not read
   int32_t head;     // K/V head
   int32_t ncols;    // query columns: members * G
   int32_t mem;      // index of the first member in the member list
-  int32_t pad;
+  int32_t w;        // work units per block (cost weight of the segment's width)
 };
 static_assert(sizeof(PlanSeg) == 40, "plan segment layout");
 
@@ -50,3 +56,8 @@ struct PlanEntry {
 
 // Most query columns one segment carries (four 8-column MMA n-tiles).
 constexpr int kPlanMaxCols = 32;
+
+// Work units per block by 8-column n-tiles (1, 2, 3-4): the split pass
+// balances units, so blocks of wide shared segments, which cost more tensor
+// work per byte, are spread over more CTAs.
+constexpr int plan_block_weight(int ncols) { return ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5); }

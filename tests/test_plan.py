@@ -36,8 +36,10 @@ def check_plan(bm, plan, seqs, G, min_tokens):
     B, H = plan["B"], plan["H"]
     segs, mem, eoff, ents = plan["segs"], plan["members"], plan["eoff"], plan["ents"]
     assert plan["G"] == G and plan["n_seq"] == len(seqs)
-    assert plan["W"] == int(sum(int(s["b1"]) - int(s["b0"]) for s in segs))
-    assert list(segs["wpre"]) == list(np.cumsum([0] + [int(s["b1"] - s["b0"]) for s in segs])[:-1])
+    units = [int(s["b1"] - s["b0"]) * int(s["w"]) for s in segs]
+    assert plan["W"] == sum(units)
+    assert list(segs["wpre"]) == list(np.cumsum([0] + units)[:-1])
+    assert all(s["w"] == (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5) for s in segs)
     for si, s in enumerate(segs):
         assert s["ncols"] % G == 0 and 0 < s["ncols"] <= 32
         members = mem[s["mem"]:s["mem"] + s["ncols"] // G]
