@@ -49,10 +49,10 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # workload, valid only for the kernel source it was taken on.
 TRAFFIC = {
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
-    # (profiles/decode_mma_qwen_2k.md, decode_mma_shared_8k.md, decode_mma_gqa70b_32k.md)
-    "qwen_2k": {"bytes": 331786000 + 3565000, "sha": "5d3f0bdbd949986c"},
-    "shared_8k": {"bytes": 177484000 + 3827000, "sha": "5d3f0bdbd949986c"},
-    "gqa70b_32k": {"bytes": 4869517000 + 4925000, "sha": "5d3f0bdbd949986c"},
+    # (profiles/decode_mma_*.md), valid while the kernel sources hash to "sha"
+    "qwen_2k": {"bytes": 331662848 + 4114432, "sha": "e305e41748889990"},
+    "shared_8k": {"bytes": 176239360 + 3795200, "sha": "e305e41748889990"},
+    "gqa70b_32k": {"bytes": 1616467000 + 6040064, "sha": "e305e41748889990"},
 }
 
 
@@ -548,8 +548,9 @@ def cpu_leg(workload: str, seconds: float):
     wl, orc, q = oracle_sample(workload)
     nbytes, dt, done = oracle_attend(wl, orc, q, seconds)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{workload}: layer-0 decode attention of {done} of {len(wl.decode_seqs)} "
-                      f"sequences (paged gather + fp64 softmax, one thread), {dt:.1f} s",
+            "sample": f"{workload}: {done} single-sequence layer-0 decode attentions, cycling "
+                      f"over the batch's {len(wl.decode_seqs)} sequences (paged gather + fp64 "
+                      f"softmax, one thread), {dt:.1f} s",
             "seconds": round(dt, 3), "sequences": done, "bytes": int(nbytes)}
 
 
