@@ -56,6 +56,9 @@ TRAFFIC = {
 }
 
 
+# KV_OPT_DECODE_PATH values
+KERNELS = {"auto": 0, "cuda": 1, "mma": 2, "tc": 3}
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for f in ("decode.cuh", "decode_mma.cuh", "ptx.cuh", "device.cu"):
@@ -228,7 +231,8 @@ def bench_ours(args):
     from paged_kv_cache_65_gb300 import _lib
 
     if args.cuda_cores:
-        cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, 1)
+        args.kernel = "cuda"
+    cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, KERNELS[args.kernel])
     cache.kv_pool_set_option(_lib.KV_OPT_PDL, 0 if args.no_pdl else 1)
     esize = wl.elem_bytes
     seqs = wl.decode_seqs
@@ -241,7 +245,7 @@ def bench_ours(args):
     # at most n_plans tokens however many steps are timed
     n_plans = min(n_steps, args.plans)
 
-    use_plan = not (args.plain or args.cuda_cores) and wl.dtype == "bf16" and \
+    use_plan = not (args.plain or args.kernel == "cuda") and wl.dtype == "bf16" and \
         wl.block_size % 8 == 0
     plans, host_plans = [], []
     max_blocks = 1
@@ -436,8 +440,8 @@ def bench_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
             "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
-                       "decode_path": ("cuda_cores" if args.cuda_cores else
-                                       "planned" if use_plan else "plain"),
+                       "decode_path": "planned" if use_plan else "plain",
+                       "kernel": args.kernel,
                        "pdl": not args.no_pdl,
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
@@ -610,6 +614,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNELS),
+                    help="split-pass kernel: automatic, CUDA cores, warp-level MMA, tcgen05")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="decode on CUDA cores even where the tensor-core pass applies")
     ap.add_argument("--no-pdl", action="store_true",

@@ -101,9 +101,13 @@ kvStatus kv_pool_check(const kvPool* pool);
 /* Reference count of one block (debugging aid). */
 kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
 
-/* Pool options.  KV_OPT_DECODE_PATH: 0 = automatic (tensor-core split pass
- * for bfloat16 pools whose block size is a multiple of 8, CUDA-core pass
- * otherwise), 1 = always the CUDA-core pass.  KV_OPT_PDL: 1 (default) =
+/* Pool options.  KV_OPT_DECODE_PATH selects the split-pass kernel:
+ * 0 = automatic (warp-level tensor-core pass for bfloat16 pools whose block
+ * size is a multiple of 8, CUDA-core pass otherwise), 1 = always the
+ * CUDA-core pass, 2 = the warp-level tensor-core pass (mma.sync) where the
+ * pool allows it, 3 = the tcgen05 pass (tensor-memory accumulators; bfloat16,
+ * D_h = 128) where the pool allows it, else as 2.  Changing it invalidates
+ * partials of earlier split passes.  KV_OPT_PDL: 1 (default) =
  * launch kernels with a programmatic dependency on the previous grid in the
  * stream (each kernel waits for its predecessors before reading their
  * results, but is scheduled while they finish), 0 = plain launches. */

@@ -188,8 +188,8 @@ kvStatus kv_pool_check(const kvPool* p) {
 
 kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
   if (!p) return KV_ERR_INVALID_ARG;
-  if (option == KV_OPT_DECODE_PATH && (value == 0 || value == 1)) {
-    p->force_cuda_cores = value == 1;
+  if (option == KV_OPT_DECODE_PATH && value >= 0 && value <= 3) {
+    p->decode_path = value;
     for (int& g : p->grid_by_g) g = 0;  // grid sizes depend on the kernel
     return KV_OK;
   }

@@ -62,6 +62,10 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs 
                        a);
 }
 
+// tcgen05 variant (bfloat16, D_h = 128, the swizzled TMA maps); one CTA per SM.
+cudaError_t launch_tc_bf16(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                           int sm_count, int max_grid, int* grid_io, cudaStream_t st, bool pdl);
+
 // Tensor-core variant for bfloat16 (swizzled TMA maps, B a multiple of 8).
 cudaError_t launch_mma_bf16(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,

@@ -57,6 +57,22 @@ kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizz
   return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
 }
 
+// Split-pass kernel for a pool (after ensure_device) and its decode-path
+// option: CUDA cores, warp-level MMA (mma.sync), or tcgen05 with TMEM
+// accumulators (bfloat16, D_h = 128).
+enum DecodeKernel { kKernelCudaCores, kKernelMma, kKernelTc };
+
+DecodeKernel decode_kernel(const kvPool* p) {
+  const bool mma = p->mma_ok;
+  const bool tc = p->mma_ok && p->D == 128;
+  switch (p->decode_path) {
+    case 1: return kKernelCudaCores;
+    case 2: return mma ? kKernelMma : kKernelCudaCores;
+    case 3: return tc ? kKernelTc : (mma ? kKernelMma : kKernelCudaCores);
+    default: return mma ? kKernelMma : kKernelCudaCores;
+  }
+}
+
 // First device use of a pool: device, SM count, TMA descriptors.
 kvStatus ensure_device(kvPool* p) {
   if (p->dev_ready) return KV_OK;
@@ -412,7 +428,14 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   int* grid_io = &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  if (p->mma_ok && !p->force_cuda_cores) {
+  const DecodeKernel kern = decode_kernel(p);
+  if (kern == kKernelTc) {
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+    e = pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io, as_stream(stream),
+                            p->pdl);
+    supported = true;
+  } else if (kern == kKernelMma) {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
     e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
@@ -509,7 +532,8 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   s = ensure_device(p);
   if (s != KV_OK) return s;
   const int G = n_q_heads / p->H;
-  if (!p->mma_ok || p->force_cuda_cores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
+  const DecodeKernel kern = decode_kernel(p);
+  if (kern == kKernelCudaCores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
   const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
   unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
   pkv::DecodeArgs a;
@@ -537,10 +561,14 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   a.plan_W = hd.W;
   const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
-  bool supported = false;
-  const cudaError_t e = pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
-                                             &p->grid_by_g[ilog2_small(G)], as_stream(stream),
-                                             p->pdl, &supported);
+  bool supported = true;
+  const cudaError_t e =
+      kern == kKernelTc
+          ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl)
+          : pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                 &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,
+                                 &supported);
   if (!supported) return KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
@@ -688,7 +716,7 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   if (!ok) return KV_ERR_CUDA;
   // sharing-aware plan on the tensor-core path (shared blocks read once)
   const int G = n_q_heads / p->H;
-  const bool planned = p->mma_ok && !p->force_cuda_cores && ilog2_small(G) >= 0 &&
+  const bool planned = decode_kernel(p) != kKernelCudaCores && ilog2_small(G) >= 0 &&
                        (p->D == 64 || p->D == 128);
   if (planned) {
     p->h_plan.resize(paged_decode_plan_bytes(p, n_seq, n_q_heads));

@@ -35,7 +35,7 @@ struct kvPool {
   int grid_by_g[4] = {0, 0, 0, 0};  // split-pass CTAs per log2(H_q / H_kv)
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
-  bool force_cuda_cores = false;            // decode on CUDA cores even when mma_ok
+  int decode_path = 0;                      // KV_OPT_DECODE_PATH
   bool pdl = true;                          // programmatic dependent launch
 
   // host staging reused by kv_decode_step_host

@@ -22,6 +22,9 @@ pytestmark = [
 
 TOL = {"f32": 1e-5, "bf16": 2e-3}
 
+# KV_OPT_DECODE_PATH: 0 automatic, 1 CUDA cores, 2 warp-level MMA, 3 tcgen05
+TENSOR_PATHS = [2, 3]
+
 
 def make(wl, zero=True, path=0, fill_nan=False):
     from paged_kv_cache_65_gb300 import PagedKVCache
@@ -153,12 +156,14 @@ SHAPES = [
 ]
 
 
-CASES = [s + (0,) for s in SHAPES] + [s + (1,) for s in SHAPES if s[0] == "bf16" and s[3] % 8 == 0]
+CASES = ([s + (0,) for s in SHAPES]
+         + [s + (p,) for p in (1, 2) for s in SHAPES if s[0] == "bf16" and s[3] % 8 == 0]
+         + [s + (3,) for s in SHAPES if s[0] == "bf16" and s[3] % 8 == 0 and s[1] == 128])
 
 
 @pytest.mark.parametrize("dtype,D,G,B,path", CASES)
 def test_ragged_shapes(dtype, D, G, B, path):
-    # path 0: automatic (tensor cores for bf16 with B % 8 == 0); 1: CUDA cores
+    # path 0: automatic; 1: CUDA cores; 2: warp-level MMA; 3: tcgen05
     lens = [1, 2, B - 1 if B > 1 else 3, B, B + 1, 3 * B + 2, 97, 700]
     lens = [max(1, l) for l in lens]
     wl = ragged_workload(dtype, D, G, B, lens, seed=D + G + B)
@@ -317,7 +322,7 @@ def test_device_checks_flag_bad_ids_without_faulting():
     assert cache.kv_pool_device_status() == 0
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2, 3])
 def test_unused_slots_holding_nan_do_not_leak(path):
     # the pool starts as NaN bit patterns: slots past each context in the last
     # block are loaded with the block but must not reach any output
@@ -340,24 +345,26 @@ def test_tensor_core_and_cuda_core_paths_agree(name):
         wl.build_ops = wl.build_ops[:10]  # two parents, eight branches: keeps the test short
         wl.decode_seqs = wl.decode_seqs[:8]
     outs = []
-    for path in (0, 1):
+    for path in (1, 2, 3):
         cache, run = make(wl, zero=False, path=path)
         q, k, v = wl.step_values(0)
         _, _, og = run.step(wl.decode_seqs, q, k, v)
         outs.append(og.cpu().numpy())
         del cache, run
         torch.cuda.empty_cache()
-    assert float(np.max(np.abs(outs[0] - outs[1]))) <= 2e-3
+    for o in outs[1:]:
+        assert float(np.max(np.abs(outs[0] - o))) <= 2e-3
 
 
 # ---------------------------------------------------------------- planned
 # The sharing-aware pass: shared prefix blocks are read once for all sharers.
 
 
-def test_planned_shared_8k_against_oracle_and_plain_pass():
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_planned_shared_8k_against_oracle_and_plain_pass(path):
     wl = synth.workload("shared_8k")
     orc = OracleRun(wl)
-    cache, run = make(wl)
+    cache, run = make(wl, path=path)
     so, co = orc.reserve_step()
     qh = orc.write_step(0, so, co)
     _, k, v = wl.step_values(0)
@@ -375,10 +382,11 @@ def test_planned_shared_8k_against_oracle_and_plain_pass():
     check_status(cache)
 
 
-def test_planned_gqa70b_32k_against_oracle():
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_planned_gqa70b_32k_against_oracle(path):
     wl = synth.workload("gqa70b_32k")
     orc = OracleRun(wl)
-    cache, run = make(wl)
+    cache, run = make(wl, path=path)
     sample = [0, 3, 21, 46]
     for step in range(2):
         so, co = orc.reserve_step()
@@ -393,9 +401,10 @@ def test_planned_gqa70b_32k_against_oracle():
     check_status(cache)
 
 
+@pytest.mark.parametrize("path", TENSOR_PATHS)
 @pytest.mark.parametrize("seed,G,B", [(0, 1, 16), (1, 2, 8), (2, 4, 16), (3, 8, 16), (4, 4, 8),
-                                      (5, 8, 32)])
-def test_planned_random_fork_trees_against_oracle(seed, G, B):
+                                      (5, 8, 32), (6, 4, 64)])
+def test_planned_random_fork_trees_against_oracle(seed, G, B, path):
     rng = np.random.default_rng(seed)
     H = 2
     ops, live, nxt = [], [], 0
@@ -414,7 +423,7 @@ def test_planned_random_fork_trees_against_oracle(seed, G, B):
     wl = synth.Workload("forks", 1, 2048, B, H * G, H, 128, "bf16", seed,
                         synth.permutation((seed, 5), 2048), ops, live)
     orc = OracleRun(wl)
-    cache, run = make(wl)
+    cache, run = make(wl, path=path)
     so, co = orc.reserve_step()
     qh = orc.write_step(0, so, co)
     _, k, v = wl.step_values(0)
@@ -428,9 +437,10 @@ def test_planned_random_fork_trees_against_oracle(seed, G, B):
     check_status(cache)
 
 
-def test_planned_equals_plain_without_sharing():
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_planned_equals_plain_without_sharing(path):
     wl = synth.workload("qwen_2k")
-    cache, run = make(wl, zero=False)
+    cache, run = make(wl, zero=False, path=path)
     q, k, v = wl.step_values(0)
     run.write(*run.reserve(wl.decode_seqs), k, v)
     d_table, d_lens, mb = run.tables(wl.decode_seqs)
@@ -441,7 +451,8 @@ def test_planned_equals_plain_without_sharing():
     assert float((a - b).abs().max()) <= 1e-6
 
 
-def test_multilayer_host_step_with_long_shared_prefix():
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_multilayer_host_step_with_long_shared_prefix(path):
     # kv_decode_step_host plans the step: sequences 0-2 share 300 tokens
     L, B, H, G, D = 2, 16, 2, 4, 128
     ops = [("append", 100, 300, 0), ("fork", 100, 0), ("fork", 100, 1), ("fork", 100, 2),
@@ -452,7 +463,10 @@ def test_multilayer_host_step_with_long_shared_prefix():
     from paged_kv_cache_65_gb300 import PagedKVCache
     from paged_kv_cache_65_gb300.driver import DeviceRun
 
+    from paged_kv_cache_65_gb300 import _lib
+
     cache = PagedKVCache(L, 128, B, H, D, "bf16", free_order=wl.free_order)
+    cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, path)
     cache.k.zero_()
     cache.v.zero_()
     run = DeviceRun(cache, H * G)
@@ -473,17 +487,53 @@ def test_multilayer_host_step_with_long_shared_prefix():
     check_status(cache)
 
 
+@pytest.mark.parametrize("path", TENSOR_PATHS)
 @pytest.mark.parametrize("planned", [False, True])
-def test_programmatic_launch_gives_identical_results(planned):
+def test_programmatic_launch_gives_identical_results(planned, path):
     # the same step with and without programmatic dependent launches
     from paged_kv_cache_65_gb300 import _lib
 
     outs = []
     for pdl in (1, 0):
         wl = ragged_workload("bf16", 128, 4, 16, [33, 1000, 2049, 5, 700], seed=31)
-        cache, run = make(wl)
+        cache, run = make(wl, path=path)
         cache.kv_pool_set_option(_lib.KV_OPT_PDL, pdl)
         q, k, v = wl.step_values(0)
         _, _, og = run.step(wl.decode_seqs, q, k, v, planned=planned)
         outs.append(og.cpu())
     assert torch.equal(outs[0], outs[1])
+
+
+class RampWorkload(synth.Workload):
+    """Keys whose scale grows along each appended run (0.25 at its start, 4
+    at its end): the largest score of a query keeps rising deep into the
+    context, so the running maximum moves in late stages of a piece, not only
+    in its first one."""
+
+    def append_values(self, value_seed, n_tokens):
+        k, v = super().append_values(value_seed, n_tokens)
+        ramp = np.linspace(0.25, 4.0, n_tokens, dtype=np.float32)[None, :, None, None]
+        if self.dtype == "bf16":
+            kf = (k.astype(np.uint32) << 16).view(np.float32)
+            k = synth.storage_values(np.ascontiguousarray(kf * ramp), "bf16")
+        else:
+            k = np.ascontiguousarray(k * ramp)
+        return k, v
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS + [1])
+@pytest.mark.parametrize("planned", [False, True])
+def test_rising_scores_move_the_maximum_inside_pieces(path, planned):
+    G, H, B = 4, 2, 16
+    ops = [("append", 0, 3000, 0), ("fork", 0, 1), ("fork", 0, 2), ("append", 1, 500, 1),
+           ("append", 3, 1800, 2), ("append", 4, 4100, 3)]
+    wl = RampWorkload("ramp", 1, 1024, B, H * G, H, 128, "bf16", 21,
+                      synth.permutation((21, 2), 1024), ops, [0, 1, 2, 3, 4])
+    orc = OracleRun(wl)
+    cache, run = make(wl, path=path)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, qh, k, v, planned=planned and path != 1)
+    assert max_err(og.cpu().numpy()[0], orc.attend(0, qh)) <= TOL["bf16"]
+    check_status(cache)
