@@ -46,14 +46,10 @@ METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and decode tokens/s"
 DEFAULT_WORKLOAD = "qwen_2k"
 
 # Per-launch DRAM traffic of the split pass from an ncu capture, keyed by
-# workload, valid only for the kernel source it was taken on.
-TRAFFIC = {
-    # ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
-    # (profiles/decode_mma_*.md), valid while the kernel sources hash to "sha"
-    "qwen_2k": {"bytes": 331662848 + 4114432, "sha": "e305e41748889990"},
-    "shared_8k": {"bytes": 176239360 + 3795200, "sha": "e305e41748889990"},
-    "gqa70b_32k": {"bytes": 1616467000 + 6040064, "sha": "e305e41748889990"},
-}
+# (workload, kernel), valid only for the kernel and plan sources it was taken
+# on: ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
+# (profiles/), valid while those sources hash to "sha".
+TRAFFIC = {}
 
 
 # KV_OPT_DECODE_PATH values
@@ -61,7 +57,8 @@ KERNELS = {"auto": 0, "cuda": 1, "mma": 2, "tc": 3}
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "ptx.cuh", "device.cu"):
+    for f in ("decode.cuh", "decode_mma.cuh", "decode_tc.cuh", "tc.cuh", "ptx.cuh", "device.cu",
+              "plan.h", "plan.cpp"):
         with open(os.path.join(ROOT, "paged_kv_cache_65_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -423,7 +420,20 @@ def bench_ours(args):
     split_s = float(np.mean(split_ms)) / 1e3
     peak, peak_kind = read_peaks()
     achieved = alg / split_s / 1e9
-    traffic = TRAFFIC.get(args.workload)
+    # the split-pass kernel that ran: a plan records its own; otherwise the option
+    tensor_shape = wl.dtype == "bf16" and wl.block_size % 8 == 0
+    if use_plan:
+        from paged_kv_cache_65_gb300.cache import parse_plan
+
+        kname = {2: "decode_mma_kernel", 3: "decode_tc_kernel"}[
+            parse_plan(host_plans[0][0])["kernel"]]
+    elif args.kernel == "cuda" or not tensor_shape:
+        kname = "decode_split_kernel"
+    elif args.kernel == "tc" and wl.head_dim == 128:
+        kname = "decode_tc_kernel"
+    else:
+        kname = "decode_mma_kernel"
+    traffic = TRAFFIC.get((args.workload, kname))
     traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha() else None
 
     # e2e through the public C-ABI call with pinned host buffers
@@ -441,7 +451,7 @@ def bench_ours(args):
             "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
             "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
                        "decode_path": "planned" if use_plan else "plain",
-                       "kernel": args.kernel,
+                       "kernel_option": args.kernel, "kernel": kname,
                        "pdl": not args.no_pdl,
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
@@ -454,7 +464,7 @@ def bench_ours(args):
             "decode_tokens_per_s_36_layers": round(toks * L / 36.0, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
-                         "kernel": "decode_mma_kernel / decode_split_kernel",
+                         "kernel": kname,
                          "peak_source": peak_kind, "timing": split_src,
                          "alg_bytes_per_launch": int(alg),
                          "mean_launch_us": round(split_s * 1e6, 2)},

@@ -106,8 +106,12 @@ kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
  * size is a multiple of 8, CUDA-core pass otherwise), 1 = always the
  * CUDA-core pass, 2 = the warp-level tensor-core pass (mma.sync) where the
  * pool allows it, 3 = the tcgen05 pass (tensor-memory accumulators; bfloat16,
- * D_h = 128) where the pool allows it, else as 2.  Changing it invalidates
- * partials of earlier split passes.  KV_OPT_PDL: 1 (default) =
+ * D_h = 128) where the pool allows it, else as 2.  A plan (paged_decode_plan)
+ * records the kernel it was built for and the planned calls run that kernel;
+ * in automatic mode the plan takes the tcgen05 pass when segments wider than
+ * 16 query columns hold at least half of the blocks it reads, else the
+ * warp-level pass.  Changing the option invalidates partials of earlier split
+ * passes.  KV_OPT_PDL: 1 (default) =
  * launch kernels with a programmatic dependency on the previous grid in the
  * stream (each kernel waits for its predecessors before reading their
  * results, but is scheduled while they finish), 0 = plain launches. */

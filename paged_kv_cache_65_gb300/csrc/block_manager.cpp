@@ -191,6 +191,7 @@ kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
   if (option == KV_OPT_DECODE_PATH && value >= 0 && value <= 3) {
     p->decode_path = value;
     for (int& g : p->grid_by_g) g = 0;  // grid sizes depend on the kernel
+    p->grid_tc = 0;
     return KV_OK;
   }
   if (option == KV_OPT_PDL && (value == 0 || value == 1)) {

@@ -9,19 +9,28 @@
 // D_h = 128, B a multiple of 8 with whole 64-row boxes per block.
 //
 // Per stage of 128 token rows of one K/V head:
-//     S^T [128 tokens x N] = K [128 x 128] . Q^T [128 x N]     (8 MMAs, K = 16)
-//     O^T [128 dims  x 32] += V^T [128 x 128] . P^T [128 x 32]  (2 x 8 MMAs)
-// N = 16 for pieces with up to 16 query columns, 32 otherwise.  K, V and Q
+//     S^T [128 tokens x N] = K [128 x 128] . Q^T [128 x N]          (8 MMAs, K = 16)
+//     O^T [128 dims  x 64] += V^T [128 x 128] . [P_hi | P_lo]^T      (8 MMAs)
+// N = 16 for pieces with up to 16 query columns, 32 otherwise (the softmax
+// handles 8, 16 or 32 columns).  K, V and Q
 // are read by the tensor core straight from shared memory (K and Q
 // K-major, V^T M-major, all with the 128-byte swizzle the TMA wrote); P is
 // written by the softmax warps into the stage's K area, which the S MMA has
-// finished with, N-major with the 64-byte swizzle, as a bf16 high part and a
-// bf16 remainder so the weights keep ~16 mantissa bits.  S^T (two buffers)
-// and O^T live in TMEM: row r of a 128-row tile is TMEM lane r.
+// finished with, N-major with the 128-byte swizzle: a bf16 high part in
+// columns 0-31 and the bf16 remainder in columns 32-63, so the weights keep
+// ~16 mantissa bits and one N = 64 MMA per 16 tokens accumulates both (O^T
+// holds the two sums side by side; the readout adds them).  S^T (two
+// buffers) and O^T live in TMEM: row r of a 128-row tile is TMEM lane r.
 //
 // Warp roles (one CTA per SM): warps 0-3 are the softmax warps (thread r owns
-// token row r of S^T and, at the end of a piece, dimension r of O^T), warp 4
-// issues the TMA loads, lane 0 of warp 5 issues the MMAs.  Softmax is
+// token row r of S^T and, at the end of a piece, dimension r of O^T), warps
+// 4 and 5 issue the TMA loads of K and of V (issuing a tensor copy costs the
+// issuing warp tens of cycles, so one warp alone cannot keep up with HBM at
+// 16-row boxes), warp 4 also stages each piece's Q tile (three buffers, so
+// the next pieces' S can start while the current one finishes), and lane 0 of
+// warp 6 issues the MMAs, starting the next stage's S first when its data
+// has already landed.
+// Softmax is
 // lazy: the reference max m of a column only moves when a new score exceeds
 // it by more than 2^8 (TAU = 8 in base-2 units), so in the steady state a
 // stage costs one barrier-reduction to confirm that nothing moved, and the
@@ -30,8 +39,8 @@
 // previous stage's MMAs have completed.
 //
 // A parity wait is exact only while the waiter is never two phases ahead of
-// the barrier: each role waits every phase of full, s_full, p_full, q_full
-// and o_free in order, and the MMAs of a stage are awaited through that
+// the barrier: each role waits every phase of full, s_full, p_full, q_full,
+// q_empty and o_free in order, and the MMAs of a stage are awaited through that
 // stage's empty barrier, whose phases are NST stages apart.
 //
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -45,7 +54,7 @@
 
 namespace pkv {
 
-constexpr int kTcWarps = 6;
+constexpr int kTcWarps = 7;
 constexpr int kTcThreads = kTcWarps * 32;
 
 struct TcCfg {
@@ -54,21 +63,22 @@ struct TcCfg {
   static constexpr int HALF = TS * 128;     // one 64-element half of K (or V): 16 KiB
   static constexpr int STAGE = 2 * HALF;    // K (or V) of one stage: 32 KiB
   static constexpr int NST = 3;             // stages in the ring
-  static constexpr int QHALF = 32 * 128;    // one half of the Q tile: 4 KiB
-  static constexpr int PLO = 8192;          // P remainder after the high part
+  static constexpr int QHALF = 32 * 128;    // one half of a Q tile: 4 KiB
+  static constexpr int QTILE = 2 * QHALF;   // Q tile: 32 columns x 128 dims
+  static constexpr int QBUF = 3;            // Q tiles in flight
   static constexpr int TM_S = 0;            // TMEM columns: S^T buffers at 0 and 32,
-  static constexpr int TM_O = 64;           // O^T at 64
+  static constexpr int TM_O = 64;           // O^T: high-part sums at 64, remainder at 96
   static constexpr int TM_COLS = 128;
   static constexpr float TAU = 8.f;
 };
 
 constexpr int decode_tc_smem_bytes() {
   return 2 * TcCfg::NST * TcCfg::STAGE  // K, V stages
-         + 2 * TcCfg::QHALF             // Q tile
+         + TcCfg::QBUF * TcCfg::QTILE   // Q tiles
          + 3 * 4 * 32 * 4               // column maxima, per-warp broadcast, l sums
-         + 16 * 8                       // mbarriers
+         + 20 * 8                       // mbarriers
          + 4 * 8 + 16                   // walk state, TMEM address
-         + kTableCache * 4              // producer table cache
+         + 2 * kTableCache * 4          // producer table caches
          + 1024;                        // alignment
 }
 
@@ -95,20 +105,25 @@ template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
   if constexpr (N == 32)
     tmem_ld32(taddr, r);
-  else
+  else if constexpr (N == 16)
     tmem_ld16(taddr, r);
+  else
+    tmem_ld8(taddr, r);
 }
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]) {
   if constexpr (N == 32)
     tmem_st32(taddr, r);
-  else
+  else if constexpr (N == 16)
     tmem_st16(taddr, r);
+  else
+    tmem_st8(taddr, r);
 }
 
 // Column reduction across a warp: lane i holds v[0..N) (one row per lane);
 // returns the reduction over the 32 rows of column (lane mod N).  Halving
-// exchange: 31 shuffles for N = 32, 16 for N = 16.
+// exchange (N - 1 shuffles), then folds over the lanes holding the same
+// column (32 / N - 1 more).
 template <int N, bool MAX>
 __device__ __forceinline__ float warp_column_reduce(float (&v)[N]) {
   const int lane = threadIdx.x & 31;
@@ -124,8 +139,9 @@ __device__ __forceinline__ float warp_column_reduce(float (&v)[N]) {
     }
   }
   float r = v[0];
-  if (N == 16) {
-    const float o = __shfl_xor_sync(0xffffffffu, r, 16);
+#pragma unroll
+  for (int off = N; off < 32; off <<= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, r, off);
     r = MAX ? fmaxf(r, o) : r + o;
   }
   return r;
@@ -136,13 +152,12 @@ struct TcSoftmax {
   const DecodeArgs* a;
   unsigned char* k_st;
   unsigned char* v_st;
-  unsigned char* q_s;
   float* red;   // [4][32] column maxima per warp
   float* cmx;   // [4][32] per-warp broadcast of the stage maxima
   float* lsum;  // [4][32] column sums of l per warp (end of a piece)
-  uint64_t *full, *empty, *s_full, *p_full, *q_full, *o_free;
+  uint64_t *full, *empty, *s_full, *p_full, *o_free;
   uint32_t tmem;
-  int G, B, cstride;
+  int B, cstride;
   bool alive;
   int stage;
 
@@ -154,44 +169,14 @@ struct TcSoftmax {
     return alive;
   }
 
-  // One piece with at least one stage; NCP = 16 or 32 query columns.
-  template <int NCP, bool PLAN>
+  // One piece with at least one stage; NCP = 8, 16 or 32 query columns.
+  template <int NCP>
   __device__ void run(const Piece& p, int n_st) {
     using C = TcCfg;
     const int t = threadIdx.x;  // token row of a stage / dimension of O^T
     const int warp = t >> 5, lane = t & 31;
     const uint32_t tl = static_cast<uint32_t>(warp * 32) << 16;
     const int ncols = p.ncols;
-    // ---- Q tile: row c = query column c, 128 dims, K-major, 128-byte swizzle
-    {
-      const int col = t >> 2, qtr = t & 3;
-      uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                    make_uint4(0, 0, 0, 0)};
-      if (col < ncols) {
-        int seqm = p.rep, gi = col;
-        if constexpr (PLAN) {
-          const int mi = col / G;
-          gi = col - mi * G;
-          seqm = a->members[p.mem + mi];
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const unsigned char*>(a->q) +
-            (((long long)seqm * a->n_q_heads + (long long)p.head * G + gi) * C::D + qtr * 32) * 2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = src[i];
-      }
-      const uint32_t qb = smem_u32(q_s);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int cg = qtr * 4 + i, h = cg >> 3, c = cg & 7;
-        sts128(qb + h * C::QHALF + col * 128 + ((c ^ (col & 7)) << 4), v[i].x, v[i].y, v[i].z,
-               v[i].w);
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
-
     float m_ref[NCP], l_part[NCP];
 #pragma unroll
     for (int c = 0; c < NCP; ++c) {
@@ -248,15 +233,18 @@ struct TcSoftmax {
           wait(&empty[(stage - 1) % C::NST], ((stage - 1) / C::NST) & 1);
           __syncwarp();
           tc_fence_after();
-          uint32_t o[NCP];
-          tmem_ld<NCP>(tmem + C::TM_O + tl, o);
 #pragma unroll
-          for (int c = 0; c < NCP; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * al[c]);
-          tmem_st<NCP>(tmem + C::TM_O + tl, o);
+          for (int part = 0; part < 2; ++part) {
+            uint32_t o[NCP];
+            tmem_ld<NCP>(tmem + C::TM_O + part * 32 + tl, o);
+#pragma unroll
+            for (int c = 0; c < NCP; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * al[c]);
+            tmem_st<NCP>(tmem + C::TM_O + part * 32 + tl, o);
+          }
         }
       }
-      // ---- weights: bf16 high part and remainder, row t of P (N-major,
-      // 64-byte swizzle: 16-byte chunk c of row t at chunk c ^ ((t >> 1) & 3))
+      // ---- weights: bf16 high part (chunks 0-3) and remainder (chunks 4-7)
+      // of row t of P (N-major, 128-byte swizzle: chunk c at c ^ (t & 7))
       const uint32_t pb = smem_u32(k_st + slot * C::STAGE);
 #pragma unroll
       for (int c8 = 0; c8 < NCP / 8; ++c8) {
@@ -272,9 +260,8 @@ struct TcSoftmax {
           lo[k] = pack_bf16(p0 - __uint_as_float(hi[k] << 16),
                             p1 - __uint_as_float(hi[k] & 0xffff0000u));
         }
-        const uint32_t off = t * 64 + ((c8 ^ ((t >> 1) & 3)) << 4);
-        sts128(pb + off, hi[0], hi[1], hi[2], hi[3]);
-        sts128(pb + C::PLO + off, lo[0], lo[1], lo[2], lo[3]);
+        sts128(pb + t * 128 + ((c8 ^ (t & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+        sts128(pb + t * 128 + (((4 + c8) ^ (t & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
       }
       // rows past the context inside the last 16-row MMA step: V must be
       // finite there (unused slots may hold anything), so it is zeroed
@@ -296,18 +283,24 @@ struct TcSoftmax {
     wait(&empty[(stage - 1) % C::NST], ((stage - 1) / C::NST) & 1);
     __syncwarp();
     tc_fence_after();
-    uint32_t o[NCP];
-    tmem_ld<NCP>(tmem + C::TM_O + tl, o);
+    const long long slot_id = (long long)blockIdx.x + p.seg;
+#pragma unroll
+    for (int c0 = 0; c0 < NCP; c0 += 8) {
+      uint32_t oh[8], ol[8];
+      tmem_ld8(tmem + C::TM_O + c0 + tl, oh);
+      tmem_ld8(tmem + C::TM_O + 32 + c0 + tl, ol);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c0 + c < ncols)
+          a->ws_o[(slot_id * cstride + c0 + c) * C::D + t] =
+              __uint_as_float(oh[c]) + __uint_as_float(ol[c]);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(o_free);
     const float ls = warp_column_reduce<NCP, false>(l_part);
     if (lane < NCP) lsum[warp * 32 + lane] = ls;
     named_bar_sync(1, 128);
-    const long long slot_id = (long long)blockIdx.x + p.seg;
-#pragma unroll
-    for (int c = 0; c < NCP; ++c)
-      if (c < ncols) a->ws_o[(slot_id * cstride + c) * C::D + t] = __uint_as_float(o[c]);
     if (warp == 0 && lane < ncols) {
       float mc = m_ref[0];
 #pragma unroll
@@ -332,18 +325,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE;
-  unsigned char* q_s = v_st + NST * C::STAGE;
-  float* red = reinterpret_cast<float*>(q_s + 2 * C::QHALF);
+  unsigned char* q_s = v_st + NST * C::STAGE;  // QBUF Q tiles
+  float* red = reinterpret_cast<float*>(q_s + C::QBUF * C::QTILE);
   float* cmx = red + 128;
   float* lsum = cmx + 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(lsum + 128);
   uint64_t* empty = full + NST;
   uint64_t* s_full = empty + NST;  // [2]
   uint64_t* p_full = s_full + 2;   // [2]
-  uint64_t* q_full = p_full + 2;
-  uint64_t* o_free = q_full + 1;
+  uint64_t* q_full = p_full + 2;           // [QBUF]
+  uint64_t* q_empty = q_full + C::QBUF;    // [QBUF]
+  uint64_t* o_free = q_empty + C::QBUF;
   uint64_t* fin = o_free + 1;
-  long long* walk = reinterpret_cast<long long*>(full + 16);
+  long long* walk = reinterpret_cast<long long*>(full + 20);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(walk + 4);
   int32_t* tcache = reinterpret_cast<int32_t*>(tmem_slot + 4);
 
@@ -361,14 +355,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 2);  // the K and the V producer
       mbar_init(&empty[i], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(&p_full[0], 4);
     mbar_init(&p_full[1], 4);
-    mbar_init(q_full, 4);
+    for (int i = 0; i < C::QBUF; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
     mbar_init(o_free, 4);
     mbar_init(fin, 1);
     fence_barrier_init();
@@ -454,19 +451,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return n > 0 ? (n + C::TS - 1) / C::TS : 0;
   };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_v);
-    }
+  if (warp == 4 || warp == 5) {
+    // ----------------------------------------------- producers (K, V)
+    const bool kp = warp == 4;  // K producer, also stages Q
+    const CUtensorMap* tmap = kp ? &tmap_k : &tmap_v;
+    unsigned char* dst_st = kp ? k_st : v_st;
+    if (lane == 0) prefetch_tmap(tmap);
     bool alive = true;
-    int stage = 0;
+    int stage = 0, npiece = 0;
     TableCache tc;
-    tc.ent = tcache;
-    Piece p;
-    while (next_piece(p)) {
+    tc.ent = tcache + (warp - 4) * kTableCache;
+    // Q tile of a piece: row c = query column c (zero past the piece's
+    // columns), 128 dims, K-major, 128-byte swizzle.  Lane l holds the
+    // 16-byte chunks l, l + 32, ... of the tile; the loads for the next piece
+    // are issued before the current piece's copies, so their latency is
+    // hidden behind them.
+    uint4 qv[16];
+    auto load_q = [&](const Piece& x) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int idx = k * 32 + lane;
+        const int col = idx >> 4, cg = idx & 15;
+        qv[k] = make_uint4(0, 0, 0, 0);
+        if (col < x.ncols) {
+          int seqm = x.rep, gi = col;
+          if constexpr (PLAN) {
+            const int mi = col / G;
+            gi = col - mi * G;
+            seqm = a.members[x.mem + mi];
+          }
+          qv[k] = *reinterpret_cast<const uint4*>(
+              reinterpret_cast<const unsigned char*>(a.q) +
+              (((long long)seqm * a.n_q_heads + (long long)x.head * G + gi) * C::D + cg * 8) * 2);
+        }
+      }
+    };
+    auto next_nonempty = [&](Piece& x) {
+      while (next_piece(x))
+        if (stages_of(x) > 0) return true;
+      return false;
+    };
+    // Q tile of piece number np into its buffer, once the S MMAs of the
+    // piece QBUF before are done with that buffer
+    auto stage_q = [&](int np) {
+      const int qb = np % C::QBUF;
+      if (kp && np >= C::QBUF && alive) {
+        if (!mbar_wait_bounded(&q_empty[qb], ((np / C::QBUF) - 1) & 1, kWaitLimitNs)) {
+          alive = false;
+          if (lane == 0) record_status(a.status, 8);
+        }
+      }
+      alive = __all_sync(0xffffffffu, alive);
+      if (kp && alive) {
+        const uint32_t qs = smem_u32(q_s + qb * C::QTILE);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int idx = k * 32 + lane;
+          const int col = idx >> 4, cg = idx & 15;
+          const int h = cg >> 3, c = cg & 7;
+          sts128(qs + h * C::QHALF + col * 128 + ((c ^ (col & 7)) << 4), qv[k].x, qv[k].y,
+                 qv[k].z, qv[k].w);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[qb]);
+      }
+    };
+    Piece p, pn;
+    bool have = next_nonempty(p);
+    if (have && kp) load_q(p);
+    while (have) {
       const int n_st = stages_of(p);
+      bool have_next = false;
       for (int i = 0; i < n_st; ++i, ++stage) {
         const int slot = stage % NST;
         if (stage >= NST && alive) {
@@ -481,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nvalid = p.tok_end - tok0 < C::TS ? p.tok_end - tok0 : C::TS;
         const int nunits = (nvalid + UR - 1) / UR;
         tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * UR * C::D * 2);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 1u * nunits * UR * C::D * 2);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int tk = tok0 + u * UR;
@@ -497,23 +553,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int h = 0; h < 2; ++h) {
             const int x = p.head * C::D + h * 64;
             const int off = slot * C::STAGE + h * C::HALF + u * UR * 128;
-            tma_load_2d(k_st + off, &tmap_k, x, y, &full[slot]);
-            tma_load_2d(v_st + off, &tmap_v, x, y, &full[slot]);
+            tma_load_2d(dst_st + off, tmap, x, y, &full[slot]);
           }
         }
+        if (i == 0) {
+          // the piece's Q goes in behind its first copies (their latency
+          // covers it), then the next piece's Q loads are issued
+          stage_q(npiece);
+          have_next = next_nonempty(pn);
+          if (have_next && kp) load_q(pn);
+        }
       }
+      ++npiece;  // (after a failed wait the walk stops here: have_next stays false)
+      p = pn;
+      have = have_next;
     }
     // copies still in flight land before the CTA may exit
     const int first = stage > NST ? stage - NST : 0;
     for (int k = first; k < stage && alive; ++k)
       alive = mbar_wait_bounded(&full[k % NST], (k / NST) & 1, kWaitLimitNs);
-  } else if (warp == 5) {
+  } else if (warp == 6) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t kb = smem_u32(k_st), vb = smem_u32(v_st), qb = smem_u32(q_s);
       constexpr uint32_t idS16 = idesc_bf16(128, 16, false, false);
       constexpr uint32_t idS32 = idesc_bf16(128, 32, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, 32, true, true);
+      constexpr uint32_t idPV = idesc_bf16(128, 64, true, true);
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (alive && !mbar_wait_bounded(bar, parity, kWaitLimitNs)) {
@@ -522,14 +587,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         return alive;
       };
-      auto issue_s = [&](int st, uint32_t idS) {
+      auto issue_s = [&](int st, uint32_t idS, uint32_t qbase) {
         const uint32_t ks = kb + (st % NST) * C::STAGE;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
           const uint32_t qoff = (k >> 2) * C::QHALF + (k & 3) * 32;
           tc_mma(tmem + C::TM_S + (st & 1) * 32, smem_desc(ks + off, 16, 1024, kSwizzle128),
-                 smem_desc(qb + qoff, 16, 1024, kSwizzle128), idS, k > 0);
+                 smem_desc(qbase + qoff, 16, 1024, kSwizzle128), idS, k > 0);
         }
         tc_commit(&s_full[st & 1]);
       };
@@ -539,41 +604,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int n_st = stages_of(p);
         if (n_st == 0) continue;
         const uint32_t idS = p.ncols <= 16 ? idS16 : idS32;
-        wait(q_full, npiece & 1);
+        const int qbi = npiece % C::QBUF;
+        const uint32_t qbase = qb + qbi * C::QTILE;
+        wait(&q_full[qbi], (npiece / C::QBUF) & 1);
         if (npiece > 0) wait(o_free, (npiece - 1) & 1);
-        if (wait(&full[stage % NST], (stage / NST) & 1)) {
+        int issued = 0;  // S issued for stages stage .. stage + issued - 1
+        // S of the next stage; blocking, or only when its data is already in
+        auto issue_next = [&](bool block) {
+          const int st = stage + issued;
+          const bool ok = block ? wait(&full[st % NST], (st / NST) & 1)
+                                : alive && mbar_test_wait(&full[st % NST], (st / NST) & 1);
+          if (!ok) return;
           tc_fence_after();
-          issue_s(stage, idS);
-        }
+          issue_s(st, idS, qbase);
+          if (++issued == n_st) tc_commit(&q_empty[qbi]);  // Q tile free once these are done
+        };
+        issue_next(true);
         for (int i = 0; i < n_st; ++i) {
-          const int cur = stage + i, nx = cur + 1;
-          // the next stage's S goes ahead of this stage's P.V when its data is in
-          bool s_next = false;
-          if (i + 1 < n_st && alive && mbar_try_wait(&full[nx % NST], (nx / NST) & 1)) {
-            tc_fence_after();
-            issue_s(nx, idS);
-            s_next = true;
-          }
-          if (wait(&p_full[cur & 1], (cur >> 1) & 1)) {
+          const int cur = stage + i;
+          // the next stage's S goes first when its data is already in (its S
+          // buffer was released with P of the stage before); the wait for P
+          // suspends the thread rather than spinning, since this lane shares
+          // a scheduler with a softmax warp
+          if (issued == i + 1 && issued < n_st) issue_next(false);
+          wait(&p_full[cur & 1], (cur >> 1) & 1);
+          if (alive) {
             tc_fence_after();
             const int tok0 = p.b0 * B + i * C::TS;
             const int nvalid = p.tok_end - tok0 < C::TS ? p.tok_end - tok0 : C::TS;
             const int nk = (nvalid + 15) >> 4;
             const uint32_t vs = vb + (cur % NST) * C::STAGE;
             const uint32_t ps = kb + (cur % NST) * C::STAGE;
-            for (int k = 0; k < nk; ++k) {
-              const uint64_t da = smem_desc(vs + k * 2048, C::HALF, 1024, kSwizzle128);
-              tc_mma(tmem + C::TM_O, da, smem_desc(ps + k * 1024, 8192, 512, kSwizzle64), idPV,
+            for (int k = 0; k < nk; ++k)
+              tc_mma(tmem + C::TM_O, smem_desc(vs + k * 2048, C::HALF, 1024, kSwizzle128),
+                     smem_desc(ps + k * 2048, C::HALF, 1024, kSwizzle128), idPV,
                      (i > 0 || k > 0) ? 1u : 0u);
-              tc_mma(tmem + C::TM_O, da, smem_desc(ps + C::PLO + k * 1024, 8192, 512, kSwizzle64),
-                     idPV, 1u);
-            }
             tc_commit(&empty[cur % NST]);
           }
-          if (i + 1 < n_st && !s_next && wait(&full[nx % NST], (nx / NST) & 1)) {
-            tc_fence_after();
-            issue_s(nx, idS);
-          }
+          if (issued == i + 1 && issued < n_st) issue_next(true);
         }
         stage += n_st;
         ++npiece;
@@ -589,7 +657,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sm.a = &a;
     sm.k_st = k_st;
     sm.v_st = v_st;
-    sm.q_s = q_s;
     sm.red = red;
     sm.cmx = cmx;
     sm.lsum = lsum;
@@ -597,10 +664,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sm.s_full = s_full;
     sm.p_full = p_full;
     sm.empty = empty;
-    sm.q_full = q_full;
     sm.o_free = o_free;
     sm.tmem = tmem;
-    sm.G = G;
     sm.B = B;
     sm.cstride = PLAN ? a.c_max : G;
     sm.alive = true;
@@ -619,10 +684,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         continue;
       }
-      if (p.ncols <= 16)
-        sm.run<16, PLAN>(p, n_st);
+      if (p.ncols <= 8)
+        sm.run<8>(p, n_st);
+      else if (p.ncols <= 16)
+        sm.run<16>(p, n_st);
       else
-        sm.run<32, PLAN>(p, n_st);
+        sm.run<32>(p, n_st);
     }
   }
 

@@ -64,7 +64,7 @@ enum DecodeKernel { kKernelCudaCores, kKernelMma, kKernelTc };
 
 DecodeKernel decode_kernel(const kvPool* p) {
   const bool mma = p->mma_ok;
-  const bool tc = p->mma_ok && p->D == 128;
+  const bool tc = p->mma_ok && pool_tc_shape(p);
   switch (p->decode_path) {
     case 1: return kKernelCudaCores;
     case 2: return mma ? kKernelMma : kKernelCudaCores;
@@ -90,12 +90,9 @@ kvStatus ensure_device(kvPool* p) {
     if (s != KV_OK) return s;
     s = encode_cache_map(p, p->v, p->D, rows, false, reinterpret_cast<CUtensorMap*>(p->tmap[1]));
     if (s != KV_OK) return s;
-    // tensor-core path: rows of 64 bf16 (128 bytes) with the 128-byte swizzle;
-    // each box must start on a 1 KiB boundary, hence B a multiple of 8, and
-    // a stage must hold whole blocks or a block whole stages
-    const int tsm = pkv::mma_stage_tokens(p->D);
-    const bool fits = p->B <= tsm ? tsm % p->B == 0 : p->B % tsm == 0;
-    if (p->dtype == KV_DTYPE_BF16 && p->B % 8 == 0 && fits) {
+    // tensor-core passes: rows of 64 bf16 (128 bytes) with the 128-byte swizzle
+    if (pool_tensor_core_shape(p)) {
+      const int tsm = pkv::mma_stage_tokens(p->D);
       const int rm = p->B < tsm ? p->B : tsm;
       s = encode_cache_map(p, p->k, 64, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
       if (s != KV_OK) return s;
@@ -425,10 +422,10 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   a.n_segs = 0;
   a.c_max = G;
   a.plan_W = 0;
-  int* grid_io = &p->grid_by_g[ilog2_small(G)];
+  const DecodeKernel kern = decode_kernel(p);
+  int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  const DecodeKernel kern = decode_kernel(p);
   if (kern == kKernelTc) {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
@@ -463,7 +460,9 @@ kvStatus paged_decode_merge(kvPool* p, int n_q_heads, const int32_t* d_context_l
   if (!d_context_lens || !d_out || !d_workspace) return KV_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(p, n_seq, G);
   if (workspace_bytes < w.total || !aligned16(d_workspace)) return KV_ERR_INVALID_ARG;
-  const int grid = p->grid_by_g[ilog2_small(G)];
+  // the CTA count of the split pass that wrote the partials
+  const int grid = p->dev_ready && decode_kernel(p) == kKernelTc ? p->grid_tc
+                                                                 : p->grid_by_g[ilog2_small(G)];
   if (grid <= 0) return KV_ERR_INVALID_ARG;  // no split pass has run on this pool
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(d_workspace);
   const long long* pre = reinterpret_cast<const long long*>(ws + w.pre);
@@ -505,7 +504,8 @@ kvStatus read_plan_header(const kvPool* p, int n_q_heads, const void* h_plan, Pl
   std::memcpy(hd, h_plan, sizeof(*hd));
   const int G = n_q_heads / p->H;
   if (hd->n_kv_heads != p->H || hd->group != G || hd->block_size != p->B || hd->n_seq < 0 ||
-      hd->c_max < G || hd->c_max > kPlanMaxCols || hd->n_segs < 0)
+      hd->c_max < G || hd->c_max > kPlanMaxCols || hd->n_segs < 0 ||
+      (hd->kernel != kPlanKernelMma && hd->kernel != kPlanKernelTc))
     return KV_ERR_INVALID_ARG;
   return KV_OK;
 }
@@ -532,8 +532,11 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   s = ensure_device(p);
   if (s != KV_OK) return s;
   const int G = n_q_heads / p->H;
-  const DecodeKernel kern = decode_kernel(p);
-  if (kern == kKernelCudaCores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
+  // the kernel the plan's work units were weighted for; the CUDA-core
+  // option turns the planned pass off
+  if (decode_kernel(p) == kKernelCudaCores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
+  const bool tc = hd.kernel == kPlanKernelTc;
+  if (tc && !pool_tc_shape(p)) return KV_ERR_UNSUPPORTED;
   const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
   unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
   pkv::DecodeArgs a;
@@ -563,10 +566,9 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   bool supported = true;
   const cudaError_t e =
-      kern == kKernelTc
-          ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas,
-                                &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl)
-          : pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+      tc ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
+                               as_stream(stream), p->pdl)
+         : pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
                                  &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,
                                  &supported);
   if (!supported) return KV_ERR_UNSUPPORTED;
@@ -586,7 +588,7 @@ kvStatus paged_decode_merge_planned(kvPool* p, int n_q_heads, const void* d_plan
   if (workspace_bytes < plan_workspace_bytes(hd.n_segs, hd.c_max, p->D)) return KV_ERR_INVALID_ARG;
   const int G = n_q_heads / p->H;
   if (ilog2_small(G) < 0 || (p->D != 64 && p->D != 128)) return KV_ERR_UNSUPPORTED;
-  const int grid = p->grid_by_g[ilog2_small(G)];
+  const int grid = hd.kernel == kPlanKernelTc ? p->grid_tc : p->grid_by_g[ilog2_small(G)];
   if (hd.W > 0 && grid <= 0) return KV_ERR_INVALID_ARG;  // no split pass has run on this pool
   const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(d_workspace);

@@ -124,10 +124,13 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   }
 
   // ---- segments, members, entries.  Order: per group and K/V head, the
-  // shared segment followed by the members' private rests, then the
-  // ungrouped sequences; tiny private rests are thus spread over the work
-  // list instead of piling up at its end (the split balances blocks, and
-  // every piece has a fixed cost).
+  // shared segment followed by the members' private rests of that head;
+  // these (group, head) items are spread evenly among the ungrouped
+  // sequences (item i before ungrouped sequence ceil(i * n_ungrouped /
+  // n_items)).  Tiny private rests are thus spread over the work list
+  // instead of piling up at its end, and the wide shared segments, whose
+  // blocks cost more, fall to different CTAs (the split balances work
+  // units, and every piece has a fixed cost).
   std::vector<PlanSeg> segs;
   std::vector<int32_t> members;
   std::vector<std::vector<PlanEntry>> ents(static_cast<size_t>(n_seq) * H);
@@ -156,35 +159,62 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     ents[static_cast<size_t>(i) * H + h].push_back({si, 0});
   };
   std::vector<char> grouped(n_seq, 0);
-  for (size_t c = 0; c < chunks.size(); ++c) {
-    const int mem0 = static_cast<int>(members.size());
-    for (int m : chunks[c]) {
-      members.push_back(m);
-      grouped[m] = 1;
+  for (const auto& ch : chunks)
+    for (int m : ch) grouped[m] = 1;
+  std::vector<int> group_mem0(chunks.size(), -1);  // member-list slot of each group
+  auto push_group_head = [&](size_t c, int h) {
+    if (group_mem0[c] < 0) {
+      group_mem0[c] = static_cast<int>(members.size());
+      for (int m : chunks[c]) members.push_back(m);
     }
     const int ncols = static_cast<int>(chunks[c].size()) * G;
     c_max = std::max(c_max, ncols);
-    for (int h = 0; h < H; ++h) {
-      PlanSeg s{};
-      s.rep = chunks[c][0];
-      s.b0 = 0;
-      s.b1 = chunk_p[c];
-      s.tok_end = chunk_p[c] * B;
-      s.head = h;
-      s.ncols = ncols;
-      s.mem = mem0;
-      const int si = static_cast<int>(segs.size());
-      segs.push_back(s);
-      for (int m : chunks[c]) ents[static_cast<size_t>(m) * H + h].push_back({si, pos_in[m] * G});
-      for (int m : chunks[c]) push_private(m, h);
+    PlanSeg s{};
+    s.rep = chunks[c][0];
+    s.b0 = 0;
+    s.b1 = chunk_p[c];
+    s.tok_end = chunk_p[c] * B;
+    s.head = h;
+    s.ncols = ncols;
+    s.mem = group_mem0[c];
+    const int si = static_cast<int>(segs.size());
+    segs.push_back(s);
+    for (int m : chunks[c]) ents[static_cast<size_t>(m) * H + h].push_back({si, pos_in[m] * G});
+    for (int m : chunks[c]) push_private(m, h);
+  };
+  std::vector<int> ungrouped;
+  for (int i = 0; i < n_seq; ++i)
+    if (!grouped[i]) ungrouped.push_back(i);
+  const size_t n_i = chunks.size() * H, n_u = ungrouped.size();
+  size_t it = 0;
+  auto push_item = [&](size_t i) { push_group_head(i % chunks.size(), static_cast<int>(i / chunks.size())); };
+  for (size_t k = 0; k < n_u; ++k) {
+    while (it < n_i && it * n_u <= k * n_i) push_item(it++);
+    for (int h = 0; h < H; ++h) push_private(ungrouped[k], h);
+  }
+  while (it < n_i) push_item(it++);
+
+  // ---- the kernel the work units are weighted for: the pool's decode path;
+  // automatic: tcgen05 when segments of more than 16 columns hold at least
+  // half of the blocks read (many sharers of long prefixes: its S and P.V
+  // cost little per byte at any width), else the warp-level MMA pass (which
+  // streams narrow segments faster)
+  int kernel = kPlanKernelMma;
+  if (pool_tc_shape(p)) {
+    if (p->decode_path == 3) {
+      kernel = kPlanKernelTc;
+    } else if (p->decode_path == 0) {
+      int64_t wide = 0, all = 0;
+      for (const PlanSeg& s : segs) {
+        all += s.b1 - s.b0;
+        if (s.ncols > 16) wide += s.b1 - s.b0;
+      }
+      if (all > 0 && 2 * wide >= all) kernel = kPlanKernelTc;
     }
   }
-  for (int i = 0; i < n_seq; ++i)
-    if (!grouped[i])
-      for (int h = 0; h < H; ++h) push_private(i, h);
   int64_t W = 0;
   for (PlanSeg& s : segs) {
-    s.w = plan_block_weight(s.ncols);
+    s.w = plan_block_weight(s.ncols, kernel);
     s.wpre = W;
     W += static_cast<int64_t>(s.b1 - s.b0) * s.w;
   }
@@ -212,6 +242,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   hd.eoff_off = static_cast<int32_t>(l.eoff);
   hd.ent_off = static_cast<int32_t>(l.ent);
   hd.n_shared_segs = static_cast<int32_t>(chunks.size()) * H;
+  hd.kernel = kernel;
   std::memcpy(out, &hd, sizeof(hd));
   if (!segs.empty()) std::memcpy(out + l.seg, segs.data(), sizeof(PlanSeg) * segs.size());
   if (!members.empty()) std::memcpy(out + l.mem, members.data(), sizeof(int32_t) * members.size());

@@ -33,7 +33,8 @@ struct PlanHeader {
   int32_t eoff_off;
   int32_t ent_off;
   int32_t n_shared_segs;
-  int32_t pad[5];
+  int32_t kernel;     // split-pass kernel the work units are weighted for (kPlanKernel*)
+  int32_t pad[4];
 };
 static_assert(sizeof(PlanHeader) == 80, "plan header layout");
 
@@ -57,7 +58,18 @@ struct PlanEntry {
 // Most query columns one segment carries (four 8-column MMA n-tiles).
 constexpr int kPlanMaxCols = 32;
 
-// Work units per block by 8-column n-tiles (1, 2, 3-4): the split pass
-// balances units, so blocks of wide shared segments, which cost more tensor
-// work per byte, are spread over more CTAs.
-constexpr int plan_block_weight(int ncols) { return ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5); }
+// Split-pass kernels a plan can be built for (the values of the pool's
+// decode-path option).
+constexpr int kPlanKernelMma = 2;  // warp-level MMA (mma.sync)
+constexpr int kPlanKernelTc = 3;   // tcgen05, TMEM accumulators
+
+// Work units per block.  The split pass balances units.  On the warp-level
+// MMA kernel a block costs more the more 8-column n-tiles it carries (1, 2,
+// 3-4 tiles: 3, 4, 5 units), so blocks of wide shared segments are spread
+// over more CTAs; on the tcgen05 kernel the tensor work is small against the
+// block's bytes, and only the 32-column softmax adds to a block's time
+// (4, 4, 5 units).
+constexpr int plan_block_weight(int ncols, int kernel) {
+  return kernel == kPlanKernelTc ? (ncols <= 16 ? 4 : 5)
+                                 : (ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5));
+}

@@ -33,6 +33,7 @@ struct kvPool {
   int device = -1;
   int sm_count = 0;
   int grid_by_g[4] = {0, 0, 0, 0};  // split-pass CTAs per log2(H_q / H_kv)
+  int grid_tc = 0;                  // CTAs of the tcgen05 split pass (one per SM)
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
   int decode_path = 0;                      // KV_OPT_DECODE_PATH
@@ -43,6 +44,19 @@ struct kvPool {
   std::vector<int32_t> h_pairs, h_table, h_lens;
   std::vector<unsigned char> h_plan;
 };
+
+// Tensor-core passes read K/V through 128-byte-swizzled TMA boxes of 64
+// elements by min(B, T) rows, T = 64 tokens at D_h = 128 and 128 at 64: each
+// box starts on 1 KiB (B a multiple of 8) and a stage holds whole blocks or a
+// block whole stages.
+inline bool pool_tensor_core_shape(const kvPool* p) {
+  if (p->dtype != KV_DTYPE_BF16 || (p->D != 64 && p->D != 128) || p->B % 8 != 0) return false;
+  const int t = p->D == 64 ? 128 : 64;
+  return p->B <= t ? t % p->B == 0 : p->B % t == 0;
+}
+
+// The tcgen05 pass: the tensor-core shape with D_h = 128.
+inline bool pool_tc_shape(const kvPool* p) { return pool_tensor_core_shape(p) && p->D == 128; }
 
 // Largest CTA count the split pass uses; sizes the decode workspace.
 constexpr int kMaxDecodeCtas = 1024;

@@ -39,7 +39,12 @@ def check_plan(bm, plan, seqs, G, min_tokens):
     units = [int(s["b1"] - s["b0"]) * int(s["w"]) for s in segs]
     assert plan["W"] == sum(units)
     assert list(segs["wpre"]) == list(np.cumsum([0] + units)[:-1])
-    assert all(s["w"] == (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5) for s in segs)
+    if plan["kernel"] == 3:  # tcgen05
+        assert all(s["w"] == (4 if s["ncols"] <= 16 else 5) for s in segs)
+    else:
+        assert plan["kernel"] == 2
+        assert all(s["w"] == (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5)
+                   for s in segs)
     for si, s in enumerate(segs):
         assert s["ncols"] % G == 0 and 0 < s["ncols"] <= 32
         members = mem[s["mem"]:s["mem"] + s["ncols"] // G]
@@ -65,15 +70,28 @@ def check_plan(bm, plan, seqs, G, min_tokens):
             assert (covered == 1).all(), (sid, h)
 
 
+@pytest.mark.parametrize("path", [0, 3])
 @pytest.mark.parametrize("name", ["tiny", "qwen_2k", "shared_8k", "gqa70b_32k"])
-def test_plans_of_the_workloads(name):
+def test_plans_of_the_workloads(name, path):
+    from paged_kv_cache_65_gb300 import _lib
+
     wl = synth.workload(name)
     bm, c = build_both(wl)
+    c.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, path)
     G = wl.n_q_heads // wl.n_kv_heads
     mb = max(len(bm.tables[s]) for s in wl.decode_seqs)
     buf, ws = c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)
     plan = parse_plan(buf)
     check_plan(bm, plan, wl.decode_seqs, G, 128)
+    # the tcgen05 kernel is only for bfloat16 pools with D_h = 128 and B a multiple of 8
+    tc_shape = wl.dtype == "bf16" and wl.head_dim == 128 and wl.block_size % 8 == 0
+    # automatic: tcgen05 when segments wider than 16 columns hold half of the blocks
+    wide = sum(int(s["b1"] - s["b0"]) for s in plan["segs"] if s["ncols"] > 16)
+    total = sum(int(s["b1"] - s["b0"]) for s in plan["segs"])
+    auto_tc = 2 * wide >= total
+    assert plan["kernel"] == (3 if tc_shape and (path == 3 or auto_tc) else 2)
+    if name == "gqa70b_32k":
+        assert auto_tc
     assert ws > 0
     shared = [s for s in plan["segs"] if s["ncols"] > G]
     if name == "gqa70b_32k":
