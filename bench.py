@@ -49,7 +49,9 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # (workload, kernel), valid only for the kernel and plan sources it was taken
 # on: ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
 # (profiles/), valid while those sources hash to "sha".
-TRAFFIC = {}
+TRAFFIC = {
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615944000 + 7036672, "sha": "9590bfd7e0a0ef57"},
+}
 
 
 # KV_OPT_DECODE_PATH values
