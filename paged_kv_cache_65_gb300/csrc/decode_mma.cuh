@@ -202,10 +202,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     fence_barrier_init();
   }
-  // everything above touches only shared memory; global inputs (pool, q,
-  // tables) may come from the previous grid in the stream
-  griddep_wait();
-  griddep_launch_dependents();
+  // The walk start and the producer's first block-table entries read only
+  // host-written metadata (plan, context lengths, tables), complete before the
+  // first kernel of the stream's programmatic chain started, so they are
+  // read before waiting for the previous grid; the pool, q and the workspace
+  // only after it.
   if (warp == 0) {
     if constexpr (PLAN) {
       const long long W = a.plan_W;
@@ -221,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     } else {
       WalkStart w = find_start(a.ctx, a.n_seq, B, H, a.max_blocks, a.grid, blockIdx.x, a.status);
-      if (blockIdx.x == 0) write_prefix(a.ctx, a.n_seq, B, H, a.max_blocks, a.ws_pre);
       if (lane == 0) {
         walk[0] = w.s;
         walk[1] = w.pre;
@@ -271,6 +271,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       return true;
     }
   };
+  // the first piece of this CTA, without advancing the walk
+  auto peek_first = [&](Piece& p0) -> bool {
+    const PieceWalker pw_s = pw;
+    const PlanWalker plw_s = plw;
+    const bool ok = next_piece(p0);
+    pw = pw_s;
+    plw = plw_s;
+    return ok;
+  };
+  auto wait_previous_grid = [&]() {
+    griddep_wait();
+    griddep_launch_dependents();
+    if constexpr (!PLAN) {
+      if (blockIdx.x == 0 && warp == 0)
+        write_prefix(a.ctx, a.n_seq, B, H, a.max_blocks, a.ws_pre);
+    }
+  };
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -282,6 +299,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     int stage = 0;
     TableCache tc;
     tc.ent = tcache;
+    {
+      Piece p0;
+      if (peek_first(p0)) tc.ensure(a.table, a.max_blocks, p0.rep, p0.b0, p0.b0, lane);
+    }
+    wait_previous_grid();
     Piece p;
     while (next_piece(p)) {
       for (int tok0 = p.b0 * B; tok0 < p.tok_end; tok0 += STG) {
@@ -325,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // -------------------------------------------------------------- consumers
+  wait_previous_grid();
   const int g = lane >> 2;  // groupID: row of A / C, column of B
   const int t = lane & 3;   // thread in group
   const uint32_t k_base = smem_u32(k_st);

@@ -374,10 +374,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
   }
-  // everything above touches only on-chip state; global inputs (pool, q,
-  // tables, plan) may come from the previous grid in the stream
-  griddep_wait();
-  griddep_launch_dependents();
+  // The walk start and the producers' first block-table entries read only
+  // host-written metadata (plan, context lengths, tables), complete before the
+  // first kernel of the stream's programmatic chain started, so they are
+  // read before waiting for the previous grid; the pool, q and the workspace
+  // only after it.
   if (warp == 4) {
     if constexpr (PLAN) {
       const long long W = a.plan_W;
@@ -393,7 +394,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else {
       WalkStart w = find_start(a.ctx, a.n_seq, B, H, a.max_blocks, a.grid, blockIdx.x, a.status);
-      if (blockIdx.x == 0) write_prefix(a.ctx, a.n_seq, B, H, a.max_blocks, a.ws_pre);
       if (lane == 0) {
         walk[0] = w.s;
         walk[1] = w.pre;
@@ -446,6 +446,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return true;
     }
   };
+  // the first piece of this CTA, without advancing the walk
+  auto peek_first = [&](Piece& p0) -> bool {
+    const PieceWalker pw_s = pw;
+    const PlanWalker plw_s = plw;
+    const bool ok = next_piece(p0);
+    pw = pw_s;
+    plw = plw_s;
+    return ok;
+  };
+  auto wait_previous_grid = [&]() {
+    griddep_wait();
+    griddep_launch_dependents();
+    if constexpr (!PLAN) {
+      if (blockIdx.x == 0 && warp == 4)
+        write_prefix(a.ctx, a.n_seq, B, H, a.max_blocks, a.ws_pre);
+    }
+  };
   auto stages_of = [&](const Piece& p) -> int {
     const int n = p.tok_end - p.b0 * B;
     return n > 0 ? (n + C::TS - 1) / C::TS : 0;
@@ -461,6 +478,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int stage = 0, npiece = 0;
     TableCache tc;
     tc.ent = tcache + (warp - 4) * kTableCache;
+    {
+      Piece p0;
+      if (peek_first(p0)) tc.ensure(a.table, a.max_blocks, p0.rep, p0.b0, p0.b0, lane);
+    }
+    wait_previous_grid();
     // Q tile of a piece: row c = query column c (zero past the piece's
     // columns), 128 dims, K-major, 128-byte swizzle.  Lane l holds the
     // 16-byte chunks l, l + 32, ... of the tile; the loads for the next piece
@@ -574,6 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       alive = mbar_wait_bounded(&full[k % NST], (k / NST) & 1, kWaitLimitNs);
   } else if (warp == 6) {
     // -------------------------------------------------------- MMA issuer
+    wait_previous_grid();
     if (lane == 0) {
       const uint32_t kb = smem_u32(k_st), vb = smem_u32(v_st), qb = smem_u32(q_s);
       constexpr uint32_t idS16 = idesc_bf16(128, 16, false, false);
@@ -653,6 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------- softmax warps
+    wait_previous_grid();
     TcSoftmax sm;
     sm.a = &a;
     sm.k_st = k_st;
