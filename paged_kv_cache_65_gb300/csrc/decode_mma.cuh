@@ -523,23 +523,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);
-      for (int idx = threadIdx.x; idx < NT * C::CC * D; idx += kConsumerWarps * 32) {
-        const int wni = idx / (C::CC * D);
-        const int rem = idx - wni * C::CC * D;
-        const int cc = rem / D, d = rem - cc * D;
+      // four consecutive dimensions per thread and one 16-byte store: the
+      // stores of a piece's partials compete with the stream of K/V loads
+      // for the memory system, so their count matters more than their size
+      constexpr int D4 = D / 4;
+      for (int idx = threadIdx.x; idx < NT * C::CC * D4; idx += kConsumerWarps * 32) {
+        const int wni = idx / (C::CC * D4);
+        const int rem = idx - wni * C::CC * D4;
+        const int cc = rem / D4, d = (rem - cc * D4) * 4;
         const int col = wni * 8 + pc + cc;
         if (col >= p.ncols) continue;
         float M = -INFINITY;
         for (int j = 0; j < WT; ++j) M = fmaxf(M, cmb_ml[((wni + j * NT) * 8 + pc + cc) * 2]);
-        float L = 0.f, O = 0.f;
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < WT; ++j) {
           const int w = wni + j * NT;
           const float mw = cmb_ml[(w * 8 + pc + cc) * 2];
           const float f = mw == -INFINITY ? 0.f : exp2_approx(mw - M);
           L += f * cmb_ml[(w * 8 + pc + cc) * 2 + 1];
-          O += f * cmb_o[(w * C::CC + cc) * D + d];
+          const float4 v = *reinterpret_cast<const float4*>(&cmb_o[(w * C::CC + cc) * D + d]);
+          O.x += f * v.x;
+          O.y += f * v.y;
+          O.z += f * v.z;
+          O.w += f * v.w;
         }
-        a.ws_o[(slot_id * cstride + col) * D + d] = O;
+        *reinterpret_cast<float4*>(&a.ws_o[(slot_id * cstride + col) * D + d]) = O;
         if (d == 0) {
           a.ws_ml[(slot_id * cstride + col) * 2] = M;
           a.ws_ml[(slot_id * cstride + col) * 2 + 1] = L;
