@@ -273,12 +273,13 @@ def parse_plan(buf: np.ndarray) -> dict:
     h = np.frombuffer(buf[:80].tobytes(), dtype=np.int32)
     W = int(np.frombuffer(buf[:8].tobytes(), dtype=np.int64)[0])
     (n_segs, n_members, n_entries, c_max, n_seq, n_kv_heads, group, block_size, seg_off,
-     mem_off, eoff_off, ent_off, n_shared) = (int(x) for x in h[2:15])
+     mem_off, eoff_off, ent_off, n_shared, kernel) = (int(x) for x in h[2:16])
     segs = np.frombuffer(buf[seg_off:seg_off + 40 * n_segs].tobytes(), dtype=PLAN_SEG)
     members = np.frombuffer(buf[mem_off:mem_off + 4 * n_members].tobytes(), dtype=np.int32)
     eoff = np.frombuffer(buf[eoff_off:eoff_off + 4 * (n_seq * n_kv_heads + 1)].tobytes(),
                          dtype=np.int32)
     ents = np.frombuffer(buf[ent_off:ent_off + 8 * n_entries].tobytes(), dtype=PLAN_ENTRY)
     return dict(W=W, n_segs=n_segs, c_max=c_max, n_seq=n_seq, H=n_kv_heads, G=group,
-                B=block_size, n_shared_segs=n_shared, segs=segs, members=members, eoff=eoff,
+                B=block_size, n_shared_segs=n_shared, kernel=kernel, segs=segs,
+                members=members, eoff=eoff,
                 ents=ents)
