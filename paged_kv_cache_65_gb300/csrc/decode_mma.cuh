@@ -509,6 +509,40 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     const long long slot_id = (long long)blockIdx.x + p.seg;
+    if (WT == 1) {
+      // one warp per n-tile: its state is already the piece's; each pass
+      // hands its CC columns (contiguous in the workspace) to a bulk copy
+      // instead of storing them through the registers
+      for (int pc = 0; pc < 8; pc += C::CC) {
+        const int col0 = warp * 8 + pc;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c8 = 2 * t + k;
+          if (c8 >= pc && c8 < pc + C::CC) {
+#pragma unroll
+            for (int mt = 0; mt < C::KS; ++mt) {
+              cmb_o[(warp * C::CC + c8 - pc) * D + mt * 16 + g] = o[mt][k];
+              cmb_o[(warp * C::CC + c8 - pc) * D + mt * 16 + g + 8] = o[mt][2 + k];
+            }
+            if (g == 0 && col0 + c8 - pc < p.ncols) {
+              a.ws_ml[(slot_id * cstride + col0 + c8 - pc) * 2] = m_run[k];
+              a.ws_ml[(slot_id * cstride + col0 + c8 - pc) * 2 + 1] = l_run[k];
+            }
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        const int cnt = p.ncols - col0 < C::CC ? p.ncols - col0 : C::CC;
+        if (lane == 0 && cnt > 0) {
+          bulk_store(&a.ws_o[(slot_id * cstride + col0) * D], cmb_o + warp * C::CC * D,
+                     static_cast<uint32_t>(cnt) * D * 4);
+          bulk_commit();
+          bulk_wait_read();
+        }
+        __syncwarp();
+      }
+      continue;
+    }
     for (int pc = 0; pc < 8; pc += C::CC) {
       if (pc >= p.ncols) break;  // no column of any n-tile in this pass
 #pragma unroll
@@ -557,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       named_bar_sync(1, kConsumerWarps * 32);
     }
   }
+  if (lane == 0) bulk_wait_all();  // partials handed to bulk copies have landed
 }
 
 }  // namespace pkv
