@@ -228,65 +228,92 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
 
 // Merge pass of a planned decode: per (sequence, query head) combine the
 // partials of every piece of every segment its merge entries name (shared
-// prefix and private rest), with the same rule as merge_kernel.
+// prefix and private rest), with the same rule as merge_kernel.  The plan
+// (written by the host before the stream's kernel chain started) is read
+// before waiting for the split pass; then lanes load the pieces' (m, l) side
+// by side and the O loads of all pieces are issued together, instead of a
+// chain of dependent loads per piece.
 template <int D>
 __global__ void __launch_bounds__(128) merge_plan_kernel(
     const PlanSeg* __restrict__ segs, const int32_t* __restrict__ eoff,
     const PlanEntry* __restrict__ ents, long long W, int grid, int c_max,
     const float* __restrict__ ws_ml, const float* __restrict__ ws_o, int H, int Hq,
     float* out_f32, __nv_bfloat16* out_bf16) {
-  pkv::griddep_wait();
-  pkv::griddep_launch_dependents();
   constexpr int DL = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.y * 4 + warp;
-  if (hq >= Hq) return;
+  const bool live = hq < Hq;
   const int G = Hq / H;
-  const int h = hq / G, g = hq - h * G;
+  const int h = live ? hq / G : 0, g = live ? hq - h * G : 0;
   long long chunk = (W + grid - 1) / grid;
   if (chunk == 0) chunk = 1;
-  const int e0 = eoff[s * H + h], e1 = eoff[s * H + h + 1];
-  float M = -INFINITY;
+  const int e0 = live ? eoff[s * H + h] : 0, e1 = live ? eoff[s * H + h + 1] : 0;
+  // workspace slot of the k-th piece over the entries, or -1 past the last
+  auto piece_slot = [&](int k) -> int {
+    for (int e = e0; e < e1; ++e) {
+      const PlanEntry en = ents[e];
+      const PlanSeg sg = segs[en.seg];
+      const long long units = static_cast<long long>(sg.b1 - sg.b0) * (sg.w > 0 ? sg.w : 1);
+      const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + units - 1) / chunk;
+      const int n = static_cast<int>(c1 - c0 + 1);
+      if (k < n) return static_cast<int>((c0 + k + en.seg) * c_max + en.col_base + g);
+      k -= n;
+    }
+    return -1;
+  };
+  int np = 0;
   for (int e = e0; e < e1; ++e) {
-    const PlanEntry en = ents[e];
-    const PlanSeg sg = segs[en.seg];
+    const PlanSeg sg = segs[ents[e].seg];
     const long long units = static_cast<long long>(sg.b1 - sg.b0) * (sg.w > 0 ? sg.w : 1);
-    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + units - 1) / chunk;
-    for (long long i = c0 + lane; i <= c1; i += 32)
-      M = fmaxf(M, ws_ml[((i + en.seg) * c_max + en.col_base + g) * 2]);
+    np += static_cast<int>((sg.wpre + units - 1) / chunk - sg.wpre / chunk + 1);
   }
+  const int slot0 = lane < np ? piece_slot(lane) : -1;
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
+  if (!live) return;
+  float M = -INFINITY;
+  for (int k = lane; k < np; k += 32)
+    M = fmaxf(M, ws_ml[static_cast<long long>(k < 32 ? slot0 : piece_slot(k)) * 2]);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float o[DL];
 #pragma unroll
   for (int d = 0; d < DL; ++d) o[d] = 0.f;
   float L = 0.f;
-  for (int e = e0; e < e1; ++e) {
-    const PlanEntry en = ents[e];
-    const PlanSeg sg = segs[en.seg];
-    const long long units = static_cast<long long>(sg.b1 - sg.b0) * (sg.w > 0 ? sg.w : 1);
-    const long long c0 = sg.wpre / chunk, c1 = (sg.wpre + units - 1) / chunk;
-    for (long long i = c0; i <= c1; ++i) {
-      const long long slot = (i + en.seg) * c_max + en.col_base + g;
-      const float mi = ws_ml[slot * 2];
-      if (mi == -INFINITY) continue;  // a CTA whose range held no block start of the segment
-      const float f = pkv::exp2_approx(mi - M);
-      L += f * ws_ml[slot * 2 + 1];
-      const float* src = ws_o + slot * D + lane * DL;
+  for (int r = 0; r < np; r += 32) {
+    // lane k: weight of piece r + k (0 for a CTA whose range held no block
+    // start of the segment: m = -inf, O = 0)
+    const int k = r + lane;
+    int sl = 0;
+    float f = 0.f;
+    if (k < np) {
+      sl = r == 0 ? slot0 : piece_slot(k);
+      const float mk = ws_ml[static_cast<long long>(sl) * 2];
+      f = mk == -INFINITY ? 0.f : pkv::exp2_approx(mk - M);
+      L += f * ws_ml[static_cast<long long>(sl) * 2 + 1];
+    }
+    const int nr = np - r < 32 ? np - r : 32;
+#pragma unroll 4
+    for (int j = 0; j < nr; ++j) {
+      const float fj = __shfl_sync(0xffffffffu, f, j);
+      const int sj = __shfl_sync(0xffffffffu, sl, j);
+      const float* src = ws_o + static_cast<long long>(sj) * D + lane * DL;
       if constexpr (DL == 4) {
         const float4 v = *reinterpret_cast<const float4*>(src);
-        o[0] += f * v.x;
-        o[1] += f * v.y;
-        o[2] += f * v.z;
-        o[3] += f * v.w;
+        o[0] += fj * v.x;
+        o[1] += fj * v.y;
+        o[2] += fj * v.z;
+        o[3] += fj * v.w;
       } else {
         const float2 v = *reinterpret_cast<const float2*>(src);
-        o[0] += f * v.x;
-        o[1] += f * v.y;
+        o[0] += fj * v.x;
+        o[1] += fj * v.y;
       }
     }
   }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const long long ob = ((long long)s * Hq + hq) * D + lane * DL;
 #pragma unroll
