@@ -50,7 +50,9 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # on: ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
 # (profiles/), valid while those sources hash to "sha".
 TRAFFIC = {
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615944000 + 7036672, "sha": "9590bfd7e0a0ef57"},
+    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331664640 + 3682304, "sha": "54528254954021d9"},
+    ("shared_8k", "decode_mma_kernel"): {"bytes": 170972160 + 3401984, "sha": "54528254954021d9"},
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1616037000 + 7005696, "sha": "54528254954021d9"},
 }
 
 
@@ -59,8 +61,8 @@ KERNELS = {"auto": 0, "cuda": 1, "mma": 2, "tc": 3}
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "decode_tc.cuh", "tc.cuh", "ptx.cuh", "device.cu",
-              "plan.h", "plan.cpp"):
+    for f in ("decode.cuh", "decode_mma.cuh", "decode_tc.cuh", "tc.cuh", "ptx.cuh", "plan.h",
+              "plan.cpp"):
         with open(os.path.join(ROOT, "paged_kv_cache_65_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
