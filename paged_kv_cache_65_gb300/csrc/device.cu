@@ -359,6 +359,10 @@ kvStatus check_decode_args(const kvPool* p, int layer, const void* q, int n_q_he
 
 }  // namespace
 
+kvPool::~kvPool() {
+  if (h_pinned) cudaFreeHost(h_pinned);
+}
+
 extern "C" {
 
 kvStatus kv_pool_device_status(kvPool* p, void* stream, int* out_bits) {
@@ -656,7 +660,7 @@ kvStatus paged_decode_attention_planned(kvPool* p, int layer, const void* d_q, i
 
 namespace {
 struct StepLayout {
-  size_t q, k, v, slots, pairs, table, lens, out, plan, ws, total;
+  size_t q, k, v, slots, pairs, table, lens, plan, meta_end, out, ws, total;
 };
 
 StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks) {
@@ -677,10 +681,11 @@ StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks
   off += align256(n * static_cast<size_t>(max_blocks) * sizeof(int32_t));
   l.lens = off;
   off += align256(n * sizeof(int32_t));
-  l.out = off;
-  off += align256(L * n * n_q_heads * p->D * sizeof(float));
   l.plan = off;
   off += align256(paged_decode_plan_bytes(p, n_seq, n_q_heads));
+  l.meta_end = off;  // slots .. plan: the metadata moved by one copy
+  l.out = off;
+  off += align256(L * n * n_q_heads * p->D * sizeof(float));
   l.ws = off;
   const size_t ws_plain = ws_layout(p, n_seq, n_q_heads / p->H).total;
   const size_t ws_plan = plan_workspace_bytes(2 * n_seq * p->H, kPlanMaxCols, p->D);
@@ -713,17 +718,41 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   }
   kvStatus s = ensure_device(p);
   if (s != KV_OK) return s;
-  // host: reserve (all or nothing)
-  p->h_slots.resize(n_seq);
-  p->h_pairs.resize(2 * static_cast<size_t>(n_seq));
+  // page-locked host staging of the metadata (slots .. plan)
+  const size_t meta = l.meta_end - l.slots;
+  if (p->h_pinned_bytes < meta) {
+    if (p->h_pinned) cudaFreeHost(p->h_pinned);
+    p->h_pinned = nullptr;
+    p->h_pinned_bytes = 0;
+    void* h = nullptr;
+    if (cudaMallocHost(&h, meta) != cudaSuccess) return KV_ERR_CUDA;
+    p->h_pinned = static_cast<unsigned char*>(h);
+    p->h_pinned_bytes = meta;
+  }
+  unsigned char* hm = p->h_pinned - l.slots;  // hm + l.x: host copy of region x
+  int64_t* h_slots = reinterpret_cast<int64_t*>(hm + l.slots);
+  int32_t* h_pairs = reinterpret_cast<int32_t*>(hm + l.pairs);
+  int32_t* h_table = reinterpret_cast<int32_t*>(hm + l.table);
+  int32_t* h_lens = reinterpret_cast<int32_t*>(hm + l.lens);
+  unsigned char* h_plan = hm + l.plan;
+  // host: reserve (all or nothing), tables, and the sharing-aware plan of
+  // the tensor-core passes (shared blocks read once)
   int n_cow = 0;
-  s = seq_append_slots(p, seq_ids, n_seq, p->h_slots.data(), p->h_pairs.data(), &n_cow);
+  s = seq_append_slots(p, seq_ids, n_seq, h_slots, h_pairs, &n_cow);
   if (s != KV_OK) return s;
-  p->h_table.resize(static_cast<size_t>(n_seq) * max_blocks);
-  p->h_lens.resize(n_seq);
-  s = seq_block_table(p, seq_ids, n_seq, max_blocks, p->h_table.data(), p->h_lens.data());
+  s = seq_block_table(p, seq_ids, n_seq, max_blocks, h_table, h_lens);
   if (s != KV_OK) return s;
-  // host -> device
+  const int G = n_q_heads / p->H;
+  const bool planned = decode_kernel(p) != kKernelCudaCores && ilog2_small(G) >= 0 &&
+                       (p->D == 64 || p->D == 128);
+  if (planned) {
+    size_t ws_need = 0;
+    s = paged_decode_plan(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, h_plan,
+                          paged_decode_plan_bytes(p, n_seq, n_q_heads), &ws_need);
+    if (s != KV_OK) return s;
+  }
+  // host -> device: q, new K and V from the caller's buffers, the metadata
+  // in one copy
   cudaStream_t st = as_stream(stream);
   unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
   const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->esize;
@@ -733,30 +762,9 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
   ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
   ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.slots, p->h_slots.data(), n_seq * sizeof(int64_t),
-                        cudaMemcpyHostToDevice, st) == cudaSuccess;
-  if (n_cow)
-    ok &= cudaMemcpyAsync(d + l.pairs, p->h_pairs.data(), 2 * n_cow * sizeof(int32_t),
-                          cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.table, p->h_table.data(), p->h_table.size() * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.lens, p->h_lens.data(), n_seq * sizeof(int32_t),
+  ok &= cudaMemcpyAsync(d + l.slots, p->h_pinned, (planned ? l.meta_end : l.plan) - l.slots,
                         cudaMemcpyHostToDevice, st) == cudaSuccess;
   if (!ok) return KV_ERR_CUDA;
-  // sharing-aware plan on the tensor-core path (shared blocks read once)
-  const int G = n_q_heads / p->H;
-  const bool planned = decode_kernel(p) != kKernelCudaCores && ilog2_small(G) >= 0 &&
-                       (p->D == 64 || p->D == 128);
-  if (planned) {
-    p->h_plan.resize(paged_decode_plan_bytes(p, n_seq, n_q_heads));
-    size_t ws_need = 0;
-    s = paged_decode_plan(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, p->h_plan.data(),
-                          p->h_plan.size(), &ws_need);
-    if (s != KV_OK) return s;
-    if (cudaMemcpyAsync(d + l.plan, p->h_plan.data(), p->h_plan.size(), cudaMemcpyHostToDevice,
-                        st) != cudaSuccess)
-      return KV_ERR_CUDA;
-  }
   // device: copy shared tails, write the new token in every layer, attend
   s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
   if (s != KV_OK) return s;
@@ -768,8 +776,8 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
     if (planned)
       s = paged_decode_attention_planned(
           p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
-          reinterpret_cast<const int32_t*>(d + l.table), max_blocks, d + l.plan,
-          p->h_plan.data(), scale, d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
+          reinterpret_cast<const int32_t*>(d + l.table), max_blocks, d + l.plan, h_plan, scale,
+          d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
           d + l.ws, staging_bytes - l.ws, stream);
     else
       s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,

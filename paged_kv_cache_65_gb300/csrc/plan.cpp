@@ -24,6 +24,16 @@ namespace {
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// Length of the common prefix of a[0, n) and b[0, n): 64 entries at a time
+// with memcmp, then entry by entry.
+int common_prefix(const int32_t* a, const int32_t* b, int n) {
+  constexpr int kRun = 64;
+  int j = 0;
+  while (j + kRun <= n && std::memcmp(a + j, b + j, kRun * sizeof(int32_t)) == 0) j += kRun;
+  while (j < n && a[j] == b[j]) ++j;
+  return j;
+}
+
 struct Layout {
   size_t seg, mem, eoff, ent, total;
 };
@@ -103,14 +113,12 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
       if (c1 - c0 < 2) break;
       std::vector<int> mem(order.begin() + c0, order.begin() + c1);
       std::sort(mem.begin(), mem.end());
-      int P = static_cast<int>(seqs[mem[0]]->table.size());
-      for (int m : mem) {
-        const std::vector<int32_t>& t0 = seqs[mem[0]]->table;
-        const std::vector<int32_t>& t = seqs[m]->table;
-        int j = 0;
-        while (j < P && j < static_cast<int>(t.size()) && t[j] == t0[j]) ++j;
-        P = j;
-        P = std::min<int64_t>(P, seqs[m]->len / B);  // whole blocks inside every context
+      const std::vector<int32_t>& t0 = seqs[mem[0]]->table;
+      int P = static_cast<int>(std::min<int64_t>(t0.size(), seqs[mem[0]]->len / B));
+      for (size_t k = 1; k < mem.size() && P > 0; ++k) {
+        const std::vector<int32_t>& t = seqs[mem[k]]->table;
+        P = common_prefix(t0.data(), t.data(), std::min<int>(P, static_cast<int>(t.size())));
+        P = static_cast<int>(std::min<int64_t>(P, seqs[mem[k]]->len / B));  // whole blocks in every context
       }
       if (static_cast<int64_t>(P) * B < min_shared_tokens) continue;
       for (size_t k = 0; k < mem.size(); ++k) {
@@ -133,7 +141,12 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   // units, and every piece has a fixed cost).
   std::vector<PlanSeg> segs;
   std::vector<int32_t> members;
-  std::vector<std::vector<PlanEntry>> ents(static_cast<size_t>(n_seq) * H);
+  segs.reserve(2 * static_cast<size_t>(n_seq) * H);
+  members.reserve(2 * static_cast<size_t>(n_seq));
+  // merge entries per (sequence, head): at most a shared segment and a private rest
+  std::vector<PlanEntry> ent2(2 * static_cast<size_t>(n_seq) * H);
+  std::vector<uint8_t> n_ent(static_cast<size_t>(n_seq) * H, 0);
+  auto add_entry = [&](size_t sh, PlanEntry e) { ent2[2 * sh + n_ent[sh]++] = e; };
   int c_max = G;
   std::vector<int> priv_mem(n_seq, -1);  // member-list slot of a sequence's private rest
   auto private_member = [&](int i) {
@@ -156,7 +169,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     s.mem = private_member(i);
     const int si = static_cast<int>(segs.size());
     segs.push_back(s);
-    ents[static_cast<size_t>(i) * H + h].push_back({si, 0});
+    add_entry(static_cast<size_t>(i) * H + h, {si, 0});
   };
   std::vector<char> grouped(n_seq, 0);
   for (const auto& ch : chunks)
@@ -179,7 +192,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     s.mem = group_mem0[c];
     const int si = static_cast<int>(segs.size());
     segs.push_back(s);
-    for (int m : chunks[c]) ents[static_cast<size_t>(m) * H + h].push_back({si, pos_in[m] * G});
+    for (int m : chunks[c]) add_entry(static_cast<size_t>(m) * H + h, {si, pos_in[m] * G});
     for (int m : chunks[c]) push_private(m, h);
   };
   std::vector<int> ungrouped;
@@ -219,7 +232,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     W += static_cast<int64_t>(s.b1 - s.b0) * s.w;
   }
   int n_entries = 0;
-  for (const auto& e : ents) n_entries += static_cast<int>(e.size());
+  for (uint8_t c : n_ent) n_entries += c;
 
   // ---- serialise
   const Layout l = plan_layout(n_seq, H, static_cast<int>(segs.size()),
@@ -249,11 +262,11 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   int32_t* eoff = reinterpret_cast<int32_t*>(out + l.eoff);
   PlanEntry* ent = reinterpret_cast<PlanEntry*>(out + l.ent);
   int k = 0;
-  for (size_t i = 0; i < ents.size(); ++i) {
+  for (size_t i = 0; i < n_ent.size(); ++i) {
     eoff[i] = k;
-    for (const PlanEntry& e : ents[i]) ent[k++] = e;
+    for (int j = 0; j < n_ent[i]; ++j) ent[k++] = ent2[2 * i + j];
   }
-  eoff[ents.size()] = k;
+  eoff[n_ent.size()] = k;
   if (out_workspace_bytes) *out_workspace_bytes = plan_workspace_bytes(hd.n_segs, c_max, p->D);
   return KV_OK;
 }

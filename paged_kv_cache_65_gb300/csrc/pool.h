@@ -39,10 +39,13 @@ struct kvPool {
   int decode_path = 0;                      // KV_OPT_DECODE_PATH
   bool pdl = true;                          // programmatic dependent launch
 
-  // host staging reused by kv_decode_step_host
-  std::vector<int64_t> h_slots;
-  std::vector<int32_t> h_pairs, h_table, h_lens;
-  std::vector<unsigned char> h_plan;
+  // host staging of kv_decode_step_host: the step's metadata (slots, copy
+  // pairs, tables, lengths, plan) in page-locked memory, laid out as in the
+  // device staging buffer so that one copy moves it
+  unsigned char* h_pinned = nullptr;
+  size_t h_pinned_bytes = 0;
+
+  ~kvPool();
 };
 
 // Tensor-core passes read K/V through 128-byte-swizzled TMA boxes of 64
