@@ -12,6 +12,7 @@ from __future__ import annotations
 import numpy as np
 
 from .attention import decode_attention
+from .prefill import prefill_attention
 from .block_manager import BlockManager
 from .kv_store import KVStore, to_f64
 
@@ -80,3 +81,38 @@ class OracleRun:
         q = self.write_step(step, slots, cows)
         outs = [self.attend(layer, q) for layer in range(self.wl.n_layers)]
         return slots, cows, q, outs
+
+    # ------------------------------------------------------------ prefill
+    def prefill_step(self, step: int = 0):
+        """Host part and writes of a chunked-prefill round: each chunk's
+        slots are reserved and its K/V written (the pages compute the chunk's
+        keys and values fresh and store them; written first and read back
+        they are the same numbers).  Returns ``(slots per chunk, copy
+        pairs, q)``."""
+        q, k, v = self.wl.chunk_values(step)
+        all_slots, all_cows, t = [], [], 0
+        for seq, c in self.wl.chunks:
+            slots, cows = self.bm.append_tokens(seq, c)
+            for src, dst in cows:
+                self.st.copy_block(src, dst)
+            for layer in range(self.wl.n_layers):
+                self.st.reshape_and_cache(layer, k[layer, t:t + c], v[layer, t:t + c], slots)
+            all_slots.append(slots)
+            all_cows.extend(cows)
+            t += c
+        return all_slots, all_cows, q
+
+    def prefill_attend(self, layer: int, q, chunk_index=None):
+        """Chunked-prefill attention of the listed chunks (default: all):
+        ``{chunk index: out [c, H_q, D_h]}``."""
+        offs = np.cumsum([0] + [c for _, c in self.wl.chunks])
+        idx = range(len(self.wl.chunks)) if chunk_index is None else chunk_index
+        qf = to_f64(q, self.wl.dtype)
+        res = {}
+        for i in idx:
+            seq, c = self.wl.chunks[i]
+            n = self.bm.lengths[seq]
+            K, V = self.st.gather(layer, self.bm.tables[seq], n)
+            res[i] = prefill_attention(qf[offs[i]:offs[i] + c], K, V)
+        return res
+

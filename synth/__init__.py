@@ -17,6 +17,7 @@ from __future__ import annotations
 
 from .workloads import (  # noqa: F401
     WORKLOADS,
+    PrefillWorkload,
     Workload,
     normal_f32,
     storage_values,

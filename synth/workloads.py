@@ -23,6 +23,17 @@ Recipes follow the decode workloads the pages measure or size:
                    the first 32 (25 %) share a 6144-token prefix; B from
                    {8, 16, 32}; the pool holds the build plus 10 % headroom.
 
+Chunked-prefill rounds ("KV 缓存管理", chunked-prefill section; "第 8 章 推理优化"
+§8.2.3: chunks of 256 to 1024 tokens, a round budget of 4096 tokens):
+
+* ``prefill_tiny`` -- 1 layer, H_q = 8, H_kv = 2, D_h = 128, bf16, B = 16:
+                   chunks of 45, 130 and 1 tokens after histories of 0, 37
+                   and 200 tokens.
+* ``prefill_4k``   -- one Qwen3-8B-shaped layer; 8 prompts of 8192 tokens in
+                   512-token chunks, one chunk each in this round: chunks
+                   1, 2, 4, 6, 8, 10, 12 and 16 (histories 0 to 7680), 4096
+                   query tokens in all.
+
 Context lengths named above are the lengths after the first decode step
 (the step writes its token first, then attends over every position up to
 and including it).
@@ -125,6 +136,43 @@ class Workload:
         return q, np.ascontiguousarray(kv[:, :, 0]), np.ascontiguousarray(kv[:, :, 1])
 
 
+@dataclass
+class PrefillWorkload(Workload):
+    """A chunked-prefill round: after the build operations, each
+    ``(seq, c)`` of ``chunks`` appends a chunk of ``c`` tokens and attends
+    its ``c`` queries over the sequence's whole context."""
+    chunks: list = field(default_factory=list)
+
+    def chunk_values(self, step: int):
+        """q ``[n_tok, H_q, D_h]`` (the chunks in order, each chunk's tokens
+        in order) and the chunks' K, V ``[n_layers, n_tok, H_kv, D_h]``, as
+        stored elements."""
+        n = sum(c for _, c in self.chunks)
+        q = normal_f32((self.seed, 5, step), (n, self.n_q_heads, self.head_dim))
+        kv = normal_f32((self.seed, 6, step),
+                        (self.n_layers, n, 2, self.n_kv_heads, self.head_dim))
+        q = storage_values(q, self.dtype)
+        kv = storage_values(kv, self.dtype)
+        return q, np.ascontiguousarray(kv[:, :, 0]), np.ascontiguousarray(kv[:, :, 1])
+
+
+def _prefill(name, seed, n_q, n_kv, hist, chunk, n_blocks):
+    ops = [("append", s, h, s) for s, h in enumerate(hist) if h > 0]
+    chunks = [(s, c) for s, c in enumerate(chunk)]
+    return PrefillWorkload(name, 1, n_blocks, 16, n_q, n_kv, 128, "bf16", seed,
+                           permutation((seed, 0), n_blocks), ops, list(range(len(hist))),
+                           f"chunks {list(chunk)} after histories {list(hist)}", chunks)
+
+
+def _prefill_tiny(seed: int = 6) -> Workload:
+    return _prefill("prefill_tiny", seed, 8, 2, [0, 37, 200], [45, 130, 1], 64)
+
+
+def _prefill_4k(seed: int = 7) -> Workload:
+    hist = [512 * k for k in (0, 1, 3, 5, 7, 9, 11, 15)]
+    return _prefill("prefill_4k", seed, 32, 8, hist, [512] * 8, 2048)
+
+
 def _tiny(seed: int = 0) -> Workload:
     ctx = [7, 13, 1, 16]
     ops = []
@@ -213,6 +261,8 @@ WORKLOADS = {
     "shared_8k": _shared_8k,
     "gqa70b_32k": _gqa70b_32k,
     "pool36": _pool36,
+    "prefill_tiny": _prefill_tiny,
+    "prefill_4k": _prefill_4k,
 }
 
 
