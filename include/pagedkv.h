@@ -1,6 +1,7 @@
 /*
  * pagedkv.h -- C ABI of a GB300 (sm_103a) paged KV cache: block manager,
- * slot write, copy-on-write block copy and split-K decode attention.
+ * slot write, copy-on-write block copy, split-K decode attention and
+ * chunked-prefill attention.
  *
  * Pages followed (cited by title and section):
  *   [BT] "KV Cache 还有空间为何新请求却进不来？PagedAttention 的块表与碎片控制"
@@ -8,7 +9,7 @@
  *   [KC] "KV 缓存管理" (gptbert.com, mlsys vol. 3), sections "PagedAttention
  *        虚拟内存模型" and "通过写时复制分支实现零复制审慎推理", and the
  *        chunked-prefill section (online-softmax merge).
- *   [IO] "第 8 章 推理优化" (bojieli.github.io), sections 8.3.1-8.3.2.
+ *   [IO] "第 8 章 推理优化" (bojieli.github.io), sections 8.2.3 and 8.3.1-8.3.2.
  *
  * Layout ([BT] §06):
  *   K_cache, V_cache : [N_layers][N_blocks][B][H_kv][D_h], row-major, dtype
@@ -268,6 +269,33 @@ kvStatus paged_decode_attention_noalloc(kvPool* pool, int layer, const void* d_q
                                         const int32_t* d_block_table, int max_blocks,
                                         const int32_t* d_context_lens, int n_seq, float scale,
                                         void* d_out, int out_dtype, void* stream);
+
+/* ------------------------------------------------- chunked prefill --
+ * Attention of prompt chunks over the paged cache ([KC] chunked-prefill
+ * section; [IO] §8.2.3).  For each listed sequence s, the chunk's queries
+ * are rows d_chunk_start[s] .. d_chunk_start[s + 1] - 1 of d_q; the chunk's
+ * K and V must already be in the pool (reserve the chunk with
+ * seq_append_tokens, write it with reshape_and_cache), as the last
+ * c = d_chunk_start[s + 1] - d_chunk_start[s] of d_context_lens[s] positions.
+ * The chunk's token i (position h + i, h = context - c) attends to positions
+ * 0 .. h + i: the whole history and the chunk up to its own token.
+ *   d_q          : [n_tok][n_q_heads][D_h] bfloat16, 16-byte aligned
+ *   d_block_table: [n_seq][max_blocks] int32
+ *   d_chunk_start: [n_seq + 1] int32, non-decreasing query-row offsets
+ *   d_context_lens: [n_seq] int32, context after the chunk
+ *   max_chunk    : an upper bound on every chunk's length (sizes the grid; a
+ *                  longer chunk, or a chunk longer than its context, is
+ *                  skipped and flagged KV_DEV_BAD_CONTEXT)
+ *   d_out        : [n_tok][n_q_heads][D_h] float32 or bfloat16 (out_dtype)
+ * Runs on the tcgen05 tensor cores: bfloat16 pools with D_h = 128 and B a
+ * multiple of 8 (whole 64-row boxes), H_q / H_kv in {1, 2, 4, 8}; other
+ * pools get KV_ERR_UNSUPPORTED.  Allocates nothing; enqueues one kernel on
+ * `stream`. */
+kvStatus paged_prefill_attention(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                 const int32_t* d_block_table, int max_blocks,
+                                 const int32_t* d_chunk_start, const int32_t* d_context_lens,
+                                 int n_seq, int max_chunk, float scale, void* d_out,
+                                 int out_dtype, void* stream);
 
 /* --------------------------------------------------- whole decode step --
  * One decode step through host buffers ([BT] §10 order): reserve a slot per

@@ -88,6 +88,8 @@ SIGNATURES = [
                                                  _vp]),
     ("paged_decode_attention_noalloc", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
                                                  C.c_int, C.c_float, _vp, C.c_int, _vp]),
+    ("paged_prefill_attention", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, _vp,
+                                          C.c_int, C.c_int, C.c_float, _vp, C.c_int, _vp]),
     ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
     ("kv_decode_step_host", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
                                       C.c_float, _f32p, _vp, C.c_size_t, _vp]),

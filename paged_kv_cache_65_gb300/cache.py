@@ -226,6 +226,18 @@ class PagedKVCache:
                                                  _out_dtype(out), _stream(stream)),
               "paged_decode_attention_noalloc")
 
+    def paged_prefill_attention(self, layer, q, n_q_heads, d_table, max_blocks, d_chunk_start,
+                                d_context_lens, n_seq, max_chunk, out, scale=0.0, stream=None):
+        """Chunked-prefill attention of each sequence's chunk (rows
+        ``d_chunk_start[s] .. d_chunk_start[s + 1] - 1`` of ``q``) over its
+        paged context; the chunks' K/V must already be in the pool."""
+        check(lib.paged_prefill_attention(self.handle, int(layer), vp(q), int(n_q_heads),
+                                          vp(d_table), int(max_blocks), vp(d_chunk_start),
+                                          vp(d_context_lens), int(n_seq), int(max_chunk),
+                                          float(scale), vp(out), _out_dtype(out),
+                                          _stream(stream)),
+              "paged_prefill_attention")
+
     def kv_decode_step_staging_bytes(self, n_seq, n_q_heads, max_blocks):
         return int(lib.kv_decode_step_staging_bytes(self.handle, int(n_seq), int(n_q_heads),
                                                     int(max_blocks)))

@@ -243,26 +243,28 @@ __device__ inline void write_prefix(const int32_t* ctx, int n_seq, int B, int H,
 // (kTableCache / 32 independent loads per lane, one round trip) instead of
 // paying a dependent global load before every TMA issue.
 
-struct TableCache {
-  int32_t* ent;  // shared, kTableCache entries
+template <int N>
+struct TableCacheN {
+  int32_t* ent;  // shared, N entries
   int seq = -1;
   int base = 0;
 
   // Make blocks [jf, jl] of `seq` available; whole warp calls.
   __device__ void ensure(const int32_t* table, int max_blocks, int s, int jf, int jl, int lane) {
-    if (s == seq && jf >= base && jl < base + kTableCache) return;
+    if (s == seq && jf >= base && jl < base + N) return;
     __syncwarp();
     seq = s;
     base = jf;
     const int32_t* row = table + (long long)s * max_blocks;
 #pragma unroll
-    for (int i = 0; i < kTableCache / 32; ++i) {
+    for (int i = 0; i < N / 32; ++i) {
       const int j = base + i * 32 + lane;
       ent[i * 32 + lane] = j < max_blocks ? row[j] : 0;
     }
     __syncwarp();
   }
 };
+using TableCache = TableCacheN<kTableCache>;
 
 // Iterates the pieces of [r0, r1) in segment order.
 struct PieceWalker {

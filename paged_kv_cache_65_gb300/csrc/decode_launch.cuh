@@ -62,6 +62,11 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs 
                        a);
 }
 
+struct PrefillArgs;
+// tcgen05 chunked-prefill attention: one CTA per (sequence, K/V head, 128 query rows).
+cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
+                              int max_chunk, cudaStream_t st, bool pdl);
+
 // tcgen05 variant (bfloat16, D_h = 128, the swizzled TMA maps); one CTA per SM.
 cudaError_t launch_tc_bf16(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                            int sm_count, int max_grid, int* grid_io, cudaStream_t st, bool pdl);

@@ -147,3 +147,43 @@ class DeviceRun:
             else:
                 outs.append(self.attend(layer, ql, d_table, mb, d_lens, len(seq_ids)))
         return slots, pairs, torch.stack(outs)
+
+    def prefill_step(self, chunks, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
+                     out_dtype=None, max_chunk=None):
+        """A chunked-prefill round: for each ``(seq, c)`` of ``chunks`` reserve
+        ``c`` slots, copy any shared tail, write the chunk's K/V (all layers),
+        then attend the chunk's queries over the sequence's context.  ``q``
+        ``[n_tok, H_q, D_h]`` (chunks in order), ``k_new, v_new [L, n_tok,
+        H_kv, D_h]``.  Returns the outputs ``[L, n_tok, H_q, D_h]``."""
+        import torch
+
+        c = self.c
+        seqs = [s for s, _ in chunks]
+        t = 0
+        for seq, n in chunks:
+            if n:
+                slots, pairs = c.seq_append_tokens(seq, n)
+                if len(pairs):
+                    d_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).to(self.dev)
+                    c.cow_copy(d_pairs, len(pairs), self.stream)
+                dk = to_device(np.ascontiguousarray(k_new[:, t:t + n]), c.dtype, self.dev)
+                dv = to_device(np.ascontiguousarray(v_new[:, t:t + n]), c.dtype, self.dev)
+                c.reshape_and_cache(-1, dk, dv, torch.from_numpy(slots).to(self.dev), n,
+                                    self.stream)
+            self.lengths[seq] = self.lengths.get(seq, 0) + n
+            t += n
+        d_table, d_lens, mb = self.tables(seqs)
+        starts = np.zeros(len(chunks) + 1, dtype=np.int32)
+        starts[1:] = np.cumsum([n for _, n in chunks])
+        d_starts = torch.from_numpy(starts).to(self.dev)
+        qd = to_device(q, c.dtype, self.dev)
+        dt = out_dtype or torch.float32
+        mc = max_chunk if max_chunk is not None else max([n for _, n in chunks] + [0])
+        outs = []
+        for layer in range(c.L):
+            out = torch.zeros((int(starts[-1]), self.n_q_heads, c.D), dtype=dt, device=self.dev)
+            c.paged_prefill_attention(layer, qd, self.n_q_heads, d_table, mb, d_starts, d_lens,
+                                      len(chunks), mc, out, 0.0, self.stream)
+            outs.append(out)
+        return torch.stack(outs)
+

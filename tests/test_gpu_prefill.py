@@ -1,0 +1,121 @@
+"""GPU parity of the chunked-prefill attention (through the C ABI) with the
+oracle on the same seeded inputs: bfloat16 K/V, float32 accumulation,
+max-abs error within 2e-3."""
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.runner import OracleRun
+
+torch = pytest.importorskip("torch")
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+TOL = 2e-3
+
+
+def make(wl, fill_nan=False):
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
+                         wl.dtype, free_order=wl.free_order)
+    if fill_nan:
+        cache.k.fill_(float("nan"))
+        cache.v.fill_(float("nan"))
+    else:
+        cache.k.zero_()
+        cache.v.zero_()
+    run = DeviceRun(cache, wl.n_q_heads)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    return cache, run
+
+
+def check_against_oracle(wl, fill_nan=False, chunk_index=None, out_dtype=None):
+    """Largest error of the chunks' outputs against the oracle.  With bf16
+    outputs the error is taken after removing half a bf16 ulp of the exact
+    value (2^-8 relative): a row that sees few keys can have |out| ~ 4."""
+    orc = OracleRun(wl)
+    cache, run = make(wl, fill_nan)
+    _, _, q = orc.prefill_step(0)
+    q2, k, v = wl.chunk_values(0)
+    assert np.array_equal(q, q2)
+    og = run.prefill_step(wl.chunks, q, k, v, out_dtype=out_dtype)
+    got = og.float().cpu().numpy()[0]
+    ref = orc.prefill_attend(0, q, chunk_index)
+    offs = np.cumsum([0] + [c for _, c in wl.chunks])
+    worst = 0.0
+    for i, r in ref.items():
+        g = got[offs[i]:offs[i] + wl.chunks[i][1]]
+        assert np.isfinite(g).all()
+        err = np.abs(g - r)
+        if out_dtype is not None:
+            err = np.maximum(err - 2.0 ** -8 * np.abs(r), 0.0)
+        worst = max(worst, float(np.max(err)) if r.size else 0.0)
+    assert cache.kv_pool_device_status() == 0
+    return worst
+
+
+def test_prefill_tiny_all_rows():
+    assert check_against_oracle(synth.workload("prefill_tiny")) <= TOL
+
+
+def test_prefill_4k_round_against_oracle():
+    # 8 chunks of 512 tokens after histories 0 .. 7680 (4096 query rows)
+    assert check_against_oracle(synth.workload("prefill_4k"), chunk_index=[0, 3, 7]) <= TOL
+
+
+def ragged(G, B, hist, chunks, seed):
+    n_blocks = sum(-(-(h + c) // B) for h, c in zip(hist, chunks)) + len(hist) + 4
+    ops = [("append", s, h, s) for s, h in enumerate(hist) if h > 0]
+    return synth.PrefillWorkload("ragged_prefill", 1, n_blocks, B, 2 * G, 2, 128, "bf16", seed,
+                                 synth.permutation((seed, 1), n_blocks), ops,
+                                 list(range(len(hist))), "", list(enumerate(chunks)))
+
+
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (4, 32), (8, 64), (4, 16)])
+def test_prefill_ragged_shapes(G, B):
+    hist = [0, 5, 130, 1000, 17]
+    chunks = [1, 17, 300, 64, 129]
+    assert check_against_oracle(ragged(G, B, hist, chunks, seed=G * 100 + B)) <= TOL
+
+
+def test_prefill_unused_slots_holding_nan_do_not_leak():
+    wl = ragged(4, 16, [3, 0, 40], [9, 33, 100], seed=7)
+    assert check_against_oracle(wl, fill_nan=True) <= TOL
+
+
+def test_prefill_bf16_output():
+    wl = ragged(4, 16, [0, 200], [70, 31], seed=8)
+    assert check_against_oracle(wl, out_dtype=torch.bfloat16) <= TOL
+
+
+def test_prefill_in_chunks_equals_one_pass():
+    # "KV 缓存管理": chunked prefill is equivalent to one pass; on the device
+    # a 300-token prompt in chunks of 128 matches the same prompt at once
+    from paged_kv_cache_65_gb300.driver import to_host_bits  # noqa: F401
+
+    G, B, S = 4, 16, 300
+    wl1 = ragged(G, B, [0], [S], seed=11)
+    q, k, v = wl1.chunk_values(0)
+    cache, run = make(wl1)
+    whole = run.prefill_step([(0, S)], q, k, v).cpu().numpy()[0]
+    cache2, run2 = make(wl1)
+    parts = []
+    for a in range(0, S, 128):
+        b = min(S, a + 128)
+        parts.append(run2.prefill_step([(0, b - a)], q[a:b], k[:, a:b], v[:, a:b]).cpu().numpy()[0])
+    assert float(np.max(np.abs(np.concatenate(parts) - whole))) <= 1e-3
+
+
+def test_prefill_chunk_longer_than_max_chunk_is_flagged():
+    wl = ragged(4, 16, [0], [200], seed=12)
+    cache, run = make(wl)
+    q, k, v = wl.chunk_values(0)
+    run.prefill_step(wl.chunks, q, k, v, max_chunk=100)
+    assert cache.kv_pool_device_status() & 16
+    assert cache.kv_pool_device_status() == 0
