@@ -533,6 +533,208 @@ def bench_e2e(args, wl, cache, run, dev, world):
             "ms_per_step": round(max_s / steps * 1e3, 4), "api": "kv_decode_step_host"}
 
 
+# ------------------------------------------------------ chunked prefill
+PREFILL_METRIC = ("chunked-prefill attention TFLOP/s (% of GB300 bf16 tensor peak) and "
+                  "prefill tokens/s")
+
+
+def read_tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_flops(wl) -> float:
+    """Algorithmic flops of a round: per admitted (query, key) pair and query
+    head, 2 D for the score and 2 D for the weighted value; a chunk of c
+    tokens after h admits c h + c (c + 1) / 2 pairs ("第 8 章 推理优化"
+    §8.2.3)."""
+    pairs = 0
+    for seq, c in wl.chunks:
+        h = wl.history[seq]
+        pairs += c * h + c * (c + 1) // 2
+    return 4.0 * wl.head_dim * wl.n_q_heads * pairs
+
+
+def bench_prefill(args):
+    """Time chunked-prefill rounds: each step rewrites the chunks' K/V into
+    their slots (reserved once, before timing) and runs the prefill
+    attention of every chunk over its paged context, replayed as one CUDA
+    graph with L2 flushed between steps."""
+    import torch
+
+    rank, local, world = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl, cache, run = setup(args.workload, device=dev)
+    cache.kv_pool_set_option(_lib_mod().KV_OPT_PDL, 0 if args.no_pdl else 1)
+    wl.history = {s: run.lengths.get(s, 0) for s, _ in wl.chunks}
+    seqs = [s for s, _ in wl.chunks]
+    slot_list = []
+    for seq, c in wl.chunks:
+        slots, pairs = cache.seq_append_tokens(seq, c)
+        assert len(pairs) == 0
+        run.lengths[seq] = run.lengths.get(seq, 0) + c
+        slot_list.append(slots)
+    n_tok = sum(c for _, c in wl.chunks)
+    d_slots = torch.from_numpy(np.concatenate(slot_list)).to(dev)
+    d_table, d_lens, mb = run.tables(seqs)
+    starts = np.zeros(len(seqs) + 1, dtype=np.int32)
+    starts[1:] = np.cumsum([c for _, c in wl.chunks])
+    d_starts = torch.from_numpy(starts).to(dev)
+    max_chunk = max(c for _, c in wl.chunks)
+    g = torch.Generator(device=dev)
+    g.manual_seed(synth.torch_seed((wl.seed, 8)))
+    q = torch.randn((n_tok, wl.n_q_heads, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((wl.n_layers, n_tok, wl.n_kv_heads, wl.head_dim), generator=g,
+                    device=dev).to(torch.bfloat16)
+    v = torch.randn_like(k)
+    out = torch.empty((n_tok, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def attend(s):
+        for layer in range(wl.n_layers):
+            cache.paged_prefill_attention(layer, q, wl.n_q_heads, d_table, mb, d_starts, d_lens,
+                                          len(seqs), max_chunk, out, 0.0, s.cuda_stream)
+
+    def step(s):
+        cache.reshape_and_cache(-1, k, v, d_slots, n_tok, s.cuda_stream)
+        attend(s)
+
+    graphs = {}
+    for name, fn in (("step", step), ("attn", attend)):
+        with torch.cuda.stream(stream):
+            fn(stream)  # warm (module load, attributes)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn(stream)
+        graphs[name] = gr
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    clk = ClockSampler(local)
+    clk.start()
+
+    def timed(gr, n):
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                flush_r.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    timed(graphs["step"], args.warmup)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_ms = timed(graphs["step"], args.steps)
+    t1 = time.perf_counter()
+    attn_ms = timed(graphs["attn"], min(args.steps, 200))
+    clocks = clk.stop(t0, t1)
+    assert cache.kv_pool_device_status() == 0
+    flops = prefill_flops(wl) * wl.n_layers
+    ms = float(np.mean(step_ms))
+    tot_f, max_s = aggregate(flops * args.steps, ms * args.steps / 1e3, world, dev)
+    value = tot_f / max_s / 1e12
+    attn_s = float(np.mean(attn_ms)) / 1e3
+    peak, peak_kind = read_tensor_peak()
+    achieved = flops / attn_s / 1e12
+    traffic = TRAFFIC.get((args.workload, "prefill_tc_kernel"))
+    traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha() else None
+    e2e = bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
+                            max_chunk, n_tok, flops, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded N(0,1) pool, q and chunk K/V; torch device generator)",
+            "config": {"workload": args.workload, "n_layers": wl.n_layers,
+                       "chunks": [c for _, c in wl.chunks],
+                       "histories": [wl.history[s] for s in seqs], "kernel": "prefill_tc_kernel",
+                       "pdl": not args.no_pdl, "block_size": wl.block_size,
+                       "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads, "D_h": wl.head_dim,
+                       "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_tensor_peak": round(100 * value / peak, 2),
+            "prefill_tokens_per_s": round(n_tok * world / (ms / 1e3), 1),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic_v, "kernel": "prefill_tc_kernel",
+                         "peak_source": peak_kind,
+                         "timing": "CUDA events around a graph holding the attention launches",
+                         "alg_flops_per_launch": int(flops / wl.n_layers),
+                         "mean_launch_us": round(attn_s * 1e6 / wl.n_layers, 2),
+                         "note": "the weights go through the tensor core twice (bf16 high part "
+                                 "and remainder), so the P.V half of the flops runs twice"},
+            "gpu_launches": 1 + wl.n_layers,
+            "graphs": "one CUDA graph per step, replayed",
+            "e2e": e2e, "clocks": clocks,
+            "wall_s_timed": round(t1 - t0, 4),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
+                      max_chunk, n_tok, flops, world):
+    """The same round through the public calls with page-locked host buffers:
+    host -> device copies of q and the chunks' K/V, the slot write and the
+    attention, the device -> host copy of the outputs, and a synchronise."""
+    import torch
+
+    hq, hk, hv = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    ho = torch.empty((n_tok, wl.n_q_heads, wl.head_dim), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dout = torch.empty((n_tok, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    n = max(1, min(args.steps, 50))
+    total = 0.0
+    for i in range(args.warmup + n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        cache.reshape_and_cache(-1, dk, dv, d_slots, n_tok)
+        for layer in range(wl.n_layers):
+            cache.paged_prefill_attention(layer, dq, wl.n_q_heads, d_table, mb, d_starts, d_lens,
+                                          len(wl.chunks), max_chunk, dout)
+        ho.copy_(dout, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            total += time.perf_counter() - t0
+    tot_f, max_s = aggregate(flops * n, total, world, dev)
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    return {"value": round(tot_f / max_s / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(ho.numel() * 4),
+            "ms_per_step": round(max_s / n * 1e3, 4),
+            "api": "reshape_and_cache + paged_prefill_attention"}
+
+
+def _lib_mod():
+    from paged_kv_cache_65_gb300 import _lib
+
+    return _lib
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_sample(workload: str):
     """Build the oracle's pool for the workload and make one decode step's
@@ -563,7 +765,35 @@ def oracle_attend(wl, orc, q, seconds: float, max_seqs: int | None = None, start
     return nbytes, time.perf_counter() - t0, done
 
 
+def prefill_oracle_leg(workload: str, seconds: float):
+    """The oracle's chunked-prefill attention as it stands on whole chunks of
+    the round, one after the other, until ``seconds`` have passed."""
+    from oracle.runner import OracleRun
+
+    wl = synth.workload(workload)
+    orc = OracleRun(wl)
+    hist = {s: orc.bm.lengths.get(s, 0) for s, _ in wl.chunks}
+    _, _, q = orc.prefill_step(0)
+    flops, done = 0.0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or done == 0:
+        i = done % len(wl.chunks)
+        orc.prefill_attend(0, q, [i])
+        seq, c = wl.chunks[i]
+        flops += 4.0 * wl.head_dim * wl.n_q_heads * (c * hist[seq] + c * (c + 1) // 2)
+        done += 1
+    dt = time.perf_counter() - t0
+    return flops, dt, done
+
+
 def cpu_leg(workload: str, seconds: float):
+    if isinstance(synth.workload(workload), synth.PrefillWorkload):
+        flops, dt, done = prefill_oracle_leg(workload, seconds)
+        return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                "kind": "oracle", "seconds": round(dt, 3), "chunks": done,
+                "sample": f"{workload}: {done} whole chunks of the round, cycling over its "
+                          f"{len(synth.workload(workload).chunks)} chunks (fp64 masked "
+                          f"softmax over the paged context, one thread), {dt:.1f} s"}
     wl, orc, q = oracle_sample(workload)
     nbytes, dt, done = oracle_attend(wl, orc, q, seconds)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -618,6 +848,34 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_prefill_reference(args):
+    """Reference arm of a prefill round: the CPU oracle as it stands, each
+    step one whole chunk of the round."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(k, "1")
+    flops_all, secs = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        f, dt, _ = prefill_oracle_leg(args.workload, 0.0)
+        if i >= args.warmup:
+            flops_all += f
+            secs += dt
+    value = round(flops_all / secs / 1e12, 6)
+    sample = f"{args.workload}: per step, one whole chunk of the round (fp64, one thread)"
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -645,8 +903,11 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
+    prefill = isinstance(synth.workload(args.workload), synth.PrefillWorkload)
     if args.impl == "reference":
-        bench_reference(args)
+        (bench_prefill_reference if prefill else bench_reference)(args)
+    elif prefill:
+        bench_prefill(args)
     else:
         bench_ours(args)
 

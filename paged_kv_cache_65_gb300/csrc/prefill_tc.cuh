@@ -13,21 +13,23 @@
 // both accumulators in TMEM):
 //     S [128 rows x 128 keys] = Q [128 x 128] . K^T            (8 MMAs, K = 16)
 //     O [128 rows x 128 dims] += P_hi . V + P_lo . V           (16 MMAs)
-// Q and the K block are K-major, V is N-major, all with the 128-byte swizzle
-// (K and V written by TMA from the pool's block rows); P, the weights as a
-// bf16 high part and a bf16 remainder (~16 mantissa bits), is written by the
-// softmax threads K-major: the high part into the K area of the block (the S
-// MMA is done with it), the remainder into its own buffer.
+// Q and the K block are K-major in shared memory, V is N-major, all with the
+// 128-byte swizzle (K and V written by TMA from the pool's block rows).  P,
+// the weights as a bf16 high part and a bf16 remainder (~16 mantissa bits),
+// is written by the softmax threads over the block's own S columns in TMEM
+// and read from there as the A operand of the P.V MMAs; three S/P buffers
+// and O fill the 512 TMEM columns.  K and V have their own three-deep
+// stages: a K slot is free once its S MMAs are done, a V slot once its P.V
+// MMAs are.
 //
-// Warps 0-3: softmax, thread r owns row r (TMEM lane r) of S and O, so row
-// maxima and sums need no exchange.  The reference maximum of a row is lazy:
-// it moves only when a score exceeds it by more than 2^8 (then l and the
-// thread's O row are rescaled, after the previous block's MMAs have
+// Warps 0-3: softmax, thread r owns row r (TMEM lane r) of S, P and O, so
+// row maxima and sums need no exchange.  The reference maximum of a row is
+// lazy: it moves only when a score exceeds it by more than 2^8 (then l and
+// the thread's O row are rescaled, after the previous block's MMAs have
 // completed).  Warps 4 and 5 issue the TMA loads of K and V, lane 0 of warp
-// 6 the MMAs (the next block's S goes ahead of this block's P.V when its
-// data has landed).  Every mbarrier wait is bounded; parity waits are exact
-// because no waiter runs two phases ahead (block MMAs are awaited through the
-// block's empty barrier, whose phases are NST blocks apart).
+// 6 the MMAs (the next block's S goes ahead of this block's P.V).  Every
+// mbarrier wait is bounded; parity waits are exact because no waiter runs two
+// phases ahead.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,23 +44,23 @@ struct PfCfg {
   static constexpr int KB = 128;          // keys per block
   static constexpr int HALF = KB * 128;   // one 64-element half of a K or V block: 16 KiB
   static constexpr int STAGE = 2 * HALF;  // K (or V) of one block: 32 KiB
-  static constexpr int NST = 2;           // key blocks in flight
+  static constexpr int NST = 3;           // K and V stages
   static constexpr int QT = 2 * 128 * 128;  // Q tile, 128 rows x 128 dims: 32 KiB
-  static constexpr int PT = 2 * 128 * 128;  // one part of P, 128 rows x 128 keys: 32 KiB
-  static constexpr int TM_S = 0;            // TMEM columns: S buffers at 0 and 128,
-  static constexpr int TM_O = 256;          // O at 256
+  static constexpr int NSB = 3;             // S/P buffers in TMEM, 128 columns each
+  static constexpr int TM_O = NSB * 128;    // O after them
   static constexpr int TM_COLS = 512;
   static constexpr float TAU = 8.f;
 };
+static_assert(PfCfg::TM_O + PfCfg::D <= PfCfg::TM_COLS, "TMEM columns");
 
 constexpr int kPfWarps = 7;
 constexpr int kPfTableCache = 128;  // block-table entries per producer
 constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kPfBarriers = 4 * PfCfg::NST + 2 * PfCfg::NSB + 2;
 
 constexpr int prefill_tc_smem_bytes() {
   return PfCfg::QT + 2 * PfCfg::NST * PfCfg::STAGE  // Q, K and V blocks
-         + PfCfg::NST * PfCfg::PT                   // P remainders
-         + 16 * 8 + 16                              // mbarriers, TMEM address
+         + kPfBarriers * 8 + 16                     // mbarriers, TMEM address
          + 2 * kPfTableCache * 4                    // producer table caches
          + 1024;                                    // alignment
 }
@@ -102,14 +104,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   unsigned char* q_s = smem;
   unsigned char* k_st = q_s + C::QT;
   unsigned char* v_st = k_st + NST * C::STAGE;
-  unsigned char* plo = v_st + NST * C::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(plo + NST * C::PT);
-  uint64_t* empty = full + NST;
-  uint64_t* s_full = empty + NST;  // [2]
-  uint64_t* p_full = s_full + 2;   // [2]
-  uint64_t* q_full = p_full + 2;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(v_st + NST * C::STAGE);
+  uint64_t* k_empty = k_full + NST;  // S MMAs of the block done
+  uint64_t* v_full = k_empty + NST;
+  uint64_t* v_empty = v_full + NST;  // P.V MMAs of the block done
+  uint64_t* s_full = v_empty + NST;  // [NSB]
+  uint64_t* p_full = s_full + C::NSB;  // [NSB]
+  uint64_t* q_full = p_full + C::NSB;
   uint64_t* fin = q_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   int32_t* tcache = reinterpret_cast<int32_t*>(tmem_slot + 4);
 
   if ((smem_u32(q_s) & 1023u) != 0u) {
@@ -118,13 +121,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 2);  // the K and the V producer
-      mbar_init(&empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], 4);
-    mbar_init(&p_full[1], 4);
+    for (int i = 0; i < C::NSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+    }
     mbar_init(q_full, 4);
     mbar_init(fin, 1);
     fence_barrier_init();
@@ -143,6 +148,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool kp = warp == 4;
     const CUtensorMap* tmap = kp ? &tmap_k : &tmap_v;
     unsigned char* dst_st = kp ? k_st : v_st;
+    uint64_t* full = kp ? k_full : v_full;
+    uint64_t* empty = kp ? k_empty : v_empty;
     if (lane == 0) prefetch_tmap(tmap);
     TableCacheN<kPfTableCache> tc;
     tc.ent = tcache + (warp - 4) * kPfTableCache;
@@ -191,8 +198,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     griddep_wait();
     griddep_launch_dependents();
     if (lane == 0) {
-      const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st), vb = smem_u32(v_st),
-                     pl = smem_u32(plo);
+      const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st), vb = smem_u32(v_st);
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);
       bool alive = true;
@@ -203,45 +209,43 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         return alive;
       };
-      int issued = 0;  // S issued for blocks 0 .. issued - 1
-      auto issue_s = [&](bool block) {
-        const int j = issued;
-        const bool ok = block ? wait(&full[j % NST], (j / NST) & 1)
-                              : alive && mbar_test_wait(&full[j % NST], (j / NST) & 1);
-        if (!ok) return;
+      // S of block j into S/P buffer j % NSB, once K has landed and the
+      // P.V that last read the buffer (block j - NSB) is done
+      auto issue_s = [&](int j) {
+        if (!wait(&k_full[j % NST], (j / NST) & 1)) return;
+        if (j >= C::NSB && !wait(&v_empty[(j - C::NSB) % NST], ((j - C::NSB) / NST) & 1)) return;
         tc_fence_after();
         const uint32_t ks = kb + (j % NST) * C::STAGE;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
-          tc_mma(tmem + C::TM_S + (j & 1) * 128, smem_desc(qb + off, 16, 1024, kSwizzle128),
+          tc_mma(tmem + (j % C::NSB) * 128, smem_desc(qb + off, 16, 1024, kSwizzle128),
                  smem_desc(ks + off, 16, 1024, kSwizzle128), idS, k > 0);
         }
-        tc_commit(&s_full[j & 1]);
-        ++issued;
+        tc_commit(&k_empty[j % NST]);
+        tc_commit(&s_full[j % C::NSB]);
       };
       wait(q_full, 0);
-      issue_s(true);
+      issue_s(0);
       for (int j = 0; j < n_kb && alive; ++j) {
-        if (issued == j + 1 && issued < n_kb) issue_s(false);
-        wait(&p_full[j & 1], (j >> 1) & 1);
+        // the next block's S goes ahead of this block's P.V, so the softmax
+        // of block j + 1 can start while the tensor core runs this P.V
+        if (j + 1 < n_kb) issue_s(j + 1);
+        wait(&p_full[j % C::NSB], (j / C::NSB) & 1);
+        wait(&v_full[j % NST], (j / NST) & 1);
         if (alive) {
           tc_fence_after();
           const int nvalid = n_keys - j * C::KB < C::KB ? n_keys - j * C::KB : C::KB;
           const int nk = (nvalid + 15) >> 4;
           const uint32_t vs = vb + (j % NST) * C::STAGE;
-          const uint32_t ph = kb + (j % NST) * C::STAGE;  // P high part in the K area
-          const uint32_t pr = pl + (j % NST) * C::PT;
+          const uint32_t pt = tmem + (j % C::NSB) * 128;  // P high part; remainder at +64
           for (int k = 0; k < nk; ++k) {
-            const uint32_t poff = (k >> 2) * C::HALF + (k & 3) * 32;
             const uint64_t dv = smem_desc(vs + k * 2048, C::HALF, 1024, kSwizzle128);
-            tc_mma(tmem + C::TM_O, smem_desc(ph + poff, 16, 1024, kSwizzle128), dv, idPV,
-                   (j > 0 || k > 0) ? 1u : 0u);
-            tc_mma(tmem + C::TM_O, smem_desc(pr + poff, 16, 1024, kSwizzle128), dv, idPV, 1u);
+            tc_mma_ts(tmem + C::TM_O, pt + k * 8, dv, idPV, (j > 0 || k > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + C::TM_O, pt + 64 + k * 8, dv, idPV, 1u);
           }
-          tc_commit(&empty[j % NST]);
+          tc_commit(&v_empty[j % NST]);
         }
-        if (issued == j + 1 && issued < n_kb) issue_s(true);
       }
       tc_commit(fin);
       mbar_wait_bounded(fin, 0, kWaitLimitNs);
@@ -285,25 +289,37 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int slot = j % NST;
       const int k0 = j * C::KB;
       const int nvalid = n_keys - k0 < C::KB ? n_keys - k0 : C::KB;
-      wait(&full[slot], (j / NST) & 1);
-      wait(&s_full[j & 1], (j >> 1) & 1);
+      wait(&s_full[j % C::NSB], (j / C::NSB) & 1);
       __syncwarp();
       tc_fence_after();
-      const uint32_t sb = tmem + C::TM_S + (j & 1) * 128 + lanes;
-      const bool masked = k0 + C::KB - 1 > pos;  // some key of the block is past pos
-      // pass 1: the row maximum of the admitted scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c0 = 0; c0 < C::KB; c0 += 32) {
-        uint32_t sr[32];
-        tmem_ld32(sb + c0, sr);
+      const uint32_t sb = tmem + (j % C::NSB) * 128 + lanes;
+      // the row of S: four loads, one wait
+      uint32_t sr[4][32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool ok = !masked || k0 + c0 + i <= pos;
-          mx = ok ? fmaxf(mx, __uint_as_float(sr[i])) : mx;
-        }
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nowait(sb + q4 * 32, sr[q4]);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld32(sr[q4]);
+      // keys this row may not see (past its position; every key for a row
+      // past the chunk) become -inf, whatever the slot held; blocks with no
+      // such key in the whole warp skip this
+      const int lim = row_ok ? pos - k0 : -1;  // key i of the block is admitted iff i <= lim
+      if (__any_sync(0xffffffffu, lim < C::KB - 1)) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sr[q4][i] = q4 * 32 + i > lim ? 0xff800000u : sr[q4][i];
       }
-      mx = row_ok ? mx * qs : -INFINITY;
+      // pass 1: the row maximum (eight independent chains)
+      float mm[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mm[i] = -INFINITY;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mm[i & 7] = fmaxf(mm[i & 7], __uint_as_float(sr[q4][i]));
+      const float mx =
+          fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * qs;
       // the reference moves when a score exceeds it by more than 2^8: l and,
       // after the previous block's MMAs, this row of O are rescaled (the
       // TMEM accesses are warp-wide: lanes whose reference stays scale by 1)
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (__any_sync(0xffffffffu, upd)) {
         if (j > 0) {
-          wait(&empty[(j - 1) % NST], ((j - 1) / NST) & 1);
+          wait(&v_empty[(j - 1) % NST], ((j - 1) / NST) & 1);
           __syncwarp();
           tc_fence_after();
 #pragma unroll 1
@@ -329,37 +345,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-      // pass 2: weights, high part into the K area, remainder into its buffer
-      const uint32_t ph = smem_u32(k_st + slot * C::STAGE);
-      const uint32_t pr = smem_u32(plo + slot * C::PT);
-#pragma unroll 1
-      for (int c0 = 0; c0 < C::KB; c0 += 32) {
-        uint32_t sr[32];
-        tmem_ld32(sb + c0, sr);
+      // pass 2: p = 2^(s * qs - m), a -inf score giving 0 (a row with no
+      // admitted key so far has m = -inf and uses 0 instead, all its scores
+      // being -inf).  The high part is p's upper 16 bits (truncation); the
+      // remainder p - hi is exact in fp32 and rounded once to bf16, so the
+      // two carry ~16 bits of p.  Both go over the block's S columns (high
+      // part in the first 64, remainder in the last 64; S is in registers by
+      // now).  l sums p in four partial sums.
+      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t hi[4], lo[4];
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t hi[32], lo[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i = c8 * 8 + 2 * k;
-            const bool ok0 = row_ok && (!masked || k0 + c0 + i <= pos);
-            const bool ok1 = row_ok && (!masked || k0 + c0 + i + 1 <= pos);
-            const float p0 = ok0 ? exp2_approx(fmaf(__uint_as_float(sr[i]), qs, -m_ref)) : 0.f;
-            const float p1 =
-                ok1 ? exp2_approx(fmaf(__uint_as_float(sr[i + 1]), qs, -m_ref)) : 0.f;
-            l += p0 + p1;
-            hi[k] = pack_bf16(p0, p1);
-            lo[k] = pack_bf16(p0 - __uint_as_float(hi[k] << 16),
-                              p1 - __uint_as_float(hi[k] & 0xffff0000u));
-          }
-          const int ch = (c0 >> 3) + c8;
-          sts128(kmajor_chunk(ph, r, ch), hi[0], hi[1], hi[2], hi[3]);
-          sts128(kmajor_chunk(pr, r, ch), lo[0], lo[1], lo[2], lo[3]);
+        for (int k = 0; k < 32; ++k) {
+          const int q4 = 2 * h2 + (k >> 4), i = 2 * (k & 15);
+          const float p0 = exp2_approx(fmaf(__uint_as_float(sr[q4][i]), qs, nm));
+          const float p1 = exp2_approx(fmaf(__uint_as_float(sr[q4][i + 1]), qs, nm));
+          lp[k & 3] += p0 + p1;
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[k] = __byte_perm(b0, b1, 0x7632);
+          lo[k] = pack_bf16(p0 - __uint_as_float(b0 & 0xffff0000u),
+                            p1 - __uint_as_float(b1 & 0xffff0000u));
         }
+        tmem_st32_nowait(sb + h2 * 32, hi);
+        tmem_st32_nowait(sb + 64 + h2 * 32, lo);
       }
+      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      tmem_wait_st();
       // keys past the context inside the last 16-key step: V must be finite
       // there (unused slots may hold anything), so its rows are zeroed
       if (r >= nvalid && r < ((nvalid + 15) & ~15)) {
+        wait(&v_full[slot], (j / NST) & 1);
         const uint32_t vb = smem_u32(v_st + slot * C::STAGE) + r * 128;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
@@ -369,10 +386,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&p_full[j % C::NSB]);
     }
     // ---- O row: wait for the last block's MMAs, normalise, store
-    wait(&empty[(n_kb - 1) % NST], ((n_kb - 1) / NST) & 1);
+    wait(&v_empty[(n_kb - 1) % NST], ((n_kb - 1) / NST) & 1);
     __syncwarp();
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
