@@ -26,10 +26,13 @@
 // row maxima and sums need no exchange.  The reference maximum of a row is
 // lazy: it moves only when a score exceeds it by more than 2^8 (then l and
 // the thread's O row are rescaled, after the previous block's MMAs have
-// completed).  Warps 4 and 5 issue the TMA loads of K and V, lane 0 of warp
-// 6 the MMAs (the next block's S goes ahead of this block's P.V).  Every
-// mbarrier wait is bounded; parity waits are exact because no waiter runs two
-// phases ahead.
+// completed).  Warps 4 and 5 issue the TMA loads of K and V; lane 0 of warp
+// 6 issues the S MMAs, running ahead as far as K blocks and free S/P buffers
+// allow, and lane 0 of warp 7 the P.V MMAs (one thread issuing both kinds
+// could not keep the tensor core busy: a single thread issues an MMA every
+// ~60 cycles, about the tensor core's time for one 128 x 128 x 16 step).
+// Every mbarrier wait is bounded; parity waits are exact because no waiter
+// runs two phases ahead.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,7 +56,7 @@ struct PfCfg {
 };
 static_assert(PfCfg::TM_O + PfCfg::D <= PfCfg::TM_COLS, "TMEM columns");
 
-constexpr int kPfWarps = 7;
+constexpr int kPfWarps = 8;
 constexpr int kPfTableCache = 128;  // block-table entries per producer
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfBarriers = 4 * PfCfg::NST + 2 * PfCfg::NSB + 2;
@@ -193,14 +196,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int first = n_kb > NST ? n_kb - NST : 0;
     for (int j = first; j < n_kb && alive; ++j)
       alive = mbar_wait_bounded(&full[j % NST], (j / NST) & 1, kWaitLimitNs);
-  } else if (warp == 6) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == 6 || warp == 7) {
+    // ------------------------------------------ MMA issuers (6: S, 7: P.V)
     griddep_wait();
     griddep_launch_dependents();
     if (lane == 0) {
-      const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st), vb = smem_u32(v_st);
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (alive && !mbar_wait_bounded(bar, parity, kWaitLimitNs)) {
@@ -209,31 +209,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         return alive;
       };
-      // S of block j into S/P buffer j % NSB, once K has landed and the
-      // P.V that last read the buffer (block j - NSB) is done
-      auto issue_s = [&](int j) {
-        if (!wait(&k_full[j % NST], (j / NST) & 1)) return;
-        if (j >= C::NSB && !wait(&v_empty[(j - C::NSB) % NST], ((j - C::NSB) / NST) & 1)) return;
-        tc_fence_after();
-        const uint32_t ks = kb + (j % NST) * C::STAGE;
+      if (warp == 6) {
+        // S of block j into S/P buffer j % NSB, once K has landed and the
+        // P.V that last read the buffer (block j - NSB) is done
+        const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st);
+        constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+        wait(q_full, 0);
+        for (int j = 0; j < n_kb && alive; ++j) {
+          if (!wait(&k_full[j % NST], (j / NST) & 1)) break;
+          if (j >= C::NSB && !wait(&v_empty[(j - C::NSB) % NST], ((j - C::NSB) / NST) & 1)) break;
+          tc_fence_after();
+          const uint32_t ks = kb + (j % NST) * C::STAGE;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
-          tc_mma(tmem + (j % C::NSB) * 128, smem_desc(qb + off, 16, 1024, kSwizzle128),
-                 smem_desc(ks + off, 16, 1024, kSwizzle128), idS, k > 0);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
+            tc_mma(tmem + (j % C::NSB) * 128, smem_desc(qb + off, 16, 1024, kSwizzle128),
+                   smem_desc(ks + off, 16, 1024, kSwizzle128), idS, k > 0);
+          }
+          tc_commit(&k_empty[j % NST]);
+          tc_commit(&s_full[j % C::NSB]);
         }
-        tc_commit(&k_empty[j % NST]);
-        tc_commit(&s_full[j % C::NSB]);
-      };
-      wait(q_full, 0);
-      issue_s(0);
-      for (int j = 0; j < n_kb && alive; ++j) {
-        // the next block's S goes ahead of this block's P.V, so the softmax
-        // of block j + 1 can start while the tensor core runs this P.V
-        if (j + 1 < n_kb) issue_s(j + 1);
-        wait(&p_full[j % C::NSB], (j / C::NSB) & 1);
-        wait(&v_full[j % NST], (j / NST) & 1);
-        if (alive) {
+      } else {
+        const uint32_t vb = smem_u32(v_st);
+        constexpr uint32_t idPV = idesc_bf16(128, 128, false, true);
+        for (int j = 0; j < n_kb && alive; ++j) {
+          wait(&p_full[j % C::NSB], (j / C::NSB) & 1);
+          wait(&v_full[j % NST], (j / NST) & 1);
+          if (!alive) break;
           tc_fence_after();
           const int nvalid = n_keys - j * C::KB < C::KB ? n_keys - j * C::KB : C::KB;
           const int nk = (nvalid + 15) >> 4;
@@ -246,9 +248,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_commit(&v_empty[j % NST]);
         }
+        tc_commit(fin);
+        mbar_wait_bounded(fin, 0, kWaitLimitNs);
       }
-      tc_commit(fin);
-      mbar_wait_bounded(fin, 0, kWaitLimitNs);
     }
     __syncwarp();
   } else {
@@ -347,11 +349,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // pass 2: p = 2^(s * qs - m), a -inf score giving 0 (a row with no
       // admitted key so far has m = -inf and uses 0 instead, all its scores
-      // being -inf).  The high part is p's upper 16 bits (truncation); the
-      // remainder p - hi is exact in fp32 and rounded once to bf16, so the
-      // two carry ~16 bits of p.  Both go over the block's S columns (high
-      // part in the first 64, remainder in the last 64; S is in registers by
-      // now).  l sums p in four partial sums.
+      // being -inf).  The high part is p's upper 16 bits, the remainder
+      // p - hi (exact in fp32, below 2^-7 p) likewise truncated to its upper
+      // 16 bits, so hi + lo is within 2^-15 of p with no conversion
+      // instruction.  Both go over the block's S columns (high part in the
+      // first 64, remainder in the last 64; S is in registers by now).  l
+      // sums p in four partial sums.
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
       float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -365,8 +368,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           lp[k & 3] += p0 + p1;
           const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
           hi[k] = __byte_perm(b0, b1, 0x7632);
-          lo[k] = pack_bf16(p0 - __uint_as_float(b0 & 0xffff0000u),
-                            p1 - __uint_as_float(b1 & 0xffff0000u));
+          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          lo[k] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
         }
         tmem_st32_nowait(sb + h2 * 32, hi);
         tmem_st32_nowait(sb + 64 + h2 * 32, lo);
