@@ -68,6 +68,32 @@ constexpr int prefill_tc_smem_bytes() {
          + 1024;                                    // alignment
 }
 
+// Paired fp32 arithmetic (two lanes of fp32 in one 64-bit register, one
+// instruction for both) and the three-input maximum.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // swizzled 16-byte chunk ch (0..15 over 128 elements) of row r in a K-major
 // tile of two 64-element halves
 __device__ __forceinline__ uint32_t kmajor_chunk(uint32_t base, int r, int ch) {
@@ -311,14 +337,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) sr[q4][i] = q4 * 32 + i > lim ? 0xff800000u : sr[q4][i];
       }
-      // pass 1: the row maximum (eight independent chains)
+      // pass 1: the row maximum (eight independent chains of three-input
+      // maxima)
       float mm[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mm[i] = -INFINITY;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mm[i & 7] = fmaxf(mm[i & 7], __uint_as_float(sr[q4][i]));
+        for (int i = 0; i < 32; i += 2)
+          mm[(i >> 1) & 7] = fmax3(mm[(i >> 1) & 7], __uint_as_float(sr[q4][i]),
+                                   __uint_as_float(sr[q4][i + 1]));
       const float mx =
           fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
                 fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * qs;
@@ -354,28 +383,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // 16 bits, so hi + lo is within 2^-15 of p with no conversion
       // instruction.  Both go over the block's S columns (high part in the
       // first 64, remainder in the last 64; S is in registers by now).  l
-      // sums p in four partial sums.
+      // sums p in paired partial sums.
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t qs2 = f2_pack(qs, qs), nm2 = f2_pack(nm, nm), neg2 = f2_pack(-1.f, -1.f);
+      uint64_t lp2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int q4 = 2 * h2 + (k >> 4), i = 2 * (k & 15);
-          const float p0 = exp2_approx(fmaf(__uint_as_float(sr[q4][i]), qs, nm));
-          const float p1 = exp2_approx(fmaf(__uint_as_float(sr[q4][i + 1]), qs, nm));
-          lp[k & 3] += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1])), qs2,
+                           nm2),
+                    x0, x1);
+          const float p0 = exp2_approx(x0), p1 = exp2_approx(x1);
+          const uint64_t pp = f2_pack(p0, p1);
+          lp2[k & 1] = f2_add(lp2[k & 1], pp);
           const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
           hi[k] = __byte_perm(b0, b1, 0x7632);
-          const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-          const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+          float r0, r1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(b0 & 0xffff0000u),
+                                   __uint_as_float(b1 & 0xffff0000u)),
+                           neg2, pp),
+                    r0, r1);
           lo[k] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
         }
         tmem_st32_nowait(sb + h2 * 32, hi);
         tmem_st32_nowait(sb + 64 + h2 * 32, lo);
       }
-      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(lp2[0], a0, a1);
+        f2_unpack(lp2[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+      }
       tmem_wait_st();
       // keys past the context inside the last 16-key step: V must be finite
       // there (unused slots may hold anything), so its rows are zeroed
