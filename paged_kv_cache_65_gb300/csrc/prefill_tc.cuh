@@ -26,9 +26,10 @@
 // row maxima and sums need no exchange.  The reference maximum of a row is
 // lazy: it moves only when a score exceeds it by more than 2^8 (then l and
 // the thread's O row are rescaled, after the previous block's MMAs have
-// completed).  Warps 4 and 5 issue the TMA loads of K and V; lane 0 of warp
-// 6 issues the S MMAs, running ahead as far as K blocks and free S/P buffers
-// allow, and lane 0 of warp 7 the P.V MMAs (one thread issuing both kinds
+// completed).  Warps 4-7 issue the TMA loads of K and V (one 64-column half
+// each, so that box issue keeps up with 16-token pages); lane 0 of warp 8
+// issues the S MMAs, running ahead as far as K blocks and free S/P buffers
+// allow, and lane 0 of warp 9 the P.V MMAs (one thread issuing both kinds
 // could not keep the tensor core busy: a single thread issues an MMA every
 // ~60 cycles, about the tensor core's time for one 128 x 128 x 16 step).
 // Every mbarrier wait is bounded; parity waits are exact because no waiter
@@ -56,15 +57,22 @@ struct PfCfg {
 };
 static_assert(PfCfg::TM_O + PfCfg::D <= PfCfg::TM_COLS, "TMEM columns");
 
-constexpr int kPfWarps = 8;
-constexpr int kPfTableCache = 128;  // block-table entries per producer
+// warpgroup 0 (warps 0-3) softmax; warpgroup 1: K producers 4 (columns
+// 0-63) and 6 (64-127), V producers 5 and 7; warpgroup 2: MMA issuers 8 (S)
+// and 9 (P.V), 10 and 11 idle.  Every SM sub-partition (warp % 4) holds one
+// warp of each group.  Launched at 168 registers a thread (384 threads), the
+// groups move to 232 / 64 / 64: 128 x (232 + 64 + 64) = 46080 <= 64512.
+constexpr int kPfWarps = 12;
+constexpr int kPfRegsSoftmax = 232, kPfRegsHelper = 64;
+static_assert(128 * (kPfRegsSoftmax + 2 * kPfRegsHelper) <= 168 * 32 * kPfWarps, "register split");
+constexpr int kPfTableCache = 96;  // block-table entries per producer
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfBarriers = 4 * PfCfg::NST + 2 * PfCfg::NSB + 2;
 
 constexpr int prefill_tc_smem_bytes() {
   return PfCfg::QT + 2 * PfCfg::NST * PfCfg::STAGE  // Q, K and V blocks
          + kPfBarriers * 8 + 16                     // mbarriers, TMEM address
-         + 2 * kPfTableCache * 4                    // producer table caches
+         + 4 * kPfTableCache * 4                    // producer table caches
          + 1024;                                    // alignment
 }
 
@@ -150,9 +158,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], 2);  // the producers of the two halves
       mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], 2);
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < C::NSB; ++i) {
@@ -172,9 +180,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4 || warp == 5) {
-    // ------------------------------------------------ producers (K, V)
-    const bool kp = warp == 4;
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------ producers (K or V, one half each)
+    reg_dealloc<kPfRegsHelper>();
+    const bool kp = (warp & 1) == 0;
+    const int hf = (warp - 4) >> 1;  // 64-column half of the rows
     const CUtensorMap* tmap = kp ? &tmap_k : &tmap_v;
     unsigned char* dst_st = kp ? k_st : v_st;
     uint64_t* full = kp ? k_full : v_full;
@@ -200,7 +210,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int nvalid = n_keys - k0 < C::KB ? n_keys - k0 : C::KB;
       const int nunits = (nvalid + UR - 1) / UR;
       tc.ensure(a.table, a.max_blocks, s, k0 / B, (k0 + (nunits - 1) * UR) / B, lane);
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], 1u * nunits * UR * C::D * 2);
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], 1u * nunits * UR * 64 * 2);
       __syncwarp();
       for (int u = lane; u < nunits; u += 32) {
         const int tk = k0 + u * UR;
@@ -212,21 +222,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           pid = 0;  // stay in bounds; the result is flagged as invalid
         }
         const int y = (a.layer * a.n_blocks + pid) * B + row;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(dst_st + slot * C::STAGE + hf * C::HALF + u * UR * 128, tmap,
-                      head * C::D + hf * 64, y, &full[slot]);
+        tma_load_2d(dst_st + slot * C::STAGE + hf * C::HALF + u * UR * 128, tmap,
+                    head * C::D + hf * 64, y, &full[slot]);
       }
     }
     // copies still in flight land before the CTA may exit
     const int first = n_kb > NST ? n_kb - NST : 0;
     for (int j = first; j < n_kb && alive; ++j)
       alive = mbar_wait_bounded(&full[j % NST], (j / NST) & 1, kWaitLimitNs);
-  } else if (warp == 6 || warp == 7) {
-    // ------------------------------------------ MMA issuers (6: S, 7: P.V)
+  } else if (warp >= 8) {
+    // -------------------------------- MMA issuers (8: S, 9: P.V); 10, 11 idle
+    reg_dealloc<kPfRegsHelper>();
     griddep_wait();
     griddep_launch_dependents();
-    if (lane == 0) {
+    if (warp < 10 && lane == 0) {
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (alive && !mbar_wait_bounded(bar, parity, kWaitLimitNs)) {
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         return alive;
       };
-      if (warp == 6) {
+      if (warp == 8) {
         // S of block j into S/P buffer j % NSB, once K has landed and the
         // P.V that last read the buffer (block j - NSB) is done
         const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st);
@@ -281,6 +290,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------------- softmax rows
+    reg_alloc<kPfRegsSoftmax>();
     const int r = threadIdx.x;             // tile row = TMEM lane
     const int tl = r / G, g = r - tl * G;  // token of the tile, query head of the K/V head
     const bool row_ok = tl < ntok;

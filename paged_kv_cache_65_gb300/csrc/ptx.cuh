@@ -148,6 +148,16 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// Per-warpgroup register limits (all four warps of the group execute it).
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void record_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
