@@ -45,24 +45,31 @@ import synth  # noqa: E402
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and decode tokens/s"
 DEFAULT_WORKLOAD = "qwen_2k"
 
-# Per-launch DRAM traffic of the split pass from an ncu capture, keyed by
-# (workload, kernel), valid only for the kernel and plan sources it was taken
-# on: ncu dram__bytes_read.sum + dram__bytes_write.sum of one split launch
-# (profiles/), valid while those sources hash to "sha".
+# Per-launch DRAM traffic of the dominant kernel from an ncu capture, keyed by
+# (workload, kernel): ncu dram__bytes_read.sum + dram__bytes_write.sum of one
+# launch (profiles/), valid only while the sources of that kernel family hash
+# to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331664640 + 3682304, "sha": "54528254954021d9"},
-    ("shared_8k", "decode_mma_kernel"): {"bytes": 170972160 + 3401984, "sha": "54528254954021d9"},
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1616037000 + 7005696, "sha": "54528254954021d9"},
+    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331667968 + 3491072, "sha": "63bb18cc6a5e9b3f"},
+    ("shared_8k", "decode_mma_kernel"): {"bytes": 170978304 + 3176704, "sha": "63bb18cc6a5e9b3f"},
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1616046848 + 6752512, "sha": "63bb18cc6a5e9b3f"},
+    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 157367808 + 51861760, "sha": "3eb978eb03b932bd"},
 }
 
 
 # KV_OPT_DECODE_PATH values
 KERNELS = {"auto": 0, "cuda": 1, "mma": 2, "tc": 3}
 
-def kernel_sha() -> str:
+KERNEL_SOURCES = {
+    "decode": ("decode.cuh", "decode_mma.cuh", "decode_tc.cuh", "tc.cuh", "ptx.cuh", "plan.h",
+               "plan.cpp"),
+    "prefill": ("prefill_tc.cuh", "prefill.h", "decode.cuh", "tc.cuh", "ptx.cuh"),
+}
+
+
+def kernel_sha(family: str = "decode") -> str:
     h = hashlib.sha256()
-    for f in ("decode.cuh", "decode_mma.cuh", "decode_tc.cuh", "tc.cuh", "ptx.cuh", "plan.h",
-              "plan.cpp"):
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "paged_kv_cache_65_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -650,7 +657,7 @@ def bench_prefill(args):
     peak, peak_kind = read_tensor_peak()
     achieved = flops / attn_s / 1e12
     traffic = TRAFFIC.get((args.workload, "prefill_tc_kernel"))
-    traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha() else None
+    traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha("prefill") else None
     e2e = bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
                             max_chunk, n_tok, flops, world)
     cpu = None
