@@ -22,7 +22,12 @@ follows, not to be fast:
   控制" §07, in float64 on contiguous K/V, plus the per-range partial and the
   online-softmax merge rule of "KV 缓存管理" (chunked-prefill section).
 * ``sizing`` -- the closed-form sizing and waste formulas (Eq. 1, M_block,
-  ceil(S/B), tail waste) used to pin the manager.
+  ceil(S/B), tail waste) used to pin the manager, and the byte arithmetic of
+  narrower KV formats ("第 8 章 推理优化" §8.4.2).
+* ``fp8`` -- FP8 E4M3 codes for a quantized KV pool (one scale per pool for
+  K and for V), written from the format's definition; ``kv_store`` holds
+  such pools.
+* ``prefill`` -- chunked-prefill attention over a paged history.
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against
 values the pages print (``tests/golden/``), closed forms, brute force or

@@ -14,13 +14,20 @@ number is ``p * B + o``.
 Element storage: ``"f32"`` pools hold float32 values; ``"bf16"`` pools hold
 the raw 16-bit patterns (uint16).  A bf16 pattern ``h`` stands for the
 float32 whose bits are ``h << 16``; ``to_f64`` widens that exactly.
+``"fp8_e4m3"`` pools hold E4M3 codes (uint8) of the written values divided
+by the pool's K or V scale (``oracle.fp8``); the values written are bf16
+patterns, and a gather returns ``code value * scale``.
 """
 
 from __future__ import annotations
 
 import numpy as np
 
-STORAGE = {"f32": np.float32, "bf16": np.uint16}
+from .fp8 import e4m3_decode, e4m3_encode
+
+STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}
+# dtype of the rows a caller writes (and of q) for each pool dtype
+INPUT_DTYPE = {"f32": "f32", "bf16": "bf16", "fp8_e4m3": "bf16"}
 
 
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -34,15 +41,22 @@ def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 class KVStore:
-    def __init__(self, n_layers, n_blocks, block_size, n_kv_heads, head_dim, dtype="f32"):
+    def __init__(self, n_layers, n_blocks, block_size, n_kv_heads, head_dim, dtype="f32",
+                 k_scale=1.0, v_scale=1.0):
         self.L, self.N, self.B = n_layers, n_blocks, block_size
         self.H, self.D, self.dtype = n_kv_heads, head_dim, dtype
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
         shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
         self.K = np.zeros(shape, dtype=STORAGE[dtype])
         self.V = np.zeros(shape, dtype=STORAGE[dtype])
 
     def write_slot(self, layer: int, slot: int, k_row, v_row) -> None:
         p, o = divmod(int(slot), self.B)
+        if self.dtype == "fp8_e4m3":
+            # rows arrive as bf16 patterns; stored as codes of x / scale
+            self.K[layer, p, o] = e4m3_encode(to_f64(k_row, "bf16").astype(np.float32), self.k_scale)
+            self.V[layer, p, o] = e4m3_encode(to_f64(v_row, "bf16").astype(np.float32), self.v_scale)
+            return
         self.K[layer, p, o] = k_row
         self.V[layer, p, o] = v_row
 
@@ -75,6 +89,9 @@ class KVStore:
         return k, v
 
     def gather(self, layer: int, table, ctx: int):
-        """Same as ``gather_raw`` but widened to contiguous float64."""
+        """Same as ``gather_raw`` but widened to contiguous float64 (FP8
+        codes dequantized: value times the pool's scale, exact)."""
         k, v = self.gather_raw(layer, table, ctx)
+        if self.dtype == "fp8_e4m3":
+            return e4m3_decode(k) * self.k_scale, e4m3_decode(v) * self.v_scale
         return to_f64(k, self.dtype), to_f64(v, self.dtype)
