@@ -189,6 +189,9 @@ def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device"):
     wl = synth.workload(name, **({"block_size": block_size} if name == "pool36" else {}))
     cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
                          wl.dtype, free_order=wl.free_order, device=device)
+    fp8 = wl.dtype == "fp8_e4m3"
+    if fp8:
+        cache.kv_pool_set_fp8_scales(wl.k_scale, wl.v_scale)
     if fill == "device":
         g = torch.Generator(device=device)
         g.manual_seed(synth.torch_seed((wl.seed, 5)))
@@ -197,7 +200,9 @@ def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device"):
             step = 1 << 28
             for i in range(0, flat.numel(), step):
                 seg = flat[i:i + step]
-                seg.copy_(torch.randn(seg.numel(), generator=g, device=device, dtype=torch.float32))
+                x = torch.randn(seg.numel(), generator=g, device=device, dtype=torch.float32)
+                # FP8 pools: the values' E4M3 codes (torch's conversion; synthetic fill only)
+                seg.copy_(x.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else x)
     run = DeviceRun(cache, wl.n_q_heads)
     values = None if fill == "device" else wl.append_values
     for op in wl.build_ops:
@@ -253,7 +258,7 @@ def bench_ours(args):
     # at most n_plans tokens however many steps are timed
     n_plans = min(n_steps, args.plans)
 
-    use_plan = not (args.plain or args.kernel == "cuda") and wl.dtype == "bf16" and \
+    use_plan = not (args.plain or args.kernel == "cuda") and wl.dtype in ("bf16", "fp8_e4m3") and \
         wl.block_size % 8 == 0
     plans, host_plans = [], []
     max_blocks = 1
@@ -282,7 +287,7 @@ def bench_ours(args):
         ws_bytes = max(ws_bytes, hp[1])
     g = torch.Generator(device=dev)
     g.manual_seed(synth.torch_seed((wl.seed, 6)))
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16  # FP8 pools take bf16
     q = torch.randn((L, n, wl.n_q_heads, wl.head_dim), generator=g, device=dev).to(tdt)
     kn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
     vn = torch.randn((L, n, wl.n_kv_heads, wl.head_dim), generator=g, device=dev).to(tdt)
@@ -432,7 +437,7 @@ def bench_ours(args):
     peak, peak_kind = read_peaks()
     achieved = alg / split_s / 1e9
     # the split-pass kernel that ran: a plan records its own; otherwise the option
-    tensor_shape = wl.dtype == "bf16" and wl.block_size % 8 == 0
+    tensor_shape = wl.dtype in ("bf16", "fp8_e4m3") and wl.block_size % 8 == 0
     if use_plan:
         from paged_kv_cache_65_gb300.cache import parse_plan
 
@@ -506,7 +511,7 @@ def bench_e2e(args, wl, cache, run, dev, world):
     max_blocks = run.max_blocks(seqs) + (steps + args.warmup) // wl.block_size + 2
     staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
                           dtype=torch.uint8, device=dev)
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16  # FP8 pools take bf16
     g = torch.Generator()
     g.manual_seed(synth.torch_seed((wl.seed, 7)))
     hq = torch.randn((L, n, wl.n_q_heads, wl.head_dim), generator=g).to(tdt).pin_memory()

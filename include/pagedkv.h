@@ -58,7 +58,13 @@ enum {
   KV_ERR_SCRATCH_TOO_SMALL = 7 /* request exceeds the static scratch array    */
 };
 
-enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1 };
+/* KV_DTYPE_FP8_E4M3: a quantized pool ("第 8 章 推理优化" §8.4.2): each K or V
+ * element is one E4M3 code (sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, no infinities, NaN = all exponent and mantissa bits set) of
+ * x / scale, with one float32 scale per pool for K and one for V
+ * (kv_pool_set_fp8_scales); half the bytes of BF16.  Its q, new K/V rows and
+ * outputs are bfloat16 (outputs may also be float32). */
+enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1, KV_DTYPE_FP8_E4M3 = 2 };
 
 /* bits of the device status word */
 enum {
@@ -83,7 +89,9 @@ const char* kv_status_string(kvStatus s);
  *   d_status: device int32 the kernels OR error bits into; may be NULL.
  *   free_order: host array of n_blocks ids, a permutation of 0..n_blocks-1
  *     giving the initial FIFO free list ([BT] §05); NULL means 0..n_blocks-1.
- * Supported: block_size 1..256, head_dim 64 or 128, dtype F32 or BF16. */
+ * Supported: block_size 1..256, head_dim 64 or 128, dtype F32 or BF16;
+ * FP8_E4M3 with head_dim 128 and block_size a multiple of 8 that divides 64
+ * or is a multiple of it (decode on the warp-level MMA pass only). */
 kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_heads,
                         int head_dim, int dtype, void* k_cache, void* v_cache,
                         int32_t* d_status, const int32_t* free_order, kvPool** out);
@@ -118,6 +126,14 @@ kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
  * results, but is scheduled while they finish), 0 = plain launches. */
 enum { KV_OPT_DECODE_PATH = 1, KV_OPT_PDL = 2 };
 kvStatus kv_pool_set_option(kvPool* pool, int option, int value);
+
+/* Scales of an FP8_E4M3 pool (default 1, 1): a written value x is stored as
+ * the E4M3 code nearest to x / scale in float32 (IEEE division), ties to the
+ * even mantissa, magnitudes beyond 448 (infinities too) saturating to 448;
+ * attention reads code * scale.  Both must be positive and finite; other
+ * dtypes: KV_ERR_INVALID_ARG.  Codes already written keep their meaning only
+ * under the scales they were written with. */
+kvStatus kv_pool_set_fp8_scales(kvPool* pool, float k_scale, float v_scale);
 
 /* Synchronise `stream`, copy the device status word to *out_bits and clear
  * it.  Returns KV_ERR_DEVICE_CHECK when any bit was set. */

@@ -42,41 +42,31 @@ def e4m3_decode(codes) -> np.ndarray:
     return sign * mag
 
 
-def _encode_magnitude(a: float) -> int:
-    """Non-negative finite float64 -> 7-bit E4M3 magnitude code."""
-    if a >= E4M3_MAX:
-        return 0x7E
-    if a < 2.0 ** -6:
-        n = int(np.rint(a / 2.0 ** -9))  # subnormal grid, ties to even
-        # n == 8 is the smallest normal, which is code 0x08 as well
-        return n
-    e = int(np.floor(np.log2(a)))
-    # guard the floor against log2 rounding at exact powers of two
-    if 2.0 ** e > a:
-        e -= 1
-    elif 2.0 ** (e + 1) <= a:
-        e += 1
-    q = 2.0 ** (e - 3)  # spacing of the values in [2^e, 2^(e+1))
-    n = int(np.rint(a / q))  # 8..16, ties to even
-    if n == 16:
-        n, e = 8, e + 1
-    if e > 8 or (e == 8 and n > 14):  # beyond 448
-        return 0x7E
-    return ((e + 7) << 3) | (n - 8)
-
-
 def e4m3_encode(x, scale: float = 1.0) -> np.ndarray:
     """float32 values (any shape) -> uint8 codes of ``x / scale``."""
     xf = np.asarray(x, dtype=np.float32)
     v = (xf / np.float32(scale)).astype(np.float32)
-    out = np.empty(v.shape, dtype=np.uint8)
-    flat_v, flat_o = v.reshape(-1), out.reshape(-1)
-    for i in range(flat_v.size):
-        f = float(flat_v[i])
-        neg = bool(np.signbit(flat_v[i]))
-        if np.isnan(f):
-            code = NAN_CODE
-        else:
-            code = _encode_magnitude(abs(f))
-        flat_o[i] = code | (0x80 if neg else 0)
-    return out
+    a = np.abs(v).astype(np.float64)  # exact
+    nan = np.isnan(v)
+    code = np.zeros(v.shape, dtype=np.int64)
+    # below the smallest normal: the nearest multiple of 2^-9 (ties to even);
+    # 8 * 2^-9 = 2^-6 is the smallest normal, whose code is 0x08 as well
+    sub = ~nan & (a < 2.0 ** -6)
+    code[sub] = np.rint(a[sub] / 2.0 ** -9)
+    # normal range: a in [2^e, 2^(e+1)), spacing 2^(e-3), ties to even
+    nrm = ~nan & ~sub & (a < E4M3_MAX)
+    an = a[nrm]
+    e = np.floor(np.log2(an))
+    e -= np.exp2(e) > an  # guard the floor against log2 rounding
+    e += np.exp2(e + 1) <= an
+    n = np.rint(an / np.exp2(e - 3))  # 8 .. 16
+    carry = n == 16
+    n[carry] = 8
+    e[carry] += 1
+    c = ((e.astype(np.int64) + 7) << 3) | (n.astype(np.int64) - 8)
+    c[(e > 8) | ((e == 8) & (n > 14))] = 0x7E  # rounded beyond 448
+    code[nrm] = c
+    code[~nan & (a >= E4M3_MAX)] = 0x7E  # saturation, infinities included
+    code[nan] = NAN_CODE
+    code |= np.where(np.signbit(v), 0x80, 0)
+    return code.astype(np.uint8)

@@ -14,7 +14,7 @@ import numpy as np
 from .attention import decode_attention
 from .prefill import prefill_attention
 from .block_manager import BlockManager
-from .kv_store import KVStore, to_f64
+from .kv_store import INPUT_DTYPE, KVStore, to_f64
 
 
 class OracleRun:
@@ -22,7 +22,8 @@ class OracleRun:
         self.wl = wl
         self.bm = BlockManager(wl.n_blocks, wl.block_size, wl.free_order)
         self.st = (KVStore(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads,
-                           wl.head_dim, wl.dtype) if with_store else None)
+                           wl.head_dim, wl.dtype, k_scale=getattr(wl, "k_scale", 1.0),
+                           v_scale=getattr(wl, "v_scale", 1.0)) if with_store else None)
         self.build_cows = []
         for op in wl.build_ops:
             self.apply(op)
@@ -63,7 +64,7 @@ class OracleRun:
         listed sequence indices / heads only)."""
         wl = self.wl
         idx = range(len(wl.decode_seqs)) if seq_index is None else seq_index
-        qf = to_f64(q, wl.dtype)
+        qf = to_f64(q, INPUT_DTYPE[wl.dtype])
         out = np.zeros((len(wl.decode_seqs), wl.n_q_heads, wl.head_dim))
         for i in idx:
             s = wl.decode_seqs[i]
@@ -107,7 +108,7 @@ class OracleRun:
         ``{chunk index: out [c, H_q, D_h]}``."""
         offs = np.cumsum([0] + [c for _, c in self.wl.chunks])
         idx = range(len(self.wl.chunks)) if chunk_index is None else chunk_index
-        qf = to_f64(q, self.wl.dtype)
+        qf = to_f64(q, INPUT_DTYPE[self.wl.dtype])
         res = {}
         for i in idx:
             seq, c = self.wl.chunks[i]

@@ -32,6 +32,7 @@ KV_OPT_DECODE_PATH = 1
 KV_OPT_PDL = 2
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
+KV_DTYPE_FP8_E4M3 = 2
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -56,6 +57,7 @@ SIGNATURES = [
     ("kv_pool_check", C.c_int, [_vp]),
     ("kv_block_refcount", C.c_int, [_vp, C.c_int32, _ip]),
     ("kv_pool_set_option", C.c_int, [_vp, C.c_int, C.c_int]),
+    ("kv_pool_set_fp8_scales", C.c_int, [_vp, C.c_float, C.c_float]),
     ("kv_pool_device_status", C.c_int, [_vp, _vp, _ip]),
     ("block_alloc", C.c_int, [_vp, C.c_int, _i32p]),
     ("block_free", C.c_int, [_vp, _i32p, C.c_int]),

@@ -15,7 +15,7 @@ import numpy as np
 from . import _lib
 from ._lib import check, i32, lib, ptr_f32, ptr_i32, ptr_i64, vp
 
-DTYPES = {"f32": _lib.KV_DTYPE_F32, "bf16": _lib.KV_DTYPE_BF16}
+DTYPES = {"f32": _lib.KV_DTYPE_F32, "bf16": _lib.KV_DTYPE_BF16, "fp8_e4m3": _lib.KV_DTYPE_FP8_E4M3}
 
 
 def _stream(stream) -> C.c_void_p:
@@ -44,7 +44,7 @@ class PagedKVCache:
         if allocate and k_cache is None:
             import torch
 
-            tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+            tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[dtype]
             shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
             self.k = torch.empty(shape, dtype=tdt, device=device)
             self.v = torch.empty(shape, dtype=tdt, device=device)
@@ -82,6 +82,10 @@ class PagedKVCache:
 
     def kv_pool_set_option(self, option, value):
         check(lib.kv_pool_set_option(self.handle, int(option), int(value)), "kv_pool_set_option")
+
+    def kv_pool_set_fp8_scales(self, k_scale, v_scale):
+        check(lib.kv_pool_set_fp8_scales(self.handle, float(k_scale), float(v_scale)),
+              "kv_pool_set_fp8_scales")
 
     def kv_block_refcount(self, block_id):
         out = C.c_int()

@@ -14,6 +14,7 @@
 // handles, free blocks needed) and only then changes state, so a failing
 // call changes nothing.
 
+#include <cmath>
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -111,10 +112,11 @@ kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_hea
   if (!out) return KV_ERR_INVALID_ARG;
   *out = nullptr;
   if (n_layers <= 0 || n_blocks <= 0 || block_size <= 0 || block_size > 256 || n_kv_heads <= 0 ||
-      head_dim <= 0 || (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_BF16))
+      head_dim <= 0 ||
+      (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_BF16 && dtype != KV_DTYPE_FP8_E4M3))
     return KV_ERR_INVALID_ARG;
   if ((k_cache == nullptr) != (v_cache == nullptr)) return KV_ERR_INVALID_ARG;
-  const int esize = dtype == KV_DTYPE_F32 ? 4 : 2;
+  const int esize = dtype == KV_DTYPE_F32 ? 4 : (dtype == KV_DTYPE_BF16 ? 2 : 1);
   if (k_cache && ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15))
     return KV_ERR_INVALID_ARG;
   if ((static_cast<int64_t>(n_kv_heads) * head_dim * esize) % 16 != 0) return KV_ERR_INVALID_ARG;
@@ -137,6 +139,7 @@ kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_hea
   p->D = head_dim;
   p->dtype = dtype;
   p->esize = esize;
+  p->in_esize = dtype == KV_DTYPE_F32 ? 4 : 2;
   p->k = k_cache;
   p->v = v_cache;
   p->d_status = d_status;
@@ -199,6 +202,15 @@ kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
     return KV_OK;
   }
   return KV_ERR_INVALID_ARG;
+}
+
+kvStatus kv_pool_set_fp8_scales(kvPool* p, float k_scale, float v_scale) {
+  if (!p || p->dtype != KV_DTYPE_FP8_E4M3) return KV_ERR_INVALID_ARG;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return KV_ERR_INVALID_ARG;
+  p->k_scale = k_scale;
+  p->v_scale = v_scale;
+  return KV_OK;
 }
 
 kvStatus kv_block_refcount(const kvPool* p, int32_t id, int* out) {

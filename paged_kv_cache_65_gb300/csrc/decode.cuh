@@ -54,7 +54,8 @@ struct DecodeArgs {
   float* ws_o;   // [n_slots][columns][D]
   int32_t* status;
   int n_seq, max_blocks, layer, n_blocks, block_size, n_kv_heads, n_q_heads;
-  float qscale;  // scale * log2(e), folded into q
+  float qscale;  // scale * log2(e) (times the K scale of an FP8 pool), folded into q
+  float vscale;  // V scale of an FP8 pool (1 otherwise)
   int grid;
   // sharing-aware plan (tensor-core pass only); segs == nullptr: one segment
   // per (sequence, K/V head) taken from the context lengths

@@ -56,6 +56,31 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same MMA on fp16 operands (the FP8 pass: E4M3 codes convert exactly).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) floats -> f16x2, lo in the low half, saturating at +-65504
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// four E4M3 codes (bytes, lowest first) -> two f16x2 words (exact)
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -70,28 +95,59 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Tokens per stage of the tensor-core pass: 64 tokens (16 KiB of K and 16
-// KiB of V at D = 128).
+// KiB of V at D = 128 in bf16, 8 KiB each in FP8).
 constexpr int mma_stage_tokens(int D) { return 16 * 4 * (D == 64 ? 2 : 1); }
 
-template <int D, int G>
+// F8: the pool holds E4M3 codes; each consumer warp converts its 16-token
+// tile of K and V (exactly) into fp16 in a private buffer laid out like a
+// bf16 stage tile, and the contractions run on fp16 operands.
+template <int D, int G, bool F8 = false>
 struct MmaCfg {
   static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
   static constexpr int TILES = TS / 16;           // 16-token tiles per stage
   static constexpr int KS = D / 16;               // k-steps of Q.K and m-tiles of O^T
-  static constexpr int HALVES = D / 64;           // 64-element swizzled row halves
-  static constexpr int HALF_BYTES = TS * 128;     // one half of a K (or V) stage
-  static constexpr int STAGE_BYTES = TS * D * 2;  // K (or V) per stage
+  static constexpr int ESZ = F8 ? 1 : 2;          // bytes per stored element
+  static constexpr int HALVES = F8 ? 1 : D / 64;  // 128-byte swizzled boxes per row set
+  static constexpr int HALF_BYTES = TS * 128;     // one box column of a K (or V) stage
+  static constexpr int STAGE_BYTES = TS * D * ESZ;  // K (or V) per stage
+  static constexpr int PRIV_HALF = 16 * 128;        // F8: one half of a converted tile
+  static constexpr int PRIV_BYTES = F8 ? 2 * 2 * PRIV_HALF : 0;  // F8: K and V tiles per warp
   static constexpr int NST = 3;                   // stages in the ring
   static constexpr int CC = 4;                    // columns per combine pass
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!F8 || D == 128, "FP8 rows are 128 codes");
   static_assert(G >= 1 && G <= 8, "group size");
   static_assert(TILES % kConsumerWarps == 0, "whole tiles per warp");
 };
 
-template <int D, int G>
+// One warp: rows row0 .. row0 + 15 of an FP8 stage (128-byte rows, 128-byte
+// swizzle) into an fp16 tile of 16 rows x two 64-element halves with the
+// same swizzle (the layout the bf16 pass reads from its stage).
+__device__ __forceinline__ void fp8_tile_to_f16(uint32_t st, uint32_t dst, int row0, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = lane + 32 * i;  // (row, 16-code chunk) of 16 x 8
+    const int r = idx >> 3, c = idx & 7;
+    const int R = row0 + r;
+    uint32_t w0, w1, w2, w3;
+    lds128(st + R * 128 + ((c ^ (R & 7)) << 4), w0, w1, w2, w3);
+    uint32_t h[8];
+    e4m3x4_to_f16(w0, h[0], h[1]);
+    e4m3x4_to_f16(w1, h[2], h[3]);
+    e4m3x4_to_f16(w2, h[4], h[5]);
+    e4m3x4_to_f16(w3, h[6], h[7]);
+    const uint32_t hb = dst + (c >> 2) * (16 * 128) + r * 128;
+    const int j0 = (c & 3) * 2;
+    sts128(hb + ((j0 ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+    sts128(hb + (((j0 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
+
+template <int D, int G, bool F8 = false>
 constexpr int decode_mma_smem_bytes() {
-  using C = MmaCfg<D, G>;
+  using C = MmaCfg<D, G, F8>;
   return 2 * C::NST * C::STAGE_BYTES        // K and V stages
+         + kConsumerWarps * C::PRIV_BYTES   // F8: converted tiles
          + kConsumerWarps * C::CC * D * 4   // combine: O per warp, CC columns at a time
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
@@ -161,11 +217,11 @@ __device__ inline int plan_find(const PlanSeg* segs, int n_segs, long long r0) {
   return lo;
 }
 
-template <int D, int G, bool PLAN>
+template <int D, int G, bool PLAN, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-  using C = MmaCfg<D, G>;
+  using C = MmaCfg<D, G, F8>;
   constexpr int NST = C::NST;
   // the declared alignment stays at 16 so that the explicit round-up to the
   // 1 KiB the 128-byte swizzle needs is never folded away
@@ -174,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE_BYTES;
-  float* cmb_o = reinterpret_cast<float*>(v_st + NST * C::STAGE_BYTES);
+  unsigned char* priv = v_st + NST * C::STAGE_BYTES;  // F8: converted tiles
+  float* cmb_o = reinterpret_cast<float*>(priv + kConsumerWarps * C::PRIV_BYTES);
   float* cmb_ml = cmb_o + kConsumerWarps * C::CC * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * 8 * 2);
   uint64_t* empty = full + NST;
@@ -188,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int UR = B < C::TS ? B : C::TS;      // rows per TMA box (a multiple of 8)
   const int SB = B < C::TS ? C::TS / B : 1;  // boxes per stage
   const int STG = SB * UR;                   // tokens per stage
-  const uint32_t unit_bytes = (uint32_t)UR * D * 2;  // K (or V) bytes of one box row set
+  const uint32_t unit_bytes = (uint32_t)UR * D * C::ESZ;  // K (or V) bytes of one box row set
 
   // self-check: swizzled TMA destinations must sit on 1 KiB boundaries
   if ((smem_u32(k_st) & 1023u) != 0u) {
@@ -379,6 +436,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int ks = 0; ks < C::KS; ++ks) {
         qf[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
         qf[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
+        if constexpr (F8) {  // bf16 pairs -> fp16 pairs (exact in fp16's range)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            qf[ks][i] = pack_f16(__uint_as_float(qf[ks][i] << 16),
+                                 __uint_as_float(qf[ks][i] & 0xffff0000u));
+        }
       }
     }
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -400,6 +463,27 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 1
       for (int tt = wt; tt < C::TILES; tt += WT) {
         if (tt * 16 >= nvalid) break;
+        // tile sources: the stage itself, or (F8) this warp's converted copy
+        uint32_t kt = kb, vt = vb;
+        int hb = C::HALF_BYTES, rsub = 0;
+        if constexpr (F8) {
+          const uint32_t pk = smem_u32(priv) + warp * C::PRIV_BYTES;
+          __syncwarp();  // the previous tile's reads of the buffer are done
+          fp8_tile_to_f16(kb, pk, tt * 16, lane);
+          fp8_tile_to_f16(vb, pk + 2 * C::PRIV_HALF, tt * 16, lane);
+          __syncwarp();
+          kt = pk;
+          vt = pk + 2 * C::PRIV_HALF;
+          hb = C::PRIV_HALF;
+          rsub = tt * 16;
+        }
+        auto mma16 = [&](float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                         uint32_t b0, uint32_t b1) {
+          if constexpr (F8)
+            mma_f16(d, a0, a1, a2, a3, b0, b1);
+          else
+            mma_bf16(d, a0, a1, a2, a3, b0, b1);
+        };
         // ---- S^T = K . Q^T (two independent accumulator chains)
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -408,11 +492,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int ks = 0; ks < C::KS; ++ks) {
             const int d0 = ks * 16 + (lane >> 4) * 8;
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(swz(kb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
+            ldsm_x4(swz(kt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
             if (ks & 1)
-              mma_bf16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              mma16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             else
-              mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              mma16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           }
 #pragma unroll
           for (int i = 0; i < 4; ++i) s[i] += s2[i];
@@ -438,14 +522,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float p2 = exp2_approx(s[2] - mn0), p3 = exp2_approx(s[3] - mn1);
         l_run[0] = l_run[0] * al0 + (p0 + p2);
         l_run[1] = l_run[1] * al1 + (p1 + p3);
-        // ---- P^T fragments: bf16 high part and remainder, transposed
-        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-        const uint32_t l01 = pack_bf16(p0 - __uint_as_float(h01 << 16),
-                                       p1 - __uint_as_float(h01 & 0xffff0000u));
-        const uint32_t l23 = pack_bf16(p2 - __uint_as_float(h23 << 16),
-                                       p3 - __uint_as_float(h23 & 0xffff0000u));
-        const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
-        const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+        // ---- P^T fragments, transposed: bf16 high part and remainder (P
+        // keeps ~16 mantissa bits), or (F8) one fp16 part (P <= 1: 11 bits,
+        // far inside the tolerance)
+        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+        if constexpr (F8) {
+          bh0 = movm_t(pack_f16(p0, p1));
+          bh1 = movm_t(pack_f16(p2, p3));
+        } else {
+          const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+          const uint32_t l01 = pack_bf16(p0 - __uint_as_float(h01 << 16),
+                                         p1 - __uint_as_float(h01 & 0xffff0000u));
+          const uint32_t l23 = pack_bf16(p2 - __uint_as_float(h23 << 16),
+                                         p3 - __uint_as_float(h23 & 0xffff0000u));
+          bh0 = movm_t(h01);
+          bh1 = movm_t(h23);
+          bl0 = movm_t(l01);
+          bl1 = movm_t(l23);
+        }
         // ---- rescale O^T (columns 2t, 2t+1) and accumulate V^T . P^T.  In a
         // partial tile the rows past the context hold whatever the pool held
         // there (possibly NaN bit patterns): their V^T elements are zeroed,
@@ -468,9 +562,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int mt = 0; mt < C::KS; ++mt) {
             const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz(vb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
-            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            ldsm_x4_t(swz(vt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
+            mma16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            if constexpr (!F8) mma16(o[mt], a0, a1, a2, a3, bl0, bl1);
           }
         } else {
           const uint32_t mlo =
@@ -481,13 +575,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int mt = 0; mt < C::KS; ++mt) {
             const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz(vb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
+            ldsm_x4_t(swz(vt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
             a0 &= mlo;
             a1 &= mlo;
             a2 &= mhi;
             a3 &= mhi;
-            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            mma16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            if constexpr (!F8) mma16(o[mt], a0, a1, a2, a3, bl0, bl1);
           }
         }
       }
@@ -495,6 +589,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
 
+    if constexpr (F8) {  // V codes carry x / v_scale
+#pragma unroll
+      for (int mt = 0; mt < C::KS; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] *= a.vscale;
+    }
     // ---- combine the states of the warps that share an n-tile
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {

@@ -50,8 +50,9 @@ kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizz
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->H) * p->D * p->esize};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows)};
   const cuuint32_t estride[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      p->dtype == KV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType dt = p->dtype == KV_DTYPE_BF16     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : p->dtype == KV_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r = fn(out, dt, 2, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -82,7 +83,18 @@ kvStatus ensure_device(kvPool* p) {
   if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
       cudaSuccess)
     return KV_ERR_CUDA;
-  if (p->D == 64 || p->D == 128) {
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {
+    // FP8 codes: only the warp-level MMA pass, one 128-byte swizzled box
+    // (128 codes, all of D_h = 128) by min(B, 64) rows
+    if (!pool_tensor_core_shape(p)) return KV_ERR_UNSUPPORTED;
+    const int tsm = pkv::mma_stage_tokens(p->D);
+    const int rm = p->B < tsm ? p->B : tsm;
+    kvStatus s = encode_cache_map(p, p->k, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
+    if (s != KV_OK) return s;
+    s = encode_cache_map(p, p->v, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));
+    if (s != KV_OK) return s;
+    p->mma_ok = true;
+  } else if (p->D == 64 || p->D == 128) {
     const int ts = pkv::stage_tokens(p->esize, p->D);
     if (p->B > ts && p->B % ts != 0) return KV_ERR_UNSUPPORTED;
     const int rows = p->B < ts ? p->B : ts;
@@ -129,6 +141,56 @@ __global__ void slot_write_kernel(const uint4* __restrict__ k_new, const uint4* 
   for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
     kc[dst + v] = k_new[src + v];
     vc[dst + v] = v_new[src + v];
+  }
+}
+
+// Slot write into an FP8 pool: one CTA per (token, layer); each thread turns
+// 8 bfloat16 values of the token's K (and V) row into 8 E4M3 codes of
+// x / scale: float32 IEEE division, then the nearest code, ties to even,
+// saturating at 448 ("第 8 章 推理优化" §8.4.2's narrower KV, in the
+// format of the pool's header description).
+__global__ void slot_write_fp8_kernel(const uint4* __restrict__ k_new,
+                                      const uint4* __restrict__ v_new,
+                                      const int64_t* __restrict__ slots, int n_tok, uint2* kc,
+                                      uint2* vc, int layer, long long slots_per_layer,
+                                      int row_vecs, float k_scale, float v_scale,
+                                      int32_t* status) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
+  const int i = blockIdx.x;
+  const int ly = layer >= 0 ? layer : blockIdx.y;
+  const int64_t slot = slots[i];
+  if (slot < 0) return;
+  if (slot >= slots_per_layer) {
+    if (threadIdx.x == 0) record_status(status, KV_DEV_BAD_SLOT);
+    return;
+  }
+  // row_vecs: 8-element groups per token row (H_kv * D_h / 8)
+  const long long src = ((layer >= 0 ? 0LL : (long long)blockIdx.y * n_tok) + i) * row_vecs;
+  const long long dst = ((long long)ly * slots_per_layer + slot) * row_vecs;
+  auto quant8 = [](uint4 x, float scale) -> uint2 {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t word = w[2 * h + k];
+        const float lo = __fdiv_rn(__uint_as_float(word << 16), scale);
+        const float hi = __fdiv_rn(__uint_as_float(word & 0xffff0000u), scale);
+        uint16_t c;
+        // the first source goes to the upper byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+        b |= static_cast<uint32_t>(c) << (16 * k);
+      }
+      out[h] = b;
+    }
+    return make_uint2(out[0], out[1]);
+  };
+  for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) {
+    kc[dst + v] = quant8(k_new[src + v], k_scale);
+    vc[dst + v] = quant8(v_new[src + v], v_scale);
   }
 }
 
@@ -403,6 +465,18 @@ kvStatus reshape_and_cache(kvPool* p, int layer, const void* d_k_new, const void
   if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KV_ERR_INVALID_ARG;
   kvStatus s = ensure_device(p);
   if (s != KV_OK) return s;
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {
+    const int row_vecs = p->H * p->D / 8;
+    dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
+    const int threads = row_vecs >= 128 ? 128 : (row_vecs >= 64 ? 64 : 32);
+    const cudaError_t e = pkv::launch_kernel(
+        p->pdl, slot_write_fp8_kernel, grid, dim3(threads), 0, as_stream(stream),
+        reinterpret_cast<const uint4*>(d_k_new), reinterpret_cast<const uint4*>(d_v_new),
+        d_slot_mapping, n_tokens, reinterpret_cast<uint2*>(p->k), reinterpret_cast<uint2*>(p->v),
+        layer, static_cast<long long>(p->N) * p->B, row_vecs, p->k_scale, p->v_scale,
+        p->d_status);
+    return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  }
   const int row_vecs = p->H * p->D * p->esize / 16;
   dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
   const int threads = row_vecs >= 128 ? 128 : (row_vecs >= 64 ? 64 : 32);
@@ -448,6 +522,11 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   a.n_q_heads = n_q_heads;
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.vscale = 1.f;
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {  // codes carry x / scale
+    a.qscale *= p->k_scale;
+    a.vscale = p->v_scale;
+  }
   a.grid = 0;
   a.segs = nullptr;
   a.members = nullptr;
@@ -458,7 +537,13 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  if (kern == kKernelTc) {
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {
+    if (kern != kKernelMma) return KV_ERR_UNSUPPORTED;  // FP8: warp-level MMA pass only
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+    e = pkv::launch_mma_fp8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
+                            as_stream(stream), p->pdl, &supported);
+  } else if (kern == kKernelTc) {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
     e = pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io, as_stream(stream),
@@ -588,6 +673,11 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   a.n_q_heads = n_q_heads;
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.vscale = 1.f;
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {  // codes carry x / scale
+    a.qscale *= p->k_scale;
+    a.vscale = p->v_scale;
+  }
   a.grid = 0;
   a.segs = reinterpret_cast<const PlanSeg*>(dp + hd.seg_off);
   a.members = reinterpret_cast<const int32_t*>(dp + hd.mem_off);
@@ -600,7 +690,11 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   const cudaError_t e =
       tc ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
                                as_stream(stream), p->pdl)
-         : pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+      : p->dtype == KV_DTYPE_FP8_E4M3
+          ? pkv::launch_mma_fp8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                                &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,
+                                &supported)
+          : pkv::launch_mma_bf16(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
                                  &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,
                                  &supported);
   if (!supported) return KV_ERR_UNSUPPORTED;
@@ -669,11 +763,11 @@ StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks
   const size_t L = p->L, n = n_seq;
   size_t off = 0;
   l.q = off;
-  off += align256(L * n * n_q_heads * p->D * p->esize);
+  off += align256(L * n * n_q_heads * p->D * p->in_esize);
   l.k = off;
-  off += align256(L * n * p->H * p->D * p->esize);
+  off += align256(L * n * p->H * p->D * p->in_esize);
   l.v = off;
-  off += align256(L * n * p->H * p->D * p->esize);
+  off += align256(L * n * p->H * p->D * p->in_esize);
   l.slots = off;
   off += align256(n * sizeof(int64_t));
   l.pairs = off;
@@ -799,8 +893,8 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   // in one copy
   cudaStream_t st = as_stream(stream);
   unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
-  const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->esize;
-  const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->esize;
+  const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->in_esize;
+  const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->in_esize;
   const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
   bool ok = true;
   ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
@@ -819,12 +913,12 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   for (int layer = 0; layer < p->L; ++layer) {
     if (planned)
       s = paged_decode_attention_planned(
-          p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
+          p, layer, d + l.q + layer * q_layer * p->in_esize, n_q_heads,
           reinterpret_cast<const int32_t*>(d + l.table), max_blocks, d + l.plan, h_plan, scale,
           d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
           d + l.ws, staging_bytes - l.ws, stream);
     else
-      s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->esize, n_q_heads,
+      s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->in_esize, n_q_heads,
                                  reinterpret_cast<const int32_t*>(d + l.table), max_blocks,
                                  reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale,
                                  d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,

@@ -17,6 +17,8 @@ struct kvSeq {
 struct kvPool {
   // shape
   int L = 0, N = 0, B = 0, H = 0, D = 0, dtype = 0, esize = 0;
+  int in_esize = 0;                 // bytes of a q / new K/V element (bf16 for FP8 pools)
+  float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code = e4m3(x / scale)
   // caller-owned device memory
   void* k = nullptr;
   void* v = nullptr;
@@ -53,13 +55,20 @@ struct kvPool {
 // box starts on 1 KiB (B a multiple of 8) and a stage holds whole blocks or a
 // block whole stages.
 inline bool pool_tensor_core_shape(const kvPool* p) {
-  if (p->dtype != KV_DTYPE_BF16 || (p->D != 64 && p->D != 128) || p->B % 8 != 0) return false;
+  if (p->dtype == KV_DTYPE_FP8_E4M3) {
+    // FP8: rows of 128 one-byte codes, one 128-byte swizzled box per row set
+    if (p->D != 128 || p->B % 8 != 0) return false;
+  } else if (p->dtype != KV_DTYPE_BF16 || (p->D != 64 && p->D != 128) || p->B % 8 != 0) {
+    return false;
+  }
   const int t = p->D == 64 ? 128 : 64;
   return p->B <= t ? t % p->B == 0 : p->B % t == 0;
 }
 
 // The tcgen05 pass: the tensor-core shape with D_h = 128.
-inline bool pool_tc_shape(const kvPool* p) { return pool_tensor_core_shape(p) && p->D == 128; }
+inline bool pool_tc_shape(const kvPool* p) {
+  return p->dtype == KV_DTYPE_BF16 && pool_tensor_core_shape(p) && p->D == 128;
+}
 
 // Largest CTA count the split pass uses; sizes the decode workspace.
 constexpr int kMaxDecodeCtas = 1024;

@@ -18,8 +18,9 @@ from .cache import PagedKVCache
 
 
 def to_device(x: np.ndarray, dtype: str, device) -> torch.Tensor:
-    """Stored elements (float32, or bfloat16 bit patterns as uint16) to a
-    device tensor of the pool dtype, bit for bit."""
+    """Input elements (float32, or bfloat16 bit patterns as uint16) to a
+    device tensor of the pool's input dtype (bfloat16 for FP8 pools), bit for
+    bit."""
     if dtype == "f32":
         return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
     t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16))

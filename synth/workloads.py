@@ -34,6 +34,16 @@ Chunked-prefill rounds ("KV ç¼“å­˜ç®¡ç†", chunked-prefill section; "ç¬¬ 8 ç«  æ
                    1, 2, 4, 6, 8, 10, 12 and 16 (histories 0 to 7680), 4096
                    query tokens in all.
 
+FP8 (E4M3) pools ("ç¬¬ 8 ç«  æŽ¨ç†ä¼˜åŒ–" Â§8.4.2's narrower KV; values are written as
+bf16 rows and stored as codes of x / scale):
+
+* ``fp8_small``   -- 1 layer, H_q = 16, H_kv = 4, D_h = 128, B = 16, 128 blocks,
+                   K scale 0.5, V scale 2.0: contexts 1, 15, 16, 17, 70 and
+                   333, and two sequences forked from a 150-token prefix whose
+                   parent stays alive (171 and 151 tokens; the step copies the
+                   shared tail for the second).
+* ``qwen_2k_fp8`` -- ``qwen_2k`` with an FP8 pool (scales 1).
+
 Context lengths named above are the lengths after the first decode step
 (the step writes its token first, then attends over every position up to
 and including it).
@@ -73,7 +83,8 @@ def torch_seed(seed_words) -> int:
 
 
 def storage_dtype(dtype: str):
-    return {"f32": np.float32, "bf16": np.uint16}[dtype]
+    """Element type of the values a caller writes (FP8 pools take bf16)."""
+    return {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint16}[dtype]
 
 
 def storage_values(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -82,7 +93,7 @@ def storage_values(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "f32":
         return x
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp8_e4m3"):  # FP8 pools are written with bf16 rows
         import torch
 
         t = torch.from_numpy(x).to(torch.bfloat16)
@@ -110,10 +121,15 @@ class Workload:
     build_ops: list = field(default_factory=list)
     decode_seqs: list = field(default_factory=list)
     notes: str = ""
+    # FP8 pools: codes of x / scale (keyword-only: positional fields keep
+    # their order in subclasses)
+    k_scale: float = field(default=1.0, kw_only=True)
+    v_scale: float = field(default=1.0, kw_only=True)
 
     @property
     def elem_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        """Bytes of one stored K or V element."""
+        return {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[self.dtype]
 
     # values --------------------------------------------------------------
     def append_values(self, value_seed: int, n_tokens: int):
@@ -189,14 +205,34 @@ def _tiny(seed: int = 0) -> Workload:
                     "context lengths 7, 13, 1, 16 after the step")
 
 
-def _qwen_2k(seed: int = 1) -> Workload:
+def _qwen_2k(seed: int = 1, dtype: str = "bf16") -> Workload:
     n_seq, n_blocks = 37, 5461
     rng = np.random.Generator(np.random.PCG64(_seed_seq((seed, 4))))
     ctx = rng.integers(2048, 2303, size=n_seq, endpoint=True)
     ops = [("append", s, int(c) - 1, s) for s, c in enumerate(ctx)]
-    return Workload("qwen_2k", 1, n_blocks, 16, 32, 8, 128, "bf16", seed,
+    name = "qwen_2k" if dtype == "bf16" else "qwen_2k_fp8"
+    return Workload(name, 1, n_blocks, 16, 32, 8, 128, dtype, seed,
                     permutation((seed, 0), n_blocks), ops, list(range(n_seq)),
                     "37 independent sequences, context U[2048, 2303]")
+
+
+def _qwen_2k_fp8(seed: int = 1) -> Workload:
+    return _qwen_2k(seed, "fp8_e4m3")
+
+
+def _fp8_small(seed: int = 8) -> Workload:
+    ctx = [1, 15, 16, 17, 70, 333]
+    ops = [("append", s, c - 1, s) for s, c in enumerate(ctx) if c > 1]
+    # a 150-token prefix (a partly filled tail block) forked into two more
+    # sequences while its parent stays alive: the first append of each
+    # branch copies the shared tail
+    parent = 100
+    ops += [("append", parent, 150, 50), ("fork", parent, 6), ("fork", parent, 7),
+            ("append", 6, 20, 51)]
+    return Workload("fp8_small", 1, 128, 16, 16, 4, 128, "fp8_e4m3", seed,
+                    permutation((seed, 0), 128), ops, list(range(8)),
+                    "contexts 1, 15, 16, 17, 70, 333, 171, 151; a 150-token shared prefix",
+                    k_scale=0.5, v_scale=2.0)
 
 
 def _shared_8k(seed: int = 2) -> Workload:
@@ -263,6 +299,8 @@ WORKLOADS = {
     "pool36": _pool36,
     "prefill_tiny": _prefill_tiny,
     "prefill_4k": _prefill_4k,
+    "fp8_small": _fp8_small,
+    "qwen_2k_fp8": _qwen_2k_fp8,
 }
 
 

@@ -1,0 +1,174 @@
+"""FP8 (E4M3) pools on the GPU against the oracle: the codes the slot write
+stores and the blocks copy-on-write copies are bit-exact; decode attention
+(plain and planned, warp-level MMA pass) matches the oracle's attention over
+the dequantized values within the bf16 tolerance."""
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.runner import OracleRun
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+TOL = 2e-3
+
+
+def make(wl, fill=0):
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
+                         wl.dtype, free_order=wl.free_order)
+    cache.kv_pool_set_fp8_scales(wl.k_scale, wl.v_scale)
+    cache.k.fill_(fill)
+    cache.v.fill_(fill)
+    run = DeviceRun(cache, wl.n_q_heads)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    return cache, run
+
+
+def nan_code_equal(a, b):
+    """Byte-identical, except that any two E4M3 NaN codes (0x7F, 0xFF) match."""
+    na = (a & 0x7F) == 0x7F
+    nb = (b & 0x7F) == 0x7F
+    return bool(np.array_equal(na, nb) and np.array_equal(a[~na], b[~nb]))
+
+
+def max_err(gpu, ref):
+    return float(np.max(np.abs(gpu.astype(np.float64) - ref))) if ref.size else 0.0
+
+
+def fp8_workload(name, G, B, seed, ctxs, k_scale=1.0, v_scale=1.0, n_blocks=256):
+    H = 2
+    ops = [("append", s, c - 1, s) for s, c in enumerate(ctxs) if c > 1]
+    return synth.Workload(name, 1, n_blocks, B, H * G, H, 128, "fp8_e4m3", seed,
+                          synth.permutation((seed, 9), n_blocks), ops, list(range(len(ctxs))),
+                          k_scale=k_scale, v_scale=v_scale)
+
+
+def test_fp8_small_codes_cow_and_outputs():
+    wl = synth.workload("fp8_small")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    # the build's writes (values quantized on the device) are the oracle's codes
+    assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+    assert nan_code_equal(cache.v.cpu().numpy(), orc.st.V)
+    for step in range(2):
+        so, co, q, outs = orc.step(step)
+        _, k, v = wl.step_values(step)
+        sg, pg, og = run.step(wl.decode_seqs, q, k, v)
+        assert list(sg) == so and [tuple(p) for p in pg] == co
+        if step == 0:
+            assert len(co) == 1  # the second branch copies the shared tail
+        assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+        assert nan_code_equal(cache.v.cpu().numpy(), orc.st.V)
+        err = max_err(og.cpu().numpy()[0], outs[0])
+        assert err <= TOL, err
+    assert cache.kv_pool_device_status() == 0
+
+
+def test_fp8_small_planned_pass():
+    wl = synth.workload("fp8_small")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v, planned=True)
+    assert list(sg) == so and [tuple(p) for p in pg] == co
+    h_plan, _, _ = run.plan(wl.decode_seqs, run.max_blocks(wl.decode_seqs))
+    from paged_kv_cache_65_gb300.cache import parse_plan
+
+    plan = parse_plan(h_plan)
+    assert plan["kernel"] == 2  # FP8 pools take the warp-level MMA pass
+    assert plan["n_shared_segs"] > 0  # the two branches share 9 blocks
+    err = max_err(og.cpu().numpy()[0], orc.attend(0, qh))
+    assert err <= TOL, err
+    assert cache.kv_pool_device_status() == 0
+
+
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (4, 32), (8, 64), (8, 16)])
+def test_fp8_ragged_shapes(G, B):
+    ctxs = [1, 2, B - 1, B, B + 1, 3 * B + 2, 97, 700]
+    wl = fp8_workload("fp8_ragged", G, B, 10 + G + B, ctxs, k_scale=0.25, v_scale=4.0)
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co, q, outs = orc.step(0)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, q, k, v)
+    assert list(sg) == so
+    assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+    err = max_err(og.cpu().numpy()[0], outs[0])
+    assert err <= TOL, (G, B, err)
+    assert cache.kv_pool_device_status() == 0
+
+
+def test_fp8_unused_slots_holding_nan_codes_do_not_leak():
+    wl = synth.workload("fp8_small")
+    orc = OracleRun(wl)
+    cache, run = make(wl, fill=0xFF)  # every unused slot holds the NaN code
+    so, co, q, outs = orc.step(0)
+    _, k, v = wl.step_values(0)
+    _, _, og = run.step(wl.decode_seqs, q, k, v)
+    got = og.cpu().numpy()[0]
+    assert np.isfinite(got).all()
+    assert max_err(got, outs[0]) <= TOL
+
+
+def test_fp8_qwen_2k_sampled():
+    wl = synth.workload("qwen_2k_fp8")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+    assert list(sg) == so
+    sample = [0, 5, 18, 36]
+    ref = orc.attend(0, qh, seq_index=sample)
+    got = og.cpu().numpy()[0]
+    for i in sample:
+        assert max_err(got[i], ref[i]) <= TOL
+    # the pool's written rows are the oracle's codes
+    assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+    assert cache.kv_pool_device_status() == 0
+
+
+def test_fp8_host_buffer_step():
+    # the whole-step C entry point with host buffers: bf16 q and new K/V in,
+    # quantized on the device, float32 out
+    wl = synth.workload("fp8_small")
+    orc = OracleRun(wl)
+    cache, run = make(wl)
+    max_blocks = 32
+    n = len(wl.decode_seqs)
+    staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
+                          dtype=torch.uint8, device="cuda")
+    for step in range(2):
+        so, co = orc.reserve_step()
+        q = orc.write_step(step, so, co)
+        _, k, v = wl.step_values(step)
+        out = np.zeros((1, n, wl.n_q_heads, wl.head_dim), dtype=np.float32)
+        cache.kv_decode_step_host(wl.decode_seqs, wl.n_q_heads, max_blocks, q[None], k, v, out,
+                                  staging)
+        assert max_err(out[0], orc.attend(0, q)) <= TOL
+    assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+    assert nan_code_equal(cache.v.cpu().numpy(), orc.st.V)
+    assert cache.kv_pool_device_status() == 0
+
+
+def test_fp8_scales_are_checked():
+    from paged_kv_cache_65_gb300 import PagedKVCache
+
+    wl = synth.workload("fp8_small")
+    cache, _ = make(wl)
+    for bad in [(0.0, 1.0), (1.0, -2.0), (float("inf"), 1.0), (float("nan"), 1.0)]:
+        with pytest.raises(Exception):
+            cache.kv_pool_set_fp8_scales(*bad)
+    bf = PagedKVCache(1, 8, 16, 2, 128, "bf16")
+    with pytest.raises(Exception):
+        bf.kv_pool_set_fp8_scales(1.0, 1.0)
