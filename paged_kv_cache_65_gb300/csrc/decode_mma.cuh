@@ -98,9 +98,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // KiB of V at D = 128 in bf16, 8 KiB each in FP8).
 constexpr int mma_stage_tokens(int D) { return 16 * 4 * (D == 64 ? 2 : 1); }
 
-// F8: the pool holds E4M3 codes; each consumer warp converts its 16-token
-// tile of K and V (exactly) into fp16 in a private buffer laid out like a
-// bf16 stage tile, and the contractions run on fp16 operands.
+// F8: the pool holds E4M3 codes and the contractions run on fp16 operands
+// (codes convert exactly).  S = K . Q^T is unchanged by any permutation of
+// the head dimension applied to both operands, so the A fragments of K take
+// d = 16 ks + 4 t .. 4 t + 3 (four consecutive codes, one 32-bit load per
+// row, two conversions) and Q's fragments the same dimensions; V needs its
+// transpose, so each warp converts its 16-token V tile into a private fp16
+// buffer laid out like a bf16 stage tile and reads it with ldmatrix.trans.
 template <int D, int G, bool F8 = false>
 struct MmaCfg {
   static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
@@ -111,7 +115,7 @@ struct MmaCfg {
   static constexpr int HALF_BYTES = TS * 128;     // one box column of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * ESZ;  // K (or V) per stage
   static constexpr int PRIV_HALF = 16 * 128;        // F8: one half of a converted tile
-  static constexpr int PRIV_BYTES = F8 ? 2 * 2 * PRIV_HALF : 0;  // F8: K and V tiles per warp
+  static constexpr int PRIV_BYTES = F8 ? 2 * PRIV_HALF : 0;  // F8: the V tile of a warp
   static constexpr int NST = 3;                   // stages in the ring
   static constexpr int CC = 4;                    // columns per combine pass
   static_assert(D == 64 || D == 128, "head dim");
@@ -122,12 +126,16 @@ struct MmaCfg {
 
 // One warp: rows row0 .. row0 + 15 of an FP8 stage (128-byte rows, 128-byte
 // swizzle) into an fp16 tile of 16 rows x two 64-element halves with the
-// same swizzle (the layout the bf16 pass reads from its stage).
+// same swizzle (the layout the bf16 pass reads from its stage).  Each
+// 8-lane phase takes chunks 0-3 of one row and 4-7 of the next (or the
+// reverse), so that its 16-byte loads and its stores each fall on eight
+// distinct bank groups.
 __device__ __forceinline__ void fp8_tile_to_f16(uint32_t st, uint32_t dst, int row0, int lane) {
+  const int q = lane >> 3, k = lane & 7;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int idx = lane + 32 * i;  // (row, 16-code chunk) of 16 x 8
-    const int r = idx >> 3, c = idx & 7;
+    const int r = 2 * (2 * i + (q >> 1)) + (k >> 2);  // rows 0..15
+    const int c = k ^ ((q & 1) << 2);                // 16-code chunk 0..7
     const int R = row0 + r;
     uint32_t w0, w1, w2, w3;
     lds128(st + R * 128 + ((c ^ (R & 7)) << 4), w0, w1, w2, w3);
@@ -434,13 +442,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           ((long long)seqm * a.n_q_heads + (long long)p.head * G + (colv ? gi : 0)) * D * 2);
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        qf[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
-        qf[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
-        if constexpr (F8) {  // bf16 pairs -> fp16 pairs (exact in fp16's range)
+        if constexpr (F8) {
+          // the dimensions of the permuted K fragments, bf16 pairs -> fp16
+          // pairs (exact in fp16's range)
+          qf[ks][0] = colv ? qw[(ks * 16 + 4 * t) / 2] : 0u;
+          qf[ks][1] = colv ? qw[(ks * 16 + 4 * t + 2) / 2] : 0u;
 #pragma unroll
           for (int i = 0; i < 2; ++i)
             qf[ks][i] = pack_f16(__uint_as_float(qf[ks][i] << 16),
                                  __uint_as_float(qf[ks][i] & 0xffff0000u));
+        } else {
+          qf[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
+          qf[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
         }
       }
     }
@@ -463,17 +476,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 1
       for (int tt = wt; tt < C::TILES; tt += WT) {
         if (tt * 16 >= nvalid) break;
-        // tile sources: the stage itself, or (F8) this warp's converted copy
-        uint32_t kt = kb, vt = vb;
+        // V source: the stage itself, or (F8) this warp's converted copy
+        uint32_t vt = vb;
         int hb = C::HALF_BYTES, rsub = 0;
         if constexpr (F8) {
-          const uint32_t pk = smem_u32(priv) + warp * C::PRIV_BYTES;
+          const uint32_t pv = smem_u32(priv) + warp * C::PRIV_BYTES;
           __syncwarp();  // the previous tile's reads of the buffer are done
-          fp8_tile_to_f16(kb, pk, tt * 16, lane);
-          fp8_tile_to_f16(vb, pk + 2 * C::PRIV_HALF, tt * 16, lane);
+          fp8_tile_to_f16(vb, pv, tt * 16, lane);
           __syncwarp();
-          kt = pk;
-          vt = pk + 2 * C::PRIV_HALF;
+          vt = pv;
           hb = C::PRIV_HALF;
           rsub = tt * 16;
         }
@@ -486,21 +497,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         // ---- S^T = K . Q^T (two independent accumulator chains)
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int r = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        if constexpr (F8) {
+          // rows g and g + 8 of the tile (same swizzle phase g): codes
+          // 16 ks + 4 t .. + 3, one 32-bit load each, straight into fp16
+          const uint32_t ra = kb + (tt * 16 + g) * 128 + t * 4;
 #pragma unroll
           for (int ks = 0; ks < C::KS; ++ks) {
-            const int d0 = ks * 16 + (lane >> 4) * 8;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(swz(kt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
+            const uint32_t off = static_cast<uint32_t>(ks ^ g) << 4;
+            uint32_t wa, wb, a0, a1, a2, a3;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wa) : "r"(ra + off));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wb) : "r"(ra + 8 * 128 + off));
+            e4m3x4_to_f16(wa, a0, a2);
+            e4m3x4_to_f16(wb, a1, a3);
             if (ks & 1)
               mma16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             else
               mma16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           }
+        } else {
+          const int r = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) s[i] += s2[i];
+          for (int ks = 0; ks < C::KS; ++ks) {
+            const int d0 = ks * 16 + (lane >> 4) * 8;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(swz(kb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
+            if (ks & 1)
+              mma16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            else
+              mma16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] += s2[i];
         // ---- scale, mask, tile max per column (columns 2t, 2t+1; tokens g, g+8)
         const int row0 = tt * 16 + g;
         const bool v0 = row0 < nvalid, v1 = row0 + 8 < nvalid;
