@@ -50,9 +50,10 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331667968 + 3491072, "sha": "63bb18cc6a5e9b3f"},
-    ("shared_8k", "decode_mma_kernel"): {"bytes": 170978304 + 3176704, "sha": "63bb18cc6a5e9b3f"},
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1616046848 + 6752512, "sha": "63bb18cc6a5e9b3f"},
+    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331667200 + 3100928, "sha": "a5879904393136b1"},
+    ("shared_8k", "decode_mma_kernel"): {"bytes": 170998272 + 3209728, "sha": "a5879904393136b1"},
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615953664 + 6738432, "sha": "a5879904393136b1"},
+    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169242112 + 3386112, "sha": "a5879904393136b1"},
     ("prefill_4k", "prefill_tc_kernel"): {"bytes": 157367808 + 51861760, "sha": "3eb978eb03b932bd"},
 }
 
