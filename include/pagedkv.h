@@ -185,6 +185,51 @@ kvStatus seq_length(const kvPool* pool, int32_t seq, int* out_len);
 kvStatus seq_block_table(const kvPool* pool, const int32_t* seq_ids, int n_seq, int max_blocks,
                          int32_t* out_table, int32_t* out_context_lens);
 
+/* ------------------------------------------------------- prefix cache -- */
+/* Full-block prefix reuse across requests ("KV 缓存管理", radix-tree section:
+ * longest prefix match, block-aligned truncation, leaf-first LRU eviction;
+ * "第 11 章 KV Cache 内存管理" §11.5: block-level hashing, a key that covers
+ * everything changing the KV numbers).  Host only, no device work.
+ *
+ * With the cache on, a full block is identified by the salt and every token
+ * of its sequence up to the block's end (a chained 64-bit hash finds it; the
+ * block's tokens and its parent are compared, so no hash collision can alias
+ * two prefixes).  A block joins the cache when it fills (at the end of the
+ * append call), if its tokens are known, its key is not cached yet and the
+ * block before it in the same table is cached (or it is the first).  A
+ * cached block whose count drops to 0 stays allocated but dormant; when a
+ * block is needed and the free list is empty, the dormant leaf (no cached
+ * block after it) with the oldest access is evicted to the free list, and
+ * its parent may become such a leaf.  Accesses are stamped by a logical
+ * clock: the blocks a match takes, a block joining the cache, a block turning
+ * dormant, in table order.  kv_pool_check also checks the cache's tree,
+ * counts and eviction set; kv_pool_stats counts dormant blocks as allocated.
+ */
+/* Turn the cache on with a salt standing for the model, template, adapters
+ * and anything else that changes the KV numbers; again with the same salt:
+ * KV_OK; with another: KV_ERR_INVALID_ARG.  Positions written before are
+ * unknown tokens (their blocks never join). */
+kvStatus kv_prefix_cache_enable(kvPool* pool, uint64_t salt);
+/* A new sequence (KV_ERR_INVALID_ARG if it exists, or the cache is off)
+ * starts with the longest chain of cached full blocks matching its prompt
+ * tokens[0 .. n_tokens): *out_matched = that many tokens, a multiple of B
+ * (the tail of a partly matching block counts as a miss and is prefilled
+ * with the rest).  One more count on each taken block. */
+kvStatus seq_match_prefix(kvPool* pool, int32_t seq, const int32_t* tokens, int n_tokens,
+                          int* out_matched);
+/* seq_append_slots / seq_append_tokens with the token ids of the appended
+ * positions (token_ids: one per listed sequence / n_tokens; NULL: unknown).
+ * Blocks may be evicted from the cache to make room. */
+kvStatus seq_append_slots_ids(kvPool* pool, const int32_t* seq_ids, int n_seq,
+                              const int32_t* token_ids, int64_t* out_slots,
+                              int32_t* out_cow_pairs, int* out_n_cow);
+kvStatus seq_append_tokens_ids(kvPool* pool, int32_t seq, int n_tokens, const int32_t* token_ids,
+                               int64_t* out_slots, int32_t* out_cow_pair, int* out_n_cow);
+/* Evict dormant leaves, oldest access first, until the free list holds
+ * target_free blocks or none is left (the pages' low-water-mark round). */
+kvStatus kv_prefix_evict(kvPool* pool, int target_free, int* out_n_evicted);
+kvStatus kv_prefix_stats(const kvPool* pool, int* n_cached, int* n_dormant);
+
 /* ------------------------------------------------------------- device --
  * All pointers below are device pointers.                                */
 

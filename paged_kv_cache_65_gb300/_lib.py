@@ -67,6 +67,12 @@ SIGNATURES = [
     ("seq_append_tokens", C.c_int, [_vp, C.c_int32, C.c_int, _i64p, _i32p, _ip]),
     ("seq_fork", C.c_int, [_vp, C.c_int32, C.c_int32]),
     ("seq_release", C.c_int, [_vp, C.c_int32]),
+    ("kv_prefix_cache_enable", C.c_int, [_vp, C.c_uint64]),
+    ("seq_match_prefix", C.c_int, [_vp, C.c_int32, _i32p, C.c_int, _ip]),
+    ("seq_append_slots_ids", C.c_int, [_vp, _i32p, C.c_int, _i32p, _i64p, _i32p, _ip]),
+    ("seq_append_tokens_ids", C.c_int, [_vp, C.c_int32, C.c_int, _i32p, _i64p, _i32p, _ip]),
+    ("kv_prefix_evict", C.c_int, [_vp, C.c_int, _ip]),
+    ("kv_prefix_stats", C.c_int, [_vp, _ip, _ip]),
     ("seq_length", C.c_int, [_vp, C.c_int32, _ip]),
     ("seq_block_table", C.c_int, [_vp, _i32p, C.c_int, C.c_int, _i32p, _i32p]),
     ("cow_copy", C.c_int, [_vp, _vp, C.c_int, _vp]),

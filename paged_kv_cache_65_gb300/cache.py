@@ -110,23 +110,67 @@ class PagedKVCache:
         check(lib.block_cow(self.handle, int(block_id), C.byref(out)), "block_cow")
         return out.value
 
-    def seq_append_slots(self, seq_ids):
+    def seq_append_slots(self, seq_ids, token_ids=None):
+        """One slot per listed sequence; ``token_ids`` (one per sequence) feed
+        the prefix cache."""
         ids = i32(seq_ids)
         n = ids.size
         slots = np.zeros(max(n, 1), dtype=np.int64)
         pairs = np.zeros((max(n, 1), 2), dtype=np.int32)
         ncow = C.c_int()
-        check(lib.seq_append_slots(self.handle, ptr_i32(ids), n, ptr_i64(slots), ptr_i32(pairs),
-                                   C.byref(ncow)), "seq_append_slots")
+        if token_ids is None:
+            check(lib.seq_append_slots(self.handle, ptr_i32(ids), n, ptr_i64(slots),
+                                       ptr_i32(pairs), C.byref(ncow)), "seq_append_slots")
+        else:
+            toks = i32(token_ids)
+            if toks.size != n:
+                raise ValueError("token_ids: one per sequence")
+            check(lib.seq_append_slots_ids(self.handle, ptr_i32(ids), n, ptr_i32(toks),
+                                           ptr_i64(slots), ptr_i32(pairs), C.byref(ncow)),
+                  "seq_append_slots_ids")
         return slots[:n], pairs[:ncow.value]
 
-    def seq_append_tokens(self, seq, n_tokens):
+    def seq_append_tokens(self, seq, n_tokens, token_ids=None):
         slots = np.zeros(max(n_tokens, 1), dtype=np.int64)
         pair = np.zeros(2, dtype=np.int32)
         ncow = C.c_int()
-        check(lib.seq_append_tokens(self.handle, int(seq), int(n_tokens), ptr_i64(slots),
-                                    ptr_i32(pair), C.byref(ncow)), "seq_append_tokens")
+        if token_ids is None:
+            check(lib.seq_append_tokens(self.handle, int(seq), int(n_tokens), ptr_i64(slots),
+                                        ptr_i32(pair), C.byref(ncow)), "seq_append_tokens")
+        else:
+            toks = i32(token_ids)
+            if toks.size != n_tokens:
+                raise ValueError("token_ids: one per token")
+            check(lib.seq_append_tokens_ids(self.handle, int(seq), int(n_tokens),
+                                            ptr_i32(np.ascontiguousarray(toks)) if n_tokens else
+                                            ptr_i32(np.zeros(1, dtype=np.int32)),
+                                            ptr_i64(slots), ptr_i32(pair), C.byref(ncow)),
+                  "seq_append_tokens_ids")
         return slots[:n_tokens], pair.reshape(1, 2)[:ncow.value]
+
+    # ------------------------------------------------------ prefix cache
+    def kv_prefix_cache_enable(self, salt=0):
+        check(lib.kv_prefix_cache_enable(self.handle, int(salt) & ((1 << 64) - 1)),
+              "kv_prefix_cache_enable")
+
+    def seq_match_prefix(self, seq, tokens):
+        toks = i32(tokens)
+        out = C.c_int()
+        buf = toks if toks.size else np.zeros(1, dtype=np.int32)
+        check(lib.seq_match_prefix(self.handle, int(seq), ptr_i32(buf), int(toks.size),
+                                   C.byref(out)), "seq_match_prefix")
+        return out.value
+
+    def kv_prefix_evict(self, target_free):
+        out = C.c_int()
+        check(lib.kv_prefix_evict(self.handle, int(target_free), C.byref(out)), "kv_prefix_evict")
+        return out.value
+
+    def kv_prefix_stats(self):
+        cached, dormant = C.c_int(), C.c_int()
+        check(lib.kv_prefix_stats(self.handle, C.byref(cached), C.byref(dormant)),
+              "kv_prefix_stats")
+        return cached.value, dormant.value
 
     def seq_fork(self, parent, child):
         check(lib.seq_fork(self.handle, int(parent), int(child)), "seq_fork")

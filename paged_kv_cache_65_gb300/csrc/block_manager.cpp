@@ -28,13 +28,131 @@ int64_t blocks_for(int64_t tokens, int B) { return (tokens + B - 1) / B; }
 
 bool valid_id(const kvPool* p, int32_t id) { return id >= 0 && id < p->N; }
 
+void push_free(kvPool* p, int32_t id) { p->free_list.push_back(id); }
+
+// ------------------------------------------------------------ prefix cache
+// ("KV 缓存管理", radix-tree section: full blocks only, block-aligned
+// truncation, leaf-first LRU eviction of dormant nodes.)
+
+// splitmix64's finalizer, a 64-bit mixing step
+uint64_t mix64(uint64_t x) {
+  x ^= x >> 30;
+  x *= 0xbf58476d1ce4e5b9ULL;
+  x ^= x >> 27;
+  x *= 0x94d049bb133111ebULL;
+  x ^= x >> 31;
+  return x;
+}
+// h_k = H(h_{k-1} || tokens of block k); lookups verify the tokens and the
+// parent, so the hash only has to spread the keys
+uint64_t pc_chain(uint64_t h, const int32_t* t, int B) {
+  h = mix64(h + 0x9e3779b97f4a7c15ULL);
+  for (int i = 0; i < B; ++i) h = mix64(h ^ static_cast<uint32_t>(t[i]));
+  return h;
+}
+uint64_t pc_root(const kvPool* p) { return mix64(p->pc_salt ^ 0x632be59bd9b4e019ULL); }
+
+int64_t available(const kvPool* p) {
+  return static_cast<int64_t>(p->free_list.size()) + p->pc_n_dormant;
+}
+
+void pc_tick(kvPool* p, int32_t id) { p->pc_nodes[id].last = ++p->pc_clock; }
+
+// the cached child of `parent` holding `t` (one block of tokens), or -1
+int32_t pc_find(const kvPool* p, uint64_t h, int32_t parent, const int32_t* t) {
+  auto r = p->pc_index.equal_range(h);
+  for (auto it = r.first; it != r.second; ++it) {
+    const kvPrefixNode& n = p->pc_nodes.at(it->second);
+    if (n.parent == parent && std::equal(n.tokens.begin(), n.tokens.end(), t)) return it->second;
+  }
+  return -1;
+}
+
+// Evict the least recently used dormant leaf: its block returns to the free
+// list, and its parent becomes a candidate if it is left without children
+// and is itself dormant.
+bool pc_evict_one(kvPool* p) {
+  if (p->pc_lru.empty()) return false;
+  const int32_t id = p->pc_lru.begin()->second;
+  p->pc_lru.erase(p->pc_lru.begin());
+  const kvPrefixNode n = p->pc_nodes.at(id);
+  auto r = p->pc_index.equal_range(n.hash);
+  for (auto it = r.first; it != r.second; ++it)
+    if (it->second == id) {
+      p->pc_index.erase(it);
+      break;
+    }
+  p->pc_nodes.erase(id);
+  p->pc_dormant[id] = 0;
+  p->pc_n_dormant -= 1;
+  if (n.parent >= 0) {
+    kvPrefixNode& q = p->pc_nodes.at(n.parent);
+    q.children -= 1;
+    if (q.children == 0 && p->pc_dormant[n.parent]) p->pc_lru.insert({q.last, n.parent});
+  }
+  push_free(p, id);
+  return true;
+}
+
+// Caller has checked available(p) > 0: with an empty free list a dormant
+// leaf exists, since every descendant of a dormant node is dormant.
 int32_t pop_free(kvPool* p) {
+  if (p->free_list.empty()) pc_evict_one(p);
   int32_t id = p->free_list.front();
   p->free_list.pop_front();
   return id;
 }
 
-void push_free(kvPool* p, int32_t id) { p->free_list.push_back(id); }
+// A block's count reached zero: a cached block turns dormant, others free.
+void count_zero(kvPool* p, int32_t id) {
+  auto it = p->pc_on ? p->pc_nodes.find(id) : p->pc_nodes.end();
+  if (it == p->pc_nodes.end()) {
+    push_free(p, id);
+    return;
+  }
+  p->pc_dormant[id] = 1;
+  p->pc_n_dormant += 1;
+  pc_tick(p, id);
+  if (it->second.children == 0) p->pc_lru.insert({it->second.last, id});
+}
+
+// Publish the blocks of a sequence that are full now, from logical block
+// `first_full` on: a block joins the cache when its tokens are known, its key
+// is not cached yet and the block before it in the table is a cached node
+// (or it is the first block).
+void pc_publish(kvPool* p, int32_t seq_id, int64_t first_full) {
+  if (!p->pc_on) return;
+  kvSeq& s = p->seqs[seq_id];
+  const int B = p->B;
+  const int64_t n_full = s.len / B;
+  for (int64_t k = first_full; k < n_full; ++k) {
+    const int32_t id = s.table[k];
+    if (p->pc_nodes.count(id)) continue;
+    bool all_known = true;
+    for (int64_t i = k * B; i < (k + 1) * B; ++i) all_known = all_known && s.known[i];
+    if (!all_known) continue;
+    const int32_t parent = k > 0 ? s.table[k - 1] : -1;
+    if (k > 0 && !p->pc_nodes.count(parent)) continue;
+    const uint64_t h = pc_chain(k > 0 ? p->pc_nodes.at(parent).hash : pc_root(p), &s.tok[k * B], B);
+    if (pc_find(p, h, parent, &s.tok[k * B]) >= 0) continue;
+    kvPrefixNode n;
+    n.hash = h;
+    n.parent = parent;
+    n.tokens.assign(s.tok.begin() + k * B, s.tok.begin() + (k + 1) * B);
+    p->pc_nodes.emplace(id, std::move(n));
+    p->pc_index.insert({h, id});
+    if (parent >= 0) p->pc_nodes.at(parent).children += 1;
+    pc_tick(p, id);
+  }
+}
+
+void record_tokens(kvPool* p, kvSeq& s, const int32_t* ids, int n) {
+  if (!p->pc_on) return;
+  for (int i = 0; i < n; ++i) {
+    s.tok.push_back(ids ? ids[i] : 0);
+    s.known.push_back(ids ? 1 : 0);
+  }
+}
 
 // One token for `seq` (creating it if new).  Caller has already checked
 // that a free block is available whenever this needs one.
@@ -178,14 +296,41 @@ kvStatus kv_pool_check(const kvPool* p) {
       table_refs[id] += 1;
     }
   }
-  int64_t n_alloc = 0;
+  int64_t n_alloc = 0, n_dormant = 0;
   for (int i = 0; i < p->N; ++i) {
-    if ((p->ref[i] > 0) == static_cast<bool>(is_free[i])) return KV_ERR_REFCOUNT;
+    const bool dormant = p->pc_on && p->pc_dormant[i];
+    if ((p->ref[i] > 0) + static_cast<int>(is_free[i]) + static_cast<int>(dormant) != 1)
+      return KV_ERR_REFCOUNT;
     if (p->ref[i] < 0 || p->ext[i] < 0) return KV_ERR_REFCOUNT;
     if (p->ref[i] != table_refs[i] + p->ext[i]) return KV_ERR_REFCOUNT;
     n_alloc += p->ref[i] > 0;
+    n_dormant += dormant;
   }
-  if (static_cast<int64_t>(p->free_list.size()) + n_alloc != p->N) return KV_ERR_REFCOUNT;
+  if (static_cast<int64_t>(p->free_list.size()) + n_alloc + n_dormant != p->N)
+    return KV_ERR_REFCOUNT;
+  if (n_dormant != p->pc_n_dormant) return KV_ERR_REFCOUNT;
+  // the cache is a tree of cached blocks; the eviction set is exactly the
+  // dormant leaves
+  std::unordered_map<int32_t, int32_t> kids;
+  size_t n_leaves = 0;
+  for (const auto& kv : p->pc_nodes) {
+    const int32_t id = kv.first;
+    if (!valid_id(p, id) || is_free[id]) return KV_ERR_REFCOUNT;
+    if (kv.second.parent >= 0) {
+      if (!p->pc_nodes.count(kv.second.parent)) return KV_ERR_REFCOUNT;
+      kids[kv.second.parent] += 1;
+    }
+    if (static_cast<bool>(p->pc_dormant[id]) != (p->ref[id] == 0)) return KV_ERR_REFCOUNT;
+  }
+  for (const auto& kv : p->pc_nodes) {
+    const int32_t want = kids.count(kv.first) ? kids.at(kv.first) : 0;
+    if (kv.second.children != want) return KV_ERR_REFCOUNT;
+    const bool leaf = p->pc_dormant[kv.first] && want == 0;
+    if (leaf != static_cast<bool>(p->pc_lru.count({kv.second.last, kv.first})))
+      return KV_ERR_REFCOUNT;
+    n_leaves += leaf;
+  }
+  if (n_leaves != p->pc_lru.size()) return KV_ERR_REFCOUNT;
   return KV_OK;
 }
 
@@ -245,7 +390,7 @@ kvStatus block_free(kvPool* p, const int32_t* ids, int n) {
     int32_t id = ids[i];
     p->ref[id] -= 1;
     p->ext[id] -= 1;
-    if (p->ref[id] == 0) push_free(p, id);
+    if (p->ref[id] == 0) count_zero(p, id);
   }
   return KV_OK;
 }
@@ -270,7 +415,7 @@ kvStatus block_cow(kvPool* p, int32_t id, int32_t* out_id) {
     *out_id = id;
     return KV_OK;
   }
-  if (p->free_list.empty()) return KV_ERR_NO_FREE_BLOCK;
+  if (available(p) == 0) return KV_ERR_NO_FREE_BLOCK;
   int32_t nid = pop_free(p);
   p->ref[id] -= 1;
   p->ext[id] -= 1;
@@ -284,6 +429,12 @@ kvStatus block_cow(kvPool* p, int32_t id, int32_t* out_id) {
 
 kvStatus seq_append_slots(kvPool* p, const int32_t* seq_ids, int n_seq, int64_t* out_slots,
                           int32_t* out_cow_pairs, int* out_n_cow) {
+  return seq_append_slots_ids(p, seq_ids, n_seq, nullptr, out_slots, out_cow_pairs, out_n_cow);
+}
+
+kvStatus seq_append_slots_ids(kvPool* p, const int32_t* seq_ids, int n_seq,
+                              const int32_t* token_ids, int64_t* out_slots,
+                              int32_t* out_cow_pairs, int* out_n_cow) {
   if (!p || n_seq < 0 || (n_seq > 0 && (!seq_ids || !out_slots || !out_cow_pairs)))
     return KV_ERR_INVALID_ARG;
   {
@@ -295,8 +446,12 @@ kvStatus seq_append_slots(kvPool* p, const int32_t* seq_ids, int n_seq, int64_t*
     auto it = p->seqs.find(seq_ids[i]);
     if (it != p->seqs.end() && it->second.len >= (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
   }
-  if (blocks_needed(p, seq_ids, n_seq) > static_cast<int64_t>(p->free_list.size()))
-    return KV_ERR_NO_FREE_BLOCK;
+  if (blocks_needed(p, seq_ids, n_seq) > available(p)) return KV_ERR_NO_FREE_BLOCK;
+  std::vector<int64_t> first_full(n_seq, 0);
+  for (int i = 0; i < n_seq; ++i) {
+    auto it = p->seqs.find(seq_ids[i]);
+    first_full[i] = it == p->seqs.end() ? 0 : it->second.len / p->B;
+  }
   int n_cow = 0;
   for (int i = 0; i < n_seq; ++i) {
     int32_t src, dst;
@@ -307,12 +462,20 @@ kvStatus seq_append_slots(kvPool* p, const int32_t* seq_ids, int n_seq, int64_t*
       ++n_cow;
     }
   }
+  for (int i = 0; i < n_seq; ++i)
+    record_tokens(p, p->seqs[seq_ids[i]], token_ids ? token_ids + i : nullptr, 1);
+  for (int i = 0; i < n_seq; ++i) pc_publish(p, seq_ids[i], first_full[i]);
   if (out_n_cow) *out_n_cow = n_cow;
   return KV_OK;
 }
 
 kvStatus seq_append_tokens(kvPool* p, int32_t seq, int n_tokens, int64_t* out_slots,
                            int32_t* out_cow_pair, int* out_n_cow) {
+  return seq_append_tokens_ids(p, seq, n_tokens, nullptr, out_slots, out_cow_pair, out_n_cow);
+}
+
+kvStatus seq_append_tokens_ids(kvPool* p, int32_t seq, int n_tokens, const int32_t* token_ids,
+                               int64_t* out_slots, int32_t* out_cow_pair, int* out_n_cow) {
   if (!p || n_tokens < 0 || (n_tokens > 0 && (!out_slots || !out_cow_pair)))
     return KV_ERR_INVALID_ARG;
   int64_t len = 0, have = 0;
@@ -324,7 +487,8 @@ kvStatus seq_append_tokens(kvPool* p, int32_t seq, int n_tokens, int64_t* out_sl
     if (n_tokens > 0 && len % p->B != 0 && p->ref[it->second.table[len / p->B]] > 1) cow = true;
   }
   const int64_t need = blocks_for(len + n_tokens, p->B) - have + (cow ? 1 : 0);
-  if (need > static_cast<int64_t>(p->free_list.size())) return KV_ERR_NO_FREE_BLOCK;
+  if (need > available(p)) return KV_ERR_NO_FREE_BLOCK;
+  const int64_t first_full = len / p->B;
   int n_cow = 0;
   for (int i = 0; i < n_tokens; ++i) {
     int32_t src, dst;
@@ -334,6 +498,10 @@ kvStatus seq_append_tokens(kvPool* p, int32_t seq, int n_tokens, int64_t* out_sl
       out_cow_pair[1] = dst;
       n_cow = 1;
     }
+  }
+  if (n_tokens > 0 || p->seqs.count(seq)) {
+    record_tokens(p, p->seqs[seq], token_ids, n_tokens);
+    pc_publish(p, seq, first_full);
   }
   if (out_n_cow) *out_n_cow = n_cow;
   return KV_OK;
@@ -355,9 +523,74 @@ kvStatus seq_release(kvPool* p, int32_t seq) {
   if (it == p->seqs.end()) return KV_ERR_INVALID_ARG;
   for (int32_t id : it->second.table) {
     p->ref[id] -= 1;
-    if (p->ref[id] == 0) push_free(p, id);
+    if (p->ref[id] == 0) count_zero(p, id);
   }
   p->seqs.erase(it);
+  return KV_OK;
+}
+
+// ---------------------------------------------------------- prefix cache
+
+kvStatus kv_prefix_cache_enable(kvPool* p, uint64_t salt) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  if (p->pc_on) return p->pc_salt == salt ? KV_OK : KV_ERR_INVALID_ARG;
+  p->pc_on = true;
+  p->pc_salt = salt;
+  p->pc_dormant.assign(p->N, 0);
+  for (auto& kv : p->seqs) {  // positions written before: unknown tokens
+    kv.second.tok.assign(kv.second.len, 0);
+    kv.second.known.assign(kv.second.len, 0);
+  }
+  return KV_OK;
+}
+
+kvStatus seq_match_prefix(kvPool* p, int32_t seq, const int32_t* tokens, int n_tokens,
+                          int* out_matched) {
+  if (!p || !p->pc_on || !out_matched || n_tokens < 0 || (n_tokens > 0 && !tokens))
+    return KV_ERR_INVALID_ARG;
+  if (p->seqs.count(seq)) return KV_ERR_INVALID_ARG;
+  const int B = p->B;
+  std::vector<int32_t> blocks;
+  uint64_t h = pc_root(p);
+  int32_t prev = -1;
+  for (int k = 0; (k + 1) * B <= n_tokens; ++k) {
+    h = pc_chain(h, tokens + k * B, B);
+    const int32_t c = pc_find(p, h, prev, tokens + k * B);
+    if (c < 0) break;
+    blocks.push_back(c);
+    prev = c;
+  }
+  for (int32_t c : blocks) {
+    if (p->pc_dormant[c]) {
+      p->pc_lru.erase({p->pc_nodes.at(c).last, c});
+      p->pc_dormant[c] = 0;
+      p->pc_n_dormant -= 1;
+    }
+    p->ref[c] += 1;
+    pc_tick(p, c);
+  }
+  kvSeq s;
+  s.table = blocks;
+  s.len = static_cast<int64_t>(blocks.size()) * B;
+  s.tok.assign(tokens, tokens + s.len);
+  s.known.assign(s.len, 1);
+  p->seqs.emplace(seq, std::move(s));
+  *out_matched = static_cast<int>(blocks.size()) * B;
+  return KV_OK;
+}
+
+kvStatus kv_prefix_evict(kvPool* p, int target_free, int* out_n_evicted) {
+  if (!p || target_free < 0) return KV_ERR_INVALID_ARG;
+  int n = 0;
+  while (static_cast<int64_t>(p->free_list.size()) < target_free && pc_evict_one(p)) ++n;
+  if (out_n_evicted) *out_n_evicted = n;
+  return KV_OK;
+}
+
+kvStatus kv_prefix_stats(const kvPool* p, int* n_cached, int* n_dormant) {
+  if (!p) return KV_ERR_INVALID_ARG;
+  if (n_cached) *n_cached = static_cast<int>(p->pc_nodes.size());
+  if (n_dormant) *n_dormant = static_cast<int>(p->pc_n_dormant);
   return KV_OK;
 }
 

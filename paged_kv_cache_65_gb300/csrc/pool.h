@@ -4,7 +4,9 @@
 
 #include <cstdint>
 #include <deque>
+#include <set>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "../../include/pagedkv.h"
@@ -12,6 +14,20 @@
 struct kvSeq {
   std::vector<int32_t> table;  // logical block -> physical block
   int64_t len = 0;             // tokens with K/V present
+  // prefix cache on: the token id of every position (known[i] = 0: unknown)
+  std::vector<int32_t> tok;
+  std::vector<uint8_t> known;
+};
+
+// A cached full block of the prefix cache: its identity is the whole token
+// prefix up to its end, held as (parent node, this block's tokens); `hash`
+// chains the salt and every block's tokens for the lookup.
+struct kvPrefixNode {
+  uint64_t hash = 0;
+  int32_t parent = -1;    // cached block of the previous B tokens (-1: root)
+  int32_t children = 0;   // cached blocks whose parent this is
+  uint64_t last = 0;      // logical access clock
+  std::vector<int32_t> tokens;
 };
 
 struct kvPool {
@@ -29,6 +45,15 @@ struct kvPool {
   std::vector<int32_t> ref;       // table entries + handles per block
   std::vector<int32_t> ext;       // caller-held handles per block
   std::unordered_map<int32_t, kvSeq> seqs;
+
+  // prefix cache (off until kv_prefix_cache_enable)
+  bool pc_on = false;
+  uint64_t pc_salt = 0, pc_clock = 0;
+  std::unordered_map<int32_t, kvPrefixNode> pc_nodes;    // cached block -> node
+  std::unordered_multimap<uint64_t, int32_t> pc_index;   // chain hash -> cached blocks
+  std::set<std::pair<uint64_t, int32_t>> pc_lru;         // dormant leaves by last access
+  std::vector<uint8_t> pc_dormant;                       // cached block with count 0
+  int64_t pc_n_dormant = 0;
 
   // device-side cache, filled by the first device call
   bool dev_ready = false;
