@@ -599,6 +599,10 @@ def bench_prefill(args):
     starts[1:] = np.cumsum([c for _, c in wl.chunks])
     d_starts = torch.from_numpy(starts).to(dev)
     max_chunk = max(c for _, c in wl.chunks)
+    # heaviest-first work order from the host's copy of the chunk geometry
+    sched = cache.paged_prefill_schedule(starts, d_lens.cpu().numpy(), wl.n_q_heads)
+    d_sched = torch.from_numpy(sched).to(dev)
+    natural = args.prefill_order == "natural"
     g = torch.Generator(device=dev)
     g.manual_seed(synth.torch_seed((wl.seed, 8)))
     q = torch.randn((n_tok, wl.n_q_heads, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
@@ -610,8 +614,14 @@ def bench_prefill(args):
 
     def attend(s):
         for layer in range(wl.n_layers):
-            cache.paged_prefill_attention(layer, q, wl.n_q_heads, d_table, mb, d_starts, d_lens,
-                                          len(seqs), max_chunk, out, 0.0, s.cuda_stream)
+            if natural:
+                cache.paged_prefill_attention(layer, q, wl.n_q_heads, d_table, mb, d_starts,
+                                              d_lens, len(seqs), max_chunk, out, 0.0,
+                                              s.cuda_stream)
+            else:
+                cache.paged_prefill_attention_scheduled(layer, q, wl.n_q_heads, d_table, mb,
+                                                        d_starts, d_lens, len(seqs), d_sched,
+                                                        len(sched), out, 0.0, s.cuda_stream)
 
     def step(s):
         cache.reshape_and_cache(-1, k, v, d_slots, n_tok, s.cuda_stream)
@@ -665,7 +675,7 @@ def bench_prefill(args):
     traffic = TRAFFIC.get((args.workload, "prefill_tc_kernel"))
     traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha("prefill") else None
     e2e = bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
-                            max_chunk, n_tok, flops, world)
+                            starts, max_chunk, n_tok, flops, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
@@ -680,6 +690,8 @@ def bench_prefill(args):
                        "chunks": [c for _, c in wl.chunks],
                        "histories": [wl.history[s] for s in seqs], "kernel": "prefill_tc_kernel",
                        "pdl": not args.no_pdl, "block_size": wl.block_size,
+                       "work_order": ("natural grid" if natural else
+                                      "heaviest first (host schedule, paged_prefill_schedule)"),
                        "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads, "D_h": wl.head_dim,
                        "l2": "flushed between steps (256 MiB write + 256 MiB read)",
                        "parallelism": f"replicas x{world}"},
@@ -708,11 +720,18 @@ def bench_prefill(args):
 
 
 def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
-                      max_chunk, n_tok, flops, world):
+                      starts, max_chunk, n_tok, flops, world):
     """The same round through the public calls with page-locked host buffers:
-    host -> device copies of q and the chunks' K/V, the slot write and the
+    host -> device copies of q and the chunks' K/V, the host work order and
+    its copy (unless the natural grid is asked for), the slot write and the
     attention, the device -> host copy of the outputs, and a synchronise."""
     import torch
+
+    natural = args.prefill_order == "natural"
+    h_lens = d_lens.cpu().numpy()
+    d_sched = torch.empty((cache.paged_prefill_schedule_bytes_for(starts, wl.n_q_heads) // 16, 4),
+                          dtype=torch.int32, device=dev)
+    h_sched = torch.empty(d_sched.shape, dtype=torch.int32).pin_memory()
 
     hq, hk, hv = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
     ho = torch.empty((n_tok, wl.n_q_heads, wl.head_dim), dtype=torch.float32).pin_memory()
@@ -726,20 +745,31 @@ def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, m
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
+        if not natural:
+            sc = cache.paged_prefill_schedule(starts, h_lens, wl.n_q_heads)
+            h_sched[: len(sc)].numpy()[:] = sc
+            d_sched[: len(sc)].copy_(h_sched[: len(sc)], non_blocking=True)
         cache.reshape_and_cache(-1, dk, dv, d_slots, n_tok)
         for layer in range(wl.n_layers):
-            cache.paged_prefill_attention(layer, dq, wl.n_q_heads, d_table, mb, d_starts, d_lens,
-                                          len(wl.chunks), max_chunk, dout)
+            if natural:
+                cache.paged_prefill_attention(layer, dq, wl.n_q_heads, d_table, mb, d_starts,
+                                              d_lens, len(wl.chunks), max_chunk, dout)
+            else:
+                cache.paged_prefill_attention_scheduled(layer, dq, wl.n_q_heads, d_table, mb,
+                                                        d_starts, d_lens, len(wl.chunks), d_sched,
+                                                        len(sc), dout)
         ho.copy_(dout, non_blocking=True)
         torch.cuda.synchronize()
         if i >= args.warmup:
             total += time.perf_counter() - t0
     tot_f, max_s = aggregate(flops * n, total, world, dev)
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + (0 if natural else len(sc) * 16)
     return {"value": round(tot_f / max_s / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(ho.numel() * 4),
             "ms_per_step": round(max_s / n * 1e3, 4),
-            "api": "reshape_and_cache + paged_prefill_attention"}
+            "api": ("reshape_and_cache + paged_prefill_attention" if natural else
+                    "paged_prefill_schedule + reshape_and_cache + "
+                    "paged_prefill_attention_scheduled")}
 
 
 def _lib_mod():
@@ -980,6 +1010,9 @@ def main():
                     help="launch without programmatic dependencies between kernels")
     ap.add_argument("--plain", action="store_true",
                     help="no sharing-aware plan: one segment per (sequence, K/V head)")
+    ap.add_argument("--prefill-order", default="heaviest", choices=["heaviest", "natural"],
+                    help="chunked prefill: launch the work items heaviest first (host "
+                         "schedule) or in the natural grid order")
     ap.add_argument("--prefix-cache", action="store_true",
                     help="host prefix-cache hit of a 4096-token prompt instead of a GPU step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

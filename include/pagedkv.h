@@ -358,6 +358,45 @@ kvStatus paged_prefill_attention(kvPool* pool, int layer, const void* d_q, int n
                                  int n_seq, int max_chunk, float scale, void* d_out,
                                  int out_dtype, void* stream);
 
+/* Heaviest-first work order for chunked prefill.  A work item is one tile
+ * of 128 / G query tokens (G = n_q_heads / H_kv) of one sequence's chunk;
+ * its work is the number of 128-key blocks its queries read,
+ * ceil((h + min(c, (t + 1) * 128 / G)) / 128) for history h = context - c,
+ * chunk length c and tile t ([KC] chunked-prefill section: a chunk's token
+ * attends to the whole history and the chunk up to itself).  The natural
+ * grid starts the items of later sequences last, whatever their length;
+ * launching the longest items first lets the SMs finish together.
+ * paged_prefill_schedule builds the order on the host from host copies of
+ * the chunk geometry that paged_prefill_attention_scheduled will get:
+ *   h_chunk_start : [n_seq + 1] int32, h_context_lens: [n_seq] int32
+ *   h_sched       : caller buffer of at least
+ *                   paged_prefill_schedule_bytes(pool, n_seq, n_q_heads,
+ *                   max_chunk) bytes (max_chunk bounds every chunk), filled
+ *                   with *out_n_items records of four int32: (sequence,
+ *                   tile, chunk length, blocks), blocks non-increasing,
+ *                   equal blocks in (sequence, tile) order.
+ * Empty chunks have no items.  KV_ERR_INVALID_ARG for a negative chunk, a
+ * chunk longer than its context, or a buffer too small;
+ * paged_prefill_schedule_bytes returns 0 for invalid arguments. */
+size_t paged_prefill_schedule_bytes(const kvPool* pool, int n_seq, int n_q_heads, int max_chunk);
+kvStatus paged_prefill_schedule(const kvPool* pool, const int32_t* h_chunk_start,
+                                const int32_t* h_context_lens, int n_seq, int n_q_heads,
+                                void* h_sched, size_t sched_bytes, int* out_n_items);
+
+/* paged_prefill_attention over the work order d_sched (the device copy of
+ * h_sched, 16-byte aligned, n_items records; not written by a kernel on the
+ * stream since the previous kernel began): the same results, bit for bit,
+ * as the natural grid, one CTA per (item, K/V head) in the order's order.
+ * A sequence whose chunk length differs from the one its items were built
+ * for is skipped and flagged KV_DEV_BAD_CONTEXT; so is an item naming no
+ * listed sequence. */
+kvStatus paged_prefill_attention_scheduled(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                           const int32_t* d_block_table, int max_blocks,
+                                           const int32_t* d_chunk_start,
+                                           const int32_t* d_context_lens, int n_seq,
+                                           const void* d_sched, int n_items, float scale,
+                                           void* d_out, int out_dtype, void* stream);
+
 /* --------------------------------------------------- whole decode step --
  * One decode step through host buffers ([BT] §10 order): reserve a slot per
  * listed sequence on the host, copy q / new K,V / slots / copy pairs /

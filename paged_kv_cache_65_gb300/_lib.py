@@ -98,6 +98,12 @@ SIGNATURES = [
                                                  C.c_int, C.c_float, _vp, C.c_int, _vp]),
     ("paged_prefill_attention", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp, _vp,
                                           C.c_int, C.c_int, C.c_float, _vp, C.c_int, _vp]),
+    ("paged_prefill_schedule_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
+    ("paged_prefill_schedule", C.c_int, [_vp, _i32p, _i32p, C.c_int, C.c_int, _vp, C.c_size_t,
+                                         C.POINTER(C.c_int)]),
+    ("paged_prefill_attention_scheduled", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int,
+                                                    _vp, _vp, C.c_int, _vp, C.c_int, C.c_float,
+                                                    _vp, C.c_int, _vp]),
     ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
     ("kv_decode_step_host", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
                                       C.c_float, _f32p, _vp, C.c_size_t, _vp]),

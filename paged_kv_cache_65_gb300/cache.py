@@ -286,6 +286,43 @@ class PagedKVCache:
                                           _stream(stream)),
               "paged_prefill_attention")
 
+    def paged_prefill_schedule(self, chunk_start, context_lens, n_q_heads):
+        """Heaviest-first order of the prefill work items from host copies of
+        the chunk geometry: int32 ``[n_items, 4]`` records (sequence, tile,
+        chunk length, 128-key blocks)."""
+        st = i32(chunk_start)
+        ctx = i32(context_lens)
+        n_seq = ctx.size
+        if st.size != n_seq + 1:
+            raise ValueError("chunk_start needs n_seq + 1 entries")
+        mc = int(np.max(np.diff(st))) if n_seq else 0
+        cap = int(lib.paged_prefill_schedule_bytes(self.handle, n_seq, int(n_q_heads), max(mc, 0)))
+        buf = np.zeros((max(cap, 16) + 15) // 16 * 4, dtype=np.int32)
+        n = C.c_int()
+        check(lib.paged_prefill_schedule(self.handle, ptr_i32(st), ptr_i32(ctx), n_seq,
+                                         int(n_q_heads), vp(buf), buf.nbytes, C.byref(n)),
+              "paged_prefill_schedule")
+        return buf[: 4 * n.value].reshape(n.value, 4).copy()
+
+    def paged_prefill_schedule_bytes_for(self, chunk_start, n_q_heads):
+        """Bytes of a work order for this chunk geometry's longest chunk."""
+        st = i32(chunk_start)
+        mc = int(np.max(np.diff(st))) if st.size > 1 else 0
+        return int(lib.paged_prefill_schedule_bytes(self.handle, st.size - 1, int(n_q_heads), mc))
+
+    def paged_prefill_attention_scheduled(self, layer, q, n_q_heads, d_table, max_blocks,
+                                          d_chunk_start, d_context_lens, n_seq, d_sched, n_items,
+                                          out, scale=0.0, stream=None):
+        """paged_prefill_attention over a heaviest-first work order (the
+        device copy of ``paged_prefill_schedule``'s records)."""
+        check(lib.paged_prefill_attention_scheduled(self.handle, int(layer), vp(q),
+                                                    int(n_q_heads), vp(d_table), int(max_blocks),
+                                                    vp(d_chunk_start), vp(d_context_lens),
+                                                    int(n_seq), vp(d_sched), int(n_items),
+                                                    float(scale), vp(out), _out_dtype(out),
+                                                    _stream(stream)),
+              "paged_prefill_attention_scheduled")
+
     def kv_decode_step_staging_bytes(self, n_seq, n_q_heads, max_blocks):
         return int(lib.kv_decode_step_staging_bytes(self.handle, int(n_seq), int(n_q_heads),
                                                     int(max_blocks)))

@@ -246,6 +246,7 @@ __device__ inline void write_prefix(const int32_t* ctx, int n_seq, int B, int H,
 
 template <int N>
 struct TableCacheN {
+  static_assert(N % 32 == 0, "whole warps of entries");
   int32_t* ent;  // shared, N entries
   int seq = -1;
   int base = 0;

@@ -63,9 +63,11 @@ cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs 
 }
 
 struct PrefillArgs;
-// tcgen05 chunked-prefill attention: one CTA per (sequence, K/V head, 128 query rows).
+// tcgen05 chunked-prefill attention: one CTA per (sequence, K/V head, 128
+// query rows); in the natural grid sized by max_chunk, or one per work item
+// of a.sched (n_items of them) and K/V head.
 cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                              int max_chunk, cudaStream_t st, bool pdl);
+                              int max_chunk, int n_items, cudaStream_t st, bool pdl);
 
 // tcgen05 variant (bfloat16, D_h = 128, the swizzled TMA maps); one CTA per SM.
 cudaError_t launch_tc_bf16(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,

@@ -404,6 +404,53 @@ WsLayout ws_layout(const kvPool* p, int n_seq, int G) {
 
 bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
 
+// Checks and launch shared by the natural-grid and the scheduled prefill.
+kvStatus prefill_common(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                        const int32_t* d_block_table, int max_blocks,
+                        const int32_t* d_chunk_start, const int32_t* d_context_lens, int n_seq,
+                        int max_chunk, const int4* sched, int n_items, float scale, void* d_out,
+                        int out_dtype, void* stream) {
+  if (!p || !p->k || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0)
+    return KV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= p->L) return KV_ERR_INVALID_ARG;
+  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
+  const int G = n_q_heads / p->H;
+  if (ilog2_small(G) < 0 || !pool_tc_shape(p)) return KV_ERR_UNSUPPORTED;
+  if (n_seq == 0 || (sched ? n_items == 0 : max_chunk == 0)) return KV_OK;
+  if (!d_q || !d_block_table || !d_chunk_start || !d_context_lens || !d_out || max_blocks <= 0)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(d_q) || !aligned16(d_out)) return KV_ERR_INVALID_ARG;
+  if (n_seq > 65535 || static_cast<long long>(max_blocks) * p->B >= (1LL << 31))
+    return KV_ERR_INVALID_ARG;
+  if (sched && static_cast<long long>(n_items) * p->H > 0x7fffffffLL) return KV_ERR_INVALID_ARG;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  if (!p->mma_ok) return KV_ERR_UNSUPPORTED;
+  pkv::PrefillArgs a;
+  a.q = d_q;
+  a.table = d_block_table;
+  a.chunk_start = d_chunk_start;
+  a.ctx = d_context_lens;
+  a.out_f32 = out_dtype == KV_DTYPE_F32 ? static_cast<float*>(d_out) : nullptr;
+  a.out_bf16 = out_dtype == KV_DTYPE_BF16 ? static_cast<__nv_bfloat16*>(d_out) : nullptr;
+  a.status = p->d_status;
+  a.sched = sched;
+  a.n_seq = n_seq;
+  a.max_blocks = max_blocks;
+  a.layer = layer;
+  a.n_blocks = p->N;
+  a.block_size = p->B;
+  a.n_kv_heads = p->H;
+  a.n_q_heads = n_q_heads;
+  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
+  a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+  const cudaError_t e =
+      pkv::launch_prefill_tc(tk, tv, a, max_chunk, n_items, as_stream(stream), p->pdl);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 kvStatus check_decode_args(const kvPool* p, int layer, const void* q, int n_q_heads,
                            const int32_t* table, int max_blocks, const int32_t* ctx, int n_seq,
                            const void* ws, size_t ws_bytes) {
@@ -800,42 +847,23 @@ kvStatus paged_prefill_attention(kvPool* p, int layer, const void* d_q, int n_q_
                                  const int32_t* d_chunk_start, const int32_t* d_context_lens,
                                  int n_seq, int max_chunk, float scale, void* d_out,
                                  int out_dtype, void* stream) {
-  if (!p || !p->k || n_seq < 0 || max_chunk < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0)
+  if (max_chunk < 0) return KV_ERR_INVALID_ARG;
+  return prefill_common(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_chunk_start,
+                        d_context_lens, n_seq, max_chunk, nullptr, 0, scale, d_out, out_dtype,
+                        stream);
+}
+
+kvStatus paged_prefill_attention_scheduled(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                           const int32_t* d_block_table, int max_blocks,
+                                           const int32_t* d_chunk_start,
+                                           const int32_t* d_context_lens, int n_seq,
+                                           const void* d_sched, int n_items, float scale,
+                                           void* d_out, int out_dtype, void* stream) {
+  if (n_items < 0 || (n_items > 0 && (!d_sched || !aligned16(d_sched))))
     return KV_ERR_INVALID_ARG;
-  if (layer < 0 || layer >= p->L) return KV_ERR_INVALID_ARG;
-  if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
-  const int G = n_q_heads / p->H;
-  if (ilog2_small(G) < 0 || !pool_tc_shape(p)) return KV_ERR_UNSUPPORTED;
-  if (n_seq == 0 || max_chunk == 0) return KV_OK;
-  if (!d_q || !d_block_table || !d_chunk_start || !d_context_lens || !d_out || max_blocks <= 0)
-    return KV_ERR_INVALID_ARG;
-  if (!aligned16(d_q) || !aligned16(d_out)) return KV_ERR_INVALID_ARG;
-  if (n_seq > 65535 || static_cast<long long>(max_blocks) * p->B >= (1LL << 31))
-    return KV_ERR_INVALID_ARG;
-  kvStatus s = ensure_device(p);
-  if (s != KV_OK) return s;
-  if (!p->mma_ok) return KV_ERR_UNSUPPORTED;
-  pkv::PrefillArgs a;
-  a.q = d_q;
-  a.table = d_block_table;
-  a.chunk_start = d_chunk_start;
-  a.ctx = d_context_lens;
-  a.out_f32 = out_dtype == KV_DTYPE_F32 ? static_cast<float*>(d_out) : nullptr;
-  a.out_bf16 = out_dtype == KV_DTYPE_BF16 ? static_cast<__nv_bfloat16*>(d_out) : nullptr;
-  a.status = p->d_status;
-  a.n_seq = n_seq;
-  a.max_blocks = max_blocks;
-  a.layer = layer;
-  a.n_blocks = p->N;
-  a.block_size = p->B;
-  a.n_kv_heads = p->H;
-  a.n_q_heads = n_q_heads;
-  if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
-  a.qscale = scale * 1.4426950408889634f;  // log2(e)
-  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
-  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
-  const cudaError_t e = pkv::launch_prefill_tc(tk, tv, a, max_chunk, as_stream(stream), p->pdl);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return prefill_common(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_chunk_start,
+                        d_context_lens, n_seq, 0, static_cast<const int4*>(d_sched), n_items,
+                        scale, d_out, out_dtype, stream);
 }
 
 kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,

@@ -14,6 +14,7 @@
 // prefix once).  Prefixes shorter than `min_shared_tokens` are not shared.
 
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <vector>
 
@@ -268,6 +269,60 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   }
   eoff[n_ent.size()] = k;
   if (out_workspace_bytes) *out_workspace_bytes = plan_workspace_bytes(hd.n_segs, c_max, p->D);
+  return KV_OK;
+}
+
+
+// Heaviest-first order of the chunked-prefill work items.  An item is one
+// tile of 128 / G query tokens of one sequence's chunk (all query heads of a
+// K/V head: 128 tile rows); its work is the number of 128-key blocks its
+// queries read, ceil((h + min(c, (t + 1) T)) / 128) for history h, chunk c
+// and tile t.  One CTA runs an item per K/V head and the hardware hands
+// CTAs to free SMs in launch order, so launching the longest items first is
+// list scheduling in decreasing-time order: the last CTAs to start are short
+// and the SMs run out together, where the natural grid (sequences in
+// caller order, tiles in token order) starts the longest histories last.
+size_t paged_prefill_schedule_bytes(const kvPool* p, int n_seq, int n_q_heads, int max_chunk) {
+  if (!p || n_seq < 0 || max_chunk < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return 0;
+  const int G = n_q_heads / p->H;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return 0;
+  const long long T = 128 / G;
+  return static_cast<size_t>(n_seq) * static_cast<size_t>((max_chunk + T - 1) / T) * 16;
+}
+
+kvStatus paged_prefill_schedule(const kvPool* p, const int32_t* h_chunk_start,
+                                const int32_t* h_context_lens, int n_seq, int n_q_heads,
+                                void* h_sched, size_t sched_bytes, int* out_n_items) {
+  if (!p || n_seq < 0 || !out_n_items || n_q_heads <= 0 || n_q_heads % p->H != 0)
+    return KV_ERR_INVALID_ARG;
+  if (n_seq > 0 && (!h_chunk_start || !h_context_lens || !h_sched)) return KV_ERR_INVALID_ARG;
+  const int G = n_q_heads / p->H;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  const int T = 128 / G;
+  struct Item {
+    int32_t s, t, c, nkb;
+  };
+  std::vector<Item> items;
+  for (int s = 0; s < n_seq; ++s) {
+    const long long c = static_cast<long long>(h_chunk_start[s + 1]) - h_chunk_start[s];
+    const int32_t ctx = h_context_lens[s];
+    if (c < 0 || ctx < c || h_chunk_start[s] < 0) return KV_ERR_INVALID_ARG;
+    const long long h = ctx - c;
+    for (long long t = 0; t * T < c; ++t) {
+      const long long last = std::min(c, (t + 1) * T);  // tokens up to the tile's last
+      items.push_back({s, static_cast<int32_t>(t), static_cast<int32_t>(c),
+                       static_cast<int32_t>((h + last + 127) / 128)});
+    }
+  }
+  if (items.size() * 16 > sched_bytes ||
+      items.size() * static_cast<size_t>(p->H) > static_cast<size_t>(INT32_MAX))
+    return KV_ERR_INVALID_ARG;
+  // decreasing work; equal work in (sequence, tile) order, so the order is
+  // a function of the chunk geometry alone
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Item& x, const Item& y) { return x.nkb > y.nkb; });
+  std::memcpy(h_sched, items.data(), items.size() * sizeof(Item));
+  *out_n_items = static_cast<int>(items.size());
   return KV_OK;
 }
 

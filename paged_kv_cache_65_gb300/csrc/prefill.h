@@ -15,6 +15,10 @@ struct PrefillArgs {
   float* out_f32;              // [n_tok][H_q][D], or
   __nv_bfloat16* out_bf16;
   int32_t* status;
+  // heaviest-first work order, or null for the natural grid: item i is
+  // (sequence, tile, the chunk length the order was built for, blocks);
+  // CTA x works on item x / H_kv, K/V head x % H_kv
+  const int4* sched;
   int n_seq, max_blocks, layer, n_blocks, block_size, n_kv_heads, n_q_heads;
   float qscale;  // scale * log2(e)
 };

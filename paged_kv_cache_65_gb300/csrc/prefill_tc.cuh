@@ -22,14 +22,17 @@
 // stages: a K slot is free once its S MMAs are done, a V slot once its P.V
 // MMAs are.
 //
-// Warps 0-3: softmax, thread r owns row r (TMEM lane r) of S, P and O, so
-// row maxima and sums need no exchange.  The reference maximum of a row is
-// lazy: it moves only when a score exceeds it by more than 2^8 (then l and
-// the thread's O row are rescaled, after the previous block's MMAs have
-// completed).  Warps 4-7 issue the TMA loads of K and V (one 64-column half
-// each, so that box issue keeps up with 16-token pages); lane 0 of warp 8
+// Warps 0-7: softmax, two warpgroups on the same rows: thread r of group h
+// owns row r (TMEM lane r) and the keys 64 h .. 64 h + 63 of every block (and
+// O's columns 64 h ..).  The two halves of a row exchange their maxima
+// through shared memory (truncated to bf16, so both compute the same
+// reference) and add their sums at the end.  The reference maximum of a row
+// is lazy: it moves only when a score exceeds it by more than 2^8 (then l
+// and the row of O are rescaled, after the previous block's MMAs have
+// completed).  Warps 8-11 issue the TMA loads of K and V (one 64-column half
+// each, so that box issue keeps up with 16-token pages); lane 0 of warp 12
 // issues the S MMAs, running ahead as far as K blocks and free S/P buffers
-// allow, and lane 0 of warp 9 the P.V MMAs (one thread issuing both kinds
+// allow, and lane 0 of warp 13 the P.V MMAs (one thread issuing both kinds
 // could not keep the tensor core busy: a single thread issues an MMA every
 // ~60 cycles, about the tensor core's time for one 128 x 128 x 16 step).
 // Every mbarrier wait is bounded; parity waits are exact because no waiter
@@ -57,15 +60,16 @@ struct PfCfg {
 };
 static_assert(PfCfg::TM_O + PfCfg::D <= PfCfg::TM_COLS, "TMEM columns");
 
-// warpgroup 0 (warps 0-3) softmax; warpgroup 1: K producers 4 (columns
-// 0-63) and 6 (64-127), V producers 5 and 7; warpgroup 2: MMA issuers 8 (S)
-// and 9 (P.V), 10 and 11 idle.  Every SM sub-partition (warp % 4) holds one
-// warp of each group.  Launched at 168 registers a thread (384 threads), the
-// groups move to 232 / 64 / 64: 128 x (232 + 64 + 64) = 46080 <= 64512.
-constexpr int kPfWarps = 12;
-constexpr int kPfRegsSoftmax = 232, kPfRegsHelper = 64;
-static_assert(128 * (kPfRegsSoftmax + 2 * kPfRegsHelper) <= 168 * 32 * kPfWarps, "register split");
-constexpr int kPfTableCache = 96;  // block-table entries per producer
+// warpgroups 0 and 1 (warps 0-7): softmax, keys 0-63 and 64-127 of a block;
+// warpgroup 2: K producers 8 (columns 0-63) and 10 (64-127), V producers 9
+// and 11; warpgroup 3: MMA issuers 12 (S) and 13 (P.V), 14 and 15 idle.
+// Every SM sub-partition (warp % 4) holds one warp of each group.  Launched
+// at 128 registers a thread (512 threads), the groups move to 192 / 192 /
+// 64 / 64: 128 x (2 x 192 + 2 x 64) = 65536.
+constexpr int kPfWarps = 16;
+constexpr int kPfRegsSoftmax = 192, kPfRegsHelper = 64;
+static_assert(128 * (2 * kPfRegsSoftmax + 2 * kPfRegsHelper) <= 65536, "register split");
+constexpr int kPfTableCache = 32;  // block-table entries per producer
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kPfBarriers = 4 * PfCfg::NST + 2 * PfCfg::NSB + 2;
 
@@ -73,6 +77,7 @@ constexpr int prefill_tc_smem_bytes() {
   return PfCfg::QT + 2 * PfCfg::NST * PfCfg::STAGE  // Q, K and V blocks
          + kPfBarriers * 8 + 16                     // mbarriers, TMEM address
          + 4 * kPfTableCache * 4                    // producer table caches
+         + 2 * 2 * 128 * 2                          // row-maximum exchange (bf16)
          + 1024;                                    // alignment
 }
 
@@ -114,20 +119,40 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   using C = PfCfg;
   constexpr int NST = C::NST;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s = blockIdx.z, head = blockIdx.y;
   const int H = a.n_kv_heads, G = a.n_q_heads / H, B = a.block_size;
   const int T = 128 / G;  // tokens per tile
-  // tile geometry (host-written metadata: read before waiting on the
-  // previous grid)
+  // the work item: (sequence, tile) from the grid, or from a host-built
+  // heaviest-first order (host-written metadata, like the chunk geometry:
+  // read before waiting on the previous grid)
+  int s, head, tile, planned_c = -1;
+  if (a.sched) {
+    const int item = static_cast<int>(blockIdx.x) / H;
+    head = static_cast<int>(blockIdx.x) - item * H;
+    const int4 w = a.sched[item];
+    s = w.x;
+    tile = w.y;
+    planned_c = w.z;
+    if (s < 0 || s >= a.n_seq || tile < 0) {
+      if (threadIdx.x == 0) record_status(a.status, 16);
+      return;
+    }
+  } else {
+    s = blockIdx.z;
+    head = blockIdx.y;
+    tile = blockIdx.x;
+  }
   const int row0 = a.chunk_start[s];
   const int c = a.chunk_start[s + 1] - row0;
   const int ctx = a.ctx[s];
-  if (c < 0 || ctx < c || ctx > a.max_blocks * B || c > static_cast<int>(gridDim.x) * T) {
-    // inconsistent metadata, or a chunk longer than the grid was sized for
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_status(a.status, 16);
+  const bool sized = a.sched ? c == planned_c : c <= static_cast<int>(gridDim.x) * T;
+  if (c < 0 || ctx < c || ctx > a.max_blocks * B || !sized) {
+    // inconsistent metadata, a chunk longer than the grid was sized for, or
+    // one whose length is not the one the work order was built for
+    if (threadIdx.x == 0 && (a.sched ? head == 0 : blockIdx.x == 0 && blockIdx.y == 0))
+      record_status(a.status, 16);
     return;
   }
-  const int tok0 = blockIdx.x * T;
+  const int tok0 = tile * T;
   if (tok0 >= c) return;  // past this sequence's chunk
   const int h = ctx - c;                               // history length
   const int ntok = c - tok0 < T ? c - tok0 : T;        // tokens of this tile
@@ -151,6 +176,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* fin = q_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   int32_t* tcache = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  // [2 parities][2 halves][128 rows] bf16 maxima; at the end each row's
+  // two half sums, split over its slots of both parities
+  uint16_t* xmax = reinterpret_cast<uint16_t*>(tcache + 4 * kPfTableCache);
 
   if ((smem_u32(q_s) & 1023u) != 0u) {
     if (threadIdx.x == 0) record_status(a.status, 32);
@@ -165,9 +193,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     for (int i = 0; i < C::NSB; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);  // both softmax warpgroups
     }
-    mbar_init(q_full, 4);
+    mbar_init(q_full, 8);
     mbar_init(fin, 1);
     fence_barrier_init();
   }
@@ -180,18 +208,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 4 && warp < 8) {
+  if (warp >= 8 && warp < 12) {
     // ------------------------------------ producers (K or V, one half each)
     reg_dealloc<kPfRegsHelper>();
     const bool kp = (warp & 1) == 0;
-    const int hf = (warp - 4) >> 1;  // 64-column half of the rows
+    const int hf = (warp - 8) >> 1;  // 64-column half of the rows
     const CUtensorMap* tmap = kp ? &tmap_k : &tmap_v;
     unsigned char* dst_st = kp ? k_st : v_st;
     uint64_t* full = kp ? k_full : v_full;
     uint64_t* empty = kp ? k_empty : v_empty;
     if (lane == 0) prefetch_tmap(tmap);
     TableCacheN<kPfTableCache> tc;
-    tc.ent = tcache + (warp - 4) * kPfTableCache;
+    tc.ent = tcache + (warp - 8) * kPfTableCache;
     tc.ensure(a.table, a.max_blocks, s, 0, 0, lane);  // host-written: before the wait
     griddep_wait();
     griddep_launch_dependents();
@@ -230,12 +258,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int first = n_kb > NST ? n_kb - NST : 0;
     for (int j = first; j < n_kb && alive; ++j)
       alive = mbar_wait_bounded(&full[j % NST], (j / NST) & 1, kWaitLimitNs);
-  } else if (warp >= 8) {
-    // -------------------------------- MMA issuers (8: S, 9: P.V); 10, 11 idle
+  } else if (warp >= 12) {
+    // ------------------------------ MMA issuers (12: S, 13: P.V); 14, 15 idle
     reg_dealloc<kPfRegsHelper>();
     griddep_wait();
     griddep_launch_dependents();
-    if (warp < 10 && lane == 0) {
+    if (warp < 14 && lane == 0) {
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (alive && !mbar_wait_bounded(bar, parity, kWaitLimitNs)) {
@@ -244,7 +272,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         return alive;
       };
-      if (warp == 8) {
+      if (warp == 12) {
         // S of block j into S/P buffer j % NSB, once K has landed and the
         // P.V that last read the buffer (block j - NSB) is done
         const uint32_t qb = smem_u32(q_s), kb = smem_u32(k_st);
@@ -291,11 +319,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else {
     // -------------------------------------------------------- softmax rows
     reg_alloc<kPfRegsSoftmax>();
-    const int r = threadIdx.x;             // tile row = TMEM lane
+    const int hh = warp >> 2;              // half: keys 64 hh .. 64 hh + 63 of a block
+    const int qd = warp & 3;               // TMEM lane quadrant
+    const int r = qd * 32 + lane;          // tile row = TMEM lane
     const int tl = r / G, g = r - tl * G;  // token of the tile, query head of the K/V head
     const bool row_ok = tl < ntok;
     const int pos = h + tok0 + tl;         // the token's position: keys 0 .. pos
-    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lanes = static_cast<uint32_t>(qd * 32) << 16;
+    const int xbar = 1 + qd;               // named barrier of the row quadrant's two warps
     griddep_wait();
     griddep_launch_dependents();
     bool alive = true;
@@ -306,14 +337,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       return alive;
     };
-    // ---- Q tile: row r, K-major, 128-byte swizzle (zero past the chunk)
+    // ---- Q tile: row r, K-major, 128-byte swizzle (zero past the chunk);
+    // each half stages its 64 dimensions
     {
       const uint32_t qbase = smem_u32(q_s);
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const unsigned char*>(a.q) +
           ((static_cast<long long>(row0 + tok0 + tl) * a.n_q_heads + head * G + g) * C::D) * 2);
 #pragma unroll 4
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int c = 0; c < 8; ++c) {
+        const int ch = 8 * hh + c;
         const uint4 v = row_ok ? src[ch] : make_uint4(0, 0, 0, 0);
         sts128(kmajor_chunk(qbase, r, ch), v.x, v.y, v.z, v.w);
       }
@@ -322,7 +355,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) mbar_arrive(q_full);
     }
     const float qs = a.qscale;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // l: this half's sum
     for (int j = 0; j < n_kb; ++j) {
       const int slot = j % NST;
       const int k0 = j * C::KB;
@@ -331,39 +364,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t sb = tmem + (j % C::NSB) * 128 + lanes;
-      // the row of S: four loads, one wait
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32_nowait(sb + q4 * 32, sr[q4]);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld32(sr[q4]);
+      // this half of the row of S: two loads, one wait
+      uint32_t sr[2][32];
+      tmem_ld32_nowait(sb + 64 * hh, sr[0]);
+      tmem_ld32_nowait(sb + 64 * hh + 32, sr[1]);
+      tmem_wait_ld32(sr[0]);
+      tmem_wait_ld32(sr[1]);
       // keys this row may not see (past its position; every key for a row
       // past the chunk) become -inf, whatever the slot held; blocks with no
       // such key in the whole warp skip this
-      const int lim = row_ok ? pos - k0 : -1;  // key i of the block is admitted iff i <= lim
-      if (__any_sync(0xffffffffu, lim < C::KB - 1)) {
+      const int lim = (row_ok ? pos - k0 : -1) - 64 * hh;  // key 64 hh + i admitted iff i <= lim
+      if (__any_sync(0xffffffffu, lim < 63)) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sr[q4][i] = q4 * 32 + i > lim ? 0xff800000u : sr[q4][i];
+          for (int i = 0; i < 32; ++i) sr[q][i] = q * 32 + i > lim ? 0xff800000u : sr[q][i];
       }
-      // pass 1: the row maximum (eight independent chains of three-input
-      // maxima)
-      float mm[8];
+      // pass 1: this half's maximum (four chains of three-input maxima),
+      // then the row's: both halves take the larger of the two truncated to
+      // bf16, so they agree on the reference exactly
+      float mm[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mm[i] = -INFINITY;
+      for (int i = 0; i < 4; ++i) mm[i] = -INFINITY;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
-          mm[(i >> 1) & 7] = fmax3(mm[(i >> 1) & 7], __uint_as_float(sr[q4][i]),
-                                   __uint_as_float(sr[q4][i + 1]));
-      const float mx =
-          fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * qs;
-      // the reference moves when a score exceeds it by more than 2^8: l and,
-      // after the previous block's MMAs, this row of O are rescaled (the
-      // TMEM accesses are warp-wide: lanes whose reference stays scale by 1)
+          mm[(i >> 1) & 3] = fmax3(mm[(i >> 1) & 3], __uint_as_float(sr[q][i]),
+                                   __uint_as_float(sr[q][i + 1]));
+      const float mh = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])) * qs;
+      uint16_t* xm = xmax + (j & 1) * 256;
+      const uint16_t mine = static_cast<uint16_t>(__float_as_uint(mh) >> 16);
+      xm[hh * 128 + r] = mine;
+      named_bar_sync(xbar, 64);
+      const uint16_t other = xm[(1 - hh) * 128 + r];
+      const float mx = fmaxf(__uint_as_float(static_cast<uint32_t>(mine) << 16),
+                             __uint_as_float(static_cast<uint32_t>(other) << 16));
+      // the reference moves when the maximum exceeds it by more than 2^8: l
+      // and, after the previous block's MMAs, this half of O's row are
+      // rescaled (the TMEM accesses are warp-wide: lanes whose reference
+      // stays scale by 1)
       const bool upd = mx > m_ref + C::TAU;
       float al = 1.f;
       if (upd) {
@@ -377,7 +417,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           __syncwarp();
           tc_fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < C::D; c0 += 32) {
+          for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
             uint32_t o[32];
             tmem_ld32(tmem + C::TM_O + c0 + lanes, o);
 #pragma unroll
@@ -391,20 +431,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // being -inf).  The high part is p's upper 16 bits, the remainder
       // p - hi (exact in fp32, below 2^-7 p) likewise truncated to its upper
       // 16 bits, so hi + lo is within 2^-15 of p with no conversion
-      // instruction.  Both go over the block's S columns (high part in the
-      // first 64, remainder in the last 64; S is in registers by now).  l
-      // sums p in paired partial sums.
+      // instruction.  Both go over the block's S columns (high parts of keys
+      // 64 hh .. in columns 32 hh .., remainders in 64 + 32 hh ..; S is in
+      // registers by now).  l sums p in paired partial sums.
       const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
       const uint64_t qs2 = f2_pack(qs, qs), nm2 = f2_pack(nm, nm), neg2 = f2_pack(-1.f, -1.f);
       uint64_t lp2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
+      {
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int q4 = 2 * h2 + (k >> 4), i = 2 * (k & 15);
+          const int q = k >> 4, i = 2 * (k & 15);
           float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1])), qs2,
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1])), qs2,
                            nm2),
                     x0, x1);
           const float p0 = exp2_approx(x0), p1 = exp2_approx(x1);
@@ -419,8 +458,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     r0, r1);
           lo[k] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
         }
-        tmem_st32_nowait(sb + h2 * 32, hi);
-        tmem_st32_nowait(sb + 64 + h2 * 32, lo);
+        tmem_st32_nowait(sb + 32 * hh, hi);
+        tmem_st32_nowait(sb + 64 + 32 * hh, lo);
       }
       {
         float a0, a1, b0, b1;
@@ -430,28 +469,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tmem_wait_st();
       // keys past the context inside the last 16-key step: V must be finite
-      // there (unused slots may hold anything), so its rows are zeroed
+      // there (unused slots may hold anything), so its rows are zeroed (each
+      // half zeroes its 64 dimensions)
       if (r >= nvalid && r < ((nvalid + 15) & ~15)) {
         wait(&v_full[slot], (j / NST) & 1);
-        const uint32_t vb = smem_u32(v_st + slot * C::STAGE) + r * 128;
+        const uint32_t vb = smem_u32(v_st + slot * C::STAGE) + hh * C::HALF + r * 128;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) sts128(vb + hf * C::HALF + k * 16, 0u, 0u, 0u, 0u);
+        for (int k = 0; k < 8; ++k) sts128(vb + k * 16, 0u, 0u, 0u, 0u);
       }
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j % C::NSB]);
     }
-    // ---- O row: wait for the last block's MMAs, normalise, store
+    // ---- O row: the two halves' sums, then the last block's MMAs,
+    // normalise, store this half's 64 dimensions.  A sum crosses in the
+    // row's own two exchange slots of this half (16 bits in each parity's
+    // slot): other row quadrants may still be in their loop, reading and
+    // writing their own rows' slots, so nothing here may touch another
+    // row's bytes; both parities of this row are free once the two halves
+    // are past their last maximum read.
+    named_bar_sync(xbar, 64);
+    {
+      const uint32_t lb = __float_as_uint(l);
+      xmax[hh * 128 + r] = static_cast<uint16_t>(lb & 0xffffu);
+      xmax[256 + hh * 128 + r] = static_cast<uint16_t>(lb >> 16);
+    }
+    named_bar_sync(xbar, 64);
+    const float l0 = __uint_as_float(static_cast<uint32_t>(xmax[r]) |
+                                     (static_cast<uint32_t>(xmax[256 + r]) << 16));
+    const float l1 = __uint_as_float(static_cast<uint32_t>(xmax[128 + r]) |
+                                     (static_cast<uint32_t>(xmax[256 + 128 + r]) << 16));
+    const float lt = l0 + l1;
     wait(&v_empty[(n_kb - 1) % NST], ((n_kb - 1) / NST) & 1);
     __syncwarp();
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
     const long long orow = (static_cast<long long>(row0 + tok0 + tl) * a.n_q_heads + head * G + g);
 #pragma unroll 1
-    for (int c0 = 0; c0 < C::D; c0 += 32) {
+    for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
       uint32_t o[32];
       tmem_ld32(tmem + C::TM_O + c0 + lanes, o);
       if (row_ok) {

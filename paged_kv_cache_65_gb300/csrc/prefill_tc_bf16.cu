@@ -5,7 +5,7 @@
 namespace pkv {
 
 cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillArgs& a,
-                              int max_chunk, cudaStream_t st, bool pdl) {
+                              int max_chunk, int n_items, cudaStream_t st, bool pdl) {
   constexpr int smem = prefill_tc_smem_bytes();
   static bool attr_set[64] = {};
   int dev = 0;
@@ -19,7 +19,10 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, cons
   }
   const int G = a.n_q_heads / a.n_kv_heads;
   const int T = 128 / G;
-  const dim3 grid((max_chunk + T - 1) / T, a.n_kv_heads, a.n_seq);
+  // natural grid: (tiles of the longest chunk, K/V heads, sequences); with a
+  // work order, one CTA per (item, K/V head), heads fastest
+  const dim3 grid = a.sched ? dim3(n_items * a.n_kv_heads)
+                            : dim3((max_chunk + T - 1) / T, a.n_kv_heads, a.n_seq);
   return launch_kernel(pdl, prefill_tc_kernel, grid, dim3(kPfThreads), smem, st, tk, tv, a);
 }
 

@@ -150,12 +150,14 @@ class DeviceRun:
         return slots, pairs, torch.stack(outs)
 
     def prefill_step(self, chunks, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
-                     out_dtype=None, max_chunk=None):
+                     out_dtype=None, max_chunk=None, scheduled=False):
         """A chunked-prefill round: for each ``(seq, c)`` of ``chunks`` reserve
         ``c`` slots, copy any shared tail, write the chunk's K/V (all layers),
         then attend the chunk's queries over the sequence's context.  ``q``
         ``[n_tok, H_q, D_h]`` (chunks in order), ``k_new, v_new [L, n_tok,
-        H_kv, D_h]``.  Returns the outputs ``[L, n_tok, H_q, D_h]``."""
+        H_kv, D_h]``.  ``scheduled`` launches the work items heaviest first
+        (``paged_prefill_schedule``).  Returns the outputs ``[L, n_tok, H_q,
+        D_h]``."""
         import torch
 
         c = self.c
@@ -180,11 +182,19 @@ class DeviceRun:
         qd = to_device(q, c.dtype, self.dev)
         dt = out_dtype or torch.float32
         mc = max_chunk if max_chunk is not None else max([n for _, n in chunks] + [0])
+        if scheduled:
+            sched = c.paged_prefill_schedule(starts, d_lens.cpu().numpy(), self.n_q_heads)
+            d_sched = torch.from_numpy(sched).to(self.dev)
         outs = []
         for layer in range(c.L):
             out = torch.zeros((int(starts[-1]), self.n_q_heads, c.D), dtype=dt, device=self.dev)
-            c.paged_prefill_attention(layer, qd, self.n_q_heads, d_table, mb, d_starts, d_lens,
-                                      len(chunks), mc, out, 0.0, self.stream)
+            if scheduled:
+                c.paged_prefill_attention_scheduled(layer, qd, self.n_q_heads, d_table, mb,
+                                                    d_starts, d_lens, len(chunks), d_sched,
+                                                    len(sched), out, 0.0, self.stream)
+            else:
+                c.paged_prefill_attention(layer, qd, self.n_q_heads, d_table, mb, d_starts,
+                                          d_lens, len(chunks), mc, out, 0.0, self.stream)
             outs.append(out)
         return torch.stack(outs)
 

@@ -35,7 +35,7 @@ def make(wl, fill_nan=False):
     return cache, run
 
 
-def check_against_oracle(wl, fill_nan=False, chunk_index=None, out_dtype=None):
+def check_against_oracle(wl, fill_nan=False, chunk_index=None, out_dtype=None, scheduled=False):
     """Largest error of the chunks' outputs against the oracle.  With bf16
     outputs the error is taken after removing half a bf16 ulp of the exact
     value (2^-8 relative): a row that sees few keys can have |out| ~ 4."""
@@ -44,7 +44,7 @@ def check_against_oracle(wl, fill_nan=False, chunk_index=None, out_dtype=None):
     _, _, q = orc.prefill_step(0)
     q2, k, v = wl.chunk_values(0)
     assert np.array_equal(q, q2)
-    og = run.prefill_step(wl.chunks, q, k, v, out_dtype=out_dtype)
+    og = run.prefill_step(wl.chunks, q, k, v, out_dtype=out_dtype, scheduled=scheduled)
     got = og.float().cpu().numpy()[0]
     ref = orc.prefill_attend(0, q, chunk_index)
     offs = np.cumsum([0] + [c for _, c in wl.chunks])
@@ -119,3 +119,60 @@ def test_prefill_chunk_longer_than_max_chunk_is_flagged():
     run.prefill_step(wl.chunks, q, k, v, max_chunk=100)
     assert cache.kv_pool_device_status() & 16
     assert cache.kv_pool_device_status() == 0
+
+
+# ------------------------------------------------- heaviest-first work order
+def test_prefill_4k_scheduled_against_oracle():
+    assert check_against_oracle(synth.workload("prefill_4k"), chunk_index=[0, 4, 7],
+                                scheduled=True) <= TOL
+
+
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (8, 64), (4, 16)])
+def test_prefill_scheduled_ragged_against_oracle(G, B):
+    hist = [0, 5, 130, 1000, 17]
+    chunks = [1, 17, 300, 64, 129]
+    assert check_against_oracle(ragged(G, B, hist, chunks, seed=G * 100 + B + 1),
+                                scheduled=True) <= TOL
+
+
+@pytest.mark.parametrize("name", ["prefill_4k", "ragged"])
+def test_prefill_scheduled_equals_natural_grid_bit_for_bit(name):
+    # a CTA computes the same rows with the same arithmetic whichever order
+    # launches it: the outputs are identical, not merely close
+    wl = synth.workload(name) if name != "ragged" else ragged(4, 16, [0, 900, 33], [250, 7, 128],
+                                                             seed=21)
+    q, k, v = wl.chunk_values(0)
+    outs = []
+    for scheduled in (False, True):
+        cache, run = make(wl)
+        outs.append(run.prefill_step(wl.chunks, q, k, v, scheduled=scheduled).cpu().numpy())
+        assert cache.kv_pool_device_status() == 0
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_prefill_schedule_for_other_chunk_lengths_is_flagged():
+    # an order built for a 150-token chunk, given a 200-token chunk: that
+    # sequence is skipped and flagged, the other one still computed
+    from paged_kv_cache_65_gb300.driver import to_device
+
+    wl = ragged(4, 16, [0, 40], [200, 64], seed=13)
+    cache, run = make(wl)
+    q, k, v = wl.chunk_values(0)
+    ref = run.prefill_step(wl.chunks, q, k, v).cpu().numpy()[0]
+    assert cache.kv_pool_device_status() == 0
+    d_table, d_lens, mb = run.tables([0, 1])
+    lens = d_lens.cpu().numpy()
+    starts = np.array([0, 200, 264], dtype=np.int32)
+    planned = np.array([0, 150, 214], dtype=np.int32)
+    sched = cache.paged_prefill_schedule(planned, lens, wl.n_q_heads)
+    d_sched = torch.from_numpy(sched).to("cuda")
+    qd = to_device(q, cache.dtype, torch.device("cuda"))
+    out = torch.full((264, wl.n_q_heads, wl.head_dim), 7.0, device="cuda")
+    cache.paged_prefill_attention_scheduled(0, qd, wl.n_q_heads, d_table, mb,
+                                            torch.from_numpy(starts).to("cuda"), d_lens, 2,
+                                            d_sched, len(sched), out, 0.0, run.stream)
+    got = out.cpu().numpy()
+    assert cache.kv_pool_device_status() & 16
+    assert cache.kv_pool_device_status() == 0
+    assert (got[:200] == 7.0).all()  # skipped
+    assert np.array_equal(got[200:], ref[200:])
