@@ -306,7 +306,7 @@ def bench_ours(args):
 
     # one CUDA graph per step plan: cow copy, slot write, per layer split + merge;
     # event-record nodes around each split pass time the dominant kernel
-    def enqueue(p, ext=None):
+    def enqueue(p, ext=None, split=True):
         cnt = 0
         if p["npairs"]:
             cache.cow_copy(p["pairs"], p["npairs"])
@@ -316,10 +316,10 @@ def bench_ours(args):
         for layer in range(L):
             if ext is not None:
                 ext[layer][0].record()
-            if use_plan:
+            if use_plan and split:
                 cache.paged_decode_partials_planned(layer, q[layer], wl.n_q_heads, p["table"],
                                                     max_blocks, p["d_plan"], p["h_plan"], ws)
-            else:
+            elif split:
                 cache.paged_decode_partials(layer, q[layer], wl.n_q_heads, p["table"], max_blocks,
                                             p["lens"], n, ws, 0.0)
             if ext is not None:
@@ -340,7 +340,7 @@ def bench_ours(args):
                        for _ in range(L)] for _ in range(n_plans)]
     except TypeError:
         ext_events = None
-    graphs, instr_graphs, split_graphs = [], [], []
+    graphs, instr_graphs, split_graphs, nosplit_graphs = [], [], [], []
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
@@ -349,6 +349,10 @@ def bench_ours(args):
             with torch.cuda.graph(g_, stream=cap):
                 per_step_launches = enqueue(dplans[pi])
             graphs.append(g_)
+            gn = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gn, stream=cap):
+                enqueue(dplans[pi], split=False)
+            nosplit_graphs.append(gn)
             gi = torch.cuda.CUDAGraph()
             if ext_events is not None:
                 with torch.cuda.graph(gi, stream=cap):
@@ -422,6 +426,23 @@ def bench_ours(args):
             e0s[j][1].record(stream)
         torch.cuda.synchronize()
         split_ms = [a.elapsed_time(b) / L for a, b in e0s]
+    # the split passes' share of the step: the same step graphs without the
+    # split launches, replayed the same way (L2 flushed before each, events
+    # around the replay); per launch = the difference of the medians / L
+    n_inc = min(args.steps, 200)
+    with_ms, without_ms = [], []
+    for j in range(n_inc):
+        for gr_, acc in ((graphs, with_ms), (nosplit_graphs, without_ms)):
+            flush_l2(j)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr_[j % n_plans].replay()
+            e1.record(stream)
+            acc.append((e0, e1))
+    torch.cuda.synchronize()
+    with_ms = [a.elapsed_time(b) for a, b in with_ms]
+    without_ms = [a.elapsed_time(b) for a, b in without_ms]
+    inc_s = (float(np.median(with_ms)) - float(np.median(without_ms))) / L / 1e3
     dev_s = sum(step_ms) / 1e3
     ub = sum(dplans[i % n_plans]["ub"] for i in range(args.warmup, n_steps))
     lb = sum(dplans[i % n_plans]["lb"] for i in range(args.warmup, n_steps))
@@ -434,7 +455,8 @@ def bench_ours(args):
     # * b bytes per distinct context token row of the layer) / mean duration
     per_launch_alg = [dplans[j % n_plans]["ub"] / L for j in range(n_split)]
     alg = float(np.mean(per_launch_alg))
-    split_s = float(np.mean(split_ms)) / 1e3
+    split_ev_s = float(np.mean(split_ms)) / 1e3
+    split_s = inc_s
     peak, peak_kind = read_peaks()
     achieved = alg / split_s / 1e9
     # the split-pass kernel that ran: a plan records its own; otherwise the option
@@ -482,9 +504,15 @@ def bench_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
                          "kernel": kname,
-                         "peak_source": peak_kind, "timing": split_src,
+                         "peak_source": peak_kind,
+                         "timing": ("device time the split launches add to the step: median of "
+                                    "the step graphs minus median of the same graphs without "
+                                    "them, per launch (CUDA events around each replay, L2 "
+                                    "flushed before each)"),
                          "alg_bytes_per_launch": int(alg),
-                         "mean_launch_us": round(split_s * 1e6, 2)},
+                         "mean_launch_us": round(split_s * 1e6, 2),
+                         "event_node_launch_us": round(split_ev_s * 1e6, 2),
+                         "event_node_timing": split_src},
             "gpu_launches": launches * world,
             "graphs": "one CUDA graph per step plan, replayed",
             "e2e": e2e,

@@ -123,8 +123,13 @@ kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
  * passes.  KV_OPT_PDL: 1 (default) =
  * launch kernels with a programmatic dependency on the previous grid in the
  * stream (each kernel waits for its predecessors before reading their
- * results, but is scheduled while they finish), 0 = plain launches. */
-enum { KV_OPT_DECODE_PATH = 1, KV_OPT_PDL = 2 };
+ * results, but is scheduled while they finish), 0 = plain launches.
+ * KV_OPT_PLAN_GRID: the CTA count for which paged_decode_plan writes its
+ * per-CTA start records (value in 1 .. 1024; 0, the default = the split
+ * pass's own count once the device is known).  Records built for another
+ * count than the launch's are ignored (the kernel then searches the plan);
+ * results are the same either way. */
+enum { KV_OPT_DECODE_PATH = 1, KV_OPT_PDL = 2, KV_OPT_PLAN_GRID = 3 };
 kvStatus kv_pool_set_option(kvPool* pool, int option, int value);
 
 /* Scales of an FP8_E4M3 pool (default 1, 1): a written value x is stored as
@@ -287,7 +292,13 @@ kvStatus paged_decode_attention(kvPool* pool, int layer, const void* d_q, int n_
  * segment per K/V head carrying all members' query heads; the rest of each
  * sequence is a segment of its own.  The plan is a flat byte buffer to copy
  * to the device as-is.  *out_workspace_bytes gets the decode workspace size
- * the plan needs. */
+ * the plan needs.  Once the pool's device is known the plan also carries, per
+ * CTA of the split pass, the CTA's first piece of work and the physical ids
+ * of its first blocks (taken from the tables as they are now: the plan goes
+ * with the block table of the same state), so that the CTA's first copies
+ * start without searching the plan or reading the table; a buffer sized by
+ * paged_decode_plan_bytes before the device was known has no room for them,
+ * and the plan is then built without. */
 size_t paged_decode_plan_bytes(const kvPool* pool, int n_seq, int n_q_heads);
 kvStatus paged_decode_plan(const kvPool* pool, const int32_t* seq_ids, int n_seq, int n_q_heads,
                            int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,

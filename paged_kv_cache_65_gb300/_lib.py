@@ -30,6 +30,7 @@ KV_ERR_UNSUPPORTED = 6
 KV_ERR_SCRATCH_TOO_SMALL = 7
 KV_OPT_DECODE_PATH = 1
 KV_OPT_PDL = 2
+KV_OPT_PLAN_GRID = 3
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
 KV_DTYPE_FP8_E4M3 = 2

@@ -363,6 +363,10 @@ PLAN_SEG = np.dtype([("wpre", "<i8"), ("rep", "<i4"), ("b0", "<i4"), ("b1", "<i4
                      ("tok_end", "<i4"), ("head", "<i4"), ("ncols", "<i4"), ("mem", "<i4"),
                      ("w", "<i4")])
 PLAN_ENTRY = np.dtype([("seg", "<i4"), ("col_base", "<i4")])
+PLAN_START = np.dtype([("seg", "<i4"), ("rep", "<i4"), ("head", "<i4"), ("b0", "<i4"),
+                       ("b1", "<i4"), ("tok_end", "<i4"), ("ncols", "<i4"), ("mem", "<i4"),
+                       ("r_after", "<i8"), ("n_pid", "<i4"), ("pad0", "<i4"),
+                       ("pid", "<i4", (16,)), ("pad1", "<i4", (4,))])
 
 
 def parse_plan(buf: np.ndarray) -> dict:
@@ -370,13 +374,15 @@ def parse_plan(buf: np.ndarray) -> dict:
     h = np.frombuffer(buf[:80].tobytes(), dtype=np.int32)
     W = int(np.frombuffer(buf[:8].tobytes(), dtype=np.int64)[0])
     (n_segs, n_members, n_entries, c_max, n_seq, n_kv_heads, group, block_size, seg_off,
-     mem_off, eoff_off, ent_off, n_shared, kernel) = (int(x) for x in h[2:16])
+     mem_off, eoff_off, ent_off, n_shared, kernel, start_off, start_grid) = (
+        int(x) for x in h[2:18])
     segs = np.frombuffer(buf[seg_off:seg_off + 40 * n_segs].tobytes(), dtype=PLAN_SEG)
     members = np.frombuffer(buf[mem_off:mem_off + 4 * n_members].tobytes(), dtype=np.int32)
     eoff = np.frombuffer(buf[eoff_off:eoff_off + 4 * (n_seq * n_kv_heads + 1)].tobytes(),
                          dtype=np.int32)
     ents = np.frombuffer(buf[ent_off:ent_off + 8 * n_entries].tobytes(), dtype=PLAN_ENTRY)
+    starts = np.frombuffer(buf[start_off:start_off + 128 * start_grid].tobytes(),
+                           dtype=PLAN_START)
     return dict(W=W, n_segs=n_segs, c_max=c_max, n_seq=n_seq, H=n_kv_heads, G=group,
                 B=block_size, n_shared_segs=n_shared, kernel=kernel, segs=segs,
-                members=members, eoff=eoff,
-                ents=ents)
+                members=members, eoff=eoff, ents=ents, start_grid=start_grid, starts=starts)

@@ -346,6 +346,10 @@ kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
     p->pdl = value == 1;
     return KV_OK;
   }
+  if (option == KV_OPT_PLAN_GRID && value >= 0 && value <= kMaxDecodeCtas) {
+    p->plan_grid = value;
+    return KV_OK;
+  }
   return KV_ERR_INVALID_ARG;
 }
 

@@ -64,6 +64,10 @@ struct DecodeArgs {
   int n_segs;
   int c_max;
   long long plan_W;
+  // per-CTA start records of the plan (null: none) and the CTA count they
+  // were built for; used only when it equals `grid`
+  const PlanStart* starts;
+  int start_grid;
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }

@@ -160,7 +160,7 @@ constexpr int decode_mma_smem_bytes() {
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
          + kTableCache * 4                  // producer table cache
-         + 64 + 1024;                       // walk state + 1 KiB alignment
+         + 64 + 128 + 1024;                 // walk state, start record, 1 KiB alignment
 }
 
 // swizzled shared address of (row r, 8-element chunk c) inside a half
@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* empty = full + NST;
   long long* walk = reinterpret_cast<long long*>(empty + NST);
   int32_t* tcache = reinterpret_cast<int32_t*>(walk + 4);
+  PlanStart* rec_s = reinterpret_cast<PlanStart*>(tcache + kTableCache);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -272,13 +273,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   // first kernel of the stream's programmatic chain started, so they are
   // read before waiting for the previous grid; the pool, q and the workspace
   // only after it.
+  // a plan with start records for this grid: the CTA's first piece and its
+  // first blocks' ids come with one 128-byte read (no search, no table read)
+  const bool use_rec = PLAN && a.starts != nullptr && a.start_grid == a.grid;
   if (warp == 0) {
     if constexpr (PLAN) {
       const long long W = a.plan_W;
       long long chunk = (W + a.grid - 1) / a.grid;
       if (chunk == 0) chunk = 1;
-      const long long r0 = (long long)blockIdx.x * chunk;
-      const int s0 = r0 < W ? plan_find(a.segs, a.n_segs, r0) : a.n_segs;
+      int s0 = 0;
+      if (use_rec) {
+        reinterpret_cast<int32_t*>(rec_s)[lane] =
+            reinterpret_cast<const int32_t*>(a.starts + blockIdx.x)[lane];
+      } else {
+        const long long r0 = (long long)blockIdx.x * chunk;
+        s0 = r0 < W ? plan_find(a.segs, a.n_segs, r0) : a.n_segs;
+      }
       if (lane == 0) {
         walk[0] = s0;
         walk[1] = 0;
@@ -320,8 +330,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     pw.r = r_begin;
     pw.r1 = r_end;
   }
+  bool rec_first = use_rec;  // the first piece comes from the start record
   auto next_piece = [&](Piece& p) -> bool {
     if constexpr (PLAN) {
+      if (rec_first) {
+        rec_first = false;
+        const PlanStart& R = *rec_s;
+        if (R.seg < 0) {
+          plw.s = plw.n_segs;
+          return false;
+        }
+        p.rep = R.rep;
+        p.head = R.head;
+        p.b0 = R.b0;
+        p.b1 = R.b1;
+        p.tok_end = R.tok_end;
+        p.ncols = R.ncols;
+        p.mem = R.mem;
+        p.seg = R.seg;
+        plw.s = R.seg;
+        plw.r = R.r_after;
+        return true;
+      }
       return plw.next(p);
     } else {
       if (!pw.next()) return false;
@@ -340,9 +370,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto peek_first = [&](Piece& p0) -> bool {
     const PieceWalker pw_s = pw;
     const PlanWalker plw_s = plw;
+    const bool rf = rec_first;
     const bool ok = next_piece(p0);
     pw = pw_s;
     plw = plw_s;
+    rec_first = rf;
     return ok;
   };
   auto wait_previous_grid = [&]() {
@@ -364,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int stage = 0;
     TableCache tc;
     tc.ent = tcache;
-    {
+    if (!use_rec) {
       Piece p0;
       if (peek_first(p0)) tc.ensure(a.table, a.max_blocks, p0.rep, p0.b0, p0.b0, lane);
     }
@@ -381,14 +413,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const int nvalid = p.tok_end - tok0 < STG ? p.tok_end - tok0 : STG;
         const int nunits = (nvalid + UR - 1) / UR;
-        tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, (tok0 + (nunits - 1) * UR) / B, lane);
+        const int jl = (tok0 + (nunits - 1) * UR) / B;
+        // the first stage of the record's piece takes the record's block ids
+        const bool from_rec = use_rec && stage == 0 && p.seg == rec_s->seg &&
+                              tok0 / B >= rec_s->b0 && jl - rec_s->b0 < rec_s->n_pid;
+        if (!from_rec) tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, jl, lane);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * unit_bytes);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int t = tok0 + u * UR;
           const int j = t / B;
           const int row = t - j * B;
-          int pid = tc.ent[j - tc.base];
+          int pid = from_rec ? rec_s->pid[j - rec_s->b0] : tc.ent[j - tc.base];
           if (pid < 0 || pid >= a.n_blocks) {
             record_status(a.status, 1);
             pid = 0;  // stay in bounds; the result is flagged as invalid

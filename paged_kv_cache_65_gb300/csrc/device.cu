@@ -473,6 +473,18 @@ kvPool::~kvPool() {
   if (h_pinned) cudaFreeHost(h_pinned);
 }
 
+// SM count of the device a pool with device memory runs on (the current
+// device until its first kernel has run); 0 for a host-only pool or without
+// a device.
+int pool_sm_count(const kvPool* p) {
+  if (p->sm_count > 0) return p->sm_count;
+  if (!p->k) return 0;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 extern "C" {
 
 kvStatus kv_pool_device_status(kvPool* p, void* stream, int* out_bits) {
@@ -580,6 +592,8 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   a.n_segs = 0;
   a.c_max = G;
   a.plan_W = 0;
+  a.starts = nullptr;
+  a.start_grid = 0;
   const DecodeKernel kern = decode_kernel(p);
   int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
@@ -731,6 +745,8 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   a.n_segs = hd.n_segs;
   a.c_max = hd.c_max;
   a.plan_W = hd.W;
+  a.starts = hd.start_grid > 0 ? reinterpret_cast<const PlanStart*>(dp + hd.start_off) : nullptr;
+  a.start_grid = hd.start_grid;
   const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   bool supported = true;

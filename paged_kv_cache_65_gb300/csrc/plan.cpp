@@ -36,10 +36,10 @@ int common_prefix(const int32_t* a, const int32_t* b, int n) {
 }
 
 struct Layout {
-  size_t seg, mem, eoff, ent, total;
+  size_t seg, mem, eoff, ent, start, total;
 };
 
-Layout plan_layout(int n_seq, int H, int n_segs, int n_members, int n_entries) {
+Layout plan_layout(int n_seq, int H, int n_segs, int n_members, int n_entries, int n_start) {
   Layout l;
   size_t off = align16(sizeof(PlanHeader));
   l.seg = off;
@@ -50,8 +50,76 @@ Layout plan_layout(int n_seq, int H, int n_segs, int n_members, int n_entries) {
   off += align16(sizeof(int32_t) * (static_cast<size_t>(n_seq) * H + 1));
   l.ent = off;
   off += align16(sizeof(PlanEntry) * static_cast<size_t>(n_entries));
+  l.start = off;
+  off += sizeof(PlanStart) * static_cast<size_t>(n_start);
   l.total = off;
   return l;
+}
+
+// CTA count of the split pass for the plan's kernel: the count the launcher
+// has settled on for this pool, else the kernel's design occupancy (two CTAs
+// per SM for the warp-level MMA pass, one for the tcgen05 pass) once the
+// device is known, else 0 (no start records).  A record set built for another
+// count than the launch's is ignored by the kernels.
+int plan_grid(const kvPool* p, int kernel, int G) {
+  if (p->plan_grid > 0) return p->plan_grid < kMaxDecodeCtas ? p->plan_grid : kMaxDecodeCtas;
+  int g = 0;
+  if (kernel == kPlanKernelTc) {
+    g = p->grid_tc > 0 ? p->grid_tc : pool_sm_count(p);
+  } else {
+    const int lg = G <= 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
+    g = p->grid_by_g[lg] > 0 ? p->grid_by_g[lg] : 2 * pool_sm_count(p);
+  }
+  return g < kMaxDecodeCtas ? g : kMaxDecodeCtas;
+}
+
+// Start records for `grid` CTAs, following the device's split exactly: CTA c
+// takes the work units [c * chunk, min((c + 1) * chunk, W)), chunk =
+// ceil(W / grid) (at least 1); its walk starts at the last segment whose
+// first unit is at or before c * chunk and yields the pieces PlanWalker::next
+// does.
+void plan_starts(const std::vector<PlanSeg>& segs, int64_t W, int grid, int B,
+                 const std::vector<const kvSeq*>& seqs, PlanStart* out) {
+  int64_t chunk = (W + grid - 1) / grid;
+  if (chunk == 0) chunk = 1;
+  const int n = static_cast<int>(segs.size());
+  for (int c = 0; c < grid; ++c) {
+    PlanStart& R = out[c];
+    std::memset(&R, 0, sizeof(R));
+    R.seg = -1;
+    const int64_t r0 = static_cast<int64_t>(c) * chunk;
+    if (r0 >= W) continue;
+    const int64_t r1 = std::min(r0 + chunk, W);
+    // last segment with wpre <= r0 (segments are in wpre order)
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) / 2;
+      if (segs[mid].wpre <= r0) lo = mid; else hi = mid;
+    }
+    for (int s = lo; s < n; ++s) {
+      const PlanSeg& sg = segs[s];
+      const int64_t len = sg.b1 - sg.b0;
+      const int64_t w = sg.w > 0 ? sg.w : 1;
+      if (len <= 0 || r0 >= sg.wpre + len * w) continue;
+      const int64_t end = std::min(r1, sg.wpre + len * w);
+      const int64_t jb = (r0 - sg.wpre + w - 1) / w, je = (end - sg.wpre + w - 1) / w;
+      R.seg = s;
+      R.rep = sg.rep;
+      R.head = sg.head;
+      R.b0 = sg.b0 + static_cast<int32_t>(jb);
+      R.b1 = sg.b0 + static_cast<int32_t>(je);
+      R.tok_end = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(R.b1) * B, sg.tok_end));
+      R.ncols = sg.ncols;
+      R.mem = sg.mem;
+      R.r_after = end;
+      const std::vector<int32_t>& t = seqs[sg.rep]->table;
+      int k = 0;
+      for (; k < kPlanStartPids && R.b0 + k < R.b1 && R.b0 + k < static_cast<int>(t.size()); ++k)
+        R.pid[k] = t[R.b0 + k];
+      R.n_pid = k;
+      break;
+    }
+  }
 }
 
 }  // namespace
@@ -67,8 +135,11 @@ extern "C" {
 size_t paged_decode_plan_bytes(const kvPool* p, int n_seq, int n_q_heads) {
   if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return 0;
   // at most one private and one shared segment per (sequence, head), and
-  // two member slots and two entries per sequence (and head)
-  return plan_layout(n_seq, p->H, 2 * n_seq * p->H, 2 * n_seq, 2 * n_seq * p->H).total;
+  // two member slots and two entries per sequence (and head); start records
+  // for the larger of the two kernels' CTA counts
+  const int G = n_q_heads / p->H;
+  const int n_start = std::max(plan_grid(p, kPlanKernelMma, G), plan_grid(p, kPlanKernelTc, G));
+  return plan_layout(n_seq, p->H, 2 * n_seq * p->H, 2 * n_seq, 2 * n_seq * p->H, n_start).total;
 }
 
 kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
@@ -235,9 +306,16 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   int n_entries = 0;
   for (uint8_t c : n_ent) n_entries += c;
 
-  // ---- serialise
-  const Layout l = plan_layout(n_seq, H, static_cast<int>(segs.size()),
-                               static_cast<int>(members.size()), n_entries);
+  // ---- serialise (start records only where the buffer has room for them:
+  // a buffer sized before the device was known holds none)
+  int grid = plan_grid(p, kernel, G);
+  Layout l = plan_layout(n_seq, H, static_cast<int>(segs.size()),
+                         static_cast<int>(members.size()), n_entries, grid);
+  if (l.total > plan_bytes || W == 0) {
+    grid = 0;
+    l = plan_layout(n_seq, H, static_cast<int>(segs.size()), static_cast<int>(members.size()),
+                    n_entries, 0);
+  }
   if (l.total > plan_bytes) return KV_ERR_INVALID_ARG;
   unsigned char* out = static_cast<unsigned char*>(h_plan);
   std::memset(out, 0, l.total);
@@ -257,7 +335,11 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   hd.ent_off = static_cast<int32_t>(l.ent);
   hd.n_shared_segs = static_cast<int32_t>(chunks.size()) * H;
   hd.kernel = kernel;
+  hd.start_off = grid > 0 ? static_cast<int32_t>(l.start) : 0;
+  hd.start_grid = grid;
   std::memcpy(out, &hd, sizeof(hd));
+  if (grid > 0)
+    plan_starts(segs, W, grid, B, seqs, reinterpret_cast<PlanStart*>(out + l.start));
   if (!segs.empty()) std::memcpy(out + l.seg, segs.data(), sizeof(PlanSeg) * segs.size());
   if (!members.empty()) std::memcpy(out + l.mem, members.data(), sizeof(int32_t) * members.size());
   int32_t* eoff = reinterpret_cast<int32_t*>(out + l.eoff);

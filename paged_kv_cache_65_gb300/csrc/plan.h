@@ -34,7 +34,9 @@ struct PlanHeader {
   int32_t ent_off;
   int32_t n_shared_segs;
   int32_t kernel;     // split-pass kernel the work units are weighted for (kPlanKernel*)
-  int32_t pad[4];
+  int32_t start_off;  // byte offset of the CTA start records (0: none)
+  int32_t start_grid; // CTA count the start records were built for (0: none)
+  int32_t pad[2];
 };
 static_assert(sizeof(PlanHeader) == 80, "plan header layout");
 
@@ -49,6 +51,23 @@ struct PlanSeg {
   int32_t w;        // work units per block (cost weight of the segment's width)
 };
 static_assert(sizeof(PlanSeg) == 40, "plan segment layout");
+
+// Start record of CTA c of a split pass launched with start_grid CTAs: the
+// first piece PlanWalker::next yields from the CTA's first work unit, the
+// walk position after it, and the physical ids of the piece's first blocks
+// (the table entries of row `rep` from b0 on), so that the CTA's first copies
+// need neither a search of the segments nor a block-table read.
+constexpr int kPlanStartPids = 16;
+struct PlanStart {
+  int32_t seg;      // segment of the first piece; -1: the CTA has no work unit
+  int32_t rep, head, b0, b1, tok_end, ncols, mem;
+  int64_t r_after;  // work unit after the first piece
+  int32_t n_pid;    // valid entries of pid (blocks b0 .. b0 + n_pid - 1)
+  int32_t pad0;
+  int32_t pid[kPlanStartPids];
+  int32_t pad1[4];
+};
+static_assert(sizeof(PlanStart) == 128, "plan start record layout");
 
 struct PlanEntry {
   int32_t seg;       // segment holding partials of this (sequence, head)

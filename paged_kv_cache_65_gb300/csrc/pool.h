@@ -61,6 +61,7 @@ struct kvPool {
   int sm_count = 0;
   int grid_by_g[4] = {0, 0, 0, 0};  // split-pass CTAs per log2(H_q / H_kv)
   int grid_tc = 0;                  // CTAs of the tcgen05 split pass (one per SM)
+  int plan_grid = 0;                // KV_OPT_PLAN_GRID: CTA count plans build start records for
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
   int decode_path = 0;                      // KV_OPT_DECODE_PATH
@@ -97,6 +98,9 @@ inline bool pool_tc_shape(const kvPool* p) {
 
 // Largest CTA count the split pass uses; sizes the decode workspace.
 constexpr int kMaxDecodeCtas = 1024;
+
+// SM count of the pool's device, 0 while unknown (device.cu).
+int pool_sm_count(const kvPool* p);
 
 // Workspace bytes of a planned decode pass (plan.cpp).
 size_t plan_workspace_bytes(int n_segs, int c_max, int D);

@@ -452,6 +452,34 @@ def test_planned_equals_plain_without_sharing(path):
 
 
 @pytest.mark.parametrize("path", TENSOR_PATHS)
+@pytest.mark.parametrize("name", ["shared_8k", "gqa70b_32k"])
+def test_planned_start_records_change_no_bit(name, path):
+    # the same step twice on identical pools: once with the plan's per-CTA
+    # start records built for the launch's grid (the kernels take their first
+    # pieces and block ids from them), once with records built for another
+    # grid (ignored: the kernels search the plan); the outputs are identical
+    from paged_kv_cache_65_gb300 import _lib
+    from paged_kv_cache_65_gb300.cache import parse_plan
+
+    wl = synth.workload(name)
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    outs = []
+    for grid in (0, 7):
+        cache, run = make(wl, zero=False, path=path)
+        cache.kv_pool_set_option(_lib.KV_OPT_PLAN_GRID, grid)
+        q, k, v = wl.step_values(0)
+        _, _, og = run.step(wl.decode_seqs, q, k, v, planned=True)
+        plan = parse_plan(run.plan(wl.decode_seqs, run.max_blocks(wl.decode_seqs))[0])
+        if grid == 0:
+            assert plan["start_grid"] == (sm if plan["kernel"] == 3 else 2 * sm)
+        else:
+            assert plan["start_grid"] == 7
+        outs.append(og.cpu().numpy())
+        check_status(cache)
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS)
 def test_multilayer_host_step_with_long_shared_prefix(path):
     # kv_decode_step_host plans the step: sequences 0-2 share 300 tokens
     L, B, H, G, D = 2, 16, 2, 4, 128

@@ -129,3 +129,69 @@ def test_plans_of_random_fork_trees(seed):
     for min_tokens in (16, 128, 0):
         buf, _ = c.paged_decode_plan(live, H * G, mb, min_tokens)
         check_plan(bm, parse_plan(buf), live, G, min_tokens or 128)
+
+
+def walk_first_piece(plan, grid, c):
+    """The first piece of CTA c as the split pass walks it: units
+    [c * chunk, min((c + 1) * chunk, W)), chunk = ceil(W / grid); segments
+    are scanned from the first one, skipping those that end at or before the
+    CTA's first unit (a linear scan, independent of the builder's search)."""
+    W, B = plan["W"], plan["B"]
+    chunk = max(1, -(-W // grid))
+    r0 = c * chunk
+    if r0 >= W:
+        return None
+    r1 = min(r0 + chunk, W)
+    for si, s in enumerate(plan["segs"]):
+        n, w = int(s["b1"] - s["b0"]), max(1, int(s["w"]))
+        end_seg = int(s["wpre"]) + n * w
+        if n <= 0 or r0 >= end_seg:
+            continue
+        end = min(r1, end_seg)
+        jb, je = -(-(r0 - int(s["wpre"])) // w), -(-(end - int(s["wpre"])) // w)
+        b0, b1 = int(s["b0"]) + jb, int(s["b0"]) + je
+        return dict(seg=si, rep=int(s["rep"]), head=int(s["head"]), b0=b0, b1=b1,
+                    tok_end=min(b1 * B, int(s["tok_end"])), ncols=int(s["ncols"]),
+                    mem=int(s["mem"]), r_after=end)
+    return None
+
+
+@pytest.mark.parametrize("grid", [1, 7, 152, 304, 1024])
+@pytest.mark.parametrize("name", ["qwen_2k", "shared_8k", "gqa70b_32k"])
+def test_start_records_follow_the_walk(name, grid):
+    # one record per CTA of the grid the option names: the first piece the
+    # split pass's walk yields for that CTA, the position after it, and the
+    # piece's first physical blocks from the member's own table
+    from paged_kv_cache_65_gb300 import _lib
+
+    wl = synth.workload(name)
+    bm, c = build_both(wl)
+    c.kv_pool_set_option(_lib.KV_OPT_PLAN_GRID, grid)
+    mb = max(len(bm.tables[s]) for s in wl.decode_seqs)
+    plan = parse_plan(c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)[0])
+    assert plan["start_grid"] == grid and len(plan["starts"]) == grid
+    for cta in range(grid):
+        R = plan["starts"][cta]
+        want = walk_first_piece(plan, grid, cta)
+        if want is None:
+            assert R["seg"] == -1
+            continue
+        for k, v in want.items():
+            assert int(R[k]) == v, (cta, k)
+        table = bm.tables[wl.decode_seqs[want["rep"]]]
+        n = min(16, want["b1"] - want["b0"], len(table) - want["b0"])
+        assert int(R["n_pid"]) == n
+        assert list(R["pid"][:n]) == table[want["b0"]:want["b0"] + n]
+
+
+def test_plans_without_a_known_grid_have_no_start_records():
+    # a pool whose device is unknown (host only) and no grid option: no records
+    wl = synth.workload("qwen_2k")
+    bm, c = build_both(wl)
+    mb = max(len(bm.tables[s]) for s in wl.decode_seqs)
+    plan = parse_plan(c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)[0])
+    assert plan["start_grid"] == 0 and len(plan["starts"]) == 0
+    from paged_kv_cache_65_gb300 import _lib
+
+    with pytest.raises(Exception):
+        c.kv_pool_set_option(_lib.KV_OPT_PLAN_GRID, 1025)
