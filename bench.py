@@ -50,11 +50,11 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331667200 + 3100928, "sha": "a5879904393136b1"},
-    ("shared_8k", "decode_mma_kernel"): {"bytes": 170998272 + 3209728, "sha": "a5879904393136b1"},
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615953664 + 6738432, "sha": "a5879904393136b1"},
-    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169242112 + 3386112, "sha": "a5879904393136b1"},
-    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 157367808 + 51861760, "sha": "3eb978eb03b932bd"},
+    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331689728 + 3470592, "sha": "01e42bad69efdeb7"},
+    ("shared_8k", "decode_mma_kernel"): {"bytes": 170989056 + 2912000, "sha": "01e42bad69efdeb7"},
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615961344 + 6333440, "sha": "01e42bad69efdeb7"},
+    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169273600 + 3292416, "sha": "01e42bad69efdeb7"},
+    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 163634944 + 32672768, "sha": "30f83f19435cbb38"},
 }
 
 
