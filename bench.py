@@ -177,7 +177,8 @@ def aggregate(local_bytes: float, local_seconds: float, world: int, device=None)
 
 
 # -------------------------------------------------------------- workload
-def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device"):
+def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device",
+          placement_seed=None):
     """Build the workload's pool on the device.  ``fill="device"`` fills the
     whole pool with seeded N(0,1) values generated on the GPU by torch and
     skips history writes (the history values are whatever the pool holds);
@@ -188,6 +189,11 @@ def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device"):
     from paged_kv_cache_65_gb300.driver import DeviceRun
 
     wl = synth.workload(name, **({"block_size": block_size} if name == "pool36" else {}))
+    if placement_seed is not None:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, free_order=synth.permutation((placement_seed, 99),
+                                                                   wl.n_blocks))
     cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
                          wl.dtype, free_order=wl.free_order, device=device)
     fp8 = wl.dtype == "fp8_e4m3"
@@ -241,7 +247,8 @@ def bench_ours(args):
     rank, local, world = dist_setup()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl, cache, run = setup(args.workload, args.block_size, dev)
+    wl, cache, run = setup(args.workload, args.block_size, dev,
+                           placement_seed=args.placement_seed)
     from paged_kv_cache_65_gb300 import _lib
 
     if args.cuda_cores:
@@ -443,6 +450,12 @@ def bench_ours(args):
     with_ms = [a.elapsed_time(b) for a, b in with_ms]
     without_ms = [a.elapsed_time(b) for a, b in without_ms]
     inc_s = (float(np.median(with_ms)) - float(np.median(without_ms))) / L / 1e3
+    # steps whose plan carries copy-on-write pairs (the first step after a
+    # fork) apart from the rest
+    cow_ms = [t for i, t in zip(range(args.warmup, n_steps), step_ms)
+              if dplans[i % n_plans]["npairs"]]
+    steady_ms = [t for i, t in zip(range(args.warmup, n_steps), step_ms)
+                 if not dplans[i % n_plans]["npairs"]]
     dev_s = sum(step_ms) / 1e3
     ub = sum(dplans[i % n_plans]["ub"] for i in range(args.warmup, n_steps))
     lb = sum(dplans[i % n_plans]["lb"] for i in range(args.warmup, n_steps))
@@ -481,6 +494,7 @@ def bench_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
+        cpu_par = cpu_baseline_parallel(args.workload, args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -495,6 +509,7 @@ def bench_ours(args):
                        "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
                        "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
                        "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+                       "placement_seed": args.placement_seed,
                        "parallelism": f"replicas x{world}"},
             "pct_of_hbm_peak": round(100 * value / peak, 2),
             "pct_of_8tbs_nominal": round(100 * value / 8000.0, 2),
@@ -515,12 +530,19 @@ def bench_ours(args):
                          "event_node_timing": split_src},
             "gpu_launches": launches * world,
             "graphs": "one CUDA graph per step plan, replayed",
+            "step_us_median_p10_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2)
+                                       for q in (50, 10, 90)],
+            "cow_steps": ({"n": len(cow_ms), "pairs": int(max(d["npairs"] for d in dplans)),
+                           "median_us": round(float(np.median(cow_ms)) * 1e3, 2),
+                           "steady_median_us": round(float(np.median(steady_ms)) * 1e3, 2)}
+                          if cow_ms and steady_ms else None),
             "e2e": e2e,
             "clocks": clk,
             "wall_s_timed": round(t_wall, 4),
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
+            line["cpu_baseline_parallel"] = cpu_par
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -610,7 +632,7 @@ def bench_prefill(args):
     rank, local, world = dist_setup()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl, cache, run = setup(args.workload, device=dev)
+    wl, cache, run = setup(args.workload, device=dev, placement_seed=args.placement_seed)
     cache.kv_pool_set_option(_lib_mod().KV_OPT_PDL, 0 if args.no_pdl else 1)
     wl.history = {s: run.lengths.get(s, 0) for s, _ in wl.chunks}
     seqs = [s for s, _ in wl.chunks]
@@ -707,6 +729,7 @@ def bench_prefill(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
+        cpu_par = cpu_baseline_parallel(args.workload, args.cpu_seconds)
     if rank == 0:
         line = {
             "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s",
@@ -722,6 +745,7 @@ def bench_prefill(args):
                                       "heaviest first (host schedule, paged_prefill_schedule)"),
                        "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads, "D_h": wl.head_dim,
                        "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+                       "placement_seed": args.placement_seed,
                        "parallelism": f"replicas x{world}"},
             "pct_of_tensor_peak": round(100 * value / peak, 2),
             "prefill_tokens_per_s": round(n_tok * world / (ms / 1e3), 1),
@@ -741,6 +765,7 @@ def bench_prefill(args):
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
+            line["cpu_baseline_parallel"] = cpu_par
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -836,9 +861,10 @@ def oracle_attend(wl, orc, q, seconds: float, max_seqs: int | None = None, start
     return nbytes, time.perf_counter() - t0, done
 
 
-def prefill_oracle_leg(workload: str, seconds: float):
+def prefill_oracle_leg(workload: str, seconds: float, start: int = 0):
     """The oracle's chunked-prefill attention as it stands on whole chunks of
-    the round, one after the other, until ``seconds`` have passed."""
+    the round, one after the other (from chunk ``start``), until ``seconds``
+    have passed."""
     from oracle.runner import OracleRun
 
     wl = synth.workload(workload)
@@ -848,7 +874,7 @@ def prefill_oracle_leg(workload: str, seconds: float):
     flops, done = 0.0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds or done == 0:
-        i = done % len(wl.chunks)
+        i = (start + done) % len(wl.chunks)
         orc.prefill_attend(0, q, [i])
         seq, c = wl.chunks[i]
         flops += 4.0 * wl.head_dim * wl.n_q_heads * (c * hist[seq] + c * (c + 1) // 2)
@@ -857,16 +883,16 @@ def prefill_oracle_leg(workload: str, seconds: float):
     return flops, dt, done
 
 
-def cpu_leg(workload: str, seconds: float):
+def cpu_leg(workload: str, seconds: float, start: int = 0):
     if isinstance(synth.workload(workload), synth.PrefillWorkload):
-        flops, dt, done = prefill_oracle_leg(workload, seconds)
+        flops, dt, done = prefill_oracle_leg(workload, seconds, start)
         return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
-                "kind": "oracle", "seconds": round(dt, 3), "chunks": done,
+                "kind": "oracle", "seconds": round(dt, 3), "chunks": done, "flops": flops,
                 "sample": f"{workload}: {done} whole chunks of the round, cycling over its "
                           f"{len(synth.workload(workload).chunks)} chunks (fp64 masked "
                           f"softmax over the paged context, one thread), {dt:.1f} s"}
     wl, orc, q = oracle_sample(workload)
-    nbytes, dt, done = oracle_attend(wl, orc, q, seconds)
+    nbytes, dt, done = oracle_attend(wl, orc, q, seconds, start=start)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{workload}: {done} single-sequence layer-0 decode attentions, cycling "
                       f"over the batch's {len(wl.decode_seqs)} sequences (paged gather + fp64 "
@@ -887,6 +913,44 @@ def cpu_baseline(workload: str, seconds: float):
             return json.loads(ln)
     return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "failed: " + r.stderr[-200:]}
+
+
+def cpu_baseline_parallel(workload: str, seconds: float):
+    """The same oracle leg in one single-threaded process per host core, all
+    at once, each starting at a different sequence (or chunk) of the batch:
+    the work they finish together over the longest one's time."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    wl = synth.workload(workload)
+    n = len(wl.chunks) if isinstance(wl, synth.PrefillWorkload) else len(wl.decode_seqs)
+    P = max(1, os.cpu_count() or 1)
+    procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-leg", workload,
+                               "--cpu-seconds", str(seconds), "--cpu-start", str(k * n // P)],
+                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                              env=env) for k in range(P)]
+    legs = []
+    for pr in procs:
+        out, _ = pr.communicate(timeout=900)
+        for ln in out.splitlines()[::-1]:
+            if ln.startswith("{"):
+                legs.append(json.loads(ln))
+                break
+    if len(legs) != P:
+        return {"value": None, "kind": "oracle", "cores": P, "sample": "failed"}
+    dt = max(x["seconds"] for x in legs)
+    if "flops" in legs[0]:
+        value, unit = round(sum(x["flops"] for x in legs) / dt / 1e12, 6), "TFLOP/s"
+        done = sum(x["chunks"] for x in legs)
+        what = f"{done} whole chunks"
+    else:
+        value, unit = round(sum(x["bytes"] for x in legs) / dt / 1e9, 4), "GB/s"
+        done = sum(x["sequences"] for x in legs)
+        what = f"{done} single-sequence layer-0 decode attentions"
+    return {"value": value, "unit": unit, "cores": P, "kind": "oracle",
+            "sample": f"{workload}: {P} single-threaded oracle processes at once, "
+                      f"{what} in all, {dt:.1f} s", "seconds": round(dt, 3)}
 
 
 def bench_reference(args):
@@ -1045,9 +1109,13 @@ def main():
                     help="host prefix-cache hit of a 4096-token prompt instead of a GPU step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-leg", default=None)
+    ap.add_argument("--cpu-start", type=int, default=0)
+    ap.add_argument("--placement-seed", type=int, default=None,
+                    help="re-randomise the physical placement of the pool's blocks (the "
+                         "free-list order) with this seed; contents and lengths unchanged")
     args = ap.parse_args()
     if args.cpu_leg:
-        print(json.dumps(cpu_leg(args.cpu_leg, args.cpu_seconds)), flush=True)
+        print(json.dumps(cpu_leg(args.cpu_leg, args.cpu_seconds, args.cpu_start)), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3
