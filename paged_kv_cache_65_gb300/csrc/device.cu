@@ -195,7 +195,9 @@ __global__ void slot_write_fp8_kernel(const uint4* __restrict__ k_new,
 }
 
 // Copy-on-write copy: CTA (pair, layer, part) copies a slice of block src
-// into block dst in K and V.
+// into block dst in K and V.  Each thread loads up to four 16-byte vectors of
+// K and four of V before storing any, so the loads of cold source blocks are
+// in flight together instead of one latency per vector.
 __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, uint4* vc,
                                 int n_blocks, long long block_vecs, int32_t* status) {
   pkv::griddep_wait();
@@ -213,9 +215,25 @@ __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, ui
   const long long per = (block_vecs + gridDim.z - 1) / gridDim.z;
   const long long b = (long long)blockIdx.z * per;
   const long long e = b + per < block_vecs ? b + per : block_vecs;
-  for (long long v = b + threadIdx.x; v < e; v += blockDim.x) {
-    kc[d0 + v] = kc[s0 + v];
-    vc[d0 + v] = vc[s0 + v];
+  constexpr int U = 4;
+  for (long long v0 = b + threadIdx.x; v0 < e; v0 += (long long)U * blockDim.x) {
+    uint4 kx[U], vx[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long v = v0 + (long long)u * blockDim.x;
+      if (v < e) {
+        kx[u] = kc[s0 + v];
+        vx[u] = vc[s0 + v];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long v = v0 + (long long)u * blockDim.x;
+      if (v < e) {
+        kc[d0 + v] = kx[u];
+        vc[d0 + v] = vx[u];
+      }
+    }
   }
 }
 
@@ -507,7 +525,9 @@ kvStatus cow_copy(kvPool* p, const int32_t* d_pairs, int n_pairs, void* stream) 
   kvStatus s = ensure_device(p);
   if (s != KV_OK) return s;
   const long long block_vecs = static_cast<long long>(p->B) * p->H * p->D * p->esize / 16;
-  const int parts = block_vecs >= 4096 ? 4 : 1;
+  // about 512 vectors of K (and of V) per CTA: two per thread
+  const long long want = (block_vecs + 511) / 512;
+  const int parts = static_cast<int>(want < 1 ? 1 : (want > 16 ? 16 : want));
   dim3 grid(n_pairs, p->L, parts);
   const cudaError_t e = pkv::launch_kernel(
       p->pdl, cow_copy_kernel, grid, dim3(256), 0, as_stream(stream), d_pairs,
