@@ -83,6 +83,7 @@ void plan_starts(const std::vector<PlanSeg>& segs, int64_t W, int grid, int B,
   int64_t chunk = (W + grid - 1) / grid;
   if (chunk == 0) chunk = 1;
   const int n = static_cast<int>(segs.size());
+  int lo = 0;  // last segment with wpre <= r0; r0 grows with c, so lo only moves on
   for (int c = 0; c < grid; ++c) {
     PlanStart& R = out[c];
     std::memset(&R, 0, sizeof(R));
@@ -90,12 +91,7 @@ void plan_starts(const std::vector<PlanSeg>& segs, int64_t W, int grid, int B,
     const int64_t r0 = static_cast<int64_t>(c) * chunk;
     if (r0 >= W) continue;
     const int64_t r1 = std::min(r0 + chunk, W);
-    // last segment with wpre <= r0 (segments are in wpre order)
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) / 2;
-      if (segs[mid].wpre <= r0) lo = mid; else hi = mid;
-    }
+    while (lo + 1 < n && segs[lo + 1].wpre <= r0) ++lo;
     for (int s = lo; s < n; ++s) {
       const PlanSeg& sg = segs[s];
       const int64_t len = sg.b1 - sg.b0;
@@ -318,7 +314,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   }
   if (l.total > plan_bytes) return KV_ERR_INVALID_ARG;
   unsigned char* out = static_cast<unsigned char*>(h_plan);
-  std::memset(out, 0, l.total);
+  std::memset(out, 0, l.start);  // the start records are written whole below
   PlanHeader hd{};
   hd.W = W;
   hd.n_segs = static_cast<int32_t>(segs.size());
