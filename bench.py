@@ -313,7 +313,7 @@ def bench_ours(args):
 
     # one CUDA graph per step plan: cow copy, slot write, per layer split + merge;
     # event-record nodes around each split pass time the dominant kernel
-    def enqueue(p, ext=None, split=True):
+    def enqueue(p, ext=None, split=True, merge=True):
         cnt = 0
         if p["npairs"]:
             cache.cow_copy(p["pairs"], p["npairs"])
@@ -331,10 +331,10 @@ def bench_ours(args):
                                             p["lens"], n, ws, 0.0)
             if ext is not None:
                 ext[layer][1].record()
-            if use_plan:
+            if use_plan and merge:
                 cache.paged_decode_merge_planned(wl.n_q_heads, p["d_plan"], p["h_plan"],
                                                  out[layer], ws)
-            else:
+            elif merge:
                 cache.paged_decode_merge(wl.n_q_heads, p["lens"], n, out[layer], ws)
             cnt += 2
         return cnt
@@ -347,7 +347,7 @@ def bench_ours(args):
                        for _ in range(L)] for _ in range(n_plans)]
     except TypeError:
         ext_events = None
-    graphs, instr_graphs, split_graphs, nosplit_graphs = [], [], [], []
+    graphs, instr_graphs, split_graphs, nosplit_graphs, noattn_graphs = [], [], [], [], []
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
@@ -360,6 +360,10 @@ def bench_ours(args):
             with torch.cuda.graph(gn, stream=cap):
                 enqueue(dplans[pi], split=False)
             nosplit_graphs.append(gn)
+            ga = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ga, stream=cap):
+                enqueue(dplans[pi], split=False, merge=False)
+            noattn_graphs.append(ga)
             gi = torch.cuda.CUDAGraph()
             if ext_events is not None:
                 with torch.cuda.graph(gi, stream=cap):
@@ -437,9 +441,10 @@ def bench_ours(args):
     # split launches, replayed the same way (L2 flushed before each, events
     # around the replay); per launch = the difference of the medians / L
     n_inc = min(args.steps, 200)
-    with_ms, without_ms = [], []
+    with_ms, without_ms, noattn_ms = [], [], []
     for j in range(n_inc):
-        for gr_, acc in ((graphs, with_ms), (nosplit_graphs, without_ms)):
+        for gr_, acc in ((graphs, with_ms), (nosplit_graphs, without_ms),
+                         (noattn_graphs, noattn_ms)):
             flush_l2(j)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -449,7 +454,10 @@ def bench_ours(args):
     torch.cuda.synchronize()
     with_ms = [a.elapsed_time(b) for a, b in with_ms]
     without_ms = [a.elapsed_time(b) for a, b in without_ms]
+    noattn_ms = [a.elapsed_time(b) for a, b in noattn_ms]
     inc_s = (float(np.median(with_ms)) - float(np.median(without_ms))) / L / 1e3
+    # split and merge launches together (the attention of the layer)
+    attn_s = (float(np.median(with_ms)) - float(np.median(noattn_ms))) / L / 1e3
     # steps whose plan carries copy-on-write pairs (the first step after a
     # fork) apart from the rest
     cow_ms = [t for i, t in zip(range(args.warmup, n_steps), step_ms)
@@ -527,6 +535,8 @@ def bench_ours(args):
                          "alg_bytes_per_launch": int(alg),
                          "mean_launch_us": round(split_s * 1e6, 2),
                          "event_node_launch_us": round(split_ev_s * 1e6, 2),
+                         "split_and_merge_us": round(attn_s * 1e6, 2),
+                         "split_and_merge_frac": round(alg / attn_s / 1e9 / peak, 4),
                          "event_node_timing": split_src},
             "gpu_launches": launches * world,
             "graphs": "one CUDA graph per step plan, replayed",

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
 // prefix and private rest), with the same rule as merge_kernel.  The plan
 // (written by the host before the stream's kernel chain started) is read
 // before waiting for the split pass; then lanes load the pieces' (m, l) side
-// by side and the O loads of all pieces are issued together, instead of a
+// by side, once, and the O loads go out eight pieces at a time, instead of a
 // chain of dependent loads per piece.
 template <int D>
 __global__ void __launch_bounds__(128) merge_plan_kernel(
@@ -353,9 +353,13 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
   pkv::griddep_wait();
   pkv::griddep_launch_dependents();
   if (!live) return;
-  float M = -INFINITY;
-  for (int k = lane; k < np; k += 32)
-    M = fmaxf(M, ws_ml[static_cast<long long>(k < 32 ? slot0 : piece_slot(k)) * 2]);
+  // (m, l) of the first 32 pieces in one 8-byte load per lane, kept for the
+  // weights below
+  float2 ml0 = make_float2(-INFINITY, 0.f);
+  if (lane < np) ml0 = *reinterpret_cast<const float2*>(&ws_ml[static_cast<long long>(slot0) * 2]);
+  float M = ml0.x;
+  for (int k = lane + 32; k < np; k += 32)
+    M = fmaxf(M, ws_ml[static_cast<long long>(piece_slot(k)) * 2]);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float o[DL];
@@ -370,12 +374,13 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
     float f = 0.f;
     if (k < np) {
       sl = r == 0 ? slot0 : piece_slot(k);
-      const float mk = ws_ml[static_cast<long long>(sl) * 2];
-      f = mk == -INFINITY ? 0.f : pkv::exp2_approx(mk - M);
-      L += f * ws_ml[static_cast<long long>(sl) * 2 + 1];
+      const float2 mlk =
+          r == 0 ? ml0 : *reinterpret_cast<const float2*>(&ws_ml[static_cast<long long>(sl) * 2]);
+      f = mlk.x == -INFINITY ? 0.f : pkv::exp2_approx(mlk.x - M);
+      L += f * mlk.y;
     }
     const int nr = np - r < 32 ? np - r : 32;
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < nr; ++j) {
       const float fj = __shfl_sync(0xffffffffu, f, j);
       const int sj = __shfl_sync(0xffffffffu, sl, j);
