@@ -50,11 +50,11 @@ DEFAULT_WORKLOAD = "qwen_2k"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331689728 + 3470592, "sha": "01e42bad69efdeb7"},
-    ("shared_8k", "decode_mma_kernel"): {"bytes": 170989056 + 2912000, "sha": "01e42bad69efdeb7"},
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615961344 + 6333440, "sha": "01e42bad69efdeb7"},
-    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169273600 + 3292416, "sha": "01e42bad69efdeb7"},
-    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 163634944 + 32672768, "sha": "30f83f19435cbb38"},
+    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331703296 + 3276800, "sha": "7a574767b9923aec"},
+    ("shared_8k", "decode_mma_kernel"): {"bytes": 171004416 + 3211520, "sha": "7a574767b9923aec"},
+    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615941376 + 6079488, "sha": "7a574767b9923aec"},
+    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169274368 + 3358720, "sha": "7a574767b9923aec"},
+    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
 }
 
 
