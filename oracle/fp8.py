@@ -3,7 +3,7 @@
 "第 8 章 推理优化" §8.4.2 compares BF16 KV with narrower KV formats (an FP8
 KV cache in its H100 inter-token-latency fit; q8_0 and q4_0 with a shared
 scale per group of 32 values) and charges the read savings against the
-conversion time.  This build's quantized pool stores each K or V element
+conversion time.  The FP8 pool modelled here stores each K or V element
 as one FP8 E4M3 code of ``x / scale``, one float32 scale per pool for K and
 one for V, so a token row costs half of BF16 (32 of every 64 bytes).
 

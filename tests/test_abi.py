@@ -23,7 +23,7 @@ def lib():
     return _lib
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_pool_block_and_kernel_calls():
     names = declared_functions()
     for n in ("kv_pool_create", "block_alloc", "block_free", "block_fork", "block_cow",
               "reshape_and_cache", "paged_decode_attention", "cow_copy"):
