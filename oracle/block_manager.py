@@ -26,7 +26,7 @@ Sources, by page title and section:
 * same page §13 -- the conservation checks ``N_free + N_allocated = N_total``
   and "the set of blocks with a positive count is exactly the allocated set".
 
-Readings where the pages leave a step open (each listed in the design doc):
+Readings where the pages leave a step open:
 
 * A batch is processed in the order the caller lists its sequences; the first
   of several sharers of a partially filled tail to write copies, and once the
