@@ -312,10 +312,18 @@ __global__ void __launch_bounds__(128) merge_kernel(const long long* __restrict_
 // prefix and private rest), with the same rule as merge_kernel.  The plan
 // (written by the host before the stream's kernel chain started) is read
 // before waiting for the split pass; then lanes load the pieces' (m, l) side
-// by side, once, and the O loads go out eight pieces at a time, instead of a
-// chain of dependent loads per piece.
-template <int D>
-__global__ void __launch_bounds__(128) merge_plan_kernel(
+// by side, once, and the O rows of the first PRE pieces go out with them
+// (the rest four pieces at a time), instead of a chain of dependent loads per
+// piece.  The sums run in piece order either way.
+// Four warps per CTA.  PRE pieces' O rows are loaded ahead: 12 covers the
+// rows of a batch sharing a long prefix (about ten pieces each) at 96
+// registers a thread, five CTAs an SM; 8 keeps 80 registers, six CTAs an SM.
+// The host takes the deeper one only while the whole grid is resident at once
+// (a 48-sequence, 64-query-head batch has 768 CTAs: one wave at 8, two at 12).
+constexpr int kMergePlanWarps = 4;
+
+template <int D, int PRE>
+__global__ void __launch_bounds__(kMergePlanWarps * 32) merge_plan_kernel(
     const PlanSeg* __restrict__ segs, const int32_t* __restrict__ eoff,
     const PlanEntry* __restrict__ ents, long long W, int grid, int c_max,
     const float* __restrict__ ws_ml, const float* __restrict__ ws_o, int H, int Hq,
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
   constexpr int DL = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = blockIdx.y * 4 + warp;
+  const int hq = blockIdx.y * kMergePlanWarps + warp;
   const bool live = hq < Hq;
   const int G = Hq / H;
   const int h = live ? hq / G : 0, g = live ? hq - h * G : 0;
@@ -357,6 +365,28 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
   // weights below
   float2 ml0 = make_float2(-INFINITY, 0.f);
   if (lane < np) ml0 = *reinterpret_cast<const float2*>(&ws_ml[static_cast<long long>(slot0) * 2]);
+  // the O rows of the first kPre pieces go out with their (m, l), not after
+  // the weights: one dependent latency less after the wait
+  constexpr int kPre = PRE;
+  float pre[kPre][DL];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const int sj = __shfl_sync(0xffffffffu, slot0, j);
+    if (j < np) {
+      const float* src = ws_o + static_cast<long long>(sj) * D + lane * DL;
+      if constexpr (DL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        pre[j][0] = v.x;
+        pre[j][1] = v.y;
+        pre[j][2] = v.z;
+        pre[j][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        pre[j][0] = v.x;
+        pre[j][1] = v.y;
+      }
+    }
+  }
   float M = ml0.x;
   for (int k = lane + 32; k < np; k += 32)
     M = fmaxf(M, ws_ml[static_cast<long long>(piece_slot(k)) * 2]);
@@ -380,8 +410,20 @@ __global__ void __launch_bounds__(128) merge_plan_kernel(
       L += f * mlk.y;
     }
     const int nr = np - r < 32 ? np - r : 32;
-#pragma unroll 8
-    for (int j = 0; j < nr; ++j) {
+    int j0 = 0;
+    if (r == 0) {
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const float fj = __shfl_sync(0xffffffffu, f, j);
+        if (j < nr) {
+#pragma unroll
+          for (int d = 0; d < DL; ++d) o[d] += fj * pre[j][d];
+        }
+      }
+      j0 = kPre;
+    }
+#pragma unroll 4
+    for (int j = j0; j < nr; ++j) {
       const float fj = __shfl_sync(0xffffffffu, f, j);
       const int sj = __shfl_sync(0xffffffffu, sl, j);
       const float* src = ws_o + static_cast<long long>(sj) * D + lane * DL;
@@ -813,15 +855,28 @@ kvStatus paged_decode_merge_planned(kvPool* p, int n_q_heads, const void* d_plan
   const PlanEntry* ents = reinterpret_cast<const PlanEntry*>(dp + hd.ent_off);
   float* of = out_dtype == KV_DTYPE_F32 ? reinterpret_cast<float*>(d_out) : nullptr;
   __nv_bfloat16* ob = out_dtype == KV_DTYPE_BF16 ? reinterpret_cast<__nv_bfloat16*>(d_out) : nullptr;
-  const dim3 mg(hd.n_seq, (n_q_heads + 3) / 4);
+  const dim3 mg(hd.n_seq, (n_q_heads + kMergePlanWarps - 1) / kMergePlanWarps);
   const int gr = grid > 0 ? grid : 1;
-  const cudaError_t e =
-      p->D == 128 ? pkv::launch_kernel(p->pdl, merge_plan_kernel<128>, mg, dim3(128), 0,
-                                       as_stream(stream), segs, eoff, ents, hd.W, gr, hd.c_max, ml,
-                                       o, p->H, n_q_heads, of, ob)
-                  : pkv::launch_kernel(p->pdl, merge_plan_kernel<64>, mg, dim3(128), 0,
-                                       as_stream(stream), segs, eoff, ents, hd.W, gr, hd.c_max, ml,
-                                       o, p->H, n_q_heads, of, ob);
+  const dim3 mb(kMergePlanWarps * 32);
+  cudaError_t e = cudaSuccess;
+  if (p->merge_deep_ctas < 0) {  // resident CTAs of the deeper variant, once per pool
+    int occ = 0;
+    e = p->D == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                          &occ, merge_plan_kernel<128, 12>, kMergePlanWarps * 32, 0)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                          &occ, merge_plan_kernel<64, 12>, kMergePlanWarps * 32, 0);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+    p->merge_deep_ctas = occ * pool_sm_count(p);
+  }
+  const bool deep = static_cast<long long>(mg.x) * mg.y <= p->merge_deep_ctas;
+  auto go = [&](auto kern) {
+    return pkv::launch_kernel(p->pdl, kern, mg, mb, 0, as_stream(stream), segs, eoff, ents, hd.W,
+                              gr, hd.c_max, ml, o, p->H, n_q_heads, of, ob);
+  };
+  if (p->D == 128)
+    e = deep ? go(merge_plan_kernel<128, 12>) : go(merge_plan_kernel<128, 8>);
+  else
+    e = deep ? go(merge_plan_kernel<64, 12>) : go(merge_plan_kernel<64, 8>);
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 

@@ -61,6 +61,7 @@ struct kvPool {
   int sm_count = 0;
   int grid_by_g[4] = {0, 0, 0, 0};  // split-pass CTAs per log2(H_q / H_kv)
   int grid_tc = 0;                  // CTAs of the tcgen05 split pass (one per SM)
+  int merge_deep_ctas = -1;         // planned-merge CTAs resident at once, deep prefetch
   int plan_grid = 0;                // KV_OPT_PLAN_GRID: CTA count plans build start records for
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
