@@ -348,6 +348,7 @@ def bench_ours(args):
     except TypeError:
         ext_events = None
     graphs, instr_graphs, split_graphs, nosplit_graphs, noattn_graphs = [], [], [], [], []
+    nomerge_graphs = []
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
@@ -364,6 +365,10 @@ def bench_ours(args):
             with torch.cuda.graph(ga, stream=cap):
                 enqueue(dplans[pi], split=False, merge=False)
             noattn_graphs.append(ga)
+            gs = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs, stream=cap):
+                enqueue(dplans[pi], merge=False)
+            nomerge_graphs.append(gs)
             gi = torch.cuda.CUDAGraph()
             if ext_events is not None:
                 with torch.cuda.graph(gi, stream=cap):
@@ -437,14 +442,17 @@ def bench_ours(args):
             e0s[j][1].record(stream)
         torch.cuda.synchronize()
         split_ms = [a.elapsed_time(b) / L for a, b in e0s]
-    # the split passes' share of the step: the same step graphs without the
-    # split launches, replayed the same way (L2 flushed before each, events
-    # around the replay); per launch = the difference of the medians / L
+    # the split passes' device time: the step graphs without the merge
+    # launches (each ending with its layer's split pass) against the same
+    # graphs with neither, replayed the same way (L2 flushed before each,
+    # events around the replay); per launch = the difference of the medians
+    # / L.  The merge is left out of both, so its own speed, after the split
+    # pass or alone, does not enter the split's figure.
     n_inc = min(args.steps, 200)
-    with_ms, without_ms, noattn_ms = [], [], []
+    with_ms, without_ms, noattn_ms, nomerge_ms = [], [], [], []
     for j in range(n_inc):
         for gr_, acc in ((graphs, with_ms), (nosplit_graphs, without_ms),
-                         (noattn_graphs, noattn_ms)):
+                         (noattn_graphs, noattn_ms), (nomerge_graphs, nomerge_ms)):
             flush_l2(j)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -455,7 +463,10 @@ def bench_ours(args):
     with_ms = [a.elapsed_time(b) for a, b in with_ms]
     without_ms = [a.elapsed_time(b) for a, b in without_ms]
     noattn_ms = [a.elapsed_time(b) for a, b in noattn_ms]
+    nomerge_ms = [a.elapsed_time(b) for a, b in nomerge_ms]
+    # the step minus the step without the split launches (the merge kept)
     inc_s = (float(np.median(with_ms)) - float(np.median(without_ms))) / L / 1e3
+    split_only_s = (float(np.median(nomerge_ms)) - float(np.median(noattn_ms))) / L / 1e3
     # split and merge launches together (the attention of the layer)
     attn_s = (float(np.median(with_ms)) - float(np.median(noattn_ms))) / L / 1e3
     # steps whose plan carries copy-on-write pairs (the first step after a
@@ -477,7 +488,7 @@ def bench_ours(args):
     per_launch_alg = [dplans[j % n_plans]["ub"] / L for j in range(n_split)]
     alg = float(np.mean(per_launch_alg))
     split_ev_s = float(np.mean(split_ms)) / 1e3
-    split_s = inc_s
+    split_s = split_only_s
     peak, peak_kind = read_peaks()
     achieved = alg / split_s / 1e9
     # the split-pass kernel that ran: a plan records its own; otherwise the option
@@ -528,13 +539,14 @@ def bench_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
                          "kernel": kname,
                          "peak_source": peak_kind,
-                         "timing": ("device time the split launches add to the step: median of "
-                                    "the step graphs minus median of the same graphs without "
-                                    "them, per launch (CUDA events around each replay, L2 "
-                                    "flushed before each)"),
+                         "timing": ("device time of the split launches: median of the step "
+                                    "graphs without the merge launches minus median of the "
+                                    "same graphs without split or merge, per launch (CUDA "
+                                    "events around each replay, L2 flushed before each)"),
                          "alg_bytes_per_launch": int(alg),
                          "mean_launch_us": round(split_s * 1e6, 2),
                          "event_node_launch_us": round(split_ev_s * 1e6, 2),
+                         "step_minus_nosplit_us": round(inc_s * 1e6, 2),
                          "split_and_merge_us": round(attn_s * 1e6, 2),
                          "split_and_merge_frac": round(alg / attn_s / 1e9 / peak, 4),
                          "event_node_timing": split_src},
