@@ -76,16 +76,19 @@ class KVStore:
 
     def gather_raw(self, layer: int, table, ctx: int):
         """Positions ``0..ctx-1`` of one sequence, in logical order, as
-        stored elements ``[ctx, H_kv, D_h]``."""
+        stored elements ``[ctx, H_kv, D_h]``.  Taken block by block: logical
+        block ``j`` holds positions ``j*B .. j*B + B - 1`` in slots ``0..B-1``
+        of physical block ``table[j]``, the last one only its first
+        ``ctx - j*B`` slots."""
         ks, vs = [], []
-        for t in range(ctx):
-            p = table[t // self.B]
-            o = t % self.B
-            ks.append(self.K[layer, p, o])
-            vs.append(self.V[layer, p, o])
+        for j in range(-(-ctx // self.B)):
+            p = table[j]
+            rows = min(self.B, ctx - j * self.B)
+            ks.append(self.K[layer, p, :rows])
+            vs.append(self.V[layer, p, :rows])
         shape = (0, self.H, self.D)
-        k = np.stack(ks) if ks else np.zeros(shape, dtype=self.K.dtype)
-        v = np.stack(vs) if vs else np.zeros(shape, dtype=self.V.dtype)
+        k = np.concatenate(ks) if ks else np.zeros(shape, dtype=self.K.dtype)
+        v = np.concatenate(vs) if vs else np.zeros(shape, dtype=self.V.dtype)
         return k, v
 
     def gather(self, layer: int, table, ctx: int):
