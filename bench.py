@@ -43,18 +43,18 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and decode tokens/s"
-DEFAULT_WORKLOAD = "qwen_2k"
+DEFAULT_WORKLOAD = "pool36"
 
 # Per-launch DRAM traffic of the dominant kernel from an ncu capture, keyed by
-# (workload, kernel): ncu dram__bytes_read.sum + dram__bytes_write.sum of one
+# (workload, block size, kernel): ncu dram__bytes_read.sum + dram__bytes_write.sum of one
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", "decode_mma_kernel"): {"bytes": 331703296 + 3276800, "sha": "7a574767b9923aec"},
-    ("shared_8k", "decode_mma_kernel"): {"bytes": 171004416 + 3211520, "sha": "7a574767b9923aec"},
-    ("gqa70b_32k", "decode_tc_kernel"): {"bytes": 1615941376 + 6079488, "sha": "7a574767b9923aec"},
-    ("qwen_2k_fp8", "decode_mma_kernel"): {"bytes": 169274368 + 3358720, "sha": "7a574767b9923aec"},
-    ("prefill_4k", "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331703296 + 3276800, "sha": "7a574767b9923aec"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 171004416 + 3211520, "sha": "7a574767b9923aec"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615941376 + 6079488, "sha": "7a574767b9923aec"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169274368 + 3358720, "sha": "7a574767b9923aec"},
+    ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
 }
 
 
@@ -87,7 +87,7 @@ def read_peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms with arrival times; the
+    """nvidia-smi clock/throttle samples every 50 ms with arrival times; the
     summary keeps the samples inside the timed window (widened by 0.3 s on
     each side so that a short window still has a sample next to it)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -103,7 +103,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -117,18 +117,14 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self, t_begin: float, t_end: float):
+    def summary(self, t_begin: float, t_end: float):
+        """Samples that arrived inside [t_begin - 0.3 s, t_end + 0.3 s]."""
         if self.proc is None:
             return None
         time.sleep(0.35)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.lines:
+        for t, ln in list(self.lines):
             if not (t_begin - 0.3 <= t <= t_end + 0.3):
                 continue
             parts = [x.strip() for x in ln.split(",")]
@@ -146,6 +142,21 @@ class ClockSampler:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+    def close(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.proc = None
+
+    def stop(self, t_begin: float, t_end: float):
+        out = self.summary(t_begin, t_end)
+        self.close()
+        return out
 
 
 # ------------------------------------------------------------ distributed
@@ -178,7 +189,7 @@ def aggregate(local_bytes: float, local_seconds: float, world: int, device=None)
 
 # -------------------------------------------------------------- workload
 def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device",
-          placement_seed=None):
+          placement_seed=None, n_layers=None):
     """Build the workload's pool on the device.  ``fill="device"`` fills the
     whole pool with seeded N(0,1) values generated on the GPU by torch and
     skips history writes (the history values are whatever the pool holds);
@@ -188,7 +199,7 @@ def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device",
     from paged_kv_cache_65_gb300 import PagedKVCache
     from paged_kv_cache_65_gb300.driver import DeviceRun
 
-    wl = synth.workload(name, **({"block_size": block_size} if name == "pool36" else {}))
+    wl = recipe(name, block_size, n_layers)
     if placement_seed is not None:
         import dataclasses
 
@@ -241,16 +252,76 @@ def unique_kv_bytes(cache, seq_ids, lengths, esize):
 
 
 # ----------------------------------------------------------------- ours
-def bench_ours(args):
+def workload_config(wl, world: int, placement_seed=None) -> dict:
+    """The workload a line measures, from its recipe alone (both arms print
+    the same dict): shapes, pool, the mean context after the first decode
+    step, how L2 is handled and the replica count."""
+    lens = synth.recipe_lengths(wl)
+    ctx = [lens.get(s, 0) + 1 for s in wl.decode_seqs]
+    return {"workload": wl.name, "n_layers": wl.n_layers, "n_seq": len(wl.decode_seqs),
+            "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
+            "D_h": wl.head_dim, "kv_dtype": wl.dtype, "mean_context": round(float(np.mean(ctx)), 1),
+            "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
+            "placement_seed": placement_seed, "parallelism": f"replicas x{world}"}
+
+
+def recipe(name: str, block_size: int = 16, n_layers=None):
+    wl = synth.workload(name, **({"block_size": block_size} if name == "pool36" else {}))
+    if n_layers is not None and n_layers != wl.n_layers:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, n_layers=int(n_layers))
+    return wl
+
+
+def agree_max(x: int, world: int, device=None) -> int:
+    """The largest of the ranks' values (every rank times the same count)."""
+    if world <= 1:
+        return int(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([int(x)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return int(t.item())
+
+
+def read_stream_gbs(dev) -> float | None:
+    """Read-only HBM stream rate on this GPU: a float32 sum over 4 GiB (a
+    reduction reads every byte once and writes nothing), best of 5, CUDA
+    events; a roofline denominator beside the copy peak."""
     import torch
 
-    rank, local, world = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    wl, cache, run = setup(args.workload, args.block_size, dev,
-                           placement_seed=args.placement_seed)
+    try:
+        x = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+    except Exception:
+        return None
+    best = None
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x.sum()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    del x
+    torch.cuda.empty_cache()
+    return round(4.0 * (1 << 30) / (best / 1e3) / 1e9, 1)
+
+
+def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_s=0.0,
+                   n_layers=None):
+    """One decode workload on this rank's GPU: the step timing (``steps``
+    graph replays, or more when ``min_timed_s`` asks for a longer timed
+    region), the split pass's roofline, the host-buffer step (e2e) and the
+    clock record of the timed window.  Returns the measurement as a dict."""
+    import torch
+
     from paged_kv_cache_65_gb300 import _lib
 
+    wl, cache, run = setup(name, block_size, dev, placement_seed=args.placement_seed,
+                           n_layers=n_layers)
     if args.cuda_cores:
         args.kernel = "cuda"
     cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, KERNELS[args.kernel])
@@ -260,11 +331,10 @@ def bench_ours(args):
     n = len(seqs)
     L = wl.n_layers
     stream = torch.cuda.current_stream()
-    n_steps = args.warmup + args.steps
     # host part of the steps first (reservations + tables), then upload; the
     # timed loop cycles over n_plans distinct steps so that contexts grow by
     # at most n_plans tokens however many steps are timed
-    n_plans = min(n_steps, args.plans)
+    n_plans = args.plans if min_timed_s > 0 else min(args.warmup + steps, args.plans)
 
     use_plan = not (args.plain or args.kernel == "cuda") and wl.dtype in ("bf16", "fp8_e4m3") and \
         wl.block_size % 8 == 0
@@ -336,7 +406,7 @@ def bench_ours(args):
                                                  out[layer], ws)
             elif merge:
                 cache.paged_decode_merge(wl.n_q_heads, p["lens"], n, out[layer], ws)
-            cnt += 2
+            cnt += int(split) + int(merge)
         return cnt
 
     for i in range(args.warmup):  # eager: first launches size grids, set attributes
@@ -349,13 +419,14 @@ def bench_ours(args):
         ext_events = None
     graphs, instr_graphs, split_graphs, nosplit_graphs, noattn_graphs = [], [], [], [], []
     nomerge_graphs = []
+    launches_of = []
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(cap):
         for pi in range(n_plans):
             g_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_, stream=cap):
-                per_step_launches = enqueue(dplans[pi])
+                launches_of.append(enqueue(dplans[pi]))
             graphs.append(g_)
             gn = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gn, stream=cap):
@@ -389,17 +460,21 @@ def bench_ours(args):
                 split_graphs.append(gs)
     torch.cuda.current_stream().wait_stream(cap)
     torch.cuda.synchronize()
+    t_w0 = time.perf_counter()
     for i in range(args.warmup):
         flush_l2(i)
         graphs[i % n_plans].replay()
     torch.cuda.synchronize()
+    per_iter_s = (time.perf_counter() - t_w0) / max(1, args.warmup)
+    if min_timed_s > 0:  # a timed region of at least min_timed_s of replays
+        steps = max(steps, int(np.ceil(min_timed_s / max(per_iter_s, 1e-6))))
+    steps = agree_max(steps, world, dev)
+    n_steps = args.warmup + steps
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_steps)]
     split_ms = []
     launches = 0
-    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
-    clocks.start()
     if world > 1:
         import torch.distributed as dist
 
@@ -412,16 +487,16 @@ def bench_ours(args):
         ev[i][0].record(stream)
         graphs[pi].replay()
         ev[i][1].record(stream)
-        launches += per_step_launches
+        launches += launches_of[pi]
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     t_wall = t_wall1 - t_wall0
-    clk = clocks.stop(t_wall0, t_wall1)
+    clk = clocks.summary(t_wall0, t_wall1) if clocks is not None else None
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.warmup, n_steps)]
     # the split pass alone: the same steps replayed from graphs that hold
     # event-record nodes around each split launch (a second timed loop, so
     # that the step timing above keeps the kernels' programmatic edges)
-    n_split = min(args.steps, 200)
+    n_split = min(steps, 200)
     if ext_events is not None:
         split_src = "event-record nodes around each split launch in the step graphs"
         for j in range(n_split):
@@ -448,7 +523,7 @@ def bench_ours(args):
     # events around the replay); per launch = the difference of the medians
     # / L.  The merge is left out of both, so its own speed, after the split
     # pass or alone, does not enter the split's figure.
-    n_inc = min(args.steps, 200)
+    n_inc = min(steps, 200)
     with_ms, without_ms, noattn_ms, nomerge_ms = [], [], [], []
     for j in range(n_inc):
         for gr_, acc in ((graphs, with_ms), (nosplit_graphs, without_ms),
@@ -480,8 +555,8 @@ def bench_ours(args):
     lb = sum(dplans[i % n_plans]["lb"] for i in range(args.warmup, n_steps))
     tot_b, max_s = aggregate(float(ub), dev_s, world, dev)
     value = tot_b / max_s / 1e9
-    ms_per_step = max_s / args.steps * 1e3
-    toks = world * n * args.steps / max_s
+    ms_per_step = max_s / steps * 1e3
+    toks = world * n * steps / max_s
 
     # roofline of the split pass: algorithmic bytes per launch (2 * H_kv * D_h
     # * b bytes per distinct context token row of the layer) / mean duration
@@ -504,67 +579,119 @@ def bench_ours(args):
         kname = "decode_tc_kernel"
     else:
         kname = "decode_mma_kernel"
-    traffic = TRAFFIC.get((args.workload, kname))
+    traffic = TRAFFIC.get((name, wl.block_size, kname))
     traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha() else None
 
     # e2e through the public C-ABI call with pinned host buffers
-    e2e = bench_e2e(args, wl, cache, run, dev, world)
+    e2e = bench_e2e(args, wl, cache, run, dev, world, min(steps, args.plans))
+    res = {
+        "config": workload_config(wl, world, args.placement_seed),
+        "path": {"decode_path": "planned" if use_plan else "plain",
+                 "kernel_option": args.kernel, "kernel": kname, "pdl": not args.no_pdl},
+        "dtype": wl.dtype,
+        "value": round(value, 2), "unit": "GB/s", "steps": steps,
+        "ms_per_step": round(ms_per_step, 4),
+        "step_us_median_p10_p90": [round(1e3 * float(np.percentile(step_ms, p)), 2)
+                                   for p in (50, 10, 90)],
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "pct_of_8tbs_nominal": round(100 * value / 8000.0, 2),
+        "logical_kv_gbs": round(lb / dev_s / 1e9, 2),
+        "decode_tokens_per_s": round(toks, 1),
+        "decode_tokens_per_s_36_layers": round(toks * L / 36.0, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
+                     "kernel": kname,
+                     "peak_source": peak_kind,
+                     "timing": ("device time of the split launches: median of the step "
+                                "graphs without the merge launches minus median of the "
+                                "same graphs without split or merge, per launch (CUDA "
+                                "events around each replay, L2 flushed before each)"),
+                     "alg_bytes_per_launch": int(alg),
+                     "mean_launch_us": round(split_s * 1e6, 2),
+                     "event_node_launch_us": round(split_ev_s * 1e6, 2),
+                     "step_minus_nosplit_us": round(inc_s * 1e6, 2),
+                     "split_and_merge_us": round(attn_s * 1e6, 2),
+                     "split_and_merge_frac": round(alg / attn_s / 1e9 / peak, 4),
+                     "event_node_timing": split_src},
+        "gpu_launches": launches,
+        "graphs": "one CUDA graph per step plan, replayed",
+        "cow_steps": ({"n": len(cow_ms), "step_ms": round(float(np.mean(cow_ms)), 4),
+                       "steady_step_ms": round(float(np.mean(steady_ms)), 4)}
+                      if cow_ms and steady_ms else None),
+        "e2e": e2e,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 4),
+    }
+    del graphs, instr_graphs, split_graphs, nosplit_graphs, noattn_graphs, nomerge_graphs
+    cache.close()
+    return res
 
-    cpu = None
+
+PER_CONFIG = ("shared_8k", "gqa70b_32k", "qwen_2k")
+
+
+def free_device():
+    import gc
+
+    import torch
+
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def bench_ours(args):
+    import torch
+
+    rank, local, world = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    stream_gbs = read_stream_gbs(dev)
+    head = measure_decode(args, args.workload, args.block_size, args.steps, dev, world, clocks,
+                          n_layers=args.layers)
+    per = {}
+    if args.per_config:
+        for w in PER_CONFIG:
+            if w == args.workload:
+                continue
+            free_device()
+            per[w] = measure_decode(args, w, 16, args.steps, dev, world, clocks,
+                                    min_timed_s=args.min_timed_s)
+    clocks.close()
+    free_device()
+    cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
         cpu_par = cpu_baseline_parallel(args.workload, args.cpu_seconds)
+        for w in per:
+            per[w]["cpu_baseline"] = cpu_baseline(w, args.per_config_cpu_seconds)
 
     if rank == 0:
+        peak, peak_kind = read_peaks()
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": wl.dtype, "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
-            "config": {"workload": args.workload, "n_layers": L, "n_seq": n,
-                       "decode_path": "planned" if use_plan else "plain",
-                       "kernel_option": args.kernel, "kernel": kname,
-                       "pdl": not args.no_pdl,
-                       "block_size": wl.block_size, "H_q": wl.n_q_heads, "H_kv": wl.n_kv_heads,
-                       "D_h": wl.head_dim, "mean_context": round(dplans[-1]["ctx"] / n, 1),
-                       "n_blocks": wl.n_blocks, "l2": "flushed between steps (256 MiB write + 256 MiB read)",
-                       "placement_seed": args.placement_seed,
-                       "parallelism": f"replicas x{world}"},
-            "pct_of_hbm_peak": round(100 * value / peak, 2),
-            "pct_of_8tbs_nominal": round(100 * value / 8000.0, 2),
-            "logical_kv_gbs": round(lb / dev_s / 1e9, 2),
-            "decode_tokens_per_s": round(toks, 1),
-            "decode_tokens_per_s_36_layers": round(toks * L / 36.0, 1),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic_v,
-                         "kernel": kname,
-                         "peak_source": peak_kind,
-                         "timing": ("device time of the split launches: median of the step "
-                                    "graphs without the merge launches minus median of the "
-                                    "same graphs without split or merge, per launch (CUDA "
-                                    "events around each replay, L2 flushed before each)"),
-                         "alg_bytes_per_launch": int(alg),
-                         "mean_launch_us": round(split_s * 1e6, 2),
-                         "event_node_launch_us": round(split_ev_s * 1e6, 2),
-                         "step_minus_nosplit_us": round(inc_s * 1e6, 2),
-                         "split_and_merge_us": round(attn_s * 1e6, 2),
-                         "split_and_merge_frac": round(alg / attn_s / 1e9 / peak, 4),
-                         "event_node_timing": split_src},
-            "gpu_launches": launches * world,
-            "graphs": "one CUDA graph per step plan, replayed",
-            "step_us_median_p10_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2)
-                                       for q in (50, 10, 90)],
-            "cow_steps": ({"n": len(cow_ms), "pairs": int(max(d["npairs"] for d in dplans)),
-                           "median_us": round(float(np.median(cow_ms)) * 1e3, 2),
-                           "steady_median_us": round(float(np.median(steady_ms)) * 1e3, 2)}
-                          if cow_ms and steady_ms else None),
-            "e2e": e2e,
-            "clocks": clk,
-            "wall_s_timed": round(t_wall, 4),
+            "dtype": head["dtype"], "data": "synthetic (seeded N(0,1) K/V/q; torch device generator)",
+            "config": head["config"],
         }
+        line.update({k: v for k, v in head.items() if k not in line and k != "steps"})
+        line["peaks"] = {"measured_copy_gbs": peak, "measured_copy_source": peak_kind,
+                         "read_stream_gbs": stream_gbs,
+                         "read_stream_how": "float32 sum over 4 GiB on this GPU, best of 5",
+                         "nominal_gbs": 8000.0}
+        for res in [line] + list(per.values()):
+            rf = res["roofline"]
+            rf["frac_of_nominal"] = round(rf["achieved"] / 8000.0, 4)
+            if stream_gbs:
+                rf["frac_of_read_stream"] = round(rf["achieved"] / stream_gbs, 4)
         if cpu is not None:
             line["cpu_baseline"] = cpu
             line["cpu_baseline_parallel"] = cpu_par
+        if per:
+            line["per_config"] = per
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -573,14 +700,14 @@ def bench_ours(args):
         dist.destroy_process_group()
 
 
-def bench_e2e(args, wl, cache, run, dev, world):
+def bench_e2e(args, wl, cache, run, dev, world, steps):
     import torch
 
     seqs = wl.decode_seqs
     n = len(seqs)
     L = wl.n_layers
     # each e2e step advances the host state by one token per sequence
-    steps = max(1, min(args.steps, args.plans))
+    steps = max(1, steps)
     max_blocks = run.max_blocks(seqs) + (steps + args.warmup) // wl.block_size + 2
     staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
                           dtype=torch.uint8, device=dev)
@@ -744,7 +871,7 @@ def bench_prefill(args):
     attn_s = float(np.mean(attn_ms)) / 1e3
     peak, peak_kind = read_tensor_peak()
     achieved = flops / attn_s / 1e12
-    traffic = TRAFFIC.get((args.workload, "prefill_tc_kernel"))
+    traffic = TRAFFIC.get((args.workload, wl.block_size, "prefill_tc_kernel"))
     traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha("prefill") else None
     e2e = bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
                             starts, max_chunk, n_tok, flops, world)
@@ -854,12 +981,35 @@ def _lib_mod():
 
 
 # ------------------------------------------------------------- CPU oracle
+# Workloads whose whole oracle pool is too large (36 layers of 167 GB) or too
+# slow to build for a CPU leg of seconds: the leg runs on some of their
+# sequences (with the prefixes they share) and, for pool36, on one layer.
+CPU_SAMPLE = {"pool36": (list(range(0, 128, 16)), 1), "gqa70b_32k": (list(range(8)), None)}
+
+
+def cpu_recipe(workload: str):
+    wl = synth.workload(workload)
+    if workload in CPU_SAMPLE:
+        seqs, n_layers = CPU_SAMPLE[workload]
+        wl = synth.restrict(wl, seqs, n_layers)
+    return wl
+
+
+def cpu_subset_note(workload: str) -> str:
+    if workload not in CPU_SAMPLE:
+        return ""
+    full = synth.workload(workload)
+    seqs, n_layers = CPU_SAMPLE[workload]
+    return (f" (sequences {seqs} of the batch's {len(full.decode_seqs)}, with the prefixes "
+            f"they share{', one layer' if n_layers else ''})")
+
+
 def oracle_sample(workload: str):
     """Build the oracle's pool for the workload and make one decode step's
     host reservation and writes (setup, untimed)."""
     from oracle.runner import OracleRun
 
-    wl = synth.workload(workload)
+    wl = cpu_recipe(workload)
     orc = OracleRun(wl)
     slots, cows = orc.reserve_step()
     q = orc.write_step(0, slots, cows)
@@ -917,8 +1067,8 @@ def cpu_leg(workload: str, seconds: float, start: int = 0):
     nbytes, dt, done = oracle_attend(wl, orc, q, seconds, start=start)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{workload}: {done} single-sequence layer-0 decode attentions, cycling "
-                      f"over the batch's {len(wl.decode_seqs)} sequences (paged gather + fp64 "
-                      f"softmax, one thread), {dt:.1f} s",
+                      f"over {len(wl.decode_seqs)} sequences{cpu_subset_note(workload)} (paged "
+                      f"gather + fp64 softmax, one thread), {dt:.1f} s",
             "seconds": round(dt, 3), "sequences": done, "bytes": int(nbytes)}
 
 
@@ -945,7 +1095,7 @@ def cpu_baseline_parallel(workload: str, seconds: float):
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    wl = synth.workload(workload)
+    wl = cpu_recipe(workload)
     n = len(wl.chunks) if isinstance(wl, synth.PrefillWorkload) else len(wl.decode_seqs)
     P = max(1, os.cpu_count() or 1)
     procs = [subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-leg", workload,
@@ -971,8 +1121,8 @@ def cpu_baseline_parallel(workload: str, seconds: float):
         done = sum(x["sequences"] for x in legs)
         what = f"{done} single-sequence layer-0 decode attentions"
     return {"value": value, "unit": unit, "cores": P, "kind": "oracle",
-            "sample": f"{workload}: {P} single-threaded oracle processes at once, "
-                      f"{what} in all, {dt:.1f} s", "seconds": round(dt, 3)}
+            "sample": f"{workload}{cpu_subset_note(workload)}: {P} single-threaded oracle "
+                      f"processes at once, {what} in all, {dt:.1f} s", "seconds": round(dt, 3)}
 
 
 def bench_reference(args):
@@ -992,12 +1142,16 @@ def bench_reference(args):
             nbytes.append(b)
     value = round(sum(nbytes) / sum(secs) / 1e9, 4)
     sample = (f"{args.workload}: per step, layer-0 decode attention of 2 of "
-              f"{len(wl.decode_seqs)} sequences (paged gather + fp64 softmax, one thread)")
+              f"{len(wl.decode_seqs)} sequences{cpu_subset_note(args.workload)} (paged gather "
+              f"+ fp64 softmax, one thread)")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = workload_config(recipe(args.workload, args.block_size, args.layers), world,
+                             args.placement_seed)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
-            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(secs)), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": args.workload},
+            "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -1129,6 +1283,16 @@ def main():
                          "schedule) or in the natural grid order")
     ap.add_argument("--prefix-cache", action="store_true",
                     help="host prefix-cache hit of a 4096-token prompt instead of a GPU step")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (pool36: a one-layer pool for "
+                         "ncu captures of the same per-layer launch)")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=None,
+                    help="also measure " + ", ".join(PER_CONFIG) + " (default with the "
+                         "default workload)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false")
+    ap.add_argument("--min-timed-s", type=float, default=0.5,
+                    help="per-config workloads: replay at least this long in the timed loop")
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=8.0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-leg", default=None)
     ap.add_argument("--cpu-start", type=int, default=0)
@@ -1141,6 +1305,8 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
+    if args.per_config is None:
+        args.per_config = args.workload == DEFAULT_WORKLOAD and args.layers is None
     if args.prefix_cache:
         bench_prefix(args)
         return

@@ -23,6 +23,8 @@ from .workloads import (  # noqa: F401
     storage_values,
     storage_dtype,
     permutation,
+    recipe_lengths,
+    restrict,
     workload,
     torch_seed,
 )

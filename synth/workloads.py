@@ -306,3 +306,37 @@ WORKLOADS = {
 
 def workload(name: str, **kw) -> Workload:
     return WORKLOADS[name](**kw)
+
+
+def recipe_lengths(wl: Workload) -> dict:
+    """Token count of every live sequence after the build operations (an
+    append adds its tokens, a fork copies the parent's count, a release
+    drops the sequence).  Counting only: no block arithmetic."""
+    n: dict[int, int] = {}
+    for op in wl.build_ops:
+        if op[0] == "append":
+            n[op[1]] = n.get(op[1], 0) + op[2]
+        elif op[0] == "fork":
+            n[op[2]] = n[op[1]]
+        elif op[0] == "release":
+            n.pop(op[1], None)
+    return n
+
+
+def restrict(wl: Workload, seqs, n_layers: int | None = None) -> Workload:
+    """The same recipe cut down to the decode sequences ``seqs`` (and the
+    parents they fork from), optionally with fewer layers: a bounded sample
+    of a large workload for CPU timing.  The values drawn differ (the value
+    arrays have another shape); lengths, sharing and placement order do not."""
+    import dataclasses
+
+    keep = set(int(s) for s in seqs)
+    # parents of kept sequences are kept too (their appends build the prefix)
+    for op in reversed(wl.build_ops):
+        if op[0] == "fork" and op[2] in keep:
+            keep.add(op[1])
+    ops = [op for op in wl.build_ops
+           if (op[0] == "fork" and op[2] in keep) or (op[0] != "fork" and op[1] in keep)]
+    return dataclasses.replace(wl, build_ops=ops,
+                               decode_seqs=[s for s in wl.decode_seqs if s in keep],
+                               n_layers=wl.n_layers if n_layers is None else n_layers)

@@ -119,7 +119,10 @@ def test_fp8_unused_slots_holding_nan_codes_do_not_leak():
     assert max_err(got, outs[0]) <= TOL
 
 
-def test_fp8_qwen_2k_sampled():
+def test_fp8_qwen_2k_full():
+    # every output of all 37 sequences, per sequence and through the plan
+    from paged_kv_cache_65_gb300.driver import to_device
+
     wl = synth.workload("qwen_2k_fp8")
     orc = OracleRun(wl)
     cache, run = make(wl)
@@ -128,13 +131,15 @@ def test_fp8_qwen_2k_sampled():
     _, k, v = wl.step_values(0)
     sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
     assert list(sg) == so
-    sample = [0, 5, 18, 36]
-    ref = orc.attend(0, qh, seq_index=sample)
-    got = og.cpu().numpy()[0]
-    for i in sample:
-        assert max_err(got[i], ref[i]) <= TOL
+    ref = orc.attend(0, qh)
+    assert max_err(og.cpu().numpy()[0], ref) <= TOL
+    d_table, _, mb = run.tables(wl.decode_seqs)
+    h_plan, d_plan, ws = run.plan(wl.decode_seqs, mb)
+    got = run.attend_planned(0, to_device(qh, "bf16", "cuda"), d_table, mb, h_plan, d_plan, ws)
+    assert max_err(got.cpu().numpy(), ref) <= TOL
     # the pool's written rows are the oracle's codes
     assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
+    assert nan_code_equal(cache.v.cpu().numpy(), orc.st.V)
     assert cache.kv_pool_device_status() == 0
 
 

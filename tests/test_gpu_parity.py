@@ -95,48 +95,70 @@ def test_qwen_2k_full_parity():
     check_status(cache)
 
 
-def test_shared_8k_sampled_parity():
+def attend_four_ways(cache, run, wl, qh):
+    """The same step's attention per sequence and through the sharing-aware
+    plan, each on the warp-level MMA pass (2) and on tcgen05 (3); the
+    bench's launch configuration is the planned pass."""
+    from paged_kv_cache_65_gb300 import _lib
+
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
+    outs = {}
+    for path in TENSOR_PATHS:
+        cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, path)
+        outs[("plain", path)] = run.attend(0, qd, d_table, mb, d_lens,
+                                           len(wl.decode_seqs)).cpu().numpy()
+        h_plan, d_plan, ws_bytes = run.plan(wl.decode_seqs, mb)
+        outs[("planned", path)] = run.attend_planned(0, qd, d_table, mb, h_plan, d_plan,
+                                                     ws_bytes).cpu().numpy()
+    return outs
+
+
+def test_shared_8k_full_parity():
+    # all 16 sequences, every output, four ways
     wl = synth.workload("shared_8k")
     orc = OracleRun(wl)
     cache, run = make(wl)
     so, co = orc.reserve_step()
     qh = orc.write_step(0, so, co)
     _, k, v = wl.step_values(0)
-    sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+    sg, pg = run.reserve(wl.decode_seqs)
     assert list(sg) == so and len(pg) == 0
-    sample = [0, 7, 15]
-    ref = orc.attend(0, qh, seq_index=sample)
-    got = og.cpu().numpy()[0]
-    for i in sample:
-        assert max_err(got[i], ref[i]) <= TOL["bf16"]
+    run.write(sg, pg, k, v)
+    ref = orc.attend(0, qh)
+    for key, got in attend_four_ways(cache, run, wl, qh).items():
+        assert max_err(got, ref) <= TOL["bf16"], key
     # the 384 shared prefix blocks are read by all 16 sequences: bit-identical pools
     assert np.array_equal(host_bits(cache.k), orc.st.K)
+    assert np.array_equal(host_bits(cache.v), orc.st.V)
     check_status(cache)
 
 
-def test_gqa70b_32k_cow_and_sampled_parity():
+def test_gqa70b_32k_cow_and_full_parity():
+    # all 48 branches on both steps (the first copies 48 shared tails), four ways
     wl = synth.workload("gqa70b_32k")
     orc = OracleRun(wl)
     cache, run = make(wl)
-    sample = [0, 5, 26, 47]
     for step in range(2):
         so, co = orc.reserve_step()
         qh = orc.write_step(step, so, co)
         _, k, v = wl.step_values(step)
-        sg, pg, og = run.step(wl.decode_seqs, qh, k, v)
+        sg, pg = run.reserve(wl.decode_seqs)
         assert list(sg) == so
         assert [tuple(p) for p in pg] == co
         assert len(co) == (48 if step == 0 else 0)
+        run.write(sg, pg, k, v)
         if step == 0:
             kd = host_bits(cache.k)
             for src, dst in co:
                 assert np.array_equal(kd[:, dst], orc.st.K[:, dst])
                 # the copy kept the shared tokens and the new token went to the copy
                 assert np.array_equal(kd[:, dst, :3], kd[:, src, :3])
-        ref = orc.attend(0, qh, seq_index=sample)
-        got = og.cpu().numpy()[0]
-        for i in sample:
-            assert max_err(got[i], ref[i]) <= TOL["bf16"]
+            assert np.array_equal(kd, orc.st.K)
+            assert np.array_equal(host_bits(cache.v), orc.st.V)
+        ref = orc.attend(0, qh)
+        for key, got in attend_four_ways(cache, run, wl, qh).items():
+            assert max_err(got, ref) <= TOL["bf16"], (step, key)
     check_status(cache)
 
 
@@ -358,47 +380,6 @@ def test_tensor_core_and_cuda_core_paths_agree(name):
 
 # ---------------------------------------------------------------- planned
 # The sharing-aware pass: shared prefix blocks are read once for all sharers.
-
-
-@pytest.mark.parametrize("path", TENSOR_PATHS)
-def test_planned_shared_8k_against_oracle_and_plain_pass(path):
-    wl = synth.workload("shared_8k")
-    orc = OracleRun(wl)
-    cache, run = make(wl, path=path)
-    so, co = orc.reserve_step()
-    qh = orc.write_step(0, so, co)
-    _, k, v = wl.step_values(0)
-    run.write(*run.reserve(wl.decode_seqs), k, v)
-    d_table, d_lens, mb = run.tables(wl.decode_seqs)
-    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
-    h_plan, d_plan, ws_bytes = run.plan(wl.decode_seqs, mb)
-    got = run.attend_planned(0, qd, d_table, mb, h_plan, d_plan, ws_bytes).cpu().numpy()
-    plain = run.attend(0, qd, d_table, mb, d_lens, len(wl.decode_seqs)).cpu().numpy()
-    assert float(np.max(np.abs(got - plain))) <= TOL["bf16"]
-    sample = [0, 7, 8, 15]
-    ref = orc.attend(0, qh, seq_index=sample)
-    for i in sample:
-        assert max_err(got[i], ref[i]) <= TOL["bf16"]
-    check_status(cache)
-
-
-@pytest.mark.parametrize("path", TENSOR_PATHS)
-def test_planned_gqa70b_32k_against_oracle(path):
-    wl = synth.workload("gqa70b_32k")
-    orc = OracleRun(wl)
-    cache, run = make(wl, path=path)
-    sample = [0, 3, 21, 46]
-    for step in range(2):
-        so, co = orc.reserve_step()
-        qh = orc.write_step(step, so, co)
-        _, k, v = wl.step_values(step)
-        sg, pg, og = run.step(wl.decode_seqs, qh, k, v, planned=True)
-        assert list(sg) == so and [tuple(p) for p in pg] == co
-        ref = orc.attend(0, qh, seq_index=sample)
-        got = og.cpu().numpy()[0]
-        for i in sample:
-            assert max_err(got[i], ref[i]) <= TOL["bf16"]
-    check_status(cache)
 
 
 @pytest.mark.parametrize("path", TENSOR_PATHS)
