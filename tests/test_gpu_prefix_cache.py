@@ -160,12 +160,17 @@ def test_prefix_hits_evictions_and_decode_on_the_device():
     pp.append(3, prompt_d)
     assert pp.orc.cache_stats()[3] < cached_before + len(prompt_d) // B  # some were evicted
     pp.same_pools()
-    # E asks for A's prompt again: the surviving chain is shorter than 288
+    # D attends over blocks that held other requests' tokens before the eviction
+    pp.decode([3], [int(rng.integers(0, 151936))])
+    pp.same_pools()
+    pp.release(3)
+    # E asks for A's prompt again: the surviving chain is shorter than 288, and
+    # E's tail takes blocks evicted from D's chain
     prompt_e = prompt_a + [int(x) for x in rng.integers(0, 151936, 7)]
     m = pp.match(4, prompt_e)
     assert m % B == 0 and m < 288
     pp.append(4, prompt_e[m:])
     pp.same_pools()
     for _ in range(2):
-        pp.decode([3, 4], [int(x) for x in rng.integers(0, 151936, 2)])
+        pp.decode([4], [int(rng.integers(0, 151936))])
     pp.same_pools()
