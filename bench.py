@@ -54,6 +54,8 @@ TRAFFIC = {
     ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 171004416 + 3211520, "sha": "7a574767b9923aec"},
     ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615941376 + 6079488, "sha": "7a574767b9923aec"},
     ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169274368 + 3358720, "sha": "7a574767b9923aec"},
+    # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3456562432 + 5879040, "sha": "7a574767b9923aec"},
     ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
 }
 
@@ -1262,7 +1264,7 @@ def bench_prefix(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--plans", type=int, default=32,
                     help="distinct decode steps the timed loop cycles over")
     ap.add_argument("--warmup", type=int, default=5)

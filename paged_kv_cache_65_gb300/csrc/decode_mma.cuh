@@ -456,43 +456,58 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int cstride = PLAN ? a.c_max : G;  // columns per workspace slot
   bool alive = true;
   int stage = 0;
-  Piece p;
-
-  while (next_piece(p)) {
-    const int NT = p.ncols <= 8 ? 1 : (p.ncols <= 16 ? 2 : 4);  // n-tiles of the piece
-    const int WT = kConsumerWarps / NT;                           // warps per n-tile
-    const int wn = warp % NT, wt = warp / NT;
-    // Q^T fragments of column wn*8 + g: dims ks*16 + 2t (+1) and + 8
-    uint32_t qf[C::KS][2];
-    {
-      const int col = wn * 8 + g;
-      const bool colv = col < p.ncols;
-      int seqm = p.rep, gi = col;
-      if constexpr (PLAN) {
-        const int mi = col / G;
-        gi = col - mi * G;
-        seqm = colv ? a.members[p.mem + mi] : 0;
-      }
-      const uint32_t* qw = reinterpret_cast<const uint32_t*>(
-          reinterpret_cast<const unsigned char*>(a.q) +
-          ((long long)seqm * a.n_q_heads + (long long)p.head * G + (colv ? gi : 0)) * D * 2);
+  // Q^T fragments of this warp's column of a piece (column wn*8 + g: dims
+  // ks*16 + 2t (+1) and + 8; F8: the dimensions of the permuted K fragments,
+  // 16 ks + 4t .. + 3), as raw bf16 pairs.  They are loaded one piece ahead,
+  // so that a piece's first MMA does not wait for its member list and q rows
+  // to arrive from memory.
+  auto load_q = [&](const Piece& pc, uint32_t (&qr)[C::KS][2]) {
+    const int NTc = pc.ncols <= 8 ? 1 : (pc.ncols <= 16 ? 2 : 4);
+    const int col = (warp % NTc) * 8 + g;
+    const bool colv = col < pc.ncols;
+    int seqm = pc.rep, gi = col;
+    if constexpr (PLAN) {
+      const int mi = col / G;
+      gi = col - mi * G;
+      seqm = colv ? a.members[pc.mem + mi] : 0;
+    }
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(
+        reinterpret_cast<const unsigned char*>(a.q) +
+        ((long long)seqm * a.n_q_heads + (long long)pc.head * G + (colv ? gi : 0)) * D * 2);
 #pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        if constexpr (F8) {
-          // the dimensions of the permuted K fragments, bf16 pairs -> fp16
-          // pairs (exact in fp16's range)
-          qf[ks][0] = colv ? qw[(ks * 16 + 4 * t) / 2] : 0u;
-          qf[ks][1] = colv ? qw[(ks * 16 + 4 * t + 2) / 2] : 0u;
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            qf[ks][i] = pack_f16(__uint_as_float(qf[ks][i] << 16),
-                                 __uint_as_float(qf[ks][i] & 0xffff0000u));
-        } else {
-          qf[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
-          qf[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
-        }
+    for (int ks = 0; ks < C::KS; ++ks) {
+      if constexpr (F8) {
+        qr[ks][0] = colv ? qw[(ks * 16 + 4 * t) / 2] : 0u;
+        qr[ks][1] = colv ? qw[(ks * 16 + 4 * t + 2) / 2] : 0u;
+      } else {
+        qr[ks][0] = colv ? qw[(ks * 16 + 2 * t) / 2] : 0u;
+        qr[ks][1] = colv ? qw[(ks * 16 + 2 * t + 8) / 2] : 0u;
       }
     }
+  };
+  Piece p, pn;
+  uint32_t qn[C::KS][2];
+  bool have = next_piece(p), have_next = false;
+  if (have) load_q(p, qn);
+  for (; have; p = pn, have = have_next) {
+    const int NT = p.ncols <= 8 ? 1 : (p.ncols <= 16 ? 2 : 4);  // n-tiles of the piece
+    const int WT = kConsumerWarps / NT;                           // warps per n-tile
+    const int wt = warp / NT;
+    uint32_t qf[C::KS][2];
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks) {
+      qf[ks][0] = qn[ks][0];
+      qf[ks][1] = qn[ks][1];
+      if constexpr (F8) {
+        // bf16 pairs -> fp16 pairs (exact in fp16's range)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          qf[ks][i] = pack_f16(__uint_as_float(qf[ks][i] << 16),
+                               __uint_as_float(qf[ks][i] & 0xffff0000u));
+      }
+    }
+    have_next = next_piece(pn);
+    if (have_next) load_q(pn, qn);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[C::KS][4];
 #pragma unroll
