@@ -151,6 +151,9 @@ __device__ __forceinline__ void fp8_tile_to_f16(uint32_t st, uint32_t dst, int r
   }
 }
 
+// Piece descriptors the producer can publish ahead of the consumers.
+constexpr int kPieceRing = 4;
+
 template <int D, int G, bool F8 = false>
 constexpr int decode_mma_smem_bytes() {
   using C = MmaCfg<D, G, F8>;
@@ -160,6 +163,7 @@ constexpr int decode_mma_smem_bytes() {
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
          + kTableCache * 4                  // producer table cache
+         + kPieceRing * (32 + 16)           // piece descriptors and their mbarriers
          + 64 + 128 + 1024;                 // walk state, start record, 1 KiB alignment
 }
 
@@ -246,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   long long* walk = reinterpret_cast<long long*>(empty + NST);
   int32_t* tcache = reinterpret_cast<int32_t*>(walk + 4);
   PlanStart* rec_s = reinterpret_cast<PlanStart*>(tcache + kTableCache);
+  Piece* ring = reinterpret_cast<Piece*>(rec_s + 1);
+  uint64_t* dfull = reinterpret_cast<uint64_t*>(ring + kPieceRing);
+  uint64_t* dempty = dfull + kPieceRing;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -265,6 +272,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kPieceRing; ++i) {
+      mbar_init(&dfull[i], 1);
+      mbar_init(&dempty[i], kConsumerWarps);
     }
     fence_barrier_init();
   }
@@ -366,17 +377,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       return true;
     }
   };
-  // the first piece of this CTA, without advancing the walk
-  auto peek_first = [&](Piece& p0) -> bool {
-    const PieceWalker pw_s = pw;
-    const PlanWalker plw_s = plw;
-    const bool rf = rec_first;
-    const bool ok = next_piece(p0);
-    pw = pw_s;
-    plw = plw_s;
-    rec_first = rf;
-    return ok;
-  };
   auto wait_previous_grid = [&]() {
     griddep_wait();
     griddep_launch_dependents();
@@ -396,13 +396,47 @@ __global__ void __launch_bounds__(kThreads, 2)
     int stage = 0;
     TableCache tc;
     tc.ent = tcache;
-    if (!use_rec) {
-      Piece p0;
-      if (peek_first(p0)) tc.ensure(a.table, a.max_blocks, p0.rep, p0.b0, p0.b0, lane);
-    }
+    // The producer alone walks the work list: each piece goes to the
+    // consumers as a descriptor in shared memory, published one piece ahead
+    // of its copies, so that no consumer reads the plan or waits on it at a
+    // piece boundary.  A descriptor with rep = -1 ends the list.
+    int npub = 0;
+    auto publish = [&](const Piece& x, bool valid) {
+      const int di = npub % kPieceRing;
+      if (npub >= kPieceRing && alive) {
+        if (!mbar_wait_bounded(&dempty[di], ((npub / kPieceRing) - 1) & 1, kWaitLimitNs)) {
+          alive = false;
+          if (lane == 0) record_status(a.status, 8);
+        }
+      }
+      if (lane == 0) {
+        Piece y = x;
+        if (!valid) y.rep = -1;
+        ring[di] = y;
+        mbar_arrive(&dfull[di]);
+      }
+      __syncwarp();
+      ++npub;
+    };
+    Piece p, pn;
+    bool have = next_piece(p);
+    if (have && !use_rec) tc.ensure(a.table, a.max_blocks, p.rep, p.b0, p.b0, lane);
     wait_previous_grid();
-    Piece p;
-    while (next_piece(p)) {
+    publish(p, have);
+    while (have) {
+      const bool have_next = next_piece(pn);
+      publish(pn, have_next);
+      // the next piece's first table entries, loaded while this piece's
+      // copies are issued and installed after them
+      int32_t tnext[kTableCache / 32];
+      if (have_next) {
+        const int32_t* row = a.table + (long long)pn.rep * a.max_blocks;
+#pragma unroll
+        for (int i = 0; i < kTableCache / 32; ++i) {
+          const int j = pn.b0 + i * 32 + lane;
+          tnext[i] = j < a.max_blocks ? row[j] : 0;
+        }
+      }
       for (int tok0 = p.b0 * B; tok0 < p.tok_end; tok0 += STG) {
         const int slot = stage % NST;
         if (stage >= NST && alive) {
@@ -440,6 +474,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ++stage;
       }
+      if (have_next) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kTableCache / 32; ++i) tc.ent[i * 32 + lane] = tnext[i];
+        tc.seq = pn.rep;
+        tc.base = pn.b0;
+        __syncwarp();
+      }
+      p = pn;
+      have = have_next;
     }
     const int first = stage > NST ? stage - NST : 0;
     for (int k = first; k < stage; ++k)
@@ -485,9 +529,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   };
+  // the k-th piece descriptor the producer published (false: the list ended,
+  // or the wait gave up)
+  int nread = 0;
+  auto read_piece = [&](Piece& x) -> bool {
+    const int di = nread % kPieceRing;
+    if (alive && !mbar_wait_bounded(&dfull[di], (nread / kPieceRing) & 1, kWaitLimitNs)) {
+      alive = false;
+      if (lane == 0) record_status(a.status, 8);
+    }
+    alive = __all_sync(0xffffffffu, alive);
+    if (!alive) return false;
+    x = ring[di];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&dempty[di]);
+    ++nread;
+    return x.rep >= 0;
+  };
   Piece p, pn;
   uint32_t qn[C::KS][2];
-  bool have = next_piece(p), have_next = false;
+  bool have = read_piece(p), have_next = false;
   if (have) load_q(p, qn);
   for (; have; p = pn, have = have_next) {
     const int NT = p.ncols <= 8 ? 1 : (p.ncols <= 16 ? 2 : 4);  // n-tiles of the piece
@@ -506,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                __uint_as_float(qf[ks][i] & 0xffff0000u));
       }
     }
-    have_next = next_piece(pn);
+    have_next = read_piece(pn);
     if (have_next) load_q(pn, qn);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[C::KS][4];

@@ -295,7 +295,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   }
   int64_t W = 0;
   for (PlanSeg& s : segs) {
-    s.w = plan_block_weight(s.ncols, kernel);
+    s.w = plan_seg_weight(s.ncols, kernel, s.b1 - s.b0);
     s.wpre = W;
     W += static_cast<int64_t>(s.b1 - s.b0) * s.w;
   }

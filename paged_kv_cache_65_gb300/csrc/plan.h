@@ -84,11 +84,26 @@ constexpr int kPlanKernelTc = 3;   // tcgen05, TMEM accumulators
 
 // Work units per block.  The split pass balances units.  On the warp-level
 // MMA kernel a block costs more the more 8-column n-tiles it carries (1, 2,
-// 3-4 tiles: 3, 4, 5 units), so blocks of wide shared segments are spread
+// 3-4 tiles: 3, 4, 5 parts), so blocks of wide shared segments are spread
 // over more CTAs; on the tcgen05 kernel the tensor work is small against the
 // block's bytes, and only the 32-column softmax adds to a block's time
-// (4, 4, 5 units).
+// (4, 4, 5 parts).  A part is 8 units.
+constexpr int kPlanUnitsPerPart = 8;
 constexpr int plan_block_weight(int ncols, int kernel) {
-  return kernel == kPlanKernelTc ? (ncols <= 16 ? 4 : 5)
-                                 : (ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5));
+  return kPlanUnitsPerPart * (kernel == kPlanKernelTc ? (ncols <= 16 ? 4 : 5)
+                                                      : (ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5)));
+}
+// Fixed cost of a piece (its start and its partials), in units: about one
+// pipeline stage of narrow blocks (64 tokens on the warp-level pass, 128 on
+// tcgen05).  Each segment carries it spread over its blocks, so a CTA whose
+// range holds many short segments (the one-block private tails of forked
+// branches) is given fewer blocks.
+constexpr int plan_piece_units(int kernel) {
+  return kernel == kPlanKernelTc ? 8 * plan_block_weight(8, kernel)
+                                 : 4 * plan_block_weight(8, kernel);
+}
+// Units per block of a segment of n_blocks blocks.
+constexpr int plan_seg_weight(int ncols, int kernel, int n_blocks) {
+  return plan_block_weight(ncols, kernel) +
+         (n_blocks > 0 ? (plan_piece_units(kernel) + n_blocks - 1) / n_blocks : 0);
 }

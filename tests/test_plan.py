@@ -39,12 +39,16 @@ def check_plan(bm, plan, seqs, G, min_tokens):
     units = [int(s["b1"] - s["b0"]) * int(s["w"]) for s in segs]
     assert plan["W"] == sum(units)
     assert list(segs["wpre"]) == list(np.cumsum([0] + units)[:-1])
-    if plan["kernel"] == 3:  # tcgen05
-        assert all(s["w"] == (4 if s["ncols"] <= 16 else 5) for s in segs)
-    else:
-        assert plan["kernel"] == 2
-        assert all(s["w"] == (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5)
-                   for s in segs)
+    # units per block: 8 per part of the block's cost, plus the piece's fixed
+    # cost (one stage of narrow blocks) spread over the segment's blocks
+    for s in segs:
+        n = int(s["b1"] - s["b0"])
+        if plan["kernel"] == 3:  # tcgen05
+            base, piece = 8 * (4 if s["ncols"] <= 16 else 5), 8 * 32
+        else:
+            assert plan["kernel"] == 2
+            base, piece = 8 * (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5), 4 * 24
+        assert s["w"] == base + (-(-piece // n) if n > 0 else 0)
     for si, s in enumerate(segs):
         assert s["ncols"] % G == 0 and 0 < s["ncols"] <= 32
         members = mem[s["mem"]:s["mem"] + s["ncols"] // G]
