@@ -71,7 +71,8 @@ enum {
   KV_DEV_BAD_BLOCK_ID = 1, /* block_table entry outside [0, N_blocks)  */
   KV_DEV_BAD_SLOT = 2,     /* slot_mapping entry >= N_blocks * B       */
   KV_DEV_BAD_COW_PAIR = 4, /* copy pair id outside [0, N_blocks)       */
-  KV_DEV_WAIT_TIMEOUT = 8, /* a pipeline wait gave up (never expected) */
+  KV_DEV_WAIT_TIMEOUT = 8, /* a pipeline wait gave up (never expected;
+                              kv_device_wait_selftest sets it on purpose) */
   KV_DEV_BAD_CONTEXT = 16, /* context_lens entry < 0 or > max_blocks * B */
   KV_DEV_SMEM_ALIGN = 32   /* shared staging not 1 KiB aligned: pass skipped */
 };
@@ -143,6 +144,15 @@ kvStatus kv_pool_set_fp8_scales(kvPool* pool, float k_scale, float v_scale);
 /* Synchronise `stream`, copy the device status word to *out_bits and clear
  * it.  Returns KV_ERR_DEVICE_CHECK when any bit was set. */
 kvStatus kv_pool_device_status(kvPool* pool, void* stream, int* out_bits);
+
+/* Health check of the device's bounded waits (no counterpart on the pages):
+ * enqueues on `stream` a one-thread kernel that waits on a barrier nothing
+ * completes, with the helper every pipeline wait of the library uses; after
+ * limit_us microseconds (1 .. 1,000,000) the wait gives up and
+ * KV_DEV_WAIT_TIMEOUT is set in the pool's status word, read with
+ * kv_pool_device_status.  No copy or other work is in flight while it waits,
+ * and the device stays usable.  Returns launch errors only. */
+kvStatus kv_device_wait_selftest(kvPool* pool, int limit_us, void* stream);
 
 /* ---------------------------------------------------------- block level --
  * Caller-held handles on blocks, sharing the pool's free list and counts

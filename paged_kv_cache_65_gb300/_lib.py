@@ -34,6 +34,13 @@ KV_OPT_PLAN_GRID = 3
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
 KV_DTYPE_FP8_E4M3 = 2
+# bits of the device status word
+KV_DEV_BAD_BLOCK_ID = 1
+KV_DEV_BAD_SLOT = 2
+KV_DEV_BAD_COW_PAIR = 4
+KV_DEV_WAIT_TIMEOUT = 8
+KV_DEV_BAD_CONTEXT = 16
+KV_DEV_SMEM_ALIGN = 32
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -60,6 +67,7 @@ SIGNATURES = [
     ("kv_pool_set_option", C.c_int, [_vp, C.c_int, C.c_int]),
     ("kv_pool_set_fp8_scales", C.c_int, [_vp, C.c_float, C.c_float]),
     ("kv_pool_device_status", C.c_int, [_vp, _vp, _ip]),
+    ("kv_device_wait_selftest", C.c_int, [_vp, C.c_int, _vp]),
     ("block_alloc", C.c_int, [_vp, C.c_int, _i32p]),
     ("block_free", C.c_int, [_vp, _i32p, C.c_int]),
     ("block_fork", C.c_int, [_vp, _i32p, C.c_int]),

@@ -200,6 +200,10 @@ class PagedKVCache:
             check(st, "kv_pool_device_status")
         return bits.value
 
+    def kv_device_wait_selftest(self, limit_us, stream=None):
+        check(lib.kv_device_wait_selftest(self.handle, int(limit_us), _stream(stream)),
+              "kv_device_wait_selftest")
+
     def cow_copy(self, d_pairs, n_pairs, stream=None):
         check(lib.cow_copy(self.handle, vp(d_pairs), int(n_pairs), _stream(stream)), "cow_copy")
 

@@ -237,6 +237,19 @@ __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, ui
   }
 }
 
+// Self-test of the bounded pipeline waits: one thread waits on an mbarrier
+// that nothing completes, with the same helper every pipeline wait uses; the
+// wait gives up after limit_ns and the status word gets KV_DEV_WAIT_TIMEOUT.
+// Nothing else is in flight, so the CTA then just exits.
+__global__ void wait_selftest_kernel(int32_t* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    pkv::mbar_init(&bar, 1);
+    pkv::fence_barrier_init();
+    if (!pkv::mbar_wait_bounded(&bar, 0, limit_ns)) record_status(status, KV_DEV_WAIT_TIMEOUT);
+  }
+}
+
 // Merge pass: per (sequence, query head) combine the partials of every piece
 // of its segment: M = max m_i, L = sum l_i 2^(m_i - M),
 // out = sum O_i 2^(m_i - M) / L.  One warp per (sequence, query head), four
@@ -564,6 +577,16 @@ kvStatus kv_pool_device_status(kvPool* p, void* stream, int* out_bits) {
   if (v && cudaMemset(p->d_status, 0, sizeof(int32_t)) != cudaSuccess) return KV_ERR_CUDA;
   *out_bits = v;
   return v ? KV_ERR_DEVICE_CHECK : KV_OK;
+}
+
+kvStatus kv_device_wait_selftest(kvPool* p, int limit_us, void* stream) {
+  if (!p || limit_us < 1 || limit_us > 1000000) return KV_ERR_INVALID_ARG;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  const cudaError_t e =
+      pkv::launch_kernel(false, wait_selftest_kernel, dim3(1), dim3(32), 0, as_stream(stream),
+                         p->d_status, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 kvStatus cow_copy(kvPool* p, const int32_t* d_pairs, int n_pairs, void* stream) {
@@ -926,7 +949,7 @@ StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks
   off += align256(L * n * n_q_heads * p->D * sizeof(float));
   l.ws = off;
   const size_t ws_plain = ws_layout(p, n_seq, n_q_heads / p->H).total;
-  const size_t ws_plan = plan_workspace_bytes(2 * n_seq * p->H, kPlanMaxCols, p->D);
+  const size_t ws_plan = plan_workspace_bytes(plan_max_segs(n_seq, p->H), kPlanMaxCols, p->D);
   off += align256(ws_plain > ws_plan ? ws_plain : ws_plan);
   l.total = off;
   return l;
