@@ -130,12 +130,16 @@ extern "C" {
 
 size_t paged_decode_plan_bytes(const kvPool* p, int n_seq, int n_q_heads) {
   if (!p || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0) return 0;
-  // at most one private and one shared segment per (sequence, head), and
-  // two member slots and two entries per sequence (and head); start records
-  // for the larger of the two kernels' CTA counts
+  // per (sequence, head) at most kPlanMaxLevels shared runs and one private
+  // rest (a shared run has two or more members, so there are at most
+  // kPlanMaxLevels * n_seq / 2 of them per head), member slots and entries
+  // to match; start records for the larger of the two kernels' CTA counts
   const int G = n_q_heads / p->H;
   const int n_start = std::max(plan_grid(p, kPlanKernelMma, G), plan_grid(p, kPlanKernelTc, G));
-  return plan_layout(n_seq, p->H, 2 * n_seq * p->H, 2 * n_seq, 2 * n_seq * p->H, n_start).total;
+  const int segs_max = plan_max_segs(n_seq, p->H);
+  const int mem_max = (kPlanMaxLevels + 1) * n_seq;
+  return plan_layout(n_seq, p->H, segs_max, mem_max, (kPlanMaxLevels + 1) * n_seq * p->H,
+                     n_start).total;
 }
 
 kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
@@ -162,59 +166,121 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     seqs[i] = &it->second;
   }
   const int max_members = kPlanMaxCols / G;
+  // whole blocks of a sequence inside its context (a shared run never
+  // reaches into a partly filled block)
+  auto full_blocks = [&](int i) {
+    return static_cast<int>(std::min<int64_t>(static_cast<int64_t>(seqs[i]->table.size()),
+                                              seqs[i]->len / B));
+  };
 
-  // ---- groups: listed sequences with the same first physical block
-  std::vector<int> order;
-  for (int i = 0; i < n_seq; ++i)
-    if (!seqs[i]->table.empty()) order.push_back(i);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return seqs[a]->table[0] < seqs[b]->table[0]; });
-  std::vector<int> shared(n_seq, 0);     // shared prefix blocks per sequence
-  std::vector<int> pos_in(n_seq, -1);    // column group position in its shared segment
-  std::vector<std::vector<int>> chunks;  // sub-groups that read a prefix together
-  std::vector<int> chunk_p;              // their shared prefix length (blocks)
-  for (size_t a = 0; a < order.size();) {
-    size_t b = a + 1;
-    while (b < order.size() && seqs[order[b]]->table[0] == seqs[order[a]]->table[0]) ++b;
-    for (size_t c0 = a; b - a >= 2 && c0 < b; c0 += max_members) {
-      const size_t c1 = std::min(b, c0 + max_members);
-      if (c1 - c0 < 2) break;
-      std::vector<int> mem(order.begin() + c0, order.begin() + c1);
-      std::sort(mem.begin(), mem.end());
-      const std::vector<int32_t>& t0 = seqs[mem[0]]->table;
-      int P = static_cast<int>(std::min<int64_t>(t0.size(), seqs[mem[0]]->len / B));
-      for (size_t k = 1; k < mem.size() && P > 0; ++k) {
-        const std::vector<int32_t>& t = seqs[mem[k]]->table;
-        P = common_prefix(t0.data(), t.data(), std::min<int>(P, static_cast<int>(t.size())));
-        P = static_cast<int>(std::min<int64_t>(P, seqs[mem[k]]->len / B));  // whole blocks in every context
-      }
-      if (static_cast<int64_t>(P) * B < min_shared_tokens) continue;
-      for (size_t k = 0; k < mem.size(); ++k) {
-        shared[mem[k]] = P;
-        pos_in[mem[k]] = static_cast<int>(k);
-      }
-      chunks.push_back(mem);
-      chunk_p.push_back(P);
+  // ---- shared runs, found like a radix walk over the listed tables: the
+  // sequences with the same first physical block form a group; a group's
+  // common run from its start s0 is read once for all of its members when it
+  // is at least min_shared_tokens long (members cut into sub-groups of at
+  // most max_members, equal in size); after the run, the members are split
+  // by their next physical block and each part with two or more members goes
+  // on from there (a branch that forked deeper in a shared prompt shares
+  // that deeper run with its siblings).  A run too short to share is read
+  // privately, and the parts continue from the same start.  A sequence joins
+  // at most kPlanMaxLevels shared runs.
+  struct Node {
+    std::vector<int> mem;  // members, ascending
+    int b0, b1;            // the run of blocks [b0, b1)
+  };
+  std::vector<Node> nodes;
+  std::vector<std::vector<int>> seq_nodes(n_seq);  // shared runs of each sequence, in order
+  std::vector<int> priv_from(n_seq, 0);            // first block read privately
+  std::vector<int> roots;                          // first node of each root group
+  auto run_group = [&](auto&& self, std::vector<int> mem, int s0) -> void {
+    // common run from s0 among the members
+    int P = full_blocks(mem[0]);
+    const std::vector<int32_t>& t0 = seqs[mem[0]]->table;
+    for (size_t k = 1; k < mem.size() && P > s0; ++k) {
+      const std::vector<int32_t>& t = seqs[mem[k]]->table;
+      P = std::min(P, full_blocks(mem[k]));
+      if (P > s0) P = s0 + common_prefix(t0.data() + s0, t.data() + s0, P - s0);
     }
-    a = b;
+    if (P < s0) P = s0;
+    int next_s0 = s0;
+    bool room = true;
+    for (int m : mem) room = room && static_cast<int>(seq_nodes[m].size()) < kPlanMaxLevels;
+    if (room && static_cast<int64_t>(P - s0) * B >= min_shared_tokens) {
+      const int n_sub = static_cast<int>((mem.size() + max_members - 1) / max_members);
+      size_t c0 = 0;
+      for (int c = 0; c < n_sub; ++c) {
+        const size_t c1 = c0 + (mem.size() - c0) / static_cast<size_t>(n_sub - c);
+        Node nd;
+        nd.mem.assign(mem.begin() + static_cast<long>(c0), mem.begin() + static_cast<long>(c1));
+        nd.b0 = s0;
+        nd.b1 = P;
+        for (int m : nd.mem) {
+          seq_nodes[m].push_back(static_cast<int>(nodes.size()));
+          priv_from[m] = P;
+        }
+        nodes.push_back(std::move(nd));
+        c0 = c1;
+      }
+      next_s0 = P;
+    }
+    // the members that go on past P, split by their block there
+    std::vector<int> more;
+    for (int m : mem)
+      if (full_blocks(m) > P) more.push_back(m);
+    std::stable_sort(more.begin(), more.end(), [&](int x, int y) {
+      return seqs[x]->table[P] < seqs[y]->table[P];
+    });
+    for (size_t a0 = 0; a0 < more.size();) {
+      size_t b0 = a0 + 1;
+      while (b0 < more.size() && seqs[more[b0]]->table[P] == seqs[more[a0]]->table[P]) ++b0;
+      if (b0 - a0 >= 2) {
+        std::vector<int> part(more.begin() + static_cast<long>(a0),
+                              more.begin() + static_cast<long>(b0));
+        std::sort(part.begin(), part.end());
+        self(self, std::move(part), next_s0);
+      }
+      a0 = b0;
+    }
+  };
+  {
+    std::vector<int> order;
+    for (int i = 0; i < n_seq; ++i)
+      if (full_blocks(i) > 0) order.push_back(i);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int x, int y) { return seqs[x]->table[0] < seqs[y]->table[0]; });
+    for (size_t a0 = 0; a0 < order.size();) {
+      size_t b0 = a0 + 1;
+      while (b0 < order.size() && seqs[order[b0]]->table[0] == seqs[order[a0]]->table[0]) ++b0;
+      if (b0 - a0 >= 2) {
+        std::vector<int> grp(order.begin() + static_cast<long>(a0),
+                             order.begin() + static_cast<long>(b0));
+        std::sort(grp.begin(), grp.end());
+        const size_t before = nodes.size();
+        run_group(run_group, std::move(grp), 0);
+        if (nodes.size() > before) roots.push_back(static_cast<int>(before));
+      }
+      a0 = b0;
+    }
   }
+  // nodes of root group r: [roots[r], roots[r + 1])
+  roots.push_back(static_cast<int>(nodes.size()));
 
-  // ---- segments, members, entries.  Order: per group and K/V head, the
-  // shared segment followed by the members' private rests of that head;
-  // these (group, head) items are spread evenly among the ungrouped
-  // sequences (item i before ungrouped sequence ceil(i * n_ungrouped /
-  // n_items)).  Tiny private rests are thus spread over the work list
-  // instead of piling up at its end, and the wide shared segments, whose
-  // blocks cost more, fall to different CTAs (the split balances work
-  // units, and every piece has a fixed cost).
+  // ---- segments, members, entries.  Order: per root group and K/V head,
+  // its shared runs (in the order found) followed by the members' private
+  // rests of that head; these (group, head) items are spread evenly among
+  // the sequences outside every group (item i before ungrouped sequence
+  // ceil(i * n_ungrouped / n_items)).  Tiny private rests are thus spread over
+  // the work list instead of piling up at its end, and the wide shared
+  // segments, whose blocks cost more, fall to different CTAs (the split
+  // balances work units).
   std::vector<PlanSeg> segs;
   std::vector<int32_t> members;
-  segs.reserve(2 * static_cast<size_t>(n_seq) * H);
-  members.reserve(2 * static_cast<size_t>(n_seq));
-  // merge entries per (sequence, head): at most a shared segment and a private rest
-  std::vector<PlanEntry> ent2(2 * static_cast<size_t>(n_seq) * H);
+  segs.reserve(static_cast<size_t>(nodes.size() + n_seq) * H);
+  members.reserve(static_cast<size_t>(n_seq) * (kPlanMaxLevels + 1));
+  // merge entries per (sequence, head): its shared runs and its private rest
+  constexpr int kEnt = kPlanMaxLevels + 1;
+  std::vector<PlanEntry> entk(static_cast<size_t>(kEnt) * n_seq * H);
   std::vector<uint8_t> n_ent(static_cast<size_t>(n_seq) * H, 0);
-  auto add_entry = [&](size_t sh, PlanEntry e) { ent2[2 * sh + n_ent[sh]++] = e; };
+  auto add_entry = [&](size_t sh, PlanEntry e) { entk[kEnt * sh + n_ent[sh]++] = e; };
   int c_max = G;
   std::vector<int> priv_mem(n_seq, -1);  // member-list slot of a sequence's private rest
   auto private_member = [&](int i) {
@@ -226,10 +292,10 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   };
   auto push_private = [&](int i, int h) {
     const int nb = static_cast<int>((seqs[i]->len + B - 1) / B);
-    if (nb <= shared[i]) return;
+    if (nb <= priv_from[i]) return;
     PlanSeg s{};
     s.rep = i;
-    s.b0 = shared[i];
+    s.b0 = priv_from[i];
     s.b1 = nb;
     s.tok_end = static_cast<int32_t>(seqs[i]->len);
     s.head = h;
@@ -239,36 +305,45 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     segs.push_back(s);
     add_entry(static_cast<size_t>(i) * H + h, {si, 0});
   };
-  std::vector<char> grouped(n_seq, 0);
-  for (const auto& ch : chunks)
-    for (int m : ch) grouped[m] = 1;
-  std::vector<int> group_mem0(chunks.size(), -1);  // member-list slot of each group
-  auto push_group_head = [&](size_t c, int h) {
-    if (group_mem0[c] < 0) {
-      group_mem0[c] = static_cast<int>(members.size());
-      for (int m : chunks[c]) members.push_back(m);
+  std::vector<int> node_mem0(nodes.size(), -1);  // member-list slot of each node
+  auto push_group_head = [&](size_t r, int h) {
+    std::vector<int> grp_members;
+    for (int ni = roots[r]; ni < roots[r + 1]; ++ni) {
+      const Node& nd = nodes[ni];
+      if (node_mem0[ni] < 0) {
+        node_mem0[ni] = static_cast<int>(members.size());
+        for (int m : nd.mem) members.push_back(m);
+      }
+      const int ncols = static_cast<int>(nd.mem.size()) * G;
+      c_max = std::max(c_max, ncols);
+      PlanSeg s{};
+      s.rep = nd.mem[0];
+      s.b0 = nd.b0;
+      s.b1 = nd.b1;
+      s.tok_end = nd.b1 * B;
+      s.head = h;
+      s.ncols = ncols;
+      s.mem = node_mem0[ni];
+      const int si = static_cast<int>(segs.size());
+      segs.push_back(s);
+      for (size_t k = 0; k < nd.mem.size(); ++k)
+        add_entry(static_cast<size_t>(nd.mem[k]) * H + h, {si, static_cast<int>(k) * G});
+      grp_members.insert(grp_members.end(), nd.mem.begin(), nd.mem.end());
     }
-    const int ncols = static_cast<int>(chunks[c].size()) * G;
-    c_max = std::max(c_max, ncols);
-    PlanSeg s{};
-    s.rep = chunks[c][0];
-    s.b0 = 0;
-    s.b1 = chunk_p[c];
-    s.tok_end = chunk_p[c] * B;
-    s.head = h;
-    s.ncols = ncols;
-    s.mem = group_mem0[c];
-    const int si = static_cast<int>(segs.size());
-    segs.push_back(s);
-    for (int m : chunks[c]) add_entry(static_cast<size_t>(m) * H + h, {si, pos_in[m] * G});
-    for (int m : chunks[c]) push_private(m, h);
+    std::sort(grp_members.begin(), grp_members.end());
+    grp_members.erase(std::unique(grp_members.begin(), grp_members.end()), grp_members.end());
+    for (int m : grp_members) push_private(m, h);
   };
+  std::vector<char> grouped(n_seq, 0);
+  for (const Node& nd : nodes)
+    for (int m : nd.mem) grouped[m] = 1;
   std::vector<int> ungrouped;
   for (int i = 0; i < n_seq; ++i)
     if (!grouped[i]) ungrouped.push_back(i);
-  const size_t n_i = chunks.size() * H, n_u = ungrouped.size();
+  const size_t n_roots = roots.size() - 1;
+  const size_t n_i = n_roots * H, n_u = ungrouped.size();
   size_t it = 0;
-  auto push_item = [&](size_t i) { push_group_head(i % chunks.size(), static_cast<int>(i / chunks.size())); };
+  auto push_item = [&](size_t i) { push_group_head(i % n_roots, static_cast<int>(i / n_roots)); };
   for (size_t k = 0; k < n_u; ++k) {
     while (it < n_i && it * n_u <= k * n_i) push_item(it++);
     for (int h = 0; h < H; ++h) push_private(ungrouped[k], h);
@@ -329,7 +404,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   hd.mem_off = static_cast<int32_t>(l.mem);
   hd.eoff_off = static_cast<int32_t>(l.eoff);
   hd.ent_off = static_cast<int32_t>(l.ent);
-  hd.n_shared_segs = static_cast<int32_t>(chunks.size()) * H;
+  hd.n_shared_segs = static_cast<int32_t>(nodes.size()) * H;
   hd.kernel = kernel;
   hd.start_off = grid > 0 ? static_cast<int32_t>(l.start) : 0;
   hd.start_grid = grid;
@@ -343,7 +418,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   int k = 0;
   for (size_t i = 0; i < n_ent.size(); ++i) {
     eoff[i] = k;
-    for (int j = 0; j < n_ent[i]; ++j) ent[k++] = ent2[2 * i + j];
+    for (int j = 0; j < n_ent[i]; ++j) ent[k++] = entk[kEnt * i + j];
   }
   eoff[n_ent.size()] = k;
   if (out_workspace_bytes) *out_workspace_bytes = plan_workspace_bytes(hd.n_segs, c_max, p->D);

@@ -77,6 +77,15 @@ struct PlanEntry {
 // Most query columns one segment carries (four 8-column MMA n-tiles).
 constexpr int kPlanMaxCols = 32;
 
+// Most shared runs one sequence is read through (nested forks beyond this
+// depth are read privately).
+constexpr int kPlanMaxLevels = 3;
+
+// Most segments a plan of n_seq sequences can hold.
+constexpr int plan_max_segs(int n_seq, int n_kv_heads) {
+  return (n_seq + (kPlanMaxLevels * n_seq + 1) / 2) * n_kv_heads;
+}
+
 // Split-pass kernels a plan can be built for (the values of the pool's
 // decode-path option).
 constexpr int kPlanKernelMma = 2;  // warp-level MMA (mma.sync)

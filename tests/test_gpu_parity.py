@@ -419,6 +419,33 @@ def test_planned_random_fork_trees_against_oracle(seed, G, B, path):
 
 
 @pytest.mark.parametrize("path", TENSOR_PATHS)
+@pytest.mark.parametrize("levels,G", [(2, 4), (3, 8), (4, 2)])
+def test_planned_nested_forks_against_oracle(levels, G, path):
+    # a prompt forked into branches that grow and fork again: the plan reads
+    # the prompt once for all leaves, each branch's run once for its leaves
+    # (up to three shared runs per sequence; deeper ones privately)
+    from test_plan import nested_tree
+
+    B, H = 16, 2
+    ops, leaves = nested_tree(levels, B, run_tokens=200, leaf_tokens=21)
+    wl = synth.Workload("nested", 1, 2048, B, H * G, H, 128, "bf16", 40 + levels,
+                        synth.permutation((40 + levels, 5), 2048), ops, leaves)
+    orc = OracleRun(wl)
+    cache, run = make(wl, path=path)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg, og = run.step(wl.decode_seqs, qh, k, v, planned=True)
+    assert list(sg) == so and [tuple(p) for p in pg] == co
+    h_plan, _, _ = run.plan(wl.decode_seqs, run.max_blocks(wl.decode_seqs))
+    from paged_kv_cache_65_gb300.cache import parse_plan
+
+    assert parse_plan(h_plan)["n_shared_segs"] >= (2 ** min(levels, 3) - 1) * H
+    assert max_err(og.cpu().numpy()[0], orc.attend(0, qh)) <= TOL["bf16"]
+    check_status(cache)
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS)
 def test_planned_equals_plain_without_sharing(path):
     wl = synth.workload("qwen_2k")
     cache, run = make(wl, zero=False, path=path)

@@ -199,3 +199,50 @@ def test_plans_without_a_known_grid_have_no_start_records():
 
     with pytest.raises(Exception):
         c.kv_pool_set_option(_lib.KV_OPT_PLAN_GRID, 1025)
+
+
+def nested_tree(levels, B=16, fan=2, run_tokens=320, leaf_tokens=37):
+    """A prompt forked into branches that each grow a long run and fork again,
+    `levels` deep; returns (workload ops, leaves)."""
+    ops, nxt = [("append", 0, run_tokens, 0)], 1
+    frontier = [0]
+    for lev in range(levels):
+        new = []
+        for par in frontier:
+            for _ in range(fan):
+                ops.append(("fork", par, nxt))
+                ops.append(("append", nxt, run_tokens + 16 * lev, nxt))
+                new.append(nxt)
+                nxt += 1
+            ops.append(("release", par))
+        frontier = new
+    for k, leaf in enumerate(frontier):
+        ops.append(("append", leaf, leaf_tokens + k, 1000 + leaf))
+    return ops, frontier
+
+
+@pytest.mark.parametrize("levels,G", [(2, 4), (2, 8), (3, 2), (5, 4)])
+def test_nested_forks_read_every_shared_block_once(levels, G):
+    # a prompt shared by all leaves, runs shared by the leaves under each
+    # branch, deeper runs under each sub-branch: every block the leaves'
+    # tables name is read once per K/V head, as long as no sequence sits in
+    # more than the plan's maximum of shared runs (here 3); deeper levels are
+    # read by each sharer, but still exactly once per sequence
+    B, H = 16, 2
+    ops, leaves = nested_tree(levels, B)
+    wl = synth.Workload("nested", 1, 8192, B, H * G, H, 128, "bf16", 5, None, ops, leaves)
+    bm, c = build_both(wl)
+    mb = max(len(bm.tables[s]) for s in leaves)
+    plan = parse_plan(c.paged_decode_plan(leaves, H * G, mb)[0])
+    check_plan(bm, plan, leaves, G, 128)
+    distinct = {p for s in leaves for p in bm.tables[s][: -(-bm.lengths[s] // B)]}
+    read = [0] * H
+    for s in plan["segs"]:
+        read[int(s["head"])] += int(s["b1"] - s["b0"])
+    if levels <= 3:  # a leaf sits in `levels` shared runs
+        assert read == [len(distinct)] * H
+        # one shared segment per branch point and head (the root's prompt, then each branch)
+        n_nodes = sum(2 ** k for k in range(levels))
+        assert plan["n_shared_segs"] == n_nodes * H
+    else:
+        assert all(r > len(distinct) for r in read)  # the deepest runs are read per sharer
