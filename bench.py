@@ -50,12 +50,12 @@ DEFAULT_WORKLOAD = "pool36"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331703296 + 3276800, "sha": "7a574767b9923aec"},
-    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 171004416 + 3211520, "sha": "7a574767b9923aec"},
-    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615941376 + 6079488, "sha": "7a574767b9923aec"},
-    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169274368 + 3358720, "sha": "7a574767b9923aec"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331453440 + 3433472, "sha": "7be3a560954942c3"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170882816 + 3297536, "sha": "7be3a560954942c3"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615871232 + 5789952, "sha": "7be3a560954942c3"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169170432 + 3505408, "sha": "7be3a560954942c3"},
     # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
-    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3456562432 + 5879040, "sha": "7a574767b9923aec"},
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464092672 + 6120960, "sha": "7be3a560954942c3"},
     ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
 }
 
