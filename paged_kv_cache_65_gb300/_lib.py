@@ -100,6 +100,9 @@ SIGNATURES = [
                                                 _vp, C.c_float, _vp, C.c_size_t, _vp]),
     ("paged_decode_merge_planned", C.c_int, [_vp, C.c_int, _vp, _vp, _vp, C.c_int, _vp,
                                              C.c_size_t, _vp]),
+    ("paged_decode_partials_planned_write", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, _vp, _vp,
+                                                      C.c_int, _vp, _vp, C.c_float, _vp,
+                                                      C.c_size_t, _vp]),
     ("paged_decode_attention_planned", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
                                                  _vp, C.c_float, _vp, C.c_int, _vp, C.c_size_t,
                                                  _vp]),
@@ -114,8 +117,10 @@ SIGNATURES = [
                                                     _vp, _vp, C.c_int, _vp, C.c_int, C.c_float,
                                                     _vp, C.c_int, _vp]),
     ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
-    ("kv_decode_step_host", C.c_int, [_vp, _i32p, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
-                                      C.c_float, _f32p, _vp, C.c_size_t, _vp]),
+    # the host buffers go as plain addresses (the per-step call is marshalled
+    # with as few conversions as possible)
+    ("kv_decode_step_host", C.c_int, [_vp, _vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp,
+                                      C.c_float, _vp, _vp, C.c_size_t, _vp]),
 ]
 
 for _name, _res, _args in SIGNATURES:

@@ -253,6 +253,16 @@ class PagedKVCache:
                                                 _nbytes(workspace), _stream(stream)),
               "paged_decode_partials_planned")
 
+    def paged_decode_partials_planned_write(self, layer, q, n_q_heads, k_new, v_new, d_table,
+                                            max_blocks, d_plan, h_plan, workspace, scale=0.0,
+                                            stream=None):
+        """The planned split pass with this layer's slot write of the step's
+        newest tokens (rows of ``k_new``, ``v_new`` in plan order) fused in."""
+        check(lib.paged_decode_partials_planned_write(
+            self.handle, int(layer), vp(q), int(n_q_heads), vp(k_new), vp(v_new), vp(d_table),
+            int(max_blocks), vp(d_plan), vp(h_plan), float(scale), vp(workspace),
+            _nbytes(workspace), _stream(stream)), "paged_decode_partials_planned_write")
+
     def paged_decode_merge_planned(self, n_q_heads, d_plan, h_plan, out, workspace, stream=None):
         check(lib.paged_decode_merge_planned(self.handle, int(n_q_heads), vp(d_plan), vp(h_plan),
                                              vp(out), _out_dtype(out), vp(workspace),
@@ -333,12 +343,23 @@ class PagedKVCache:
 
     def kv_decode_step_host(self, seq_ids, n_q_heads, max_blocks, h_q, h_k_new, h_v_new, h_out,
                             staging, scale=0.0, stream=None):
-        ids = i32(seq_ids)
-        check(lib.kv_decode_step_host(self.handle, ptr_i32(ids), ids.size, int(n_q_heads),
-                                      int(max_blocks), vp(h_q), vp(h_k_new), vp(h_v_new),
-                                      float(scale), C.cast(C.c_void_p(_addr(h_out)), _lib._f32p),
-                                      vp(staging), _nbytes(staging), _stream(stream)),
+        ids = seq_ids
+        if not (isinstance(ids, np.ndarray) and ids.dtype == np.int32 and ids.flags.c_contiguous):
+            ids = i32(seq_ids)
+        check(lib.kv_decode_step_host(self.handle, ids.ctypes.data, ids.size, n_q_heads,
+                                      max_blocks, _addr(h_q), _addr(h_k_new), _addr(h_v_new),
+                                      scale, _addr(h_out), _addr(staging), _nbytes(staging),
+                                      self._raw_stream() if stream is None else _stream(stream)),
               "kv_decode_step_host")
+
+    def _raw_stream(self) -> int:
+        """The current torch stream of this pool's device as a raw handle."""
+        import torch
+
+        dev = self.k.device.index if self.k is not None and self.k.device.index is not None \
+            else torch.cuda.current_device()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        return raw(dev) if raw is not None else torch.cuda.current_stream(dev).cuda_stream
 
 
 def _addr(x) -> int:
@@ -369,7 +390,7 @@ PLAN_SEG = np.dtype([("wpre", "<i8"), ("rep", "<i4"), ("b0", "<i4"), ("b1", "<i4
 PLAN_ENTRY = np.dtype([("seg", "<i4"), ("col_base", "<i4")])
 PLAN_START = np.dtype([("seg", "<i4"), ("rep", "<i4"), ("head", "<i4"), ("b0", "<i4"),
                        ("b1", "<i4"), ("tok_end", "<i4"), ("ncols", "<i4"), ("mem", "<i4"),
-                       ("r_after", "<i8"), ("n_pid", "<i4"), ("pad0", "<i4"),
+                       ("r_after", "<i8"), ("n_pid", "<i4"), ("last", "<i4"),
                        ("pid", "<i4", (16,)), ("pad1", "<i4", (4,))])
 
 

@@ -784,10 +784,14 @@ size_t plan_ml_bytes(const PlanHeader& hd) {
 }
 }  // namespace
 
-kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
-                                       const int32_t* d_block_table, int max_blocks,
-                                       const void* d_plan, const void* h_plan, float scale,
-                                       void* d_workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// The planned split pass; with d_k_new / d_v_new, the step's slot write of
+// this layer is fused in (each listed sequence's newest token).
+kvStatus partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                          const int32_t* d_block_table, int max_blocks, const void* d_plan,
+                          const void* h_plan, float scale, void* d_workspace,
+                          size_t workspace_bytes, void* stream, const void* d_k_new,
+                          const void* d_v_new) {
   PlanHeader hd;
   kvStatus s = read_plan_header(p, n_q_heads, h_plan, &hd);
   if (s != KV_OK) return s;
@@ -837,6 +841,12 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
   a.plan_W = hd.W;
   a.starts = hd.start_grid > 0 ? reinterpret_cast<const PlanStart*>(dp + hd.start_off) : nullptr;
   a.start_grid = hd.start_grid;
+  a.k_new = d_k_new;
+  a.v_new = d_v_new;
+  a.k_pool = p->k;
+  a.v_pool = p->v;
+  a.k_scale_w = p->k_scale;
+  a.v_scale_w = p->v_scale;
   const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   bool supported = true;
@@ -852,6 +862,28 @@ kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, in
                                  &supported);
   if (!supported) return KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+}  // namespace
+
+kvStatus paged_decode_partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                       const int32_t* d_block_table, int max_blocks,
+                                       const void* d_plan, const void* h_plan, float scale,
+                                       void* d_workspace, size_t workspace_bytes, void* stream) {
+  return partials_planned(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_plan, h_plan,
+                          scale, d_workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+kvStatus paged_decode_partials_planned_write(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                             const void* d_k_new, const void* d_v_new,
+                                             const int32_t* d_block_table, int max_blocks,
+                                             const void* d_plan, const void* h_plan, float scale,
+                                             void* d_workspace, size_t workspace_bytes,
+                                             void* stream) {
+  if (!p || !d_k_new || !d_v_new || !aligned16(d_k_new) || !aligned16(d_v_new))
+    return KV_ERR_INVALID_ARG;
+  if (p->dtype != KV_DTYPE_BF16 && p->dtype != KV_DTYPE_FP8_E4M3) return KV_ERR_UNSUPPORTED;
+  return partials_planned(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_plan, h_plan,
+                          scale, d_workspace, workspace_bytes, stream, d_k_new, d_v_new);
 }
 
 kvStatus paged_decode_merge_planned(kvPool* p, int n_q_heads, const void* d_plan,
@@ -1020,11 +1052,32 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   int32_t* h_table = reinterpret_cast<int32_t*>(hm + l.table);
   int32_t* h_lens = reinterpret_cast<int32_t*>(hm + l.lens);
   unsigned char* h_plan = hm + l.plan;
-  // host: reserve (all or nothing), tables, and the sharing-aware plan of
-  // the tensor-core passes (shared blocks read once)
+  // host: reserve (all or nothing)
   int n_cow = 0;
   s = seq_append_slots(p, seq_ids, n_seq, h_slots, h_pairs, &n_cow);
   if (s != KV_OK) return s;
+  // host -> device: q, new K and V from the caller's buffers, then the slots
+  // and copy pairs; the device copies the shared tails and writes the new
+  // tokens while the host builds the tables and the plan
+  cudaStream_t st = as_stream(stream);
+  unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
+  const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->in_esize;
+  const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->in_esize;
+  const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
+  bool ok = true;
+  ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok &= cudaMemcpyAsync(d + l.slots, p->h_pinned, l.table - l.slots, cudaMemcpyHostToDevice,
+                        st) == cudaSuccess;
+  if (!ok) return KV_ERR_CUDA;
+  s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
+  if (s != KV_OK) return s;
+  s = reshape_and_cache(p, -1, d + l.k, d + l.v, reinterpret_cast<const int64_t*>(d + l.slots),
+                        n_seq, stream);
+  if (s != KV_OK) return s;
+  // host: tables, and the sharing-aware plan of the tensor-core passes
+  // (shared blocks read once); then their copy, which the attention waits for
   s = seq_block_table(p, seq_ids, n_seq, max_blocks, h_table, h_lens);
   if (s != KV_OK) return s;
   const int G = n_q_heads / p->H;
@@ -1036,26 +1089,10 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
                           paged_decode_plan_bytes(p, n_seq, n_q_heads), &ws_need);
     if (s != KV_OK) return s;
   }
-  // host -> device: q, new K and V from the caller's buffers, the metadata
-  // in one copy
-  cudaStream_t st = as_stream(stream);
-  unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
-  const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->in_esize;
-  const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->in_esize;
-  const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
-  bool ok = true;
-  ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.slots, p->h_pinned, (planned ? l.meta_end : l.plan) - l.slots,
-                        cudaMemcpyHostToDevice, st) == cudaSuccess;
-  if (!ok) return KV_ERR_CUDA;
-  // device: copy shared tails, write the new token in every layer, attend
-  s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
-  if (s != KV_OK) return s;
-  s = reshape_and_cache(p, -1, d + l.k, d + l.v, reinterpret_cast<const int64_t*>(d + l.slots),
-                        n_seq, stream);
-  if (s != KV_OK) return s;
+  if (cudaMemcpyAsync(d + l.table, p->h_pinned + (l.table - l.slots),
+                      (planned ? l.meta_end : l.plan) - l.table, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return KV_ERR_CUDA;
   const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
   for (int layer = 0; layer < p->L; ++layer) {
     if (planned)
