@@ -383,19 +383,28 @@ def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_
         flush.fill_(i & 0xFF)
         flush_r.sum()
 
-    # one CUDA graph per step plan: cow copy, slot write, per layer split + merge;
-    # event-record nodes around each split pass time the dominant kernel
+    # one CUDA graph per step plan: cow copy, slot write, per layer split + merge
+    # (with --fused-write the planned pass writes each layer's new tokens
+    # itself); event-record nodes around each split pass time the dominant kernel
+    fused = use_plan and args.fused_write
+
     def enqueue(p, ext=None, split=True, merge=True):
         cnt = 0
         if p["npairs"]:
             cache.cow_copy(p["pairs"], p["npairs"])
             cnt += 1
-        cache.reshape_and_cache(-1, kn, vn, p["slots"], n)
-        cnt += 1
+        if not fused:
+            cache.reshape_and_cache(-1, kn, vn, p["slots"], n)
+            cnt += 1
         for layer in range(L):
             if ext is not None:
                 ext[layer][0].record()
-            if use_plan and split:
+            if fused and split:
+                cache.paged_decode_partials_planned_write(layer, q[layer], wl.n_q_heads,
+                                                          kn[layer], vn[layer], p["table"],
+                                                          max_blocks, p["d_plan"], p["h_plan"],
+                                                          ws)
+            elif use_plan and split:
                 cache.paged_decode_partials_planned(layer, q[layer], wl.n_q_heads, p["table"],
                                                     max_blocks, p["d_plan"], p["h_plan"], ws)
             elif split:
@@ -589,7 +598,8 @@ def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_
     res = {
         "config": workload_config(wl, world, args.placement_seed),
         "path": {"decode_path": "planned" if use_plan else "plain",
-                 "kernel_option": args.kernel, "kernel": kname, "pdl": not args.no_pdl},
+                 "kernel_option": args.kernel, "kernel": kname, "pdl": not args.no_pdl,
+                 "slot_write": "fused into the split pass" if fused else "separate launch"},
         "dtype": wl.dtype,
         "value": round(value, 2), "unit": "GB/s", "steps": steps,
         "ms_per_step": round(ms_per_step, 4),
@@ -1280,6 +1290,9 @@ def main():
                     help="launch without programmatic dependencies between kernels")
     ap.add_argument("--plain", action="store_true",
                     help="no sharing-aware plan: one segment per (sequence, K/V head)")
+    ap.add_argument("--fused-write", action="store_true",
+                    help="planned steps: the slot write inside each layer's split pass "
+                         "(paged_decode_partials_planned_write) instead of its own launch")
     ap.add_argument("--prefill-order", default="heaviest", choices=["heaviest", "natural"],
                     help="chunked prefill: launch the work items heaviest first (host "
                          "schedule) or in the natural grid order")

@@ -325,6 +325,27 @@ kvStatus paged_decode_merge_planned(kvPool* pool, int n_q_heads, const void* d_p
                                     const void* h_plan, void* d_out, int out_dtype,
                                     const void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* The planned split pass with the step's slot write of `layer` fused in
+ * ([BT] §10's reserve -> write -> attend, the write done by the CTA that
+ * reads the block it lands in, just before that read): the same pool
+ * contents and partials as reshape_and_cache(layer, rows, slots) followed by
+ * paged_decode_partials_planned.  Every listed sequence must have its
+ * newest token, the one this step reserved, at its last context position
+ * (context_len - 1) of the tables the plan was built from, with any
+ * copy-on-write of the step already enqueued (cow_copy).
+ *   d_k_new, d_v_new: [n_seq][H_kv][D_h] bfloat16 rows of this layer, in
+ *                     plan order (FP8 pools quantize them as the slot write
+ *                     does), 16-byte aligned
+ * bfloat16 and FP8 pools only (KV_ERR_UNSUPPORTED otherwise); other
+ * arguments as paged_decode_partials_planned.  A bad block id met while
+ * writing skips the write (the read records KV_DEV_BAD_BLOCK_ID). */
+kvStatus paged_decode_partials_planned_write(kvPool* pool, int layer, const void* d_q,
+                                             int n_q_heads, const void* d_k_new,
+                                             const void* d_v_new, const int32_t* d_block_table,
+                                             int max_blocks, const void* d_plan,
+                                             const void* h_plan, float scale, void* d_workspace,
+                                             size_t workspace_bytes, void* stream);
+
 /* Decode attention of one layer following a plan: d_block_table and d_q hold
  * the listed sequences' rows in plan order; d_plan is the device copy of
  * h_plan (both are read: the host copy for sizes, the device copy by the

@@ -68,6 +68,16 @@ struct DecodeArgs {
   // were built for; used only when it equals `grid`
   const PlanStart* starts;
   int start_grid;
+  // planned pass with the step's slot write fused in (k_new == null: none):
+  // rows [plan row][H_kv][D_h] of this layer (bfloat16) of each listed
+  // sequence's newest token, its last context position, written into the
+  // pool (k_pool / v_pool, FP8 pools as codes of x / k_scale_w, v_scale_w)
+  // by the CTA that reads the block holding it, before that read
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  float k_scale_w = 1.f, v_scale_w = 1.f;
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }

@@ -154,6 +154,55 @@ __device__ __forceinline__ void fp8_tile_to_f16(uint32_t st, uint32_t dst, int r
 // Piece descriptors the producer can publish ahead of the consumers.
 constexpr int kPieceRing = 4;
 
+// Fused slot write, by one warp: the newest token's row (rep, head) of the
+// step's K (and / or V) of this layer, D bfloat16 values, into slot o of
+// physical block pid (bfloat16 pools: a copy; FP8 pools: the E4M3 code
+// nearest to x / scale, ties to even, saturating at 448), then a proxy fence
+// so that the TMA copies this warp issues next see it.
+template <int D, bool F8>
+__device__ __forceinline__ void write_new_row(const DecodeArgs& a, int rep, int head, int pid,
+                                              int o, bool do_k, bool do_v, int lane) {
+  constexpr int VECS = D * 2 / 16;  // 16-byte vectors of bf16 per row
+  const long long src = ((long long)rep * a.n_kv_heads + head) * D;
+  const long long dst = (((long long)a.layer * a.n_blocks + pid) * a.block_size + o) *
+                            a.n_kv_heads * D + (long long)head * D;
+  for (int i = lane; i < 2 * VECS; i += 32) {
+    const bool is_k = i < VECS;
+    if ((is_k && !do_k) || (!is_k && !do_v)) continue;
+    const int vi = is_k ? i : i - VECS;
+    const uint4 x = reinterpret_cast<const uint4*>(
+        reinterpret_cast<const unsigned char*>(is_k ? a.k_new : a.v_new) + src * 2)[vi];
+    void* pool = is_k ? a.k_pool : a.v_pool;
+    if constexpr (F8) {
+      const float scale = is_k ? a.k_scale_w : a.v_scale_w;
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t out[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t b = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t word = w[2 * h + k];
+          const float lo = __fdiv_rn(__uint_as_float(word << 16), scale);
+          const float hi = __fdiv_rn(__uint_as_float(word & 0xffff0000u), scale);
+          uint16_t c;
+          // the first source goes to the upper byte
+          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+          b |= static_cast<uint32_t>(c) << (16 * k);
+        }
+        out[h] = b;
+      }
+      reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(pool) + dst)[vi] =
+          make_uint2(out[0], out[1]);
+    } else {
+      reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(pool) + dst * 2)[vi] = x;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 template <int D, int G, bool F8 = false>
 constexpr int decode_mma_smem_bytes() {
   using C = MmaCfg<D, G, F8>;
@@ -163,7 +212,7 @@ constexpr int decode_mma_smem_bytes() {
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
          + kTableCache * 4                  // producer table cache
-         + kPieceRing * (32 + 16)           // piece descriptors and their mbarriers
+         + kPieceRing * (48 + 16)           // piece descriptors and their mbarriers
          + 64 + 128 + 1024;                 // walk state, start record, 1 KiB alignment
 }
 
@@ -177,6 +226,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int r, int c) {
 // from `rep` itself without a plan); `seg` numbers the segment.
 struct Piece {
   int rep, head, b0, b1, tok_end, ncols, mem, seg;
+  int last;  // the piece holds its segment's last block
 };
 
 // Walks the plan's segments over the block range [r, r1).
@@ -206,6 +256,7 @@ struct PlanWalker {
       p.ncols = sg.ncols;
       p.mem = sg.mem;
       p.seg = s;
+      p.last = p.b1 == sg.b1;
       r = end;
       return true;
     }
@@ -359,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         p.ncols = R.ncols;
         p.mem = R.mem;
         p.seg = R.seg;
+        p.last = R.last;
         plw.s = R.seg;
         plw.r = R.r_after;
         return true;
@@ -374,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       p.ncols = G;
       p.mem = -1;
       p.seg = pw.seq * H + pw.head;
+      p.last = 0;
       return true;
     }
   };
@@ -452,6 +505,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool from_rec = use_rec && stage == 0 && p.seg == rec_s->seg &&
                               tok0 / B >= rec_s->b0 && jl - rec_s->b0 < rec_s->n_pid;
         if (!from_rec) tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, jl, lane);
+        if constexpr (PLAN) {
+          // fused slot write: the stage holding a private segment's last
+          // token (the sequence's newest) writes that row first
+          if (a.k_new != nullptr && p.last && p.ncols == G && tok0 + STG >= p.tok_end) {
+            const int t = p.tok_end - 1;
+            const int j = t / B;
+            const int pid = from_rec ? rec_s->pid[j - rec_s->b0] : tc.ent[j - tc.base];
+            if (pid >= 0 && pid < a.n_blocks)
+              write_new_row<D, F8>(a, p.rep, p.head, pid, t - j * B, true, true, lane);
+          }
+        }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * unit_bytes);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {

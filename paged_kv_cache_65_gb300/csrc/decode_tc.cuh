@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         p.ncols = R.ncols;
         p.mem = R.mem;
         p.seg = R.seg;
+        p.last = R.last;
         plw.s = R.seg;
         plw.r = R.r_after;
         return true;
@@ -467,6 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       p.ncols = G;
       p.mem = -1;
       p.seg = pw.seq * H + pw.head;
+      p.last = 0;
       return true;
     }
   };
@@ -589,6 +591,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool from_rec = use_rec && stage == 0 && p.seg == rec_s->seg &&
                               tok0 / B >= rec_s->b0 && jl - rec_s->b0 < rec_s->n_pid;
         if (!from_rec) tc.ensure(a.table, a.max_blocks, p.rep, tok0 / B, jl, lane);
+        if constexpr (PLAN) {
+          // fused slot write: the stage holding a private segment's last
+          // token (the sequence's newest) writes that row first, K by the K
+          // producer and V by the V producer
+          if (a.k_new != nullptr && p.last && p.ncols == G && tok0 + C::TS >= p.tok_end) {
+            const int t = p.tok_end - 1;
+            const int j = t / B;
+            const int pid = from_rec ? rec_s->pid[j - rec_s->b0] : tc.ent[j - tc.base];
+            if (pid >= 0 && pid < a.n_blocks)
+              write_new_row<C::D, false>(a, p.rep, p.head, pid, t - j * B, kp, !kp, lane);
+          }
+        }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], 1u * nunits * UR * C::D * 2);
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {

@@ -107,6 +107,7 @@ void plan_starts(const std::vector<PlanSeg>& segs, int64_t W, int grid, int B,
       R.tok_end = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(R.b1) * B, sg.tok_end));
       R.ncols = sg.ncols;
       R.mem = sg.mem;
+      R.last = R.b1 == sg.b1 ? 1 : 0;
       R.r_after = end;
       const std::vector<int32_t>& t = seqs[sg.rep]->table;
       int k = 0;

@@ -63,7 +63,7 @@ struct PlanStart {
   int32_t rep, head, b0, b1, tok_end, ncols, mem;
   int64_t r_after;  // work unit after the first piece
   int32_t n_pid;    // valid entries of pid (blocks b0 .. b0 + n_pid - 1)
-  int32_t pad0;
+  int32_t last;     // 1: the piece holds the segment's last block
   int32_t pid[kPlanStartPids];
   int32_t pad1[4];
 };
