@@ -40,11 +40,12 @@ def check_plan(bm, plan, seqs, G, min_tokens):
     assert plan["W"] == sum(units)
     assert list(segs["wpre"]) == list(np.cumsum([0] + units)[:-1])
     # units per block: 8 per part of the block's cost, plus the piece's fixed
-    # cost (one stage of narrow blocks) spread over the segment's blocks
+    # cost (one stage of narrow blocks, two on tcgen05) spread over the
+    # segment's blocks
     for s in segs:
         n = int(s["b1"] - s["b0"])
         if plan["kernel"] == 3:  # tcgen05
-            base, piece = 8 * (4 if s["ncols"] <= 16 else 5), 8 * 32
+            base, piece = 8 * (4 if s["ncols"] <= 16 else 5), 16 * 32
         else:
             assert plan["kernel"] == 2
             base, piece = 8 * (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5), 4 * 24
