@@ -103,13 +103,13 @@ constexpr int plan_block_weight(int ncols, int kernel) {
                                                       : (ncols <= 8 ? 3 : (ncols <= 16 ? 4 : 5)));
 }
 // Fixed cost of a piece (its start and its partials), in units: about one
-// pipeline stage of narrow blocks on the warp-level pass (64 tokens), two on
-// tcgen05 (2 x 128 tokens: a piece there also waits for its Q tile and for
-// the previous piece's O^T readout).  Each segment carries it spread over
+// pipeline stage of narrow blocks on the warp-level pass (64 tokens), four
+// on tcgen05 (4 x 128 tokens: a piece there also waits for its Q tile and
+// for the previous piece's O^T readout; found by timing 1, 2 and 4).  Each segment carries it spread over
 // its blocks, so a CTA whose range holds many short segments (the one-block
 // private tails of forked branches) is given fewer blocks.
 constexpr int plan_piece_units(int kernel) {
-  return kernel == kPlanKernelTc ? 16 * plan_block_weight(8, kernel)
+  return kernel == kPlanKernelTc ? 32 * plan_block_weight(8, kernel)
                                  : 4 * plan_block_weight(8, kernel);
 }
 // Units per block of a segment of n_blocks blocks.

@@ -573,3 +573,64 @@ def test_rising_scores_move_the_maximum_inside_pieces(path, planned):
     _, _, og = run.step(wl.decode_seqs, qh, k, v, planned=planned and path != 1)
     assert max_err(og.cpu().numpy()[0], orc.attend(0, qh)) <= TOL["bf16"]
     check_status(cache)
+
+
+# ----------------------------------------------------------- maximum sizes
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_one_sequence_of_128k_tokens(path):
+    # a single 131,072-token context (8,192 blocks of 16) at G = 8: the whole
+    # grid's work is one segment per K/V head, cut into many pieces that the
+    # merge recombines; plain and planned, against the oracle
+    n = 131072
+    wl = ragged_workload("bf16", 128, 8, 16, [n], H_kv=8, seed=77, n_blocks=n // 16 + 8)
+    orc = OracleRun(wl)
+    cache, run = make(wl, zero=False, path=path)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    run.write(*run.reserve(wl.decode_seqs), k, v)
+    ref = orc.attend(0, qh)
+    d_table, d_lens, mb = run.tables(wl.decode_seqs)
+    qd = torch.from_numpy(qh.view(np.int16)).cuda().view(torch.bfloat16)
+    got = run.attend(0, qd, d_table, mb, d_lens, 1).cpu().numpy()
+    assert max_err(got, ref) <= TOL["bf16"]
+    h_plan, d_plan, ws_bytes = run.plan(wl.decode_seqs, mb)
+    got = run.attend_planned(0, qd, d_table, mb, h_plan, d_plan, ws_bytes).cpu().numpy()
+    assert max_err(got, ref) <= TOL["bf16"]
+    check_status(cache)
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_a_thousand_short_sequences(path):
+    # 1,024 sequences in one batch (more segments than CTAs by far): lengths
+    # 1 to 300, a third of them forked from one 200-token prompt; every
+    # output against the oracle, plain and planned
+    rng = np.random.default_rng(5)
+    ops, seqs = [("append", 5000, 200, 0)], []
+    for s in range(1024):
+        if s % 3 == 0:
+            ops.append(("fork", 5000, s))
+            extra = int(rng.integers(0, 60))
+        else:
+            extra = int(rng.integers(0, 300))
+        if extra:
+            ops.append(("append", s, extra, 1 + s))
+        seqs.append(s)
+    wl = synth.Workload("thousand", 1, 12288, 16, 32, 8, 128, "bf16", 88,
+                        synth.permutation((88, 1), 12288), ops, seqs)
+    orc = OracleRun(wl)
+    cache, run = make(wl, zero=False, path=path)
+    so, co = orc.reserve_step()
+    qh = orc.write_step(0, so, co)
+    _, k, v = wl.step_values(0)
+    sg, pg = run.reserve(seqs)
+    assert list(sg) == so and [tuple(p) for p in pg] == co
+    run.write(sg, pg, k, v)
+    ref = orc.attend(0, qh)
+    for key, got in attend_four_ways(cache, run, wl, qh).items():
+        if key[1] == path:
+            assert max_err(got, ref) <= TOL["bf16"], key
+    assert np.array_equal(host_bits(cache.k), orc.st.K)
+    check_status(cache)

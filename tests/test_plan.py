@@ -45,7 +45,7 @@ def check_plan(bm, plan, seqs, G, min_tokens):
     for s in segs:
         n = int(s["b1"] - s["b0"])
         if plan["kernel"] == 3:  # tcgen05
-            base, piece = 8 * (4 if s["ncols"] <= 16 else 5), 16 * 32
+            base, piece = 8 * (4 if s["ncols"] <= 16 else 5), 32 * 32
         else:
             assert plan["kernel"] == 2
             base, piece = 8 * (3 if s["ncols"] <= 8 else 4 if s["ncols"] <= 16 else 5), 4 * 24
