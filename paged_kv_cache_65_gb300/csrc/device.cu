@@ -549,6 +549,9 @@ kvStatus check_decode_args(const kvPool* p, int layer, const void* q, int n_q_he
 
 kvPool::~kvPool() {
   if (h_pinned) cudaFreeHost(h_pinned);
+  for (void* e : step_events)
+    if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
+  if (side_stream) cudaStreamDestroy(static_cast<cudaStream_t>(side_stream));
 }
 
 // SM count of the device a pool with device memory runs on (the current
@@ -1064,12 +1067,47 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->in_esize;
   const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->in_esize;
   const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
+  // several layers: layer l's q goes over on the side stream and layer l's
+  // output comes back on it, each ordered against the attention of that
+  // layer by an event, so that the copies overlap the other layers' kernels
+  const bool overlap = p->L > 1;
+  cudaStream_t cs = nullptr;
+  const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
+  if (overlap) {
+    if (!p->side_stream) {
+      cudaStream_t ns = nullptr;
+      if (cudaStreamCreateWithFlags(&ns, cudaStreamNonBlocking) != cudaSuccess) return KV_ERR_CUDA;
+      p->side_stream = ns;
+    }
+    if (p->step_events.size() != static_cast<size_t>(2 * p->L)) {
+      for (void* e : p->step_events)
+        if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
+      p->step_events.assign(2 * p->L, nullptr);
+      for (auto& e : p->step_events) {
+        cudaEvent_t ne = nullptr;
+        if (cudaEventCreateWithFlags(&ne, cudaEventDisableTiming) != cudaSuccess)
+          return KV_ERR_CUDA;
+        e = ne;
+      }
+    }
+    cs = static_cast<cudaStream_t>(p->side_stream);
+  }
   bool ok = true;
-  ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (!overlap)
+    ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
   ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
   ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
   ok &= cudaMemcpyAsync(d + l.slots, p->h_pinned, l.table - l.slots, cudaMemcpyHostToDevice,
                         st) == cudaSuccess;
+  if (overlap) {
+    for (int layer = 0; layer < p->L && ok; ++layer) {
+      const size_t off = layer * q_layer * p->in_esize;
+      ok &= cudaMemcpyAsync(d + l.q + off, static_cast<const unsigned char*>(h_q) + off,
+                            q_layer * p->in_esize, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+      ok &= cudaEventRecord(static_cast<cudaEvent_t>(p->step_events[2 * layer]), cs) ==
+            cudaSuccess;
+    }
+  }
   if (!ok) return KV_ERR_CUDA;
   s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
   if (s != KV_OK) return s;
@@ -1093,8 +1131,10 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
                       (planned ? l.meta_end : l.plan) - l.table, cudaMemcpyHostToDevice,
                       st) != cudaSuccess)
     return KV_ERR_CUDA;
-  const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
   for (int layer = 0; layer < p->L; ++layer) {
+    if (overlap && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->step_events[2 * layer]),
+                                       0) != cudaSuccess)
+      return KV_ERR_CUDA;
     if (planned)
       s = paged_decode_attention_planned(
           p, layer, d + l.q + layer * q_layer * p->in_esize, n_q_heads,
@@ -1108,9 +1148,19 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
                                  d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
                                  d + l.ws, staging_bytes - l.ws, stream);
     if (s != KV_OK) return s;
+    if (overlap) {
+      cudaEvent_t done = static_cast<cudaEvent_t>(p->step_events[2 * layer + 1]);
+      const size_t off = layer * q_layer * sizeof(float);
+      if (cudaEventRecord(done, st) != cudaSuccess || cudaStreamWaitEvent(cs, done, 0) != cudaSuccess ||
+          cudaMemcpyAsync(reinterpret_cast<unsigned char*>(h_out) + off, d + l.out + off,
+                          q_layer * sizeof(float), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return KV_ERR_CUDA;
+    }
   }
-  if (cudaMemcpyAsync(h_out, d + l.out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  if (!overlap &&
+      cudaMemcpyAsync(h_out, d + l.out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return KV_ERR_CUDA;
+  if (overlap && cudaStreamSynchronize(cs) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
   return KV_OK;
 }

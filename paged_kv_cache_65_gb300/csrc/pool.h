@@ -73,6 +73,11 @@ struct kvPool {
   // device staging buffer so that one copy moves it
   unsigned char* h_pinned = nullptr;
   size_t h_pinned_bytes = 0;
+  // kv_decode_step_host of a pool with several layers: a second stream and
+  // two events per layer, made on first use, so that each layer's q copy and
+  // output copy overlap the other layers' kernels (cudaStream_t / cudaEvent_t)
+  void* side_stream = nullptr;
+  std::vector<void*> step_events;  // [2 * L]: layer l's q landed; layer l's output written
 
   ~kvPool();
 };

@@ -621,7 +621,7 @@ def test_a_thousand_short_sequences(path):
     wl = synth.Workload("thousand", 1, 12288, 16, 32, 8, 128, "bf16", 88,
                         synth.permutation((88, 1), 12288), ops, seqs)
     orc = OracleRun(wl)
-    cache, run = make(wl, zero=False, path=path)
+    cache, run = make(wl, path=path)
     so, co = orc.reserve_step()
     qh = orc.write_step(0, so, co)
     _, k, v = wl.step_values(0)
