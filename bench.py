@@ -50,12 +50,12 @@ DEFAULT_WORKLOAD = "pool36"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331453440 + 3433472, "sha": "7be3a560954942c3"},
-    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170882816 + 3297536, "sha": "7be3a560954942c3"},
-    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615871232 + 5789952, "sha": "7be3a560954942c3"},
-    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169170432 + 3505408, "sha": "7be3a560954942c3"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331455232 + 3393536, "sha": "1de2ae01208cd982"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170890496 + 3274752, "sha": "1de2ae01208cd982"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1616025344 + 6167552, "sha": "1de2ae01208cd982"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169174784 + 3461888, "sha": "1de2ae01208cd982"},
     # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
-    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464092672 + 6120960, "sha": "7be3a560954942c3"},
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464034560 + 6081024, "sha": "1de2ae01208cd982"},
     ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165433088 + 32934400, "sha": "30f83f19435cbb38"},
 }
 
