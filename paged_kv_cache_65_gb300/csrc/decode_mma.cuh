@@ -81,6 +81,22 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
       : "r"(w));
 }
 
+// 8-bit transposing load of a 16 x 16 byte tile (lanes 0-15 give the row
+// addresses): lane 4g + t receives the bytes of rows 4t .. 4t + 3 in column g
+// (r0) and in column g + 8 (r1), lowest row in the lowest byte (layout
+// checked on the GPU with a tile of known bytes).
+__device__ __forceinline__ void ldsm8_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+// FP8 pass: the token of a 16-token tile that k-slot k of the P.V MMA (and
+// row k of S^T) stands for, so that ldsm8_t's rows 4t .. 4t + 3 land in the
+// slots 2t, 2t + 1, 2t + 8, 2t + 9 an A fragment gives lane (g, t); the sum
+// over tokens does not depend on their order, so S^T's rows take the same one.
+__device__ __forceinline__ int f8_tok(int k) { return 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3); }
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -95,61 +111,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Tokens per stage of the tensor-core pass: 64 tokens (16 KiB of K and 16
-// KiB of V at D = 128 in bf16, 8 KiB each in FP8).
-constexpr int mma_stage_tokens(int D) { return 16 * 4 * (D == 64 ? 2 : 1); }
+// KiB of V at D = 128 in bf16), 128 in FP8 (16 KiB of codes each).
+constexpr int mma_stage_tokens(int D, bool f8 = false) {
+  return f8 ? 128 : 16 * 4 * (D == 64 ? 2 : 1);
+}
+
+// Rows per TMA box for block size B and TS-token stages: a whole block when
+// it divides the stage, else the stage, else half of it (an FP8 stage of 128
+// tokens over blocks of 64 k + 64 rows); boxes never cross a block.
+constexpr int mma_box_rows(int B, int TS) {
+  return B < TS ? B : (B % TS == 0 ? TS : TS / 2);
+}
 
 // F8: the pool holds E4M3 codes and the contractions run on fp16 operands
 // (codes convert exactly).  S = K . Q^T is unchanged by any permutation of
 // the head dimension applied to both operands, so the A fragments of K take
 // d = 16 ks + 4 t .. 4 t + 3 (four consecutive codes, one 32-bit load per
-// row, two conversions) and Q's fragments the same dimensions; V needs its
-// transpose, so each warp converts its 16-token V tile into a private fp16
-// buffer laid out like a bf16 stage tile and reads it with ldmatrix.trans.
+// row, two conversions) and Q's fragments the same dimensions; V's transpose
+// comes from the 8-bit transposing ldmatrix (ldsm8_t), whose byte order fixes
+// the order of the tile's tokens in both contractions (f8_tok), and is
+// converted to fp16 in registers.  FP8 stages hold 128 tokens (16 KiB of
+// codes each of K and V): every consumer warp then takes two 16-token tiles
+// of a stage, whose dependency chains the unrolled tile loop interleaves.
 template <int D, int G, bool F8 = false>
 struct MmaCfg {
-  static constexpr int TS = mma_stage_tokens(D);  // tokens per stage
+  static constexpr int TS = mma_stage_tokens(D, F8);  // tokens per stage
   static constexpr int TILES = TS / 16;           // 16-token tiles per stage
   static constexpr int KS = D / 16;               // k-steps of Q.K and m-tiles of O^T
   static constexpr int ESZ = F8 ? 1 : 2;          // bytes per stored element
   static constexpr int HALVES = F8 ? 1 : D / 64;  // 128-byte swizzled boxes per row set
   static constexpr int HALF_BYTES = TS * 128;     // one box column of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * ESZ;  // K (or V) per stage
-  static constexpr int PRIV_HALF = 16 * 128;        // F8: one half of a converted tile
-  static constexpr int PRIV_BYTES = F8 ? 2 * PRIV_HALF : 0;  // F8: the V tile of a warp
+
   static constexpr int NST = 3;                   // stages in the ring
   static constexpr int CC = 4;                    // columns per combine pass
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!F8 || D == 128, "FP8 rows are 128 codes");
   static_assert(G >= 1 && G <= 8, "group size");
-  static_assert(TILES % kConsumerWarps == 0, "whole tiles per warp");
+  static_assert(TILES % ((F8 ? 2 : 1) * kConsumerWarps) == 0, "whole tiles (pairs) per warp");
 };
-
-// One warp: rows row0 .. row0 + 15 of an FP8 stage (128-byte rows, 128-byte
-// swizzle) into an fp16 tile of 16 rows x two 64-element halves with the
-// same swizzle (the layout the bf16 pass reads from its stage).  Each
-// 8-lane phase takes chunks 0-3 of one row and 4-7 of the next (or the
-// reverse), so that its 16-byte loads and its stores each fall on eight
-// distinct bank groups.
-__device__ __forceinline__ void fp8_tile_to_f16(uint32_t st, uint32_t dst, int row0, int lane) {
-  const int q = lane >> 3, k = lane & 7;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 2 * (2 * i + (q >> 1)) + (k >> 2);  // rows 0..15
-    const int c = k ^ ((q & 1) << 2);                // 16-code chunk 0..7
-    const int R = row0 + r;
-    uint32_t w0, w1, w2, w3;
-    lds128(st + R * 128 + ((c ^ (R & 7)) << 4), w0, w1, w2, w3);
-    uint32_t h[8];
-    e4m3x4_to_f16(w0, h[0], h[1]);
-    e4m3x4_to_f16(w1, h[2], h[3]);
-    e4m3x4_to_f16(w2, h[4], h[5]);
-    e4m3x4_to_f16(w3, h[6], h[7]);
-    const uint32_t hb = dst + (c >> 2) * (16 * 128) + r * 128;
-    const int j0 = (c & 3) * 2;
-    sts128(hb + ((j0 ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
-    sts128(hb + (((j0 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
-  }
-}
 
 // Piece descriptors the producer can publish ahead of the consumers.
 constexpr int kPieceRing = 4;
@@ -207,7 +207,6 @@ template <int D, int G, bool F8 = false>
 constexpr int decode_mma_smem_bytes() {
   using C = MmaCfg<D, G, F8>;
   return 2 * C::NST * C::STAGE_BYTES        // K and V stages
-         + kConsumerWarps * C::PRIV_BYTES   // F8: converted tiles
          + kConsumerWarps * C::CC * D * 4   // combine: O per warp, CC columns at a time
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
@@ -293,8 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE_BYTES;
-  unsigned char* priv = v_st + NST * C::STAGE_BYTES;  // F8: converted tiles
-  float* cmb_o = reinterpret_cast<float*>(priv + kConsumerWarps * C::PRIV_BYTES);
+  float* cmb_o = reinterpret_cast<float*>(v_st + NST * C::STAGE_BYTES);
   float* cmb_ml = cmb_o + kConsumerWarps * C::CC * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * 8 * 2);
   uint64_t* empty = full + NST;
@@ -309,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int lane = threadIdx.x & 31;
   const int B = a.block_size;
   const int H = a.n_kv_heads;
-  const int UR = B < C::TS ? B : C::TS;      // rows per TMA box (a multiple of 8)
-  const int SB = B < C::TS ? C::TS / B : 1;  // boxes per stage
+  const int UR = mma_box_rows(B, C::TS);     // rows per TMA box (a multiple of 8)
+  const int SB = C::TS / UR;                 // boxes per stage
   const int STG = SB * UR;                   // tokens per stage
   const uint32_t unit_bytes = (uint32_t)UR * D * C::ESZ;  // K (or V) bytes of one box row set
 
@@ -649,48 +647,130 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nvalid = p.tok_end - tok0 < STG ? p.tok_end - tok0 : STG;
       const uint32_t kb = k_base + slot * C::STAGE_BYTES;
       const uint32_t vb = v_base + slot * C::STAGE_BYTES;
+      if constexpr (F8) {
+        // two tiles per pass, tt and tt + WT: their K.Q^T chains, their
+        // softmax and their V products interleave, and one running-max
+        // update covers both (the second may lie past the context: its
+        // scores are masked to -inf and its V rows zeroed)
+#pragma unroll 1
+        for (int tt = wt; tt < C::TILES; tt += 2 * WT) {
+          if (tt * 16 >= nvalid) break;
+          int rlo[2], rhi[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            // rows g and g + 8 of S^T stand for tokens f8_tok(g), f8_tok(g + 8)
+            rlo[i] = (tt + i * WT) * 16 + f8_tok(g);
+            rhi[i] = (tt + i * WT) * 16 + f8_tok(g + 8);
+          }
+          // ---- S^T = K . Q^T: codes 16 ks + 4 t .. + 3 of each token row,
+          // one 32-bit load each, straight into fp16; two chains per tile
+          float s[2][4], s2[2][4];
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[i][j] = s2[i][j] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < C::KS; ++ks) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint32_t wa, wb, a0, a1, a2, a3;
+              asm volatile("ld.shared.b32 %0, [%1];"
+                           : "=r"(wa)
+                           : "r"(kb + rlo[i] * 128 + t * 4 +
+                                 (static_cast<uint32_t>(ks ^ (rlo[i] & 7)) << 4)));
+              asm volatile("ld.shared.b32 %0, [%1];"
+                           : "=r"(wb)
+                           : "r"(kb + rhi[i] * 128 + t * 4 +
+                                 (static_cast<uint32_t>(ks ^ (rhi[i] & 7)) << 4)));
+              e4m3x4_to_f16(wa, a0, a2);
+              e4m3x4_to_f16(wb, a1, a3);
+              if (ks & 1)
+                mma_f16(s2[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              else
+                mma_f16(s[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+          }
+          // ---- scale, mask, max over both tiles per column
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const bool v0 = rlo[i] < nvalid, v1 = rhi[i] < nvalid;
+            s[i][0] = v0 ? (s[i][0] + s2[i][0]) * a.qscale : -INFINITY;
+            s[i][1] = v0 ? (s[i][1] + s2[i][1]) * a.qscale : -INFINITY;
+            s[i][2] = v1 ? (s[i][2] + s2[i][2]) * a.qscale : -INFINITY;
+            s[i][3] = v1 ? (s[i][3] + s2[i][3]) * a.qscale : -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(s[i][0], s[i][2]));
+            mx1 = fmaxf(mx1, fmaxf(s[i][1], s[i][3]));
+          }
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+          const float al0 = exp2_approx(m_run[0] - mn0), al1 = exp2_approx(m_run[1] - mn1);
+          m_run[0] = mn0;
+          m_run[1] = mn1;
+          // ---- P^T fragments (P <= 1 in fp16: 11 bits, far inside the
+          // tolerance), transposed
+          uint32_t bh[2][2];
+          float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float p0 = exp2_approx(s[i][0] - mn0), p1 = exp2_approx(s[i][1] - mn1);
+            const float p2 = exp2_approx(s[i][2] - mn0), p3 = exp2_approx(s[i][3] - mn1);
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            bh[i][0] = movm_t(pack_f16(p0, p1));
+            bh[i][1] = movm_t(pack_f16(p2, p3));
+          }
+          l_run[0] = l_run[0] * al0 + ls0;
+          l_run[1] = l_run[1] * al1 + ls1;
+          if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
+#pragma unroll
+            for (int mt = 0; mt < C::KS; ++mt) {
+              o[mt][0] *= al0;
+              o[mt][1] *= al1;
+              o[mt][2] *= al0;
+              o[mt][3] *= al1;
+            }
+          }
+          // ---- V^T fragments straight from the codes: one 8-bit transposing
+          // load per tile and m-tile (16 dimensions = one 16-byte chunk of the
+          // 16 token rows, 128-byte swizzle) gives lane (g, t) tokens
+          // 4t .. 4t + 3 of dimensions g and g + 8, converted exactly to
+          // fp16; tokens past the context are zeroed (unused slots may hold
+          // NaN codes, and 0 * NaN would reach the sum)
+          uint32_t vrow[2], vsw[2], mlo[2], mhi[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int vr = (tt + i * WT) * 16 + (lane & 15);
+            const int nv = nvalid - (tt + i * WT) * 16;
+            vrow[i] = vb + vr * 128;
+            vsw[i] = vr & 7;
+            mlo[i] = (4 * t < nv ? 0x0000ffffu : 0u) | (4 * t + 1 < nv ? 0xffff0000u : 0u);
+            mhi[i] = (4 * t + 2 < nv ? 0x0000ffffu : 0u) | (4 * t + 3 < nv ? 0xffff0000u : 0u);
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::KS; ++mt) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint32_t r0, r1, a0, a1, a2, a3;
+              ldsm8_t(vrow[i] + ((static_cast<uint32_t>(mt) ^ vsw[i]) << 4), r0, r1);
+              e4m3x4_to_f16(r0, a0, a2);
+              e4m3x4_to_f16(r1, a1, a3);
+              mma_f16(o[mt], a0 & mlo[i], a1 & mlo[i], a2 & mhi[i], a3 & mhi[i], bh[i][0],
+                      bh[i][1]);
+            }
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int tt = wt; tt < C::TILES; tt += WT) {
         if (tt * 16 >= nvalid) break;
-        // V source: the stage itself, or (F8) this warp's converted copy
-        uint32_t vt = vb;
-        int hb = C::HALF_BYTES, rsub = 0;
-        if constexpr (F8) {
-          const uint32_t pv = smem_u32(priv) + warp * C::PRIV_BYTES;
-          __syncwarp();  // the previous tile's reads of the buffer are done
-          fp8_tile_to_f16(vb, pv, tt * 16, lane);
-          __syncwarp();
-          vt = pv;
-          hb = C::PRIV_HALF;
-          rsub = tt * 16;
-        }
-        auto mma16 = [&](float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                         uint32_t b0, uint32_t b1) {
-          if constexpr (F8)
-            mma_f16(d, a0, a1, a2, a3, b0, b1);
-          else
-            mma_bf16(d, a0, a1, a2, a3, b0, b1);
-        };
         // ---- S^T = K . Q^T (two independent accumulator chains)
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (F8) {
-          // rows g and g + 8 of the tile (same swizzle phase g): codes
-          // 16 ks + 4 t .. + 3, one 32-bit load each, straight into fp16
-          const uint32_t ra = kb + (tt * 16 + g) * 128 + t * 4;
-#pragma unroll
-          for (int ks = 0; ks < C::KS; ++ks) {
-            const uint32_t off = static_cast<uint32_t>(ks ^ g) << 4;
-            uint32_t wa, wb, a0, a1, a2, a3;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wa) : "r"(ra + off));
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wb) : "r"(ra + 8 * 128 + off));
-            e4m3x4_to_f16(wa, a0, a2);
-            e4m3x4_to_f16(wb, a1, a3);
-            if (ks & 1)
-              mma16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            else
-              mma16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-          }
-        } else {
+        {
           const int r = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
           for (int ks = 0; ks < C::KS; ++ks) {
@@ -698,9 +778,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t a0, a1, a2, a3;
             ldsm_x4(swz(kb + (d0 >> 6) * C::HALF_BYTES, r, (d0 & 63) >> 3), a0, a1, a2, a3);
             if (ks & 1)
-              mma16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              mma_bf16(s2, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             else
-              mma16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           }
         }
 #pragma unroll
@@ -727,23 +807,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         l_run[0] = l_run[0] * al0 + (p0 + p2);
         l_run[1] = l_run[1] * al1 + (p1 + p3);
         // ---- P^T fragments, transposed: bf16 high part and remainder (P
-        // keeps ~16 mantissa bits), or (F8) one fp16 part (P <= 1: 11 bits,
-        // far inside the tolerance)
-        uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-        if constexpr (F8) {
-          bh0 = movm_t(pack_f16(p0, p1));
-          bh1 = movm_t(pack_f16(p2, p3));
-        } else {
-          const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-          const uint32_t l01 = pack_bf16(p0 - __uint_as_float(h01 << 16),
-                                         p1 - __uint_as_float(h01 & 0xffff0000u));
-          const uint32_t l23 = pack_bf16(p2 - __uint_as_float(h23 << 16),
-                                         p3 - __uint_as_float(h23 & 0xffff0000u));
-          bh0 = movm_t(h01);
-          bh1 = movm_t(h23);
-          bl0 = movm_t(l01);
-          bl1 = movm_t(l23);
-        }
+        // keeps ~16 mantissa bits)
+        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+        const uint32_t l01 = pack_bf16(p0 - __uint_as_float(h01 << 16),
+                                       p1 - __uint_as_float(h01 & 0xffff0000u));
+        const uint32_t l23 = pack_bf16(p2 - __uint_as_float(h23 << 16),
+                                       p3 - __uint_as_float(h23 & 0xffff0000u));
+        const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);
+        const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
         // ---- rescale O^T (columns 2t, 2t+1) and accumulate V^T . P^T.  In a
         // partial tile the rows past the context hold whatever the pool held
         // there (possibly NaN bit patterns): their V^T elements are zeroed,
@@ -761,14 +832,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const int nv = nvalid - tt * 16;
         const int r = tt * 16 + (lane & 7) + (lane >> 4) * 8;
+        constexpr int hb = C::HALF_BYTES;
         if (nv >= 16) {
 #pragma unroll
           for (int mt = 0; mt < C::KS; ++mt) {
             const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz(vt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
-            mma16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            if constexpr (!F8) mma16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            ldsm_x4_t(swz(vb + (d0 >> 6) * hb, r, (d0 & 63) >> 3), a0, a1, a2, a3);
+            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
           }
         } else {
           const uint32_t mlo =
@@ -779,15 +851,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int mt = 0; mt < C::KS; ++mt) {
             const int d0 = mt * 16 + ((lane >> 3) & 1) * 8;
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(swz(vt + (d0 >> 6) * hb, r - rsub, (d0 & 63) >> 3), a0, a1, a2, a3);
+            ldsm_x4_t(swz(vb + (d0 >> 6) * hb, r, (d0 & 63) >> 3), a0, a1, a2, a3);
             a0 &= mlo;
             a1 &= mlo;
             a2 &= mhi;
             a3 &= mhi;
-            mma16(o[mt], a0, a1, a2, a3, bh0, bh1);
-            if constexpr (!F8) mma16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
           }
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);

@@ -85,10 +85,9 @@ kvStatus ensure_device(kvPool* p) {
     return KV_ERR_CUDA;
   if (p->dtype == KV_DTYPE_FP8_E4M3) {
     // FP8 codes: only the warp-level MMA pass, one 128-byte swizzled box
-    // (128 codes, all of D_h = 128) by min(B, 64) rows
+    // (128 codes, all of D_h = 128) by mma_box_rows(B, 128) rows
     if (!pool_tensor_core_shape(p)) return KV_ERR_UNSUPPORTED;
-    const int tsm = pkv::mma_stage_tokens(p->D);
-    const int rm = p->B < tsm ? p->B : tsm;
+    const int rm = pkv::mma_box_rows(p->B, pkv::mma_stage_tokens(p->D, true));
     kvStatus s = encode_cache_map(p, p->k, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
     if (s != KV_OK) return s;
     s = encode_cache_map(p, p->v, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));
@@ -105,8 +104,7 @@ kvStatus ensure_device(kvPool* p) {
     if (s != KV_OK) return s;
     // tensor-core passes: rows of 64 bf16 (128 bytes) with the 128-byte swizzle
     if (pool_tensor_core_shape(p)) {
-      const int tsm = pkv::mma_stage_tokens(p->D);
-      const int rm = p->B < tsm ? p->B : tsm;
+      const int rm = pkv::mma_box_rows(p->B, pkv::mma_stage_tokens(p->D));
       s = encode_cache_map(p, p->k, 64, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
       if (s != KV_OK) return s;
       s = encode_cache_map(p, p->v, 64, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[3]));

@@ -91,7 +91,10 @@ def test_fp8_small_planned_pass():
     assert cache.kv_pool_device_status() == 0
 
 
-@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (4, 32), (8, 64), (8, 16)])
+# block sizes below, at and above the 128-token FP8 stage, and one (192) whose
+# blocks the stage covers in 64-row boxes
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (4, 32), (8, 64), (8, 16), (4, 128), (2, 192),
+                                 (1, 256)])
 def test_fp8_ragged_shapes(G, B):
     ctxs = [1, 2, B - 1, B, B + 1, 3 * B + 2, 97, 700]
     wl = fp8_workload("fp8_ragged", G, B, 10 + G + B, ctxs, k_scale=0.25, v_scale=4.0)
