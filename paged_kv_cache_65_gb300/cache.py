@@ -344,22 +344,36 @@ class PagedKVCache:
     def kv_decode_step_host(self, seq_ids, n_q_heads, max_blocks, h_q, h_k_new, h_v_new, h_out,
                             staging, scale=0.0, stream=None):
         ids = seq_ids
-        if not (isinstance(ids, np.ndarray) and ids.dtype == np.int32 and ids.flags.c_contiguous):
-            ids = i32(seq_ids)
-        check(lib.kv_decode_step_host(self.handle, ids.ctypes.data, ids.size, n_q_heads,
+        if ids is self._step_ids:
+            addr = self._step_ids_addr  # the same int32 array as last call: same buffer
+        else:
+            if not (isinstance(ids, np.ndarray) and ids.dtype == np.int32
+                    and ids.flags.c_contiguous):
+                ids = i32(seq_ids)
+            addr = ids.ctypes.data
+            if ids is seq_ids:  # the caller's own array: kept, so its buffer stays put
+                self._step_ids, self._step_ids_addr = ids, addr
+        check(lib.kv_decode_step_host(self.handle, addr, ids.size, n_q_heads,
                                       max_blocks, _addr(h_q), _addr(h_k_new), _addr(h_v_new),
                                       scale, _addr(h_out), _addr(staging), _nbytes(staging),
                                       self._raw_stream() if stream is None else _stream(stream)),
               "kv_decode_step_host")
 
+    _step_ids = None
+    _step_ids_addr = 0
+    _stream_fn = None
+
     def _raw_stream(self) -> int:
         """The current torch stream of this pool's device as a raw handle."""
-        import torch
+        if self._stream_fn is None:
+            import torch
 
-        dev = self.k.device.index if self.k is not None and self.k.device.index is not None \
-            else torch.cuda.current_device()
-        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-        return raw(dev) if raw is not None else torch.cuda.current_stream(dev).cuda_stream
+            dev = self.k.device.index if self.k is not None and self.k.device.index is not None \
+                else torch.cuda.current_device()
+            raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            self._stream_fn = (lambda: raw(dev)) if raw is not None else \
+                (lambda: torch.cuda.current_stream(dev).cuda_stream)
+        return self._stream_fn()
 
 
 def _addr(x) -> int:

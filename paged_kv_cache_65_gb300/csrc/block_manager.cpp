@@ -154,10 +154,9 @@ void record_tokens(kvPool* p, kvSeq& s, const int32_t* ids, int n) {
   }
 }
 
-// One token for `seq` (creating it if new).  Caller has already checked
-// that a free block is available whenever this needs one.
-void append_one(kvPool* p, int32_t seq_id, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
-  kvSeq& s = p->seqs[seq_id];
+// One token for sequence s.  Caller has already checked that a free block
+// is available whenever this needs one.
+void append_one(kvPool* p, kvSeq& s, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
   const int64_t j = s.len / p->B;  // logical block
   const int64_t o = s.len % p->B;  // offset in block
   *cow_src = -1;
@@ -180,31 +179,41 @@ void append_one(kvPool* p, int32_t seq_id, int64_t* slot, int32_t* cow_src, int3
 }
 
 // Blocks a batch of single-token appends would take from the free list,
-// counting copy-on-writes with the counts as they evolve inside the batch.
-int64_t blocks_needed(const kvPool* p, const int32_t* seq_ids, int n) {
-  std::unordered_map<int32_t, int32_t> drop;  // tail id -> counts dropped so far
+// counting copy-on-writes with the counts as they evolve inside the batch
+// (seqs[i]: the i-th listed sequence, nullptr for a new one).
+int64_t blocks_needed(const kvPool* p, kvSeq* const* seqs, int n) {
+  std::unordered_map<int32_t, int32_t> drop;  // shared tail id -> counts dropped so far
   int64_t need = 0;
   for (int i = 0; i < n; ++i) {
-    auto it = p->seqs.find(seq_ids[i]);
-    if (it == p->seqs.end()) {
+    const kvSeq* s = seqs[i];
+    if (!s) {
       need += 1;
       continue;
     }
-    const kvSeq& s = it->second;
-    const int64_t j = s.len / p->B;
-    if (j == static_cast<int64_t>(s.table.size())) {
+    const int64_t j = s->len / p->B;
+    if (j == static_cast<int64_t>(s->table.size())) {
       need += 1;
     } else {
-      int32_t tail = s.table[j];
-      int32_t cnt = p->ref[tail] - drop[tail];
-      if (cnt > 1) {
+      const int32_t tail = s->table[j];
+      if (p->ref[tail] <= 1) continue;  // a private tail takes the token in place
+      int32_t& d = drop[tail];
+      if (p->ref[tail] - d > 1) {
         need += 1;
-        drop[tail] += 1;
+        d += 1;
       }
     }
   }
   return need;
 }
+
+// Per-thread working arrays of the batch reservation (reused across calls).
+struct AppendScratch {
+  std::vector<int32_t> sorted;
+  std::vector<kvSeq*> seqs;
+  std::vector<const kvSeq*> cseqs;
+  std::vector<int64_t> first_full;
+};
+thread_local AppendScratch t_append;
 
 }  // namespace
 
@@ -441,34 +450,43 @@ kvStatus seq_append_slots_ids(kvPool* p, const int32_t* seq_ids, int n_seq,
                               int32_t* out_cow_pairs, int* out_n_cow) {
   if (!p || n_seq < 0 || (n_seq > 0 && (!seq_ids || !out_slots || !out_cow_pairs)))
     return KV_ERR_INVALID_ARG;
+  AppendScratch& sc = t_append;
   {
-    std::vector<int32_t> sorted(seq_ids, seq_ids + n_seq);
+    std::vector<int32_t>& sorted = sc.sorted;
+    sorted.assign(seq_ids, seq_ids + n_seq);
     std::sort(sorted.begin(), sorted.end());
     if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return KV_ERR_INVALID_ARG;
   }
+  // each listed sequence looked up once (elements of the map keep their
+  // addresses when others are inserted)
+  std::vector<kvSeq*>& seqs = sc.seqs;
+  seqs.assign(n_seq, nullptr);
   for (int i = 0; i < n_seq; ++i) {
     auto it = p->seqs.find(seq_ids[i]);
-    if (it != p->seqs.end() && it->second.len >= (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
+    if (it == p->seqs.end()) continue;
+    if (it->second.len >= (int64_t(1) << 40)) return KV_ERR_INVALID_ARG;
+    seqs[i] = &it->second;
   }
-  if (blocks_needed(p, seq_ids, n_seq) > available(p)) return KV_ERR_NO_FREE_BLOCK;
-  std::vector<int64_t> first_full(n_seq, 0);
-  for (int i = 0; i < n_seq; ++i) {
-    auto it = p->seqs.find(seq_ids[i]);
-    first_full[i] = it == p->seqs.end() ? 0 : it->second.len / p->B;
-  }
+  if (blocks_needed(p, seqs.data(), n_seq) > available(p)) return KV_ERR_NO_FREE_BLOCK;
+  std::vector<int64_t>& first_full = sc.first_full;
+  first_full.assign(n_seq, 0);
+  for (int i = 0; i < n_seq; ++i) first_full[i] = seqs[i] ? seqs[i]->len / p->B : 0;
   int n_cow = 0;
   for (int i = 0; i < n_seq; ++i) {
+    if (!seqs[i]) seqs[i] = &p->seqs[seq_ids[i]];  // a new sequence
     int32_t src, dst;
-    append_one(p, seq_ids[i], &out_slots[i], &src, &dst);
+    append_one(p, *seqs[i], &out_slots[i], &src, &dst);
     if (src >= 0) {
       out_cow_pairs[2 * n_cow] = src;
       out_cow_pairs[2 * n_cow + 1] = dst;
       ++n_cow;
     }
   }
-  for (int i = 0; i < n_seq; ++i)
-    record_tokens(p, p->seqs[seq_ids[i]], token_ids ? token_ids + i : nullptr, 1);
-  for (int i = 0; i < n_seq; ++i) pc_publish(p, seq_ids[i], first_full[i]);
+  if (p->pc_on) {
+    for (int i = 0; i < n_seq; ++i)
+      record_tokens(p, *seqs[i], token_ids ? token_ids + i : nullptr, 1);
+    for (int i = 0; i < n_seq; ++i) pc_publish(p, seq_ids[i], first_full[i]);
+  }
   if (out_n_cow) *out_n_cow = n_cow;
   return KV_OK;
 }
@@ -496,7 +514,7 @@ kvStatus seq_append_tokens_ids(kvPool* p, int32_t seq, int n_tokens, const int32
   int n_cow = 0;
   for (int i = 0; i < n_tokens; ++i) {
     int32_t src, dst;
-    append_one(p, seq, &out_slots[i], &src, &dst);
+    append_one(p, p->seqs[seq], &out_slots[i], &src, &dst);
     if (src >= 0) {
       out_cow_pair[0] = src;
       out_cow_pair[1] = dst;
@@ -611,14 +629,17 @@ kvStatus seq_block_table(const kvPool* p, const int32_t* seq_ids, int n_seq, int
   if (!p || n_seq < 0 || max_blocks < 0 || (n_seq > 0 && (!seq_ids || !out_context_lens)))
     return KV_ERR_INVALID_ARG;
   if (n_seq > 0 && max_blocks > 0 && !out_table) return KV_ERR_INVALID_ARG;
+  std::vector<const kvSeq*>& seqs = t_append.cseqs;
+  seqs.assign(n_seq, nullptr);
   for (int i = 0; i < n_seq; ++i) {
     auto it = p->seqs.find(seq_ids[i]);
     if (it == p->seqs.end()) return KV_ERR_INVALID_ARG;
     if (static_cast<int64_t>(it->second.table.size()) > max_blocks) return KV_ERR_INVALID_ARG;
     if (it->second.len > INT32_MAX) return KV_ERR_INVALID_ARG;
+    seqs[i] = &it->second;
   }
   for (int i = 0; i < n_seq; ++i) {
-    const kvSeq& s = p->seqs.find(seq_ids[i])->second;
+    const kvSeq& s = *seqs[i];
     int32_t* row = out_table + static_cast<int64_t>(i) * max_blocks;
     const int nb = static_cast<int>(s.table.size());
     if (nb) std::memcpy(row, s.table.data(), sizeof(int32_t) * nb);

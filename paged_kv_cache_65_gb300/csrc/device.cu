@@ -455,6 +455,15 @@ __global__ void __launch_bounds__(kMergePlanWarps * 32) merge_plan_kernel(
   for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const long long ob = ((long long)s * Hq + hq) * D + lane * DL;
+  if constexpr (DL == 4) {
+    if (out_f32 && (reinterpret_cast<uintptr_t>(out_f32) & 15u) == 0u) {
+      // one 16-byte store per lane (the output may be page-locked host
+      // memory written in place, which whole vectors cross in fewer writes)
+      *reinterpret_cast<float4*>(out_f32 + ob) =
+          make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+      return;
+    }
+  }
 #pragma unroll
   for (int d = 0; d < DL; ++d) {
     if (out_f32)
@@ -957,6 +966,18 @@ struct StepLayout {
   size_t q, k, v, slots, pairs, table, lens, plan, meta_end, out, ws, total;
 };
 
+// The device address of a caller's host buffer that is page-locked and
+// mapped into the device's address space (cudaMallocHost / cudaHostAlloc, or
+// a mapped cudaHostRegister, under unified addressing), else nullptr.
+void* host_mapped(const void* h) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear this call's own error
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 StepLayout step_layout(const kvPool* p, int n_seq, int n_q_heads, int max_blocks) {
   StepLayout l;
   const size_t L = p->L, n = n_seq;
@@ -1053,22 +1074,25 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   int32_t* h_table = reinterpret_cast<int32_t*>(hm + l.table);
   int32_t* h_lens = reinterpret_cast<int32_t*>(hm + l.lens);
   unsigned char* h_plan = hm + l.plan;
-  // host: reserve (all or nothing)
-  int n_cow = 0;
-  s = seq_append_slots(p, seq_ids, n_seq, h_slots, h_pairs, &n_cow);
-  if (s != KV_OK) return s;
-  // host -> device: q, new K and V from the caller's buffers, then the slots
-  // and copy pairs; the device copies the shared tails and writes the new
-  // tokens while the host builds the tables and the plan
   cudaStream_t st = as_stream(stream);
   unsigned char* d = reinterpret_cast<unsigned char*>(d_staging);
   const size_t qb = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * p->in_esize;
   const size_t kb = static_cast<size_t>(p->L) * n_seq * p->H * p->D * p->in_esize;
   const size_t ob = static_cast<size_t>(p->L) * n_seq * n_q_heads * p->D * sizeof(float);
-  // several layers: layer l's q goes over on the side stream and layer l's
-  // output comes back on it, each ordered against the attention of that
-  // layer by an event, so that the copies overlap the other layers' kernels
-  const bool overlap = p->L > 1;
+  // the caller's buffers, where the device can address them in place
+  // (page-locked host memory mapped into its address space): the kernels
+  // then read q and the new K / V rows and the merge writes the outputs
+  // through the mapping, with no staging copy; other buffers are copied
+  const unsigned char* mq = static_cast<const unsigned char*>(host_mapped(h_q));
+  const void* mk = host_mapped(h_k_new);
+  const void* mv = host_mapped(h_v_new);
+  float* mo = static_cast<float*>(host_mapped(h_out));
+  const bool kv_direct = mk != nullptr && mv != nullptr;
+  // several layers: layer l's q goes over on the side stream (and, when
+  // copied back, layer l's output too), each ordered against the attention
+  // of that layer by an event, so that the copies overlap the other layers'
+  // kernels
+  const bool overlap = p->L > 1 && (!mq || !mo);
   cudaStream_t cs = nullptr;
   const size_t q_layer = static_cast<size_t>(n_seq) * n_q_heads * p->D;
   if (overlap) {
@@ -1090,14 +1114,23 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
     }
     cs = static_cast<cudaStream_t>(p->side_stream);
   }
+  // a step that fails after its copies were issued waits for them before
+  // returning, so that the caller may reuse its buffers at once
+  auto fail = [&](kvStatus e) {
+    if (overlap) cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(st);
+    return e;
+  };
+  // host -> device, first: what needs no reservation (q; K and V unless
+  // read in place), so that the copies run while the host reserves
   bool ok = true;
-  if (!overlap)
+  if (!overlap && !mq)
     ok &= cudaMemcpyAsync(d + l.q, h_q, qb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok &= cudaMemcpyAsync(d + l.slots, p->h_pinned, l.table - l.slots, cudaMemcpyHostToDevice,
-                        st) == cudaSuccess;
-  if (overlap) {
+  if (!kv_direct) {
+    ok &= cudaMemcpyAsync(d + l.k, h_k_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    ok &= cudaMemcpyAsync(d + l.v, h_v_new, kb, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  }
+  if (overlap && !mq) {
     for (int layer = 0; layer < p->L && ok; ++layer) {
       const size_t off = layer * q_layer * p->in_esize;
       ok &= cudaMemcpyAsync(d + l.q + off, static_cast<const unsigned char*>(h_q) + off,
@@ -1106,16 +1139,14 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
             cudaSuccess;
     }
   }
-  if (!ok) return KV_ERR_CUDA;
-  s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
-  if (s != KV_OK) return s;
-  s = reshape_and_cache(p, -1, d + l.k, d + l.v, reinterpret_cast<const int64_t*>(d + l.slots),
-                        n_seq, stream);
-  if (s != KV_OK) return s;
-  // host: tables, and the sharing-aware plan of the tensor-core passes
-  // (shared blocks read once); then their copy, which the attention waits for
+  if (!ok) return fail(KV_ERR_CUDA);
+  // host: reserve (all or nothing), the tables, and the sharing-aware plan
+  // of the tensor-core passes (shared blocks read once)
+  int n_cow = 0;
+  s = seq_append_slots(p, seq_ids, n_seq, h_slots, h_pairs, &n_cow);
+  if (s != KV_OK) return fail(s);
   s = seq_block_table(p, seq_ids, n_seq, max_blocks, h_table, h_lens);
-  if (s != KV_OK) return s;
+  if (s != KV_OK) return fail(s);
   const int G = n_q_heads / p->H;
   const bool planned = decode_kernel(p) != kKernelCudaCores && ilog2_small(G) >= 0 &&
                        (p->D == 64 || p->D == 128);
@@ -1123,41 +1154,66 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
     size_t ws_need = 0;
     s = paged_decode_plan(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, h_plan,
                           paged_decode_plan_bytes(p, n_seq, n_q_heads), &ws_need);
-    if (s != KV_OK) return s;
+    if (s != KV_OK) return fail(s);
   }
-  if (cudaMemcpyAsync(d + l.table, p->h_pinned + (l.table - l.slots),
-                      (planned ? l.meta_end : l.plan) - l.table, cudaMemcpyHostToDevice,
-                      st) != cudaSuccess)
-    return KV_ERR_CUDA;
+  // the step's metadata (slots, copy pairs, tables, lengths, plan) in one copy
+  if (cudaMemcpyAsync(d + l.slots, p->h_pinned, (planned ? l.meta_end : l.plan) - l.slots,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return fail(KV_ERR_CUDA);
+  // device: copy shared tails, write the new token in every layer, attend.
+  // With a plan on a bfloat16 or FP8 pool the split pass of each layer
+  // writes that layer's new rows itself (the CTA reading a sequence's last
+  // block writes its newest token first), one launch less per step.
+  const bool fused = planned && (p->dtype == KV_DTYPE_BF16 || p->dtype == KV_DTYPE_FP8_E4M3);
+  s = cow_copy(p, reinterpret_cast<const int32_t*>(d + l.pairs), n_cow, stream);
+  if (s != KV_OK) return fail(s);
+  const unsigned char* kn = kv_direct ? static_cast<const unsigned char*>(mk) : d + l.k;
+  const unsigned char* vn = kv_direct ? static_cast<const unsigned char*>(mv) : d + l.v;
+  if (!fused) {
+    s = reshape_and_cache(p, -1, kn, vn, reinterpret_cast<const int64_t*>(d + l.slots), n_seq,
+                          stream);
+    if (s != KV_OK) return fail(s);
+  }
+  const size_t kv_layer = static_cast<size_t>(n_seq) * p->H * p->D * p->in_esize;
   for (int layer = 0; layer < p->L; ++layer) {
-    if (overlap && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->step_events[2 * layer]),
-                                       0) != cudaSuccess)
-      return KV_ERR_CUDA;
-    if (planned)
-      s = paged_decode_attention_planned(
-          p, layer, d + l.q + layer * q_layer * p->in_esize, n_q_heads,
-          reinterpret_cast<const int32_t*>(d + l.table), max_blocks, d + l.plan, h_plan, scale,
-          d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
-          d + l.ws, staging_bytes - l.ws, stream);
-    else
-      s = paged_decode_attention(p, layer, d + l.q + layer * q_layer * p->in_esize, n_q_heads,
-                                 reinterpret_cast<const int32_t*>(d + l.table), max_blocks,
-                                 reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale,
-                                 d + l.out + layer * q_layer * sizeof(float), KV_DTYPE_F32,
-                                 d + l.ws, staging_bytes - l.ws, stream);
-    if (s != KV_OK) return s;
-    if (overlap) {
+    if (overlap && !mq &&
+        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->step_events[2 * layer]), 0) !=
+            cudaSuccess)
+      return fail(KV_ERR_CUDA);
+    const unsigned char* q = (mq ? mq : d + l.q) + layer * q_layer * p->in_esize;
+    float* out = mo ? mo + layer * q_layer
+                    : reinterpret_cast<float*>(d + l.out) + layer * q_layer;
+    const int32_t* table = reinterpret_cast<const int32_t*>(d + l.table);
+    void* ws = d + l.ws;
+    const size_t ws_bytes = staging_bytes - l.ws;
+    if (fused) {
+      s = paged_decode_partials_planned_write(p, layer, q, n_q_heads, kn + layer * kv_layer,
+                                              vn + layer * kv_layer, table, max_blocks,
+                                              d + l.plan, h_plan, scale, ws, ws_bytes, stream);
+      if (s == KV_OK)
+        s = paged_decode_merge_planned(p, n_q_heads, d + l.plan, h_plan, out, KV_DTYPE_F32, ws,
+                                       ws_bytes, stream);
+    } else if (planned) {
+      s = paged_decode_attention_planned(p, layer, q, n_q_heads, table, max_blocks, d + l.plan,
+                                         h_plan, scale, out, KV_DTYPE_F32, ws, ws_bytes, stream);
+    } else {
+      s = paged_decode_attention(p, layer, q, n_q_heads, table, max_blocks,
+                                 reinterpret_cast<const int32_t*>(d + l.lens), n_seq, scale, out,
+                                 KV_DTYPE_F32, ws, ws_bytes, stream);
+    }
+    if (s != KV_OK) return fail(s);
+    if (overlap && !mo) {
       cudaEvent_t done = static_cast<cudaEvent_t>(p->step_events[2 * layer + 1]);
       const size_t off = layer * q_layer * sizeof(float);
       if (cudaEventRecord(done, st) != cudaSuccess || cudaStreamWaitEvent(cs, done, 0) != cudaSuccess ||
           cudaMemcpyAsync(reinterpret_cast<unsigned char*>(h_out) + off, d + l.out + off,
                           q_layer * sizeof(float), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
-        return KV_ERR_CUDA;
+        return fail(KV_ERR_CUDA);
     }
   }
-  if (!overlap &&
+  if (!overlap && !mo &&
       cudaMemcpyAsync(h_out, d + l.out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return KV_ERR_CUDA;
+    return fail(KV_ERR_CUDA);
   if (overlap && cudaStreamSynchronize(cs) != cudaSuccess) return KV_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KV_ERR_CUDA;
   return KV_OK;

@@ -119,6 +119,20 @@ void plan_starts(const std::vector<PlanSeg>& segs, int64_t W, int grid, int B,
   }
 }
 
+// Working arrays of the plan builder, kept per thread so that a step's plan
+// reuses the previous one's allocations.
+struct PlanScratch {
+  std::vector<const kvSeq*> seqs;
+  std::vector<int32_t> sorted;
+  std::vector<int> n_levels, priv_from, priv_mem, node_mem0, ungrouped, order;
+  std::vector<char> grouped;
+  std::vector<PlanSeg> segs;
+  std::vector<int32_t> members;
+  std::vector<PlanEntry> entk;
+  std::vector<uint8_t> n_ent;
+};
+thread_local PlanScratch t_scratch;
+
 }  // namespace
 
 size_t plan_workspace_bytes(int n_segs, int c_max, int D) {
@@ -153,9 +167,12 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
   if (plan_bytes < paged_decode_plan_bytes(p, n_seq, n_q_heads)) return KV_ERR_INVALID_ARG;
   if (min_shared_tokens <= 0) min_shared_tokens = 128;
-  std::vector<const kvSeq*> seqs(n_seq);
+  PlanScratch& sc = t_scratch;
+  std::vector<const kvSeq*>& seqs = sc.seqs;
+  seqs.assign(n_seq, nullptr);
   {
-    std::vector<int32_t> sorted(seq_ids, seq_ids + n_seq);
+    std::vector<int32_t>& sorted = sc.sorted;
+    sorted.assign(seq_ids, seq_ids + n_seq);
     std::sort(sorted.begin(), sorted.end());
     if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return KV_ERR_INVALID_ARG;
   }
@@ -189,9 +206,11 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     int b0, b1;            // the run of blocks [b0, b1)
   };
   std::vector<Node> nodes;
-  std::vector<std::vector<int>> seq_nodes(n_seq);  // shared runs of each sequence, in order
-  std::vector<int> priv_from(n_seq, 0);            // first block read privately
-  std::vector<int> roots;                          // first node of each root group
+  std::vector<int>& n_levels = sc.n_levels;    // shared runs each sequence has joined
+  std::vector<int>& priv_from = sc.priv_from;  // first block read privately
+  n_levels.assign(n_seq, 0);
+  priv_from.assign(n_seq, 0);
+  std::vector<int> roots;  // first node of each root group
   auto run_group = [&](auto&& self, std::vector<int> mem, int s0) -> void {
     // common run from s0 among the members
     int P = full_blocks(mem[0]);
@@ -204,7 +223,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     if (P < s0) P = s0;
     int next_s0 = s0;
     bool room = true;
-    for (int m : mem) room = room && static_cast<int>(seq_nodes[m].size()) < kPlanMaxLevels;
+    for (int m : mem) room = room && n_levels[m] < kPlanMaxLevels;
     if (room && static_cast<int64_t>(P - s0) * B >= min_shared_tokens) {
       const int n_sub = static_cast<int>((mem.size() + max_members - 1) / max_members);
       size_t c0 = 0;
@@ -215,7 +234,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
         nd.b0 = s0;
         nd.b1 = P;
         for (int m : nd.mem) {
-          seq_nodes[m].push_back(static_cast<int>(nodes.size()));
+          n_levels[m] += 1;
           priv_from[m] = P;
         }
         nodes.push_back(std::move(nd));
@@ -243,11 +262,16 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     }
   };
   {
-    std::vector<int> order;
+    std::vector<int>& order = sc.order;
+    order.clear();
     for (int i = 0; i < n_seq; ++i)
       if (full_blocks(i) > 0) order.push_back(i);
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int x, int y) { return seqs[x]->table[0] < seqs[y]->table[0]; });
+    // by first block, listing order among equals (a stable sort without its
+    // temporary buffer)
+    std::sort(order.begin(), order.end(), [&](int x, int y) {
+      const int32_t bx = seqs[x]->table[0], by = seqs[y]->table[0];
+      return bx < by || (bx == by && x < y);
+    });
     for (size_t a0 = 0; a0 < order.size();) {
       size_t b0 = a0 + 1;
       while (b0 < order.size() && seqs[order[b0]]->table[0] == seqs[order[a0]]->table[0]) ++b0;
@@ -273,17 +297,23 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   // the work list instead of piling up at its end, and the wide shared
   // segments, whose blocks cost more, fall to different CTAs (the split
   // balances work units).
-  std::vector<PlanSeg> segs;
-  std::vector<int32_t> members;
+  std::vector<PlanSeg>& segs = sc.segs;
+  std::vector<int32_t>& members = sc.members;
+  segs.clear();
+  members.clear();
   segs.reserve(static_cast<size_t>(nodes.size() + n_seq) * H);
   members.reserve(static_cast<size_t>(n_seq) * (kPlanMaxLevels + 1));
   // merge entries per (sequence, head): its shared runs and its private rest
   constexpr int kEnt = kPlanMaxLevels + 1;
-  std::vector<PlanEntry> entk(static_cast<size_t>(kEnt) * n_seq * H);
-  std::vector<uint8_t> n_ent(static_cast<size_t>(n_seq) * H, 0);
+  std::vector<PlanEntry>& entk = sc.entk;  // entries of (sequence, head) sh: kEnt * sh ..
+  std::vector<uint8_t>& n_ent = sc.n_ent;   // .. + n_ent[sh] - 1
+  if (entk.size() < static_cast<size_t>(kEnt) * n_seq * H)
+    entk.resize(static_cast<size_t>(kEnt) * n_seq * H);
+  n_ent.assign(static_cast<size_t>(n_seq) * H, 0);
   auto add_entry = [&](size_t sh, PlanEntry e) { entk[kEnt * sh + n_ent[sh]++] = e; };
   int c_max = G;
-  std::vector<int> priv_mem(n_seq, -1);  // member-list slot of a sequence's private rest
+  std::vector<int>& priv_mem = sc.priv_mem;  // member-list slot of a sequence's private rest
+  priv_mem.assign(n_seq, -1);
   auto private_member = [&](int i) {
     if (priv_mem[i] < 0) {
       priv_mem[i] = static_cast<int>(members.size());
@@ -306,7 +336,8 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     segs.push_back(s);
     add_entry(static_cast<size_t>(i) * H + h, {si, 0});
   };
-  std::vector<int> node_mem0(nodes.size(), -1);  // member-list slot of each node
+  std::vector<int>& node_mem0 = sc.node_mem0;  // member-list slot of each node
+  node_mem0.assign(nodes.size(), -1);
   auto push_group_head = [&](size_t r, int h) {
     std::vector<int> grp_members;
     for (int ni = roots[r]; ni < roots[r + 1]; ++ni) {
@@ -335,10 +366,12 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
     grp_members.erase(std::unique(grp_members.begin(), grp_members.end()), grp_members.end());
     for (int m : grp_members) push_private(m, h);
   };
-  std::vector<char> grouped(n_seq, 0);
+  std::vector<char>& grouped = sc.grouped;
+  grouped.assign(n_seq, 0);
   for (const Node& nd : nodes)
     for (int m : nd.mem) grouped[m] = 1;
-  std::vector<int> ungrouped;
+  std::vector<int>& ungrouped = sc.ungrouped;
+  ungrouped.clear();
   for (int i = 0; i < n_seq; ++i)
     if (!grouped[i]) ungrouped.push_back(i);
   const size_t n_roots = roots.size() - 1;

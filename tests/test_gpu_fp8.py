@@ -146,9 +146,11 @@ def test_fp8_qwen_2k_full():
     assert cache.kv_pool_device_status() == 0
 
 
-def test_fp8_host_buffer_step():
+@pytest.mark.parametrize("pinned", [False, True])
+def test_fp8_host_buffer_step(pinned):
     # the whole-step C entry point with host buffers: bf16 q and new K/V in,
-    # quantized on the device, float32 out
+    # quantized on the device, float32 out; pageable buffers go through the
+    # staging area, page-locked ones are read and written in place
     wl = synth.workload("fp8_small")
     orc = OracleRun(wl)
     cache, run = make(wl)
@@ -160,10 +162,16 @@ def test_fp8_host_buffer_step():
         so, co = orc.reserve_step()
         q = orc.write_step(step, so, co)
         _, k, v = wl.step_values(step)
-        out = np.zeros((1, n, wl.n_q_heads, wl.head_dim), dtype=np.float32)
-        cache.kv_decode_step_host(wl.decode_seqs, wl.n_q_heads, max_blocks, q[None], k, v, out,
-                                  staging)
-        assert max_err(out[0], orc.attend(0, q)) <= TOL
+        if pinned:
+            out = torch.zeros((1, n, wl.n_q_heads, wl.head_dim), dtype=torch.float32).pin_memory()
+            args = [torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+                    for a in (q[None], k, v)]
+        else:
+            out = np.zeros((1, n, wl.n_q_heads, wl.head_dim), dtype=np.float32)
+            args = [q[None], k, v]
+        cache.kv_decode_step_host(wl.decode_seqs, wl.n_q_heads, max_blocks, *args, out, staging)
+        got = out if isinstance(out, np.ndarray) else out.numpy()
+        assert max_err(got[0], orc.attend(0, q)) <= TOL
     assert nan_code_equal(cache.k.cpu().numpy(), orc.st.K)
     assert nan_code_equal(cache.v.cpu().numpy(), orc.st.V)
     assert cache.kv_pool_device_status() == 0

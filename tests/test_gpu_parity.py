@@ -289,7 +289,29 @@ def test_bf16_output():
     assert np.all(np.abs(got - ref) <= 2e-3 + np.abs(ref) * 2.0 ** -8)
 
 
-def test_multilayer_decode_step_host_buffers():
+def host_buffer(a, pinned):
+    """A caller's host buffer: the NumPy array itself (pageable: the step copies
+    it through its staging area), or a page-locked copy that the device
+    addresses in place (new K / V read and outputs written through the
+    mapping)."""
+    if not pinned:
+        return a
+    flat = a.view(np.int16) if a.dtype == np.uint16 else a
+    return torch.from_numpy(np.ascontiguousarray(flat)).pin_memory()
+
+
+def host_out(shape, pinned):
+    if not pinned:
+        return np.zeros(shape, dtype=np.float32)
+    return torch.zeros(shape, dtype=torch.float32).pin_memory()
+
+
+def as_np(out):
+    return out if isinstance(out, np.ndarray) else out.numpy()
+
+
+@pytest.mark.parametrize("pinned", [False, True])
+def test_multilayer_decode_step_host_buffers(pinned):
     # the whole-step C entry point with host buffers, 3 layers, shared prefix
     L, B, H, G, D = 3, 8, 2, 4, 128
     # sequences 0 and 1 share a prefix whose tail block holds 3 of 8 slots:
@@ -317,11 +339,12 @@ def test_multilayer_decode_step_host_buffers():
         q = orc.write_step(step, so, co)
         qL = np.ascontiguousarray(np.broadcast_to(q, (L,) + q.shape))
         _, k, v = wl.step_values(step)
-        out = np.zeros((L, 3, H * G, D), dtype=np.float32)
-        cache.kv_decode_step_host([0, 1, 2], H * G, max_blocks, qL, k, v, out, staging)
+        out = host_out((L, 3, H * G, D), pinned)
+        cache.kv_decode_step_host([0, 1, 2], H * G, max_blocks, host_buffer(qL, pinned),
+                                  host_buffer(k, pinned), host_buffer(v, pinned), out, staging)
         for layer in range(L):
             ref = orc.attend(layer, q)
-            assert max_err(out[layer], ref) <= TOL["bf16"]
+            assert max_err(as_np(out)[layer], ref) <= TOL["bf16"]
     assert np.array_equal(host_bits(cache.k), orc.st.K)
     assert np.array_equal(host_bits(cache.v), orc.st.V)
     check_status(cache)
@@ -487,8 +510,9 @@ def test_planned_start_records_change_no_bit(name, path):
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("pinned", [False, True])
 @pytest.mark.parametrize("path", TENSOR_PATHS)
-def test_multilayer_host_step_with_long_shared_prefix(path):
+def test_multilayer_host_step_with_long_shared_prefix(path, pinned):
     # kv_decode_step_host plans the step: sequences 0-2 share 300 tokens
     L, B, H, G, D = 2, 16, 2, 4, 128
     ops = [("append", 100, 300, 0), ("fork", 100, 0), ("fork", 100, 1), ("fork", 100, 2),
@@ -516,11 +540,61 @@ def test_multilayer_host_step_with_long_shared_prefix(path):
         q = orc.write_step(step, so, co)
         qL = np.ascontiguousarray(np.broadcast_to(q, (L,) + q.shape))
         _, k, v = wl.step_values(step)
-        out = np.zeros((L, 4, H * G, D), dtype=np.float32)
-        cache.kv_decode_step_host([0, 1, 2, 3], H * G, max_blocks, qL, k, v, out, staging)
+        out = host_out((L, 4, H * G, D), pinned)
+        cache.kv_decode_step_host([0, 1, 2, 3], H * G, max_blocks, host_buffer(qL, pinned),
+                                  host_buffer(k, pinned), host_buffer(v, pinned), out, staging)
         for layer in range(L):
-            assert max_err(out[layer], orc.attend(layer, q)) <= TOL["bf16"]
+            assert max_err(as_np(out)[layer], orc.attend(layer, q)) <= TOL["bf16"]
     check_status(cache)
+
+
+@pytest.mark.parametrize("path", TENSOR_PATHS)
+def test_single_layer_host_step_page_locked_and_pageable_agree(path):
+    # one layer (the outputs come back in one piece): the same three steps,
+    # two copy-on-write copies among them, through page-locked buffers (new K / V
+    # read in place, outputs written in place) and through pageable ones
+    # (staging copies) give the same bits in the outputs and the pools, and
+    # match the oracle
+    B, H, G, D = 16, 2, 4, 128
+    ops = [("append", 100, 150, 0), ("fork", 100, 0), ("fork", 100, 1), ("append", 2, 700, 1),
+           ("append", 3, 31, 2)]
+    wl = synth.Workload("host_step", 1, 160, B, H * G, H, D, "bf16", 12,
+                        synth.permutation((12, 1), 160), ops, [0, 1, 2, 3, 100])
+    from paged_kv_cache_65_gb300 import PagedKVCache, _lib
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    results = []
+    for pinned in (False, True):
+        orc = OracleRun(wl)
+        cache = PagedKVCache(1, 160, B, H, D, "bf16", free_order=wl.free_order)
+        cache.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, path)
+        cache.k.zero_()
+        cache.v.zero_()
+        run = DeviceRun(cache, H * G)
+        for op in wl.build_ops:
+            run.apply(op, wl.append_values)
+        n, max_blocks = len(wl.decode_seqs), 64
+        staging = torch.empty(cache.kv_decode_step_staging_bytes(n, H * G, max_blocks),
+                              dtype=torch.uint8, device="cuda")
+        outs = []
+        for step in range(3):
+            so, co = orc.reserve_step()
+            assert len(co) == (2 if step == 0 else 0)  # the shared tail, for 0 and 1
+            q = orc.write_step(step, so, co)
+            _, k, v = wl.step_values(step)
+            out = host_out((1, n, H * G, D), pinned)
+            cache.kv_decode_step_host(wl.decode_seqs, H * G, max_blocks,
+                                      host_buffer(q[None], pinned), host_buffer(k, pinned),
+                                      host_buffer(v, pinned), out, staging)
+            got = as_np(out).copy()
+            assert max_err(got[0], orc.attend(0, q)) <= TOL["bf16"]
+            outs.append(got)
+        assert np.array_equal(host_bits(cache.k), orc.st.K)
+        assert np.array_equal(host_bits(cache.v), orc.st.V)
+        check_status(cache)
+        results.append(outs)
+    for a, b in zip(*results):
+        assert np.array_equal(a, b)
 
 
 @pytest.mark.parametrize("path", TENSOR_PATHS)
