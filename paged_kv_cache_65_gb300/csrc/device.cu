@@ -1151,9 +1151,12 @@ kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n
   const bool planned = decode_kernel(p) != kKernelCudaCores && ilog2_small(G) >= 0 &&
                        (p->D == 64 || p->D == 128);
   if (planned) {
+    // the per-CTA start records cost the host about as much as three or
+    // four split launches save with them (each CTA otherwise finds its
+    // first piece itself): built when the plan serves four or more layers
     size_t ws_need = 0;
-    s = paged_decode_plan(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, h_plan,
-                          paged_decode_plan_bytes(p, n_seq, n_q_heads), &ws_need);
+    s = plan_build(p, seq_ids, n_seq, n_q_heads, max_blocks, 0, h_plan,
+                   paged_decode_plan_bytes(p, n_seq, n_q_heads), &ws_need, p->L >= 4);
     if (s != KV_OK) return fail(s);
   }
   // the step's metadata (slots, copy pairs, tables, lengths, plan) in one copy

@@ -160,6 +160,15 @@ size_t paged_decode_plan_bytes(const kvPool* p, int n_seq, int n_q_heads) {
 kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
                            int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
                            size_t* out_workspace_bytes) {
+  return plan_build(p, seq_ids, n_seq, n_q_heads, max_blocks, min_shared_tokens, h_plan,
+                    plan_bytes, out_workspace_bytes, true);
+}
+
+}  // extern "C"
+
+kvStatus plan_build(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                    int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
+                    size_t* out_workspace_bytes, bool start_records) {
   if (!p || n_seq < 0 || (n_seq > 0 && !seq_ids) || !h_plan || max_blocks <= 0)
     return KV_ERR_INVALID_ARG;
   if (n_q_heads <= 0 || n_q_heads % p->H != 0) return KV_ERR_INVALID_ARG;
@@ -413,7 +422,7 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
 
   // ---- serialise (start records only where the buffer has room for them:
   // a buffer sized before the device was known holds none)
-  int grid = plan_grid(p, kernel, G);
+  int grid = start_records ? plan_grid(p, kernel, G) : 0;
   Layout l = plan_layout(n_seq, H, static_cast<int>(segs.size()),
                          static_cast<int>(members.size()), n_entries, grid);
   if (l.total > plan_bytes || W == 0) {
@@ -458,6 +467,8 @@ kvStatus paged_decode_plan(const kvPool* p, const int32_t* seq_ids, int n_seq, i
   if (out_workspace_bytes) *out_workspace_bytes = plan_workspace_bytes(hd.n_segs, c_max, p->D);
   return KV_OK;
 }
+
+extern "C" {
 
 
 // Heaviest-first order of the chunked-prefill work items.  An item is one

@@ -110,3 +110,10 @@ int pool_sm_count(const kvPool* p);
 
 // Workspace bytes of a planned decode pass (plan.cpp).
 size_t plan_workspace_bytes(int n_segs, int c_max, int D);
+
+// paged_decode_plan with the per-CTA start records optional (plan.cpp): a
+// plan without them is valid for any grid (each CTA then finds its first
+// piece itself).
+kvStatus plan_build(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,
+                    int max_blocks, int min_shared_tokens, void* h_plan, size_t plan_bytes,
+                    size_t* out_workspace_bytes, bool start_records);
