@@ -91,11 +91,20 @@ __device__ __forceinline__ void ldsm8_t(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-// FP8 pass: the token of a 16-token tile that k-slot k of the P.V MMA (and
-// row k of S^T) stands for, so that ldsm8_t's rows 4t .. 4t + 3 land in the
-// slots 2t, 2t + 1, 2t + 8, 2t + 9 an A fragment gives lane (g, t); the sum
-// over tokens does not depend on their order, so S^T's rows take the same one.
-__device__ __forceinline__ int f8_tok(int k) { return 4 * ((k & 7) >> 1) + (k & 1) + 2 * (k >> 3); }
+// FP8 pass, token order inside a 16-token tile.  ldsm8_t hands lane (g, t)
+// the rows that lanes 4t .. 4t + 3 address, which an fp16 A fragment holds
+// in its k-slots 2t, 2t + 1, 2t + 8, 2t + 9; lane i addresses tile row
+// f8_vrow(i).  Row k of S^T (= k-slot k of P^T) then stands for token
+// f8_srow(k): k itself for k < 8, a rotation of 8 .. 15 above (the sum over
+// tokens does not depend on their order).  This choice keeps both the K
+// loads (rows f8_srow(g), f8_srow(g + 8) over the eight g) and each 8-row
+// phase of ldsm8_t on eight distinct 128-byte swizzle phases: no bank
+// conflicts (the order 0, 1, 4, 5, 8, 9, 12, 13 / 2, 3, 6, 7, 10, 11, 14, 15
+// of natural row addresses put rows r and r + 8 in one K load).
+__device__ __forceinline__ int f8_vrow(int i) {
+  return (i & 3) < 2 ? 2 * (i >> 2) + (i & 3) : 8 + ((2 * (i >> 2) + (i & 1) + 4) & 7);
+}
+__device__ __forceinline__ int f8_srow(int k) { return k < 8 ? k : 8 + ((k + 4) & 7); }
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
@@ -128,9 +137,9 @@ constexpr int mma_box_rows(int B, int TS) {
 // the head dimension applied to both operands, so the A fragments of K take
 // d = 16 ks + 4 t .. 4 t + 3 (four consecutive codes, one 32-bit load per
 // row, two conversions) and Q's fragments the same dimensions; V's transpose
-// comes from the 8-bit transposing ldmatrix (ldsm8_t), whose byte order fixes
-// the order of the tile's tokens in both contractions (f8_tok), and is
-// converted to fp16 in registers.  FP8 stages hold 128 tokens (16 KiB of
+// comes from the 8-bit transposing ldmatrix (ldsm8_t), whose byte order and
+// row addresses fix the order of the tile's tokens in both contractions
+// (f8_vrow, f8_srow), and is converted to fp16 in registers.  FP8 stages hold 128 tokens (16 KiB of
 // codes each of K and V): every consumer warp then takes two 16-token tiles
 // of a stage, whose dependency chains the unrolled tile loop interleaves.
 template <int D, int G, bool F8 = false>
@@ -658,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           int rlo[2], rhi[2];
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            // rows g and g + 8 of S^T stand for tokens f8_tok(g), f8_tok(g + 8)
-            rlo[i] = (tt + i * WT) * 16 + f8_tok(g);
-            rhi[i] = (tt + i * WT) * 16 + f8_tok(g + 8);
+            // rows g and g + 8 of S^T stand for tokens f8_srow(g), f8_srow(g + 8)
+            rlo[i] = (tt + i * WT) * 16 + f8_srow(g);
+            rhi[i] = (tt + i * WT) * 16 + f8_srow(g + 8);
           }
           // ---- S^T = K . Q^T: codes 16 ks + 4 t .. + 3 of each token row,
           // one 32-bit load each, straight into fp16; two chains per tile
@@ -737,19 +746,21 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           // ---- V^T fragments straight from the codes: one 8-bit transposing
           // load per tile and m-tile (16 dimensions = one 16-byte chunk of the
-          // 16 token rows, 128-byte swizzle) gives lane (g, t) tokens
-          // 4t .. 4t + 3 of dimensions g and g + 8, converted exactly to
-          // fp16; tokens past the context are zeroed (unused slots may hold
-          // NaN codes, and 0 * NaN would reach the sum)
+          // 16 token rows, 128-byte swizzle; lane i addresses row f8_vrow(i))
+          // gives lane (g, t) tokens f8_vrow(4t .. 4t + 3) = f8_srow of its
+          // k-slots, dimensions g and g + 8, converted exactly to fp16;
+          // tokens past the context are zeroed (unused slots may hold NaN
+          // codes, and 0 * NaN would reach the sum)
           uint32_t vrow[2], vsw[2], mlo[2], mhi[2];
+          const int tk0 = 2 * t, tk2 = f8_srow(2 * t + 8), tk3 = f8_srow(2 * t + 9);
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int vr = (tt + i * WT) * 16 + (lane & 15);
+            const int vr = (tt + i * WT) * 16 + f8_vrow(lane & 15);
             const int nv = nvalid - (tt + i * WT) * 16;
             vrow[i] = vb + vr * 128;
             vsw[i] = vr & 7;
-            mlo[i] = (4 * t < nv ? 0x0000ffffu : 0u) | (4 * t + 1 < nv ? 0xffff0000u : 0u);
-            mhi[i] = (4 * t + 2 < nv ? 0x0000ffffu : 0u) | (4 * t + 3 < nv ? 0xffff0000u : 0u);
+            mlo[i] = (tk0 < nv ? 0x0000ffffu : 0u) | (tk0 + 1 < nv ? 0xffff0000u : 0u);
+            mhi[i] = (tk2 < nv ? 0x0000ffffu : 0u) | (tk3 < nv ? 0xffff0000u : 0u);
           }
 #pragma unroll
           for (int mt = 0; mt < C::KS; ++mt) {
