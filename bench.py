@@ -50,12 +50,12 @@ DEFAULT_WORKLOAD = "pool36"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331453440 + 3543552, "sha": "1df4fc2978c86a52"},
-    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170887424 + 3725312, "sha": "1df4fc2978c86a52"},
-    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615913216 + 6217728, "sha": "1df4fc2978c86a52"},
-    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169168640 + 3441664, "sha": "1df4fc2978c86a52"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331455232 + 3451136, "sha": "6c5c4e7a9c758658"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170890240 + 3348224, "sha": "6c5c4e7a9c758658"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615915264 + 6194944, "sha": "6c5c4e7a9c758658"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169176064 + 3486720, "sha": "6c5c4e7a9c758658"},
     # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
-    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464030208 + 6028800, "sha": "1df4fc2978c86a52"},
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464052480 + 5925888, "sha": "6c5c4e7a9c758658"},
     ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165332992 + 33006080, "sha": "3cbb130b0a704a82"},
 }
 

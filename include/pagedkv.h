@@ -443,16 +443,27 @@ kvStatus paged_prefill_attention_scheduled(kvPool* pool, int layer, const void* 
                                            void* d_out, int out_dtype, void* stream);
 
 /* --------------------------------------------------- whole decode step --
- * One decode step through host buffers ([BT] §10 order): reserve a slot per
- * listed sequence on the host, copy q / new K,V / slots / copy pairs /
- * tables / lengths to the device, run cow_copy, then per layer
- * reshape_and_cache and paged_decode_attention, copy the float32 outputs
- * back and synchronise the stream.
- *   h_q     : [N_layers][n_seq][n_q_heads][D_h]  (pool dtype)
- *   h_k_new : [N_layers][n_seq][H_kv][D_h]        (pool dtype), same h_v_new
+ * One decode step through host buffers ([BT] §10 order: reserve, upload,
+ * launch, read back): reserve a slot per listed sequence on the host, build
+ * the tables (and, on the tensor-core passes, the sharing-aware plan), copy
+ * them with the slots and copy pairs to the device in one copy, run
+ * cow_copy, write the new token of every layer, attend per layer, and
+ * synchronise the stream.
+ *   h_q     : [N_layers][n_seq][n_q_heads][D_h]  (pool dtype; bf16 for FP8)
+ *   h_k_new : [N_layers][n_seq][H_kv][D_h]        same dtype, same h_v_new
  *   h_out   : [N_layers][n_seq][n_q_heads][D_h]  float32
  *   d_staging: caller device buffer of kv_decode_step_staging_bytes() bytes.
- * max_blocks bounds every listed table after the step. */
+ * Page-locked host buffers that are mapped into the device's address space
+ * (cudaMallocHost / cudaHostAlloc, a mapped cudaHostRegister, or torch's
+ * pin_memory, under unified addressing) are used in place: the kernels read
+ * q and the new rows and the merge writes the outputs through the mapping.
+ * Other host buffers go through d_staging with copies.  With a plan on a
+ * bfloat16 or FP8 pool the split pass writes the new rows itself (the
+ * fused slot write); otherwise reshape_and_cache does.  In-place and
+ * staged buffers give the same outputs and pools, bit for bit.  A step
+ * that fails after issuing copies synchronises before returning; a failure
+ * after the reservation leaves the reservation in place.  max_blocks bounds
+ * every listed table after the step. */
 size_t kv_decode_step_staging_bytes(const kvPool* pool, int n_seq, int n_q_heads, int max_blocks);
 kvStatus kv_decode_step_host(kvPool* pool, const int32_t* seq_ids, int n_seq, int n_q_heads,
                              int max_blocks, const void* h_q, const void* h_k_new,
