@@ -822,10 +822,20 @@ def bench_prefill(args):
     v = torch.randn_like(k)
     out = torch.empty((n_tok, wl.n_q_heads, wl.head_dim), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    # an FP8 pool goes through a bfloat16 copy of the blocks read (the staged
+    # call: a conversion launch before each layer's attention)
+    fp8 = wl.dtype == "fp8_e4m3"
+    ws = (torch.empty(cache.paged_prefill_staging_bytes(len(seqs), mb), dtype=torch.uint8,
+                      device=dev) if fp8 else None)
 
     def attend(s):
         for layer in range(wl.n_layers):
-            if natural:
+            if fp8:
+                cache.paged_prefill_attention_staged(
+                    layer, q, wl.n_q_heads, d_table, mb, d_starts, d_lens, len(seqs), out, ws,
+                    max_chunk=max_chunk if natural else 0, d_sched=None if natural else d_sched,
+                    n_items=0 if natural else len(sched), stream=s.cuda_stream)
+            elif natural:
                 cache.paged_prefill_attention(layer, q, wl.n_q_heads, d_table, mb, d_starts,
                                               d_lens, len(seqs), max_chunk, out, 0.0,
                                               s.cuda_stream)
@@ -886,7 +896,7 @@ def bench_prefill(args):
     traffic = TRAFFIC.get((args.workload, wl.block_size, "prefill_tc_kernel"))
     traffic_v = traffic["bytes"] if traffic and traffic.get("sha") == kernel_sha("prefill") else None
     e2e = bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
-                            starts, max_chunk, n_tok, flops, world)
+                            starts, max_chunk, n_tok, flops, world, ws)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, args.cpu_seconds)
@@ -901,6 +911,9 @@ def bench_prefill(args):
             "config": {"workload": args.workload, "n_layers": wl.n_layers,
                        "chunks": [c for _, c in wl.chunks],
                        "histories": [wl.history[s] for s in seqs], "kernel": "prefill_tc_kernel",
+                       "kv_dtype": wl.dtype,
+                       "staging": ("prefill_stage_fp8_kernel: the blocks read, as exact "
+                                   "bfloat16, before each layer's attention" if fp8 else None),
                        "pdl": not args.no_pdl, "block_size": wl.block_size,
                        "work_order": ("natural grid" if natural else
                                       "heaviest first (host schedule, paged_prefill_schedule)"),
@@ -914,12 +927,14 @@ def bench_prefill(args):
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic_v, "kernel": "prefill_tc_kernel",
                          "peak_source": peak_kind,
-                         "timing": "CUDA events around a graph holding the attention launches",
+                         "timing": ("CUDA events around a graph holding the attention launches"
+                                    + (" (each layer's conversion launch included)"
+                                       if fp8 else "")),
                          "alg_flops_per_launch": int(flops / wl.n_layers),
                          "mean_launch_us": round(attn_s * 1e6 / wl.n_layers, 2),
                          "note": "the weights go through the tensor core twice (bf16 high part "
                                  "and remainder), so the P.V half of the flops runs twice"},
-            "gpu_launches": 1 + wl.n_layers,
+            "gpu_launches": 1 + wl.n_layers * (2 if fp8 else 1),
             "graphs": "one CUDA graph per step, replayed",
             "e2e": e2e, "clocks": clocks,
             "wall_s_timed": round(t1 - t0, 4),
@@ -934,7 +949,7 @@ def bench_prefill(args):
 
 
 def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, mb, d_starts,
-                      starts, max_chunk, n_tok, flops, world):
+                      starts, max_chunk, n_tok, flops, world, ws=None):
     """The same round through the public calls with page-locked host buffers:
     host -> device copies of q and the chunks' K/V, the host work order and
     its copy (unless the natural grid is asked for), the slot write and the
@@ -965,7 +980,12 @@ def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, m
             d_sched[: len(sc)].copy_(h_sched[: len(sc)], non_blocking=True)
         cache.reshape_and_cache(-1, dk, dv, d_slots, n_tok)
         for layer in range(wl.n_layers):
-            if natural:
+            if ws is not None:
+                cache.paged_prefill_attention_staged(
+                    layer, dq, wl.n_q_heads, d_table, mb, d_starts, d_lens, len(wl.chunks), dout,
+                    ws, max_chunk=max_chunk if natural else 0,
+                    d_sched=None if natural else d_sched, n_items=0 if natural else len(sc))
+            elif natural:
                 cache.paged_prefill_attention(layer, dq, wl.n_q_heads, d_table, mb, d_starts,
                                               d_lens, len(wl.chunks), max_chunk, dout)
             else:
@@ -981,9 +1001,11 @@ def bench_prefill_e2e(args, wl, cache, dev, q, k, v, d_slots, d_table, d_lens, m
     return {"value": round(tot_f / max_s / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(ho.numel() * 4),
             "ms_per_step": round(max_s / n * 1e3, 4),
-            "api": ("reshape_and_cache + paged_prefill_attention" if natural else
+            "api": ("reshape_and_cache + paged_prefill_attention"
+                    + ("_staged" if ws is not None else "") if natural else
                     "paged_prefill_schedule + reshape_and_cache + "
-                    "paged_prefill_attention_scheduled")}
+                    + ("paged_prefill_attention_staged" if ws is not None
+                       else "paged_prefill_attention_scheduled"))}
 
 
 def _lib_mod():

@@ -442,6 +442,34 @@ kvStatus paged_prefill_attention_scheduled(kvPool* pool, int layer, const void* 
                                            const void* d_sched, int n_items, float scale,
                                            void* d_out, int out_dtype, void* stream);
 
+/* Chunked prefill for any pool dtype.  A bfloat16 pool is read in place, as
+ * by paged_prefill_attention (d_sched null: the natural grid over max_chunk)
+ * or paged_prefill_attention_scheduled (d_sched, n_items), and the
+ * workspace is not used.  An FP8 (E4M3) pool (D_h = 128, the tensor-core
+ * block shapes) is read through a bfloat16 copy in the caller's workspace:
+ * a first kernel turns the codes of every block each listed sequence reads
+ * (its first ceil(context_lens[s] / B) table entries of layer `layer`) into
+ * their exact bfloat16 values, then the same tcgen05 pass attends over the
+ * copy with the K scale folded into the score scale and the outputs
+ * multiplied by the V scale, so the results are those of attention over the
+ * pool's dequantized values ([IO] §8.4.2: narrower KV read, wider
+ * arithmetic).  Slots past a context are copied as zeros.
+ *   d_workspace : device buffer, 256-byte aligned, of at least
+ *                 paged_prefill_staging_bytes(pool, n_seq, max_blocks)
+ *                 bytes (0 for a bfloat16 pool); reused across calls, it
+ *                 must not be written while a call on it is in flight.
+ * Errors as paged_prefill_attention; KV_ERR_UNSUPPORTED for other dtypes
+ * or shapes; an out-of-range table entry is flagged KV_DEV_BAD_BLOCK_ID and
+ * its block copied as zeros. */
+size_t paged_prefill_staging_bytes(const kvPool* pool, int n_seq, int max_blocks);
+kvStatus paged_prefill_attention_staged(kvPool* pool, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const int32_t* d_chunk_start,
+                                        const int32_t* d_context_lens, int n_seq, int max_chunk,
+                                        const void* d_sched, int n_items, float scale,
+                                        void* d_out, int out_dtype, void* d_workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* --------------------------------------------------- whole decode step --
  * One decode step through host buffers ([BT] §10 order: reserve, upload,
  * launch, read back): reserve a slot per listed sequence on the host, build

@@ -116,6 +116,10 @@ SIGNATURES = [
     ("paged_prefill_attention_scheduled", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int,
                                                     _vp, _vp, C.c_int, _vp, C.c_int, C.c_float,
                                                     _vp, C.c_int, _vp]),
+    ("paged_prefill_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int]),
+    ("paged_prefill_attention_staged", C.c_int, [_vp, C.c_int, _vp, C.c_int, _vp, C.c_int, _vp,
+                                                 _vp, C.c_int, C.c_int, _vp, C.c_int, C.c_float,
+                                                 _vp, C.c_int, _vp, C.c_size_t, _vp]),
     ("kv_decode_step_staging_bytes", C.c_size_t, [_vp, C.c_int, C.c_int, C.c_int]),
     # the host buffers go as plain addresses (the per-step call is marshalled
     # with as few conversions as possible)

@@ -337,6 +337,23 @@ class PagedKVCache:
                                                     _stream(stream)),
               "paged_prefill_attention_scheduled")
 
+    def paged_prefill_staging_bytes(self, n_seq, max_blocks):
+        return int(lib.paged_prefill_staging_bytes(self.handle, int(n_seq), int(max_blocks)))
+
+    def paged_prefill_attention_staged(self, layer, q, n_q_heads, d_table, max_blocks,
+                                       d_chunk_start, d_context_lens, n_seq, out, workspace,
+                                       max_chunk=0, d_sched=None, n_items=0, scale=0.0,
+                                       stream=None):
+        """Chunked prefill for any pool dtype (an FP8 pool through a bfloat16
+        copy in ``workspace``); natural grid over ``max_chunk``, or the work
+        order ``d_sched`` of ``n_items`` records."""
+        check(lib.paged_prefill_attention_staged(
+            self.handle, int(layer), vp(q), int(n_q_heads), vp(d_table), int(max_blocks),
+            vp(d_chunk_start), vp(d_context_lens), int(n_seq), int(max_chunk), vp(d_sched),
+            int(n_items), float(scale), vp(out), _out_dtype(out), vp(workspace),
+            _nbytes(workspace) if workspace is not None else 0, _stream(stream)),
+            "paged_prefill_attention_staged")
+
     def kv_decode_step_staging_bytes(self, n_seq, n_q_heads, max_blocks):
         return int(lib.kv_decode_step_staging_bytes(self.handle, int(n_seq), int(n_q_heads),
                                                     int(max_blocks)))

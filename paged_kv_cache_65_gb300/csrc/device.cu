@@ -3,6 +3,7 @@
 // decode attention, and the whole-step driver over host buffers.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -30,11 +31,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Encode a 2-D view of one cache: inner dimension H_kv * D_h elements (one
-// token row of every head), outer dimension N_layers * N_blocks * B rows; a
-// box is D_h elements of one head by `rows` token rows.
-kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizzle128,
-                          CUtensorMap* out) {
+// 2-D TMA descriptor over n_rows rows of `cols` elements (of esize bytes,
+// type dt), box inner x rows.
+kvStatus encode_rows_map(const void* base, unsigned long long n_rows, unsigned long long cols,
+                         int esize, CUtensorMapDataType dt, int inner, int rows, bool swizzle128,
+                         CUtensorMap* out) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
@@ -45,18 +46,28 @@ kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizz
       return KV_ERR_CUDA;
     fn = reinterpret_cast<EncodeTiledFn>(f);
   }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->H) * p->D,
-                              static_cast<cuuint64_t>(p->L) * p->N * p->B};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->H) * p->D * p->esize};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esize};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows)};
   const cuuint32_t estride[2] = {1, 1};
-  const CUtensorMapDataType dt = p->dtype == KV_DTYPE_BF16     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                 : p->dtype == KV_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  CUresult r = fn(out, dt, 2, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = fn(out, dt, 2, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
+}
+
+// A 2-D view of one cache: inner dimension H_kv * D_h elements (one token
+// row of every head), outer dimension N_layers * N_blocks * B rows; a box is
+// `inner` elements of one head by `rows` token rows.
+kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizzle128,
+                          CUtensorMap* out) {
+  const CUtensorMapDataType dt = p->dtype == KV_DTYPE_BF16     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : p->dtype == KV_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                               : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return encode_rows_map(base, static_cast<unsigned long long>(p->L) * p->N * p->B,
+                         static_cast<unsigned long long>(p->H) * p->D, p->esize, dt, inner, rows,
+                         swizzle128, out);
 }
 
 // Split-pass kernel for a pool (after ensure_device) and its decode-path
@@ -117,6 +128,63 @@ kvStatus ensure_device(kvPool* p) {
 }
 
 // ------------------------------------------------------------- kernels
+
+// Two E4M3 codes (low byte first) as two bfloat16 values, exactly (every
+// E4M3 value has at most four significant bits and an exponent inside
+// bfloat16's range); NaN codes stay NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Staged chunked prefill of an FP8 pool: the codes of every block a listed
+// sequence reads (its first ceil(ctx / B) table entries, layer `layer`)
+// become their exact bfloat16 values in the workspace, logical block j of
+// sequence i at copy block i * max_blocks + j, whose table entry the kernel
+// writes too; slots past the context are written as zeros.  The scales stay
+// out (the attention applies them).  One CTA per (logical block, sequence).
+__global__ void __launch_bounds__(128) prefill_stage_fp8_kernel(
+    const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
+    const int32_t* __restrict__ table, const int32_t* __restrict__ ctx, int max_blocks,
+    int layer, int n_blocks, int B, int row_vecs, uint4* __restrict__ k_stage,
+    uint4* __restrict__ v_stage, int32_t* __restrict__ stage_table, int32_t* status) {
+  const int j = blockIdx.x, i = blockIdx.y;
+  const long long sb = static_cast<long long>(i) * max_blocks + j;
+  if (threadIdx.x == 0) stage_table[sb] = static_cast<int32_t>(sb);
+  pkv::griddep_wait();  // the pool's newest rows come from the kernels before
+  pkv::griddep_launch_dependents();
+  const int len = ctx[i];
+  if (len <= 0 || j >= (len + B - 1) / B) return;
+  const int pid = table[sb];
+  const bool ok = pid >= 0 && pid < n_blocks;
+  if (!ok && threadIdx.x == 0) record_status(status, KV_DEV_BAD_BLOCK_ID);
+  const int rows = len - j * B < B ? len - j * B : B;  // slots inside the context
+  // row_vecs: 16-code vectors per token row (H_kv * D_h / 16)
+  const long long src = (static_cast<long long>(layer) * n_blocks + (ok ? pid : 0)) * B * row_vecs;
+  const long long dst = sb * B * row_vecs * 2;
+  for (int idx = threadIdx.x; idx < B * row_vecs; idx += blockDim.x) {
+    const bool live = ok && idx / row_vecs < rows;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+      if (live) {
+        const uint4 c = (kv ? v_pool : k_pool)[src + idx];
+        o0 = make_uint4(e4m3x2_to_bf16x2(c.x), e4m3x2_to_bf16x2(c.x >> 16),
+                        e4m3x2_to_bf16x2(c.y), e4m3x2_to_bf16x2(c.y >> 16));
+        o1 = make_uint4(e4m3x2_to_bf16x2(c.z), e4m3x2_to_bf16x2(c.z >> 16),
+                        e4m3x2_to_bf16x2(c.w), e4m3x2_to_bf16x2(c.w >> 16));
+      }
+      uint4* out = kv ? v_stage : k_stage;
+      out[dst + 2 * idx] = o0;
+      out[dst + 2 * idx + 1] = o1;
+    }
+  }
+}
 
 // Slot write: one CTA per (token, layer); 16-byte copies of the token's row
 // [H_kv][D_h] into K_cache[layer][slot / B][slot % B] and the same for V.
@@ -490,17 +558,33 @@ WsLayout ws_layout(const kvPool* p, int n_seq, int G) {
 bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; }
 
 // Checks and launch shared by the natural-grid and the scheduled prefill.
+// Staged prefill of an FP8 pool: the bfloat16 copy the attention reads
+// instead of the pool (its TMA descriptors, its table, its block count).
+struct PrefillStage {
+  const CUtensorMap* tk;
+  const CUtensorMap* tv;
+  const int32_t* table;
+  int n_blocks;
+};
+
+// Whether a pool can run the chunked-prefill pass: bfloat16 in place, or
+// FP8 (D_h = 128, the tensor-core block shapes) through a bfloat16 copy.
+bool prefill_shape(const kvPool* p, bool staged) {
+  return staged ? p->dtype == KV_DTYPE_FP8_E4M3 && p->D == 128 && pool_tensor_core_shape(p)
+                : pool_tc_shape(p);
+}
+
 kvStatus prefill_common(kvPool* p, int layer, const void* d_q, int n_q_heads,
                         const int32_t* d_block_table, int max_blocks,
                         const int32_t* d_chunk_start, const int32_t* d_context_lens, int n_seq,
                         int max_chunk, const int4* sched, int n_items, float scale, void* d_out,
-                        int out_dtype, void* stream) {
+                        int out_dtype, void* stream, const PrefillStage* stage = nullptr) {
   if (!p || !p->k || n_seq < 0 || n_q_heads <= 0 || n_q_heads % p->H != 0)
     return KV_ERR_INVALID_ARG;
   if (layer < 0 || layer >= p->L) return KV_ERR_INVALID_ARG;
   if (out_dtype != KV_DTYPE_F32 && out_dtype != KV_DTYPE_BF16) return KV_ERR_INVALID_ARG;
   const int G = n_q_heads / p->H;
-  if (ilog2_small(G) < 0 || !pool_tc_shape(p)) return KV_ERR_UNSUPPORTED;
+  if (ilog2_small(G) < 0 || !prefill_shape(p, stage != nullptr)) return KV_ERR_UNSUPPORTED;
   if (n_seq == 0 || (sched ? n_items == 0 : max_chunk == 0)) return KV_OK;
   if (!d_q || !d_block_table || !d_chunk_start || !d_context_lens || !d_out || max_blocks <= 0)
     return KV_ERR_INVALID_ARG;
@@ -513,7 +597,7 @@ kvStatus prefill_common(kvPool* p, int layer, const void* d_q, int n_q_heads,
   if (!p->mma_ok) return KV_ERR_UNSUPPORTED;
   pkv::PrefillArgs a;
   a.q = d_q;
-  a.table = d_block_table;
+  a.table = stage ? stage->table : d_block_table;
   a.chunk_start = d_chunk_start;
   a.ctx = d_context_lens;
   a.out_f32 = out_dtype == KV_DTYPE_F32 ? static_cast<float*>(d_out) : nullptr;
@@ -522,15 +606,18 @@ kvStatus prefill_common(kvPool* p, int layer, const void* d_q, int n_q_heads,
   a.sched = sched;
   a.n_seq = n_seq;
   a.max_blocks = max_blocks;
-  a.layer = layer;
-  a.n_blocks = p->N;
+  a.layer = stage ? 0 : layer;
+  a.n_blocks = stage ? stage->n_blocks : p->N;
   a.block_size = p->B;
   a.n_kv_heads = p->H;
   a.n_q_heads = n_q_heads;
   if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(p->D));
-  a.qscale = scale * 1.4426950408889634f;  // log2(e)
-  const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
-  const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+  // an FP8 copy holds the codes' values: K's scale joins the score scale,
+  // V's scales the outputs
+  a.qscale = scale * 1.4426950408889634f * (stage ? p->k_scale : 1.f);  // log2(e)
+  a.vscale = stage ? p->v_scale : 1.f;
+  const CUtensorMap& tk = stage ? *stage->tk : *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+  const CUtensorMap& tv = stage ? *stage->tv : *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   const cudaError_t e =
       pkv::launch_prefill_tc(tk, tv, a, max_chunk, n_items, as_stream(stream), p->pdl);
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
@@ -1037,6 +1124,90 @@ kvStatus paged_prefill_attention_scheduled(kvPool* p, int layer, const void* d_q
   return prefill_common(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_chunk_start,
                         d_context_lens, n_seq, 0, static_cast<const int4*>(d_sched), n_items,
                         scale, d_out, out_dtype, stream);
+}
+
+namespace {
+// Workspace of a staged prefill: bfloat16 copies of K and V as rows
+// (copy block, slot) of H_kv * D_h values, then the copy's table.
+struct StageLayout {
+  long long rows;
+  size_t k, v, table, total;
+};
+StageLayout stage_layout(const kvPool* p, int n_seq, int max_blocks) {
+  StageLayout l;
+  l.rows = static_cast<long long>(n_seq) * max_blocks * p->B;
+  const size_t kv = align256(static_cast<size_t>(l.rows) * p->H * p->D * 2);
+  l.k = 0;
+  l.v = kv;
+  l.table = 2 * kv;
+  l.total = l.table + align256(static_cast<size_t>(n_seq) * max_blocks * sizeof(int32_t));
+  return l;
+}
+}  // namespace
+
+size_t paged_prefill_staging_bytes(const kvPool* p, int n_seq, int max_blocks) {
+  if (!p || n_seq < 0 || max_blocks <= 0 || p->dtype != KV_DTYPE_FP8_E4M3) return 0;
+  return stage_layout(p, n_seq, max_blocks).total;
+}
+
+kvStatus paged_prefill_attention_staged(kvPool* p, int layer, const void* d_q, int n_q_heads,
+                                        const int32_t* d_block_table, int max_blocks,
+                                        const int32_t* d_chunk_start,
+                                        const int32_t* d_context_lens, int n_seq, int max_chunk,
+                                        const void* d_sched, int n_items, float scale,
+                                        void* d_out, int out_dtype, void* d_workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!p || !p->k || n_seq < 0 || max_chunk < 0 || n_items < 0) return KV_ERR_INVALID_ARG;
+  if (d_sched && !aligned16(d_sched)) return KV_ERR_INVALID_ARG;
+  const int4* sched = static_cast<const int4*>(d_sched);
+  if (p->dtype != KV_DTYPE_FP8_E4M3)  // read in place
+    return prefill_common(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_chunk_start,
+                          d_context_lens, n_seq, sched ? 0 : max_chunk, sched, n_items, scale,
+                          d_out, out_dtype, stream);
+  if (layer < 0 || layer >= p->L || n_q_heads <= 0 || n_q_heads % p->H != 0)
+    return KV_ERR_INVALID_ARG;
+  if (ilog2_small(n_q_heads / p->H) < 0 || !prefill_shape(p, true)) return KV_ERR_UNSUPPORTED;
+  if (n_seq == 0 || (sched ? n_items == 0 : max_chunk == 0)) return KV_OK;
+  if (!d_block_table || !d_context_lens || max_blocks <= 0 || n_seq > 65535)
+    return KV_ERR_INVALID_ARG;
+  const StageLayout l = stage_layout(p, n_seq, max_blocks);
+  if (l.rows >= (1LL << 31)) return KV_ERR_INVALID_ARG;
+  if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0 ||
+      workspace_bytes < l.total)
+    return KV_ERR_INVALID_ARG;
+  kvStatus s = ensure_device(p);
+  if (s != KV_OK) return s;
+  unsigned char* w = static_cast<unsigned char*>(d_workspace);
+  int32_t* stage_table = reinterpret_cast<int32_t*>(w + l.table);
+  const int row_vecs = p->H * p->D / 16;
+  const cudaError_t e = pkv::launch_kernel(
+      p->pdl, prefill_stage_fp8_kernel, dim3(max_blocks, n_seq), dim3(128), 0, as_stream(stream),
+      reinterpret_cast<const uint4*>(p->k), reinterpret_cast<const uint4*>(p->v), d_block_table,
+      d_context_lens, max_blocks, layer, p->N, p->B, row_vecs, reinterpret_cast<uint4*>(w + l.k),
+      reinterpret_cast<uint4*>(w + l.v), stage_table, p->d_status);
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  // descriptors of the copy, kept while the workspace and its size stay
+  if (p->stage_base != d_workspace || p->stage_rows != l.rows) {
+    const int rm = pkv::mma_box_rows(p->B, pkv::mma_stage_tokens(p->D));
+    for (int kv = 0; kv < 2; ++kv) {
+      s = encode_rows_map(w + (kv ? l.v : l.k), static_cast<unsigned long long>(l.rows),
+                          static_cast<unsigned long long>(p->H) * p->D, 2,
+                          CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, rm, true,
+                          reinterpret_cast<CUtensorMap*>(p->tmap_stage[kv]));
+      if (s != KV_OK) {
+        p->stage_base = nullptr;
+        return s;
+      }
+    }
+    p->stage_base = d_workspace;
+    p->stage_rows = l.rows;
+  }
+  const PrefillStage st{reinterpret_cast<const CUtensorMap*>(p->tmap_stage[0]),
+                        reinterpret_cast<const CUtensorMap*>(p->tmap_stage[1]), stage_table,
+                        n_seq * max_blocks};
+  return prefill_common(p, layer, d_q, n_q_heads, d_block_table, max_blocks, d_chunk_start,
+                        d_context_lens, n_seq, sched ? 0 : max_chunk, sched, n_items, scale,
+                        d_out, out_dtype, stream, &st);
 }
 
 kvStatus kv_decode_step_host(kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_heads,

@@ -64,6 +64,12 @@ struct kvPool {
   int merge_deep_ctas = -1;         // planned-merge CTAs resident at once, deep prefetch
   int plan_grid = 0;                // KV_OPT_PLAN_GRID: CTA count plans build start records for
   alignas(64) unsigned char tmap[4][128];  // TMA descriptors: K, V plain; K, V swizzled
+  // staged prefill of an FP8 pool: swizzled TMA descriptors of the bfloat16
+  // copies of K and V in the caller's workspace, valid for (stage_base,
+  // stage_rows)
+  alignas(64) unsigned char tmap_stage[2][128];
+  const void* stage_base = nullptr;
+  long long stage_rows = -1;
   bool mma_ok = false;                      // swizzled descriptors valid (bf16, B % 8 == 0)
   int decode_path = 0;                      // KV_OPT_DECODE_PATH
   bool pdl = true;                          // programmatic dependent launch

@@ -20,7 +20,8 @@ struct PrefillArgs {
   // CTA x works on item x / H_kv, K/V head x % H_kv
   const int4* sched;
   int n_seq, max_blocks, layer, n_blocks, block_size, n_kv_heads, n_q_heads;
-  float qscale;  // scale * log2(e)
+  float qscale;  // scale * log2(e) (times the K scale of an FP8 pool's codes)
+  float vscale;  // factor of the outputs: 1, or the V scale of an FP8 pool's codes
 };
 
 }  // namespace pkv

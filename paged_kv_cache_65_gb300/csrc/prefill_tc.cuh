@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     wait(&v_empty[(n_kb - 1) % NST], ((n_kb - 1) / NST) & 1);
     __syncwarp();
     tc_fence_after();
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const float inv = lt > 0.f ? a.vscale / lt : 0.f;
     const long long orow = (static_cast<long long>(row0 + tok0 + tl) * a.n_q_heads + head * G + g);
 #pragma unroll 1
     for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {

@@ -42,6 +42,7 @@ class DeviceRun:
         self.lengths: dict[int, int] = {}
         self.build_cows = []
         self._ws = None
+        self._stage_ws = None
 
     # -------------------------------------------------------------- build
     def apply(self, op, values_fn) -> None:
@@ -186,9 +187,20 @@ class DeviceRun:
             sched = c.paged_prefill_schedule(starts, d_lens.cpu().numpy(), self.n_q_heads)
             d_sched = torch.from_numpy(sched).to(self.dev)
         outs = []
+        staged = c.dtype == "fp8_e4m3"  # FP8 pools: through a bfloat16 copy
+        if staged:
+            nbytes = c.paged_prefill_staging_bytes(len(chunks), mb)
+            if self._stage_ws is None or self._stage_ws.numel() < nbytes:
+                self._stage_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
         for layer in range(c.L):
             out = torch.zeros((int(starts[-1]), self.n_q_heads, c.D), dtype=dt, device=self.dev)
-            if scheduled:
+            if staged:
+                c.paged_prefill_attention_staged(
+                    layer, qd, self.n_q_heads, d_table, mb, d_starts, d_lens, len(chunks), out,
+                    self._stage_ws, max_chunk=0 if scheduled else mc,
+                    d_sched=d_sched if scheduled else None,
+                    n_items=len(sched) if scheduled else 0, stream=self.stream)
+            elif scheduled:
                 c.paged_prefill_attention_scheduled(layer, qd, self.n_q_heads, d_table, mb,
                                                     d_starts, d_lens, len(chunks), d_sched,
                                                     len(sched), out, 0.0, self.stream)

@@ -43,6 +43,7 @@ bf16 rows and stored as codes of x / scale):
                    parent stays alive (171 and 151 tokens; the step copies the
                    shared tail for the second).
 * ``qwen_2k_fp8`` -- ``qwen_2k`` with an FP8 pool (scales 1).
+* ``prefill_4k_fp8`` -- ``prefill_4k`` over an FP8 pool (scales 1).
 
 Context lengths named above are the lengths after the first decode step
 (the step writes its token first, then attends over every position up to
@@ -189,6 +190,12 @@ def _prefill_4k(seed: int = 7) -> Workload:
     return _prefill("prefill_4k", seed, 32, 8, hist, [512] * 8, 2048)
 
 
+def _prefill_4k_fp8(seed: int = 7) -> Workload:
+    import dataclasses
+
+    return dataclasses.replace(_prefill_4k(seed), name="prefill_4k_fp8", dtype="fp8_e4m3")
+
+
 def _tiny(seed: int = 0) -> Workload:
     ctx = [7, 13, 1, 16]
     ops = []
@@ -299,6 +306,7 @@ WORKLOADS = {
     "pool36": _pool36,
     "prefill_tiny": _prefill_tiny,
     "prefill_4k": _prefill_4k,
+    "prefill_4k_fp8": _prefill_4k_fp8,
     "fp8_small": _fp8_small,
     "qwen_2k_fp8": _qwen_2k_fp8,
 }

@@ -177,3 +177,151 @@ def test_prefill_schedule_for_other_chunk_lengths_is_flagged():
     assert cache.kv_pool_device_status() == 0
     assert (got[:200] == 7.0).all()  # skipped
     assert np.array_equal(got[200:], ref[200:])
+
+
+# ------------------------------------------------------------ FP8 pools
+# paged_prefill_attention_staged: an FP8 (E4M3) pool is read through an exact
+# bfloat16 copy of the blocks each chunk's sequence reads; the outputs are
+# attention over the pool's dequantized values, which is what the oracle's
+# FP8 store gathers.
+
+def fp8_prefill(G, B, hist, chunks, seed, k_scale=0.5, v_scale=2.0, H=2, n_blocks=None):
+    n_blocks = n_blocks or sum(-(-(h + c) // B) for h, c in zip(hist, chunks)) + len(hist) + 4
+    ops = [("append", s, h, s) for s, h in enumerate(hist) if h > 0]
+    return synth.PrefillWorkload("fp8_prefill", 1, n_blocks, B, H * G, H, 128, "fp8_e4m3", seed,
+                                 synth.permutation((seed, 1), n_blocks), ops,
+                                 list(range(len(hist))), "", list(enumerate(chunks)),
+                                 k_scale=k_scale, v_scale=v_scale)
+
+
+def make_fp8(wl, fill=0):
+    from paged_kv_cache_65_gb300 import PagedKVCache
+    from paged_kv_cache_65_gb300.driver import DeviceRun
+
+    cache = PagedKVCache(wl.n_layers, wl.n_blocks, wl.block_size, wl.n_kv_heads, wl.head_dim,
+                         wl.dtype, free_order=wl.free_order)
+    cache.kv_pool_set_fp8_scales(wl.k_scale, wl.v_scale)
+    cache.k.fill_(fill)
+    cache.v.fill_(fill)
+    run = DeviceRun(cache, wl.n_q_heads)
+    for op in wl.build_ops:
+        run.apply(op, wl.append_values)
+    return cache, run
+
+
+def fp8_round(wl, fill=0, scheduled=False):
+    """Outputs of one FP8 prefill round and the oracle's, per chunk."""
+    orc = OracleRun(wl)
+    cache, run = make_fp8(wl, fill)
+    _, _, q = orc.prefill_step(0)
+    _, k, v = wl.chunk_values(0)
+    og = run.prefill_step(wl.chunks, q, k, v, scheduled=scheduled)
+    got = og.float().cpu().numpy()[0]
+    ref = orc.prefill_attend(0, q)
+    assert cache.kv_pool_device_status() == 0
+    return cache, got, ref
+
+
+def fp8_worst(wl, got, ref):
+    offs = np.cumsum([0] + [c for _, c in wl.chunks])
+    worst = 0.0
+    for i, r in ref.items():
+        g = got[offs[i]:offs[i] + wl.chunks[i][1]]
+        assert np.isfinite(g).all()
+        worst = max(worst, float(np.max(np.abs(g - r))) if r.size else 0.0)
+    return worst
+
+
+def test_prefill_fp8_tiny_all_rows():
+    wl = synth.workload("prefill_tiny")
+    import dataclasses
+
+    wl = dataclasses.replace(wl, dtype="fp8_e4m3", k_scale=0.25, v_scale=4.0)
+    _, got, ref = fp8_round(wl)
+    assert fp8_worst(wl, got, ref) <= TOL
+
+
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 8), (4, 32), (8, 64), (2, 32)])
+def test_prefill_fp8_ragged_shapes(G, B):
+    # chunks starting and ending inside blocks, a chunk of one token, a
+    # sequence with no history; unused slots hold NaN codes (0xFF)
+    wl = fp8_prefill(G, B, [0, 5, B - 1, 3 * B + 7], [1, B + 3, 2 * B, 130], 40 + G + B)
+    _, got, ref = fp8_round(wl, fill=0xFF)
+    assert fp8_worst(wl, got, ref) <= TOL
+
+
+def test_prefill_fp8_scheduled_matches_natural():
+    wl = fp8_prefill(4, 16, [0, 300, 1000, 70], [200, 33, 128, 400], 51)
+    _, nat, ref = fp8_round(wl)
+    _, sch, _ = fp8_round(wl, scheduled=True)
+    assert np.array_equal(nat, sch)
+    assert fp8_worst(wl, nat, ref) <= TOL
+
+
+def test_prefill_fp8_4k_round():
+    # the 4096-token round (8 chunks of 512 after histories 0 .. 7680) over an
+    # FP8 pool, every row against the oracle
+    import dataclasses
+
+    wl = dataclasses.replace(synth.workload("prefill_4k"), dtype="fp8_e4m3", k_scale=0.5,
+                             v_scale=1.0)
+    _, got, ref = fp8_round(wl, scheduled=True)
+    assert fp8_worst(wl, got, ref) <= TOL
+
+
+def test_prefill_staged_bf16_pool_reads_in_place():
+    # a bfloat16 pool needs no workspace and gives the plain call's bits
+    import torch as T
+
+    from paged_kv_cache_65_gb300 import _lib
+
+    wl = ragged(4, 16, [0, 37, 200], [45, 130, 1], 61)
+    cache, run = make(wl)
+    orc = OracleRun(wl)
+    _, _, q = orc.prefill_step(0)
+    _, k, v = wl.chunk_values(0)
+    plain = run.prefill_step(wl.chunks, q, k, v)[0]
+    assert cache.paged_prefill_staging_bytes(3, 64) == 0
+    from paged_kv_cache_65_gb300.driver import to_device
+
+    seqs = [s for s, _ in wl.chunks]
+    d_table, d_lens, mb = run.tables(seqs)
+    starts = np.zeros(len(wl.chunks) + 1, dtype=np.int32)
+    starts[1:] = np.cumsum([n for _, n in wl.chunks])
+    out = T.zeros_like(plain)
+    cache.paged_prefill_attention_staged(0, to_device(q, "bf16", "cuda"), wl.n_q_heads, d_table,
+                                         mb, T.from_numpy(starts).cuda(), d_lens, len(seqs), out,
+                                         None, max_chunk=int(max(n for _, n in wl.chunks)))
+    T.cuda.synchronize()
+    assert T.equal(out, plain)
+    assert _lib.KV_OK == 0
+
+
+def test_prefill_fp8_bad_table_entry_is_flagged_not_read():
+    # an out-of-range block id in a table: flagged, its copy zeroed, no read
+    # outside the pool, the other rows unchanged in kind (finite)
+    import torch as T
+
+    from paged_kv_cache_65_gb300 import _lib
+    from paged_kv_cache_65_gb300.driver import to_device
+
+    wl = fp8_prefill(4, 16, [40, 0], [20, 17], 77)
+    cache, run = make_fp8(wl)
+    orc = OracleRun(wl)
+    _, _, q = orc.prefill_step(0)
+    _, k, v = wl.chunk_values(0)
+    run.prefill_step(wl.chunks, q, k, v)
+    assert cache.kv_pool_device_status() == 0
+    seqs = [s for s, _ in wl.chunks]
+    d_table, d_lens, mb = run.tables(seqs)
+    d_table[0, 1] = wl.n_blocks + 9
+    starts = np.zeros(len(wl.chunks) + 1, dtype=np.int32)
+    starts[1:] = np.cumsum([n for _, n in wl.chunks])
+    ws = T.empty(cache.paged_prefill_staging_bytes(len(seqs), mb), dtype=T.uint8, device="cuda")
+    out = T.zeros((int(starts[-1]), wl.n_q_heads, 128), dtype=T.float32, device="cuda")
+    cache.paged_prefill_attention_staged(0, to_device(q, "bf16", "cuda"), wl.n_q_heads, d_table,
+                                         mb, T.from_numpy(starts).cuda(), d_lens, len(seqs), out,
+                                         ws, max_chunk=20)
+    T.cuda.synchronize()
+    assert cache.kv_pool_device_status() & _lib.KV_DEV_BAD_BLOCK_ID
+    assert T.isfinite(out).all()
