@@ -90,3 +90,20 @@ def test_schedule_errors_and_sizes():
 
     assert _lib.lib.paged_prefill_schedule_bytes(c.handle, 3, 8, 100) == 3 * 4 * 16  # T = 32
     assert _lib.lib.paged_prefill_schedule_bytes(c.handle, 3, 7, 100) == 0
+
+
+def test_staged_prefill_workspace_size():
+    # an FP8 pool's staged prefill needs bfloat16 copies of K and V for
+    # n_seq x max_blocks blocks of one layer (each 256-byte aligned) and the
+    # copy's int32 table; a bfloat16 pool reads in place (0 bytes); invalid
+    # arguments give 0
+    n_seq, mb, B, H, D = 3, 7, 16, 2, 128
+    f8 = PagedKVCache(2, 64, B, H, D, "fp8_e4m3", allocate=False)
+    kv = n_seq * mb * B * H * D * 2
+    up = lambda x: -(-x // 256) * 256  # noqa: E731
+    assert f8.paged_prefill_staging_bytes(n_seq, mb) == 2 * up(kv) + up(n_seq * mb * 4)
+    assert f8.paged_prefill_staging_bytes(0, mb) == 0 + 0
+    assert f8.paged_prefill_staging_bytes(n_seq, 0) == 0
+    assert f8.paged_prefill_staging_bytes(-1, mb) == 0
+    bf = PagedKVCache(2, 64, B, H, D, "bf16", allocate=False)
+    assert bf.paged_prefill_staging_bytes(n_seq, mb) == 0
