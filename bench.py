@@ -56,7 +56,10 @@ TRAFFIC = {
     ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169176064 + 3486720, "sha": "6c5c4e7a9c758658"},
     # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
     ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464052480 + 5925888, "sha": "6c5c4e7a9c758658"},
-    ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165332992 + 33006080, "sha": "3cbb130b0a704a82"},
+    ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165507328 + 32500992, "sha": "7dfcd9cff622ca93"},
+    # the attention launch over the bfloat16 copy of the FP8 pool's blocks
+    ("prefill_4k_fp8", 16, "prefill_tc_kernel"): {"bytes": 166452480 + 33987584,
+                                                  "sha": "7dfcd9cff622ca93"},
 }
 
 
