@@ -1,10 +1,9 @@
 // Decode attention for callers that cannot allocate device memory.
 //
 // paged_decode_attention() takes its split-K workspace from the caller.  Some
-// callers have no way to provide one: code running inside a CUDA stream
-// capture in global mode (where cudaMalloc is refused), serving loops whose
-// device memory is entirely pre-reserved by another allocator, or plain C
-// hosts that want no allocator at all.  For them this file keeps the
+// callers have no way to provide one: serving loops whose device memory is
+// entirely pre-reserved by another allocator, or plain C hosts that want no
+// allocator at all.  For them this file keeps the
 // workspace in a fixed-size array in the library's own static device memory
 // and passes its address to the same kernels.
 //

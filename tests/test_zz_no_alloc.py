@@ -1,6 +1,6 @@
 """The no-allocation decode entry point, for callers that cannot allocate
-device memory (inside a global-mode stream capture, or under an allocator
-that already owns all device memory).
+device memory (under an allocator that already owns all device memory, or
+with no allocator at all).
 
 Its workspace is the library's static scratch array and it runs the same
 kernels as the entry point that takes a caller workspace, so on two calls in
