@@ -27,6 +27,9 @@ follows, not to be fast:
 * ``fp8`` -- FP8 E4M3 codes for a quantized KV pool (one scale per pool for
   K and for V), written from the format's definition; ``kv_store`` holds
   such pools.
+* ``q8`` -- q8_0 codes (one fp16 scale per group of 32 values), the
+  plainest rounding rule the pages' byte layout supports; ``kv_store`` holds
+  such pools.
 * ``prefill`` -- chunked-prefill attention over a paged history.
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against

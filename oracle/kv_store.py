@@ -16,7 +16,11 @@ the raw 16-bit patterns (uint16).  A bf16 pattern ``h`` stands for the
 float32 whose bits are ``h << 16``; ``to_f64`` widens that exactly.
 ``"fp8_e4m3"`` pools hold E4M3 codes (uint8) of the written values divided
 by the pool's K or V scale (``oracle.fp8``); the values written are bf16
-patterns, and a gather returns ``code value * scale``.
+patterns, and a gather returns ``code value * scale``.  ``"q8_0"`` pools
+hold int8 codes (uint8 bits) of the written values and one fp16 scale per
+group of 32 values of a (slot, head) row, ``Ks`` / ``Vs [N_layers,
+N_blocks, B, H_kv, D_h / 32]`` (uint16 bits; ``oracle.q8``); a gather
+returns ``code * scale``.
 """
 
 from __future__ import annotations
@@ -24,10 +28,11 @@ from __future__ import annotations
 import numpy as np
 
 from .fp8 import e4m3_decode, e4m3_encode
+from .q8 import GROUP, q8_decode, q8_encode
 
-STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8}
+STORAGE = {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint8, "q8_0": np.uint8}
 # dtype of the rows a caller writes (and of q) for each pool dtype
-INPUT_DTYPE = {"f32": "f32", "bf16": "bf16", "fp8_e4m3": "bf16"}
+INPUT_DTYPE = {"f32": "f32", "bf16": "bf16", "fp8_e4m3": "bf16", "q8_0": "bf16"}
 
 
 def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -49,9 +54,20 @@ class KVStore:
         shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
         self.K = np.zeros(shape, dtype=STORAGE[dtype])
         self.V = np.zeros(shape, dtype=STORAGE[dtype])
+        if dtype == "q8_0":
+            sshape = shape[:-1] + (head_dim // GROUP,)
+            self.Ks = np.zeros(sshape, dtype=np.uint16)
+            self.Vs = np.zeros(sshape, dtype=np.uint16)
 
     def write_slot(self, layer: int, slot: int, k_row, v_row) -> None:
         p, o = divmod(int(slot), self.B)
+        if self.dtype == "q8_0":
+            # rows arrive as bf16 patterns; each head's row in groups of 32
+            kc, ks = q8_encode(to_f64(k_row, "bf16").astype(np.float32))
+            vc, vs = q8_encode(to_f64(v_row, "bf16").astype(np.float32))
+            self.K[layer, p, o], self.Ks[layer, p, o] = kc, ks
+            self.V[layer, p, o], self.Vs[layer, p, o] = vc, vs
+            return
         if self.dtype == "fp8_e4m3":
             # rows arrive as bf16 patterns; stored as codes of x / scale
             self.K[layer, p, o] = e4m3_encode(to_f64(k_row, "bf16").astype(np.float32), self.k_scale)
@@ -73,6 +89,9 @@ class KVStore:
         K and V, into block ``dst``."""
         self.K[:, dst] = self.K[:, src]
         self.V[:, dst] = self.V[:, src]
+        if self.dtype == "q8_0":
+            self.Ks[:, dst] = self.Ks[:, src]
+            self.Vs[:, dst] = self.Vs[:, src]
 
     def gather_raw(self, layer: int, table, ctx: int):
         """Positions ``0..ctx-1`` of one sequence, in logical order, as
@@ -97,4 +116,14 @@ class KVStore:
         k, v = self.gather_raw(layer, table, ctx)
         if self.dtype == "fp8_e4m3":
             return e4m3_decode(k) * self.k_scale, e4m3_decode(v) * self.v_scale
+        if self.dtype == "q8_0":
+            ks, vs = [], []
+            for j in range(-(-ctx // self.B)):
+                rows = min(self.B, ctx - j * self.B)
+                ks.append(self.Ks[layer, table[j], :rows])
+                vs.append(self.Vs[layer, table[j], :rows])
+            shape = (0, self.H, self.D // GROUP)
+            sk = np.concatenate(ks) if ks else np.zeros(shape, dtype=np.uint16)
+            sv = np.concatenate(vs) if vs else np.zeros(shape, dtype=np.uint16)
+            return q8_decode(k, sk), q8_decode(v, sv)
         return to_f64(k, self.dtype), to_f64(v, self.dtype)
