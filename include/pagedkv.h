@@ -63,8 +63,18 @@ enum {
  * bits, no infinities, NaN = all exponent and mantissa bits set) of
  * x / scale, with one float32 scale per pool for K and one for V
  * (kv_pool_set_fp8_scales); half the bytes of BF16.  Its q, new K/V rows and
- * outputs are bfloat16 (outputs may also be float32). */
-enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1, KV_DTYPE_FP8_E4M3 = 2 };
+ * outputs are bfloat16 (outputs may also be float32).
+ * KV_DTYPE_Q8_0: the pages' q8_0 ([IO] §8.4.2, Fig. 8-23): every group of 32
+ * consecutive values of a (slot, head) row shares one fp16 scale d and keeps
+ * one int8 code each, x ~ code * d (34 bytes per 32 values, against 64 for
+ * BF16).  The codes fill K_cache / V_cache ([N_layers][N_blocks][B][H_kv]
+ * [D_h], one byte each); the scales live in two more arrays given by
+ * kv_pool_set_q8_scales.  A written group's scale is the fp16 nearest to
+ * max |x| / 127 (float32 division), each code the integer nearest to x / d
+ * (float32 division, ties to even) clamped to [-127, 127], an all-zero group
+ * having d = 0 and zero codes.  q, new K/V rows and outputs as for FP8.
+ * D_h a multiple of 32; device work needs the scale arrays. */
+enum { KV_DTYPE_F32 = 0, KV_DTYPE_BF16 = 1, KV_DTYPE_FP8_E4M3 = 2, KV_DTYPE_Q8_0 = 3 };
 
 /* bits of the device status word */
 enum {
@@ -140,6 +150,13 @@ kvStatus kv_pool_set_option(kvPool* pool, int option, int value);
  * dtypes: KV_ERR_INVALID_ARG.  Codes already written keep their meaning only
  * under the scales they were written with. */
 kvStatus kv_pool_set_fp8_scales(kvPool* pool, float k_scale, float v_scale);
+
+/* Scale arrays of a Q8_0 pool: fp16, [N_layers][N_blocks][H_kv][B][D_h / 32]
+ * each (the scales of one block and head side by side, B * D_h / 16 bytes),
+ * 16-byte aligned device memory owned by the caller.  The pool's copy-on-write
+ * copies them with the codes.  Other dtypes or null / misaligned pointers:
+ * KV_ERR_INVALID_ARG. */
+kvStatus kv_pool_set_q8_scales(kvPool* pool, void* k_scales, void* v_scales);
 
 /* Synchronise `stream`, copy the device status word to *out_bits and clear
  * it.  Returns KV_ERR_DEVICE_CHECK when any bit was set. */

@@ -34,6 +34,7 @@ KV_OPT_PLAN_GRID = 3
 KV_DTYPE_F32 = 0
 KV_DTYPE_BF16 = 1
 KV_DTYPE_FP8_E4M3 = 2
+KV_DTYPE_Q8_0 = 3
 # bits of the device status word
 KV_DEV_BAD_BLOCK_ID = 1
 KV_DEV_BAD_SLOT = 2
@@ -66,6 +67,7 @@ SIGNATURES = [
     ("kv_block_refcount", C.c_int, [_vp, C.c_int32, _ip]),
     ("kv_pool_set_option", C.c_int, [_vp, C.c_int, C.c_int]),
     ("kv_pool_set_fp8_scales", C.c_int, [_vp, C.c_float, C.c_float]),
+    ("kv_pool_set_q8_scales", C.c_int, [_vp, _vp, _vp]),
     ("kv_pool_device_status", C.c_int, [_vp, _vp, _ip]),
     ("kv_device_wait_selftest", C.c_int, [_vp, C.c_int, _vp]),
     ("block_alloc", C.c_int, [_vp, C.c_int, _i32p]),

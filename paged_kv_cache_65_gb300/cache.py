@@ -15,7 +15,8 @@ import numpy as np
 from . import _lib
 from ._lib import check, i32, lib, ptr_f32, ptr_i32, ptr_i64, vp
 
-DTYPES = {"f32": _lib.KV_DTYPE_F32, "bf16": _lib.KV_DTYPE_BF16, "fp8_e4m3": _lib.KV_DTYPE_FP8_E4M3}
+DTYPES = {"f32": _lib.KV_DTYPE_F32, "bf16": _lib.KV_DTYPE_BF16, "fp8_e4m3": _lib.KV_DTYPE_FP8_E4M3,
+          "q8_0": _lib.KV_DTYPE_Q8_0}
 
 
 def _stream(stream) -> C.c_void_p:
@@ -40,14 +41,20 @@ class PagedKVCache:
         self.H, self.D, self.dtype = n_kv_heads, head_dim, dtype
         self.k = k_cache
         self.v = v_cache
+        self.k_sc = self.v_sc = None  # q8_0: fp16 scales [L, N, H_kv, B, D_h / 32]
         self.status = None
         if allocate and k_cache is None:
             import torch
 
-            tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[dtype]
+            tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+                   "q8_0": torch.uint8}[dtype]
             shape = (n_layers, n_blocks, block_size, n_kv_heads, head_dim)
             self.k = torch.empty(shape, dtype=tdt, device=device)
             self.v = torch.empty(shape, dtype=tdt, device=device)
+            if dtype == "q8_0":
+                sshape = (n_layers, n_blocks, n_kv_heads, block_size, head_dim // 32)
+                self.k_sc = torch.zeros(sshape, dtype=torch.float16, device=device)
+                self.v_sc = torch.zeros(sshape, dtype=torch.float16, device=device)
         if self.k is not None:
             import torch
 
@@ -59,6 +66,9 @@ class PagedKVCache:
                                  ptr_i32(order) if order is not None else None, C.byref(h)),
               "kv_pool_create")
         self.handle = h
+        if self.k_sc is not None:
+            check(lib.kv_pool_set_q8_scales(h, vp(self.k_sc), vp(self.v_sc)),
+                  "kv_pool_set_q8_scales")
 
     def close(self):
         if getattr(self, "handle", None):

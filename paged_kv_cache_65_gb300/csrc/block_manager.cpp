@@ -240,7 +240,14 @@ kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_hea
   *out = nullptr;
   if (n_layers <= 0 || n_blocks <= 0 || block_size <= 0 || block_size > 256 || n_kv_heads <= 0 ||
       head_dim <= 0 ||
-      (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_BF16 && dtype != KV_DTYPE_FP8_E4M3))
+      (dtype != KV_DTYPE_F32 && dtype != KV_DTYPE_BF16 && dtype != KV_DTYPE_FP8_E4M3 &&
+       dtype != KV_DTYPE_Q8_0))
+    return KV_ERR_INVALID_ARG;
+  // q8_0: whole groups of 32 per head row, and one block's scales of a head
+  // (B * D_h / 32 fp16) times H_kv in whole 16-byte vectors
+  if (dtype == KV_DTYPE_Q8_0 &&
+      (head_dim % 32 != 0 ||
+       (static_cast<int64_t>(n_kv_heads) * block_size * (head_dim / 32) * 2) % 16 != 0))
     return KV_ERR_INVALID_ARG;
   if ((k_cache == nullptr) != (v_cache == nullptr)) return KV_ERR_INVALID_ARG;
   const int esize = dtype == KV_DTYPE_F32 ? 4 : (dtype == KV_DTYPE_BF16 ? 2 : 1);
@@ -360,6 +367,15 @@ kvStatus kv_pool_set_option(kvPool* p, int option, int value) {
     return KV_OK;
   }
   return KV_ERR_INVALID_ARG;
+}
+
+kvStatus kv_pool_set_q8_scales(kvPool* p, void* k_scales, void* v_scales) {
+  if (!p || p->dtype != KV_DTYPE_Q8_0 || !k_scales || !v_scales) return KV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_scales) | reinterpret_cast<uintptr_t>(v_scales)) & 15)
+    return KV_ERR_INVALID_ARG;
+  p->k_sc = k_scales;
+  p->v_sc = v_scales;
+  return KV_OK;
 }
 
 kvStatus kv_pool_set_fp8_scales(kvPool* p, float k_scale, float v_scale) {

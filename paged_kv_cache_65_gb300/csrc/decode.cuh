@@ -78,6 +78,9 @@ struct DecodeArgs {
   void* k_pool = nullptr;
   void* v_pool = nullptr;
   float k_scale_w = 1.f, v_scale_w = 1.f;
+  // q8_0 pools: the fp16 scales [L][N][H_kv][B][D / 32] of K and V
+  const void* k_sc = nullptr;
+  const void* v_sc = nullptr;
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }

@@ -30,12 +30,12 @@ cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArg
   return launch_kernel(pdl, kern, dim3(a.grid), dim3(kThreads), smem, st, tk, tv, a);
 }
 
-template <int D, int G, bool F8 = false>
+template <int D, int G, bool F8 = false, bool Q8 = false>
 cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, DecodeArgs a, int sm_count,
                        int max_grid, int* grid_io, cudaStream_t st, bool pdl) {
-  constexpr int smem = decode_mma_smem_bytes<D, G, F8>();
-  auto k_plain = decode_mma_kernel<D, G, false, F8>;
-  auto k_plan = decode_mma_kernel<D, G, true, F8>;
+  constexpr int smem = decode_mma_smem_bytes<D, G, F8, Q8>();
+  auto k_plain = decode_mma_kernel<D, G, false, F8, Q8>;
+  auto k_plan = decode_mma_kernel<D, G, true, F8, Q8>;
   // the dynamic shared-memory limit is a per-function, per-device attribute
   static bool attr_set[2][64] = {};
   int dev = 0;
@@ -82,6 +82,12 @@ cudaError_t launch_mma_bf16(int D, int G, const CUtensorMap& tk, const CUtensorM
 cudaError_t launch_mma_fp8(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                            const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
                            cudaStream_t st, bool pdl, bool* supported);
+
+// The same pass over a q8_0 pool (int8 codes, fp16 scales per 32 values,
+// a.k_sc / a.v_sc), D_h = 128.
+cudaError_t launch_mma_q8(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,
+                          cudaStream_t st, bool pdl, bool* supported);
 
 // Dispatch over (D, G) for one element size; *supported = false when the
 // shape has no compiled instantiation.

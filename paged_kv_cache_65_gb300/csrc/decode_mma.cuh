@@ -29,6 +29,8 @@
 // the piece.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "decode.cuh"
 
 namespace pkv {
@@ -106,6 +108,37 @@ __device__ __forceinline__ int f8_vrow(int i) {
 }
 __device__ __forceinline__ int f8_srow(int k) { return k < 8 ? k : 8 + ((k + 4) & 7); }
 
+// q8_0 pass: four int8 codes (lowest byte first) as two fp16 pairs, exactly:
+// the half 0x6400 | (c + 128) is 1024 + c + 128, and subtracting 1152 leaves
+// c (every step exact in fp16's 11-bit significand).
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // 1152, 1152
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(bias));
+}
+
+// fp16 halves of a 32-bit word as floats
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -142,7 +175,7 @@ constexpr int mma_box_rows(int B, int TS) {
 // (f8_vrow, f8_srow), and is converted to fp16 in registers.  FP8 stages hold 128 tokens (16 KiB of
 // codes each of K and V): every consumer warp then takes two 16-token tiles
 // of a stage, whose dependency chains the unrolled tile loop interleaves.
-template <int D, int G, bool F8 = false>
+template <int D, int G, bool F8 = false, bool Q8 = false>
 struct MmaCfg {
   static constexpr int TS = mma_stage_tokens(D, F8);  // tokens per stage
   static constexpr int TILES = TS / 16;           // 16-token tiles per stage
@@ -151,11 +184,14 @@ struct MmaCfg {
   static constexpr int HALVES = F8 ? 1 : D / 64;  // 128-byte swizzled boxes per row set
   static constexpr int HALF_BYTES = TS * 128;     // one box column of a K (or V) stage
   static constexpr int STAGE_BYTES = TS * D * ESZ;  // K (or V) per stage
+  // Q8 (with F8's one-byte layout): the codes' fp16 scales of a stage, K or V
+  static constexpr int SC_BYTES = Q8 ? TS * (D / 32) * 2 : 0;
 
   static constexpr int NST = 3;                   // stages in the ring
   static constexpr int CC = 4;                    // columns per combine pass
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!F8 || D == 128, "FP8 rows are 128 codes");
+  static_assert(!Q8 || F8, "q8_0 shares the one-byte code layout");
   static_assert(G >= 1 && G <= 8, "group size");
   static_assert(TILES % ((F8 ? 2 : 1) * kConsumerWarps) == 0, "whole tiles (pairs) per warp");
 };
@@ -212,10 +248,11 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs& a, int rep, int 
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <int D, int G, bool F8 = false>
+template <int D, int G, bool F8 = false, bool Q8 = false>
 constexpr int decode_mma_smem_bytes() {
-  using C = MmaCfg<D, G, F8>;
+  using C = MmaCfg<D, G, F8, Q8>;
   return 2 * C::NST * C::STAGE_BYTES        // K and V stages
+         + 2 * C::NST * C::SC_BYTES         // Q8: their scales
          + kConsumerWarps * C::CC * D * 4   // combine: O per warp, CC columns at a time
          + kConsumerWarps * 8 * 2 * 4       // combine: m, l per warp and column
          + 2 * C::NST * 8                   // mbarriers
@@ -288,11 +325,11 @@ __device__ inline int plan_find(const PlanSeg* segs, int n_segs, long long r0) {
   return lo;
 }
 
-template <int D, int G, bool PLAN, bool F8 = false>
+template <int D, int G, bool PLAN, bool F8 = false, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
-  using C = MmaCfg<D, G, F8>;
+  using C = MmaCfg<D, G, F8, Q8>;
   constexpr int NST = C::NST;
   // the declared alignment stays at 16 so that the explicit round-up to the
   // 1 KiB the 128-byte swizzle needs is never folded away
@@ -301,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
   unsigned char* v_st = k_st + NST * C::STAGE_BYTES;
-  float* cmb_o = reinterpret_cast<float*>(v_st + NST * C::STAGE_BYTES);
+  unsigned char* sc_st = v_st + NST * C::STAGE_BYTES;  // Q8: K scales, then V scales
+  float* cmb_o = reinterpret_cast<float*>(sc_st + 2 * NST * C::SC_BYTES);
   float* cmb_ml = cmb_o + kConsumerWarps * C::CC * D;
   uint64_t* full = reinterpret_cast<uint64_t*>(cmb_ml + kConsumerWarps * 8 * 2);
   uint64_t* empty = full + NST;
@@ -523,7 +561,10 @@ __global__ void __launch_bounds__(kThreads, 2)
               write_new_row<D, F8>(a, p.rep, p.head, pid, t - j * B, true, true, lane);
           }
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * nunits * unit_bytes);
+        // Q8: each box's rows also bring their scales (D / 32 fp16 a row)
+        constexpr uint32_t kScRow = Q8 ? D / 32 * 2 : 0;
+        if (lane == 0)
+          mbar_arrive_expect_tx(&full[slot], 2u * nunits * (unit_bytes + UR * kScRow));
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int t = tok0 + u * UR;
@@ -541,6 +582,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int off = slot * C::STAGE_BYTES + h * C::HALF_BYTES + u * UR * 128;
             tma_load_2d(k_st + off, &tmap_k, x, y, &full[slot]);
             tma_load_2d(v_st + off, &tmap_v, x, y, &full[slot]);
+          }
+          if constexpr (Q8) {
+            // scales [L][N][H][B][D / 32]: the box's UR rows side by side
+            const long long src =
+                (((long long)a.layer * a.n_blocks + pid) * H + p.head) * B + row;
+            const int so = slot * C::SC_BYTES + u * UR * kScRow;
+            bulk_load(sc_st + so, reinterpret_cast<const unsigned char*>(a.k_sc) + src * kScRow,
+                      UR * kScRow, &full[slot]);
+            bulk_load(sc_st + NST * C::SC_BYTES + so,
+                      reinterpret_cast<const unsigned char*>(a.v_sc) + src * kScRow, UR * kScRow,
+                      &full[slot]);
           }
         }
         ++stage;
@@ -678,6 +730,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) s[i][j] = s2[i][j] = 0.f;
+          // Q8: one accumulator per 32-dimension group (k-steps 2 grp and
+          // 2 grp + 1: the dimension permutation stays inside a k-step), each
+          // weighted by its rows' K scales afterwards
+          float sg[2][Q8 ? 4 : 1][4];
+          if constexpr (Q8) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sg[i][q][j] = 0.f;
+          }
 #pragma unroll
           for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
@@ -691,12 +755,41 @@ __global__ void __launch_bounds__(kThreads, 2)
                            : "=r"(wb)
                            : "r"(kb + rhi[i] * 128 + t * 4 +
                                  (static_cast<uint32_t>(ks ^ (rhi[i] & 7)) << 4)));
-              e4m3x4_to_f16(wa, a0, a2);
-              e4m3x4_to_f16(wb, a1, a3);
-              if (ks & 1)
-                mma_f16(s2[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-              else
-                mma_f16(s[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              if constexpr (Q8) {
+                i8x4_to_f16(wa, a0, a2);
+                i8x4_to_f16(wb, a1, a3);
+                mma_f16(sg[i][Q8 ? ks >> 1 : 0], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              } else {
+                e4m3x4_to_f16(wa, a0, a2);
+                e4m3x4_to_f16(wb, a1, a3);
+                if (ks & 1)
+                  mma_f16(s2[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                else
+                  mma_f16(s[i], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              }
+            }
+          }
+          if constexpr (Q8) {
+            // rows rlo / rhi: their four K scales (fp16) side by side
+            const uint32_t kscb = smem_u32(sc_st) + slot * C::SC_BYTES;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint32_t l0, l1, h0, h1;
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                           : "=r"(l0), "=r"(l1)
+                           : "r"(kscb + rlo[i] * 8));
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                           : "=r"(h0), "=r"(h1)
+                           : "r"(kscb + rhi[i] * 8));
+              const float kl[4] = {half_lo(l0), half_hi(l0), half_lo(l1), half_hi(l1)};
+              const float kh[4] = {half_lo(h0), half_hi(h0), half_lo(h1), half_hi(h1)};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                s[i][0] = fmaf(kl[q], sg[i][Q8 ? q : 0][0], s[i][0]);
+                s[i][1] = fmaf(kl[q], sg[i][Q8 ? q : 0][1], s[i][1]);
+                s[i][2] = fmaf(kh[q], sg[i][Q8 ? q : 0][2], s[i][2]);
+                s[i][3] = fmaf(kh[q], sg[i][Q8 ? q : 0][3], s[i][3]);
+              }
             }
           }
           // ---- scale, mask, max over both tiles per column
@@ -722,7 +815,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           m_run[1] = mn1;
           // ---- P^T fragments (P <= 1 in fp16: 11 bits, far inside the
           // tolerance), transposed
-          uint32_t bh[2][2];
+          // Q8: per 32-dimension group, P times its rows' V scales (a row
+          // past the context takes 0, whatever its scale bytes hold)
+          uint32_t bh[2][Q8 ? 4 : 1][2];
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -730,8 +825,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float p2 = exp2_approx(s[i][2] - mn0), p3 = exp2_approx(s[i][3] - mn1);
             ls0 += p0 + p2;
             ls1 += p1 + p3;
-            bh[i][0] = movm_t(pack_f16(p0, p1));
-            bh[i][1] = movm_t(pack_f16(p2, p3));
+            if constexpr (Q8) {
+              const uint32_t vscb = smem_u32(sc_st) + (NST + slot) * C::SC_BYTES;
+              uint32_t l0, l1, h0, h1;
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                           : "=r"(l0), "=r"(l1)
+                           : "r"(vscb + rlo[i] * 8));
+              asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                           : "=r"(h0), "=r"(h1)
+                           : "r"(vscb + rhi[i] * 8));
+              const bool okl = rlo[i] < nvalid, okh = rhi[i] < nvalid;
+              const float vl[4] = {half_lo(l0), half_hi(l0), half_lo(l1), half_hi(l1)};
+              const float vh[4] = {half_lo(h0), half_hi(h0), half_lo(h1), half_hi(h1)};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float fl = okl ? vl[q] : 0.f, fh = okh ? vh[q] : 0.f;
+                bh[i][Q8 ? q : 0][0] = movm_t(pack_f16(p0 * fl, p1 * fl));
+                bh[i][Q8 ? q : 0][1] = movm_t(pack_f16(p2 * fh, p3 * fh));
+              }
+            } else {
+              bh[i][0][0] = movm_t(pack_f16(p0, p1));
+              bh[i][0][1] = movm_t(pack_f16(p2, p3));
+            }
           }
           l_run[0] = l_run[0] * al0 + ls0;
           l_run[1] = l_run[1] * al1 + ls1;
@@ -768,10 +883,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i < 2; ++i) {
               uint32_t r0, r1, a0, a1, a2, a3;
               ldsm8_t(vrow[i] + ((static_cast<uint32_t>(mt) ^ vsw[i]) << 4), r0, r1);
-              e4m3x4_to_f16(r0, a0, a2);
-              e4m3x4_to_f16(r1, a1, a3);
-              mma_f16(o[mt], a0 & mlo[i], a1 & mlo[i], a2 & mhi[i], a3 & mhi[i], bh[i][0],
-                      bh[i][1]);
+              if constexpr (Q8) {
+                i8x4_to_f16(r0, a0, a2);
+                i8x4_to_f16(r1, a1, a3);
+              } else {
+                e4m3x4_to_f16(r0, a0, a2);
+                e4m3x4_to_f16(r1, a1, a3);
+              }
+              const int q = Q8 ? (mt >> 1) : 0;  // Q8: the m-tile's 32-dimension group
+              mma_f16(o[mt], a0 & mlo[i], a1 & mlo[i], a2 & mhi[i], a3 & mhi[i], bh[i][q][0],
+                      bh[i][q][1]);
             }
           }
         }

@@ -94,9 +94,11 @@ kvStatus ensure_device(kvPool* p) {
   if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
       cudaSuccess)
     return KV_ERR_CUDA;
-  if (p->dtype == KV_DTYPE_FP8_E4M3) {
-    // FP8 codes: only the warp-level MMA pass, one 128-byte swizzled box
-    // (128 codes, all of D_h = 128) by mma_box_rows(B, 128) rows
+  if (p->dtype == KV_DTYPE_Q8_0 && (!p->k_sc || !p->v_sc))
+    return KV_ERR_INVALID_ARG;  // a q8_0 pool needs its scale arrays
+  if (pool_codes8(p)) {
+    // FP8 / q8_0 codes: only the warp-level MMA pass, one 128-byte swizzled
+    // box (128 codes, all of D_h = 128) by mma_box_rows(B, 128) rows
     if (!pool_tensor_core_shape(p)) return KV_ERR_UNSUPPORTED;
     const int rm = pkv::mma_box_rows(p->B, pkv::mma_stage_tokens(p->D, true));
     kvStatus s = encode_cache_map(p, p->k, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
@@ -264,6 +266,76 @@ __global__ void slot_write_fp8_kernel(const uint4* __restrict__ k_new,
 // into block dst in K and V.  Each thread loads up to four 16-byte vectors of
 // K and four of V before storing any, so the loads of cold source blocks are
 // in flight together instead of one latency per vector.
+// Slot write into a q8_0 pool: one CTA per (token, layer); each thread takes
+// one group of 32 bfloat16 values of the token's K (and V) row: amax =
+// max |x|, d = the fp16 nearest to amax / 127 (float32 IEEE division), codes
+// = the integers nearest to x / d (float32 IEEE division, ties to even)
+// clamped to [-127, 127], all zero when d is 0 ("第 8 章 推理优化" §8.4.2's
+// q8_0 groups).  Codes go to the row's slot, the scale to
+// scales[layer][block][head][slot][group].
+__global__ void slot_write_q8_kernel(const uint4* __restrict__ k_new,
+                                     const uint4* __restrict__ v_new,
+                                     const int64_t* __restrict__ slots, int n_tok, uint4* kc,
+                                     uint4* vc, __half* ksc, __half* vsc, int layer,
+                                     int n_blocks, int B, int H, int groups_per_head,
+                                     int32_t* status) {
+  pkv::griddep_wait();
+  pkv::griddep_launch_dependents();
+  const int i = blockIdx.x;
+  const int ly = layer >= 0 ? layer : blockIdx.y;
+  const int64_t slot = slots[i];
+  if (slot < 0) return;
+  const long long slots_per_layer = static_cast<long long>(n_blocks) * B;
+  if (slot >= slots_per_layer) {
+    if (threadIdx.x == 0) record_status(status, KV_DEV_BAD_SLOT);
+    return;
+  }
+  const int n_groups = H * groups_per_head;  // groups of 32 in a token row
+  const long long src = ((layer >= 0 ? 0LL : (long long)blockIdx.y * n_tok) + i) * n_groups * 4;
+  const long long dst = ((long long)ly * slots_per_layer + slot) * n_groups * 2;
+  const long long blk = slot / B;
+  const int o = static_cast<int>(slot - blk * B);
+  for (int g = threadIdx.x; g < 2 * n_groups; g += blockDim.x) {
+    const bool is_k = g < n_groups;
+    const int gg = is_k ? g : g - n_groups;
+    const uint4* in = (is_k ? k_new : v_new) + src + gg * 4;
+    float x[32];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 w = in[v];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        x[v * 8 + 2 * k] = __uint_as_float(ws[k] << 16);
+        x[v * 8 + 2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(x[k]));
+    const __half d16 = __float2half_rn(__fdiv_rn(amax, 127.f));
+    const float d = __half2float(d16);
+    uint32_t packed[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float q = d > 0.f ? rintf(__fdiv_rn(x[4 * k + b], d)) : 0.f;
+        q = fminf(fmaxf(q, -127.f), 127.f);
+        w |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xffu) << (8 * b);
+      }
+      packed[k] = w;
+    }
+    uint4* out = (is_k ? kc : vc) + dst + gg * 2;
+    out[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    out[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    const int h = gg / groups_per_head, q = gg - h * groups_per_head;
+    (is_k ? ksc : vsc)[(((long long)ly * n_blocks + blk) * H + h) * B * groups_per_head +
+                       static_cast<long long>(o) * groups_per_head + q] = d16;
+  }
+}
+
 __global__ void cow_copy_kernel(const int32_t* __restrict__ pairs, uint4* kc, uint4* vc,
                                 int n_blocks, long long block_vecs, int32_t* status) {
   pkv::griddep_wait();
@@ -696,10 +768,17 @@ kvStatus cow_copy(kvPool* p, const int32_t* d_pairs, int n_pairs, void* stream) 
   const long long want = (block_vecs + 511) / 512;
   const int parts = static_cast<int>(want < 1 ? 1 : (want > 16 ? 16 : want));
   dim3 grid(n_pairs, p->L, parts);
-  const cudaError_t e = pkv::launch_kernel(
+  cudaError_t e = pkv::launch_kernel(
       p->pdl, cow_copy_kernel, grid, dim3(256), 0, as_stream(stream), d_pairs,
       reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v), p->N, block_vecs,
       p->d_status);
+  if (e == cudaSuccess && p->dtype == KV_DTYPE_Q8_0) {
+    // the blocks' scales ([L][N][H][B][D / 32] fp16) go with their codes
+    const long long sc_vecs = static_cast<long long>(p->H) * p->B * (p->D / 32) * 2 / 16;
+    e = pkv::launch_kernel(p->pdl, cow_copy_kernel, dim3(n_pairs, p->L, 1), dim3(256), 0,
+                           as_stream(stream), d_pairs, reinterpret_cast<uint4*>(p->k_sc),
+                           reinterpret_cast<uint4*>(p->v_sc), p->N, sc_vecs, p->d_status);
+  }
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -711,6 +790,18 @@ kvStatus reshape_and_cache(kvPool* p, int layer, const void* d_k_new, const void
   if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KV_ERR_INVALID_ARG;
   kvStatus s = ensure_device(p);
   if (s != KV_OK) return s;
+  if (p->dtype == KV_DTYPE_Q8_0) {
+    const int groups = p->H * p->D / 32;
+    dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
+    const int threads = 2 * groups >= 128 ? 128 : (2 * groups >= 64 ? 64 : 32);
+    const cudaError_t e = pkv::launch_kernel(
+        p->pdl, slot_write_q8_kernel, grid, dim3(threads), 0, as_stream(stream),
+        reinterpret_cast<const uint4*>(d_k_new), reinterpret_cast<const uint4*>(d_v_new),
+        d_slot_mapping, n_tokens, reinterpret_cast<uint4*>(p->k), reinterpret_cast<uint4*>(p->v),
+        reinterpret_cast<__half*>(p->k_sc), reinterpret_cast<__half*>(p->v_sc), layer, p->N,
+        p->B, p->H, p->D / 32, p->d_status);
+    return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  }
   if (p->dtype == KV_DTYPE_FP8_E4M3) {
     const int row_vecs = p->H * p->D / 8;
     dim3 grid(n_tokens, layer >= 0 ? 1 : p->L);
@@ -785,12 +876,17 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  if (p->dtype == KV_DTYPE_FP8_E4M3) {
-    if (kern != kKernelMma) return KV_ERR_UNSUPPORTED;  // FP8: warp-level MMA pass only
+  if (pool_codes8(p)) {
+    if (kern != kKernelMma) return KV_ERR_UNSUPPORTED;  // codes: warp-level MMA pass only
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
-    e = pkv::launch_mma_fp8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
-                            as_stream(stream), p->pdl, &supported);
+    a.k_sc = p->k_sc;
+    a.v_sc = p->v_sc;
+    e = p->dtype == KV_DTYPE_Q8_0
+            ? pkv::launch_mma_q8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
+                                 as_stream(stream), p->pdl, &supported)
+            : pkv::launch_mma_fp8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io,
+                                  as_stream(stream), p->pdl, &supported);
   } else if (kern == kKernelTc) {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
@@ -944,12 +1040,18 @@ kvStatus partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
   a.v_pool = p->v;
   a.k_scale_w = p->k_scale;
   a.v_scale_w = p->v_scale;
+  a.k_sc = p->k_sc;
+  a.v_sc = p->v_sc;
   const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   bool supported = true;
   const cudaError_t e =
       tc ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
                                as_stream(stream), p->pdl)
+      : p->dtype == KV_DTYPE_Q8_0
+          ? pkv::launch_mma_q8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
+                               &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,
+                               &supported)
       : p->dtype == KV_DTYPE_FP8_E4M3
           ? pkv::launch_mma_fp8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
                                 &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,

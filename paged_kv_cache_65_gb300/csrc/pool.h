@@ -34,6 +34,8 @@ struct kvPool {
   // shape
   int L = 0, N = 0, B = 0, H = 0, D = 0, dtype = 0, esize = 0;
   int in_esize = 0;                 // bytes of a q / new K/V element (bf16 for FP8 pools)
+  void* k_sc = nullptr;             // Q8_0: fp16 scales [L][N][H][B][D / 32] of K and V
+  void* v_sc = nullptr;
   float k_scale = 1.f, v_scale = 1.f;  // FP8 pools: stored code = e4m3(x / scale)
   // caller-owned device memory
   void* k = nullptr;
@@ -92,9 +94,14 @@ struct kvPool {
 // elements by min(B, T) rows, T = 64 tokens at D_h = 128 and 128 at 64: each
 // box starts on 1 KiB (B a multiple of 8) and a stage holds whole blocks or a
 // block whole stages.
+// Pools of one-byte codes (FP8 E4M3, q8_0).
+inline bool pool_codes8(const kvPool* p) {
+  return p->dtype == KV_DTYPE_FP8_E4M3 || p->dtype == KV_DTYPE_Q8_0;
+}
+
 inline bool pool_tensor_core_shape(const kvPool* p) {
-  if (p->dtype == KV_DTYPE_FP8_E4M3) {
-    // FP8: rows of 128 one-byte codes, one 128-byte swizzled box per row set
+  if (pool_codes8(p)) {
+    // FP8 / q8_0: rows of 128 one-byte codes, one 128-byte swizzled box per row set
     if (p->D != 128 || p->B % 8 != 0) return false;
   } else if (p->dtype != KV_DTYPE_BF16 || (p->D != 64 && p->D != 128) || p->B % 8 != 0) {
     return false;

@@ -43,6 +43,8 @@ bf16 rows and stored as codes of x / scale):
                    parent stays alive (171 and 151 tokens; the step copies the
                    shared tail for the second).
 * ``qwen_2k_fp8`` -- ``qwen_2k`` with an FP8 pool (scales 1).
+* ``qwen_2k_q8``  -- ``qwen_2k`` with a q8_0 pool (one fp16 scale per 32
+                   values, "第 8 章 推理优化" §8.4.2 Fig. 8-23).
 * ``prefill_4k_fp8`` -- ``prefill_4k`` over an FP8 pool (scales 1).
 
 Context lengths named above are the lengths after the first decode step
@@ -85,7 +87,7 @@ def torch_seed(seed_words) -> int:
 
 def storage_dtype(dtype: str):
     """Element type of the values a caller writes (FP8 pools take bf16)."""
-    return {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint16}[dtype]
+    return {"f32": np.float32, "bf16": np.uint16, "fp8_e4m3": np.uint16, "q8_0": np.uint16}[dtype]
 
 
 def storage_values(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -94,7 +96,7 @@ def storage_values(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "f32":
         return x
-    if dtype in ("bf16", "fp8_e4m3"):  # FP8 pools are written with bf16 rows
+    if dtype in ("bf16", "fp8_e4m3", "q8_0"):  # code pools are written with bf16 rows
         import torch
 
         t = torch.from_numpy(x).to(torch.bfloat16)
@@ -128,9 +130,10 @@ class Workload:
     v_scale: float = field(default=1.0, kw_only=True)
 
     @property
-    def elem_bytes(self) -> int:
-        """Bytes of one stored K or V element."""
-        return {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[self.dtype]
+    def elem_bytes(self) -> float:
+        """Bytes of one stored K or V element (q8_0: its code and its share
+        of the group's 2-byte scale, 34 / 32)."""
+        return {"f32": 4, "bf16": 2, "fp8_e4m3": 1, "q8_0": 34 / 32}[self.dtype]
 
     # values --------------------------------------------------------------
     def append_values(self, value_seed: int, n_tokens: int):
@@ -217,7 +220,7 @@ def _qwen_2k(seed: int = 1, dtype: str = "bf16") -> Workload:
     rng = np.random.Generator(np.random.PCG64(_seed_seq((seed, 4))))
     ctx = rng.integers(2048, 2303, size=n_seq, endpoint=True)
     ops = [("append", s, int(c) - 1, s) for s, c in enumerate(ctx)]
-    name = "qwen_2k" if dtype == "bf16" else "qwen_2k_fp8"
+    name = {"bf16": "qwen_2k", "fp8_e4m3": "qwen_2k_fp8", "q8_0": "qwen_2k_q8"}[dtype]
     return Workload(name, 1, n_blocks, 16, 32, 8, 128, dtype, seed,
                     permutation((seed, 0), n_blocks), ops, list(range(n_seq)),
                     "37 independent sequences, context U[2048, 2303]")
@@ -225,6 +228,10 @@ def _qwen_2k(seed: int = 1, dtype: str = "bf16") -> Workload:
 
 def _qwen_2k_fp8(seed: int = 1) -> Workload:
     return _qwen_2k(seed, "fp8_e4m3")
+
+
+def _qwen_2k_q8(seed: int = 1) -> Workload:
+    return _qwen_2k(seed, "q8_0")
 
 
 def _fp8_small(seed: int = 8) -> Workload:
@@ -307,6 +314,7 @@ WORKLOADS = {
     "prefill_tiny": _prefill_tiny,
     "prefill_4k": _prefill_4k,
     "prefill_4k_fp8": _prefill_4k_fp8,
+    "qwen_2k_q8": _qwen_2k_q8,
     "fp8_small": _fp8_small,
     "qwen_2k_fp8": _qwen_2k_fp8,
 }
