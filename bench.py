@@ -224,8 +224,15 @@ def setup(name: str, block_size: int = 16, device="cuda", fill: str = "device",
             for i in range(0, flat.numel(), step):
                 seg = flat[i:i + step]
                 x = torch.randn(seg.numel(), generator=g, device=device, dtype=torch.float32)
+                if wl.dtype == "q8_0":  # codes of N(0,1) values at scale 1/32
+                    seg.copy_(torch.clamp(torch.round(x * 32), -127, 127).to(torch.int8)
+                              .view(torch.uint8))
+                    continue
                 # FP8 pools: the values' E4M3 codes (torch's conversion; synthetic fill only)
                 seg.copy_(x.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else x)
+        if wl.dtype == "q8_0":
+            cache.k_sc.fill_(1.0 / 32)
+            cache.v_sc.fill_(1.0 / 32)
     run = DeviceRun(cache, wl.n_q_heads)
     values = None if fill == "device" else wl.append_values
     for op in wl.build_ops:
@@ -341,7 +348,8 @@ def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_
     # at most n_plans tokens however many steps are timed
     n_plans = args.plans if min_timed_s > 0 else min(args.warmup + steps, args.plans)
 
-    use_plan = not (args.plain or args.kernel == "cuda") and wl.dtype in ("bf16", "fp8_e4m3") and \
+    use_plan = not (args.plain or args.kernel == "cuda") and \
+        wl.dtype in ("bf16", "fp8_e4m3", "q8_0") and \
         wl.block_size % 8 == 0
     plans, host_plans = [], []
     max_blocks = 1
@@ -581,7 +589,7 @@ def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_
     peak, peak_kind = read_peaks()
     achieved = alg / split_s / 1e9
     # the split-pass kernel that ran: a plan records its own; otherwise the option
-    tensor_shape = wl.dtype in ("bf16", "fp8_e4m3") and wl.block_size % 8 == 0
+    tensor_shape = wl.dtype in ("bf16", "fp8_e4m3", "q8_0") and wl.block_size % 8 == 0
     if use_plan:
         from paged_kv_cache_65_gb300.cache import parse_plan
 
@@ -752,7 +760,9 @@ def bench_e2e(args, wl, cache, run, dev, world, steps):
             total_s += dt
             ub, _ = unique_kv_bytes(cache, seqs, run.lengths, esize)
             total_b += ub
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * esize + n * 8 + n * 8 + n * max_blocks * 4 + n * 4
+    # q and the new rows as the caller holds them (bf16 for code pools)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + n * 8 + n * 8 + \
+        n * max_blocks * 4 + n * 4
     d2h = ho.numel() * 4
     tot_b, max_s = aggregate(float(total_b), total_s, world, dev)
     return {"value": round(tot_b / max_s / 1e9, 2), "unit": "GB/s",
