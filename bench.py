@@ -50,16 +50,17 @@ DEFAULT_WORKLOAD = "pool36"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331455232 + 3451136, "sha": "6c5c4e7a9c758658"},
-    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170890240 + 3348224, "sha": "6c5c4e7a9c758658"},
-    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615915264 + 6194944, "sha": "6c5c4e7a9c758658"},
-    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169176064 + 3486720, "sha": "6c5c4e7a9c758658"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331465472 + 3789824, "sha": "bd159cc715a68af0"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170884864 + 3303680, "sha": "bd159cc715a68af0"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615901952 + 6168064, "sha": "bd159cc715a68af0"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169169664 + 3423744, "sha": "bd159cc715a68af0"},
+    ("qwen_2k_q8", 16, "decode_mma_kernel"): {"bytes": 179525120 + 3512064, "sha": "bd159cc715a68af0"},
     # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
-    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464052480 + 5925888, "sha": "6c5c4e7a9c758658"},
-    ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 165507328 + 32500992, "sha": "7dfcd9cff622ca93"},
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464344832 + 5829888, "sha": "bd159cc715a68af0"},
+    ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 164881920 + 33188864, "sha": "2d5b25821dda64ad"},
     # the attention launch over the bfloat16 copy of the FP8 pool's blocks
-    ("prefill_4k_fp8", 16, "prefill_tc_kernel"): {"bytes": 166452480 + 33987584,
-                                                  "sha": "7dfcd9cff622ca93"},
+    ("prefill_4k_fp8", 16, "prefill_tc_kernel"): {"bytes": 166232832 + 34139136,
+                                                  "sha": "2d5b25821dda64ad"},
 }
 
 
