@@ -52,3 +52,29 @@ def test_device_calls_fail_cleanly_on_host_only_pool(lib):
     assert e.value.status == lib.KV_ERR_INVALID_ARG
     assert c.paged_decode_workspace_bytes(4, 8) > 0
     assert c.paged_decode_workspace_bytes(4, 7) == 0  # H_q not a multiple of H_kv
+
+
+def test_q8_pools_check_their_shapes_and_scale_arrays(lib):
+    # q8_0: whole 32-value groups per head row, and a block's scales of all
+    # heads in whole 16-byte vectors; the scale arrays must be non-null,
+    # 16-byte aligned, and only q8_0 pools take them
+    import ctypes as C
+
+    from paged_kv_cache_65_gb300 import PagedKVCache, _lib
+    from paged_kv_cache_65_gb300._lib import KVError
+
+    with pytest.raises(KVError):
+        PagedKVCache(1, 8, 16, 2, 48, "q8_0", allocate=False)   # 48 is not 32 k
+    with pytest.raises(KVError):
+        PagedKVCache(1, 8, 1, 1, 32, "q8_0", allocate=False)    # 1 * 1 * 1 * 2 bytes of scales
+    c = PagedKVCache(1, 8, 16, 2, 128, "q8_0", allocate=False)
+    buf = (C.c_uint8 * 64)()
+    base = (C.addressof(buf) + 15) & ~15
+    assert lib.lib.kv_pool_set_q8_scales(c.handle, None, C.c_void_p(base)) == _lib.KV_ERR_INVALID_ARG
+    assert lib.lib.kv_pool_set_q8_scales(c.handle, C.c_void_p(base + 4),
+                                     C.c_void_p(base)) == _lib.KV_ERR_INVALID_ARG
+    assert lib.lib.kv_pool_set_q8_scales(c.handle, C.c_void_p(base),
+                                     C.c_void_p(base + 16)) == _lib.KV_OK
+    bf = PagedKVCache(1, 8, 16, 2, 128, "bf16", allocate=False)
+    assert lib.lib.kv_pool_set_q8_scales(bf.handle, C.c_void_p(base),
+                                     C.c_void_p(base)) == _lib.KV_ERR_INVALID_ARG
