@@ -102,7 +102,12 @@ const char* kv_status_string(kvStatus s);
  *     giving the initial FIFO free list ([BT] §05); NULL means 0..n_blocks-1.
  * Supported: block_size 1..256, head_dim 64 or 128, dtype F32 or BF16;
  * FP8_E4M3 with head_dim 128 and block_size a multiple of 8 that divides 64
- * or is a multiple of it (decode on the warp-level MMA pass only). */
+ * or is a multiple of it (decode on either tensor-core pass); Q8_0 with
+ * FP8's shapes (decode on the warp-level pass).  Creation itself fails with
+ * KV_ERR_INVALID_ARG only for non-positive sizes, block_size > 256, an
+ * unknown dtype, or (Q8_0) a head_dim not a multiple of 32 or H_kv *
+ * block_size * head_dim / 16 scale bytes per block not a multiple of 16;
+ * device calls on other unsupported shapes return KV_ERR_UNSUPPORTED. */
 kvStatus kv_pool_create(int n_layers, int n_blocks, int block_size, int n_kv_heads,
                         int head_dim, int dtype, void* k_cache, void* v_cache,
                         int32_t* d_status, const int32_t* free_order, kvPool** out);
@@ -123,10 +128,11 @@ kvStatus kv_block_refcount(const kvPool* pool, int32_t id, int* out);
 
 /* Pool options.  KV_OPT_DECODE_PATH selects the split-pass kernel:
  * 0 = automatic (warp-level tensor-core pass for bfloat16 pools whose block
- * size is a multiple of 8, CUDA-core pass otherwise), 1 = always the
- * CUDA-core pass, 2 = the warp-level tensor-core pass (mma.sync) where the
- * pool allows it, 3 = the tcgen05 pass (tensor-memory accumulators; bfloat16,
- * D_h = 128) where the pool allows it, else as 2.  A plan (paged_decode_plan)
+ * size is a multiple of 8 and for FP8 and q8_0 pools, CUDA-core pass
+ * otherwise), 1 = always the CUDA-core pass (not for FP8 or q8_0 pools), 2 =
+ * the warp-level tensor-core pass (mma.sync) where the pool allows it, 3 =
+ * the tcgen05 pass (tensor-memory accumulators; bfloat16 or FP8, D_h = 128)
+ * where the pool allows it, else as 2.  A plan (paged_decode_plan)
  * records the kernel it was built for and the planned calls run that kernel;
  * in automatic mode the plan takes the tcgen05 pass when segments wider than
  * 16 query columns hold at least half of the blocks it reads, else the

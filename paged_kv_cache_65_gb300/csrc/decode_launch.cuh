@@ -73,6 +73,11 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tk, const CUtensorMap& tv, cons
 cudaError_t launch_tc_bf16(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
                            int sm_count, int max_grid, int* grid_io, cudaStream_t st, bool pdl);
 
+// The same over an FP8 (E4M3) pool (the code tensor maps: one 128-code box
+// per row set).
+cudaError_t launch_tc_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a,
+                          int sm_count, int max_grid, int* grid_io, cudaStream_t st, bool pdl);
+
 // Tensor-core variant for bfloat16 (swizzled TMA maps, B a multiple of 8).
 cudaError_t launch_mma_bf16(int D, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a, int sm_count, int max_grid, int* grid_io,

@@ -5,8 +5,8 @@
 // piece (a block range of one segment) it writes the base-2 online-softmax
 // statistics m, l and the unnormalised O of each of the segment's query
 // columns ("PagedAttention 的块表与碎片控制" §07 for the attention, "KV 缓存管理"
-// chunked-prefill section for the split and merge rule).  bfloat16 K/V,
-// D_h = 128, B a multiple of 8 with whole 64-row boxes per block.
+// chunked-prefill section for the split and merge rule).  bfloat16 or FP8
+// (E4M3) K/V, D_h = 128, B a multiple of 8 with whole 64-row boxes per block.
 //
 // Per stage of 128 token rows of one K/V head:
 //     S^T [128 tokens x N] = K [128 x 128] . Q^T [128 x N]          (8 MMAs, K = 16)
@@ -27,9 +27,12 @@
 // 4 and 5 issue the TMA loads of K and of V (issuing a tensor copy costs the
 // issuing warp tens of cycles, so one warp alone cannot keep up with HBM at
 // 16-row boxes), warp 4 also stages each piece's Q tile (three buffers, so
-// the next pieces' S can start while the current one finishes), and lane 0 of
-// warp 6 issues the MMAs, starting the next stage's S first when its data
-// has already landed.
+// the next pieces' S can start while the current one finishes), lane 0 of
+// warp 6 issues the S MMAs and lane 0 of warp 7 the P.V MMAs.  Issuing one
+// of these small MMAs costs the issuing thread tens of cycles, so one thread
+// issuing both would hold the next stage's S back behind this stage's P.V;
+// with two, S of a stage goes out as soon as its K is in and the softmax
+// has read the S buffer it overwrites.
 // Softmax is
 // lazy: the reference max m of a column only moves when a new score exceeds
 // it by more than 2^8 (TAU = 8 in base-2 units), so in the steady state a
@@ -39,9 +42,30 @@
 // previous stage's MMAs have completed.
 //
 // A parity wait is exact only while the waiter is never two phases ahead of
-// the barrier: each role waits every phase of full, s_full, p_full, q_full,
-// q_empty and o_free in order, and the MMAs of a stage are awaited through that
-// stage's empty barrier, whose phases are NST stages apart.
+// the barrier, nor two behind it: each role waits every phase of full,
+// s_full, p_full, q_full, q_empty and o_free in order; p_full has one barrier
+// per ring slot, so the softmax cannot complete a slot's next phase before
+// the P.V issuer has seen this one (that stage's copies wait for its P.V);
+// and the MMAs of a stage are awaited through that stage's empty barrier,
+// whose phases are NST stages apart.
+//
+// FP8 (E4M3) pools: the codes take half the bytes, so a stage's converted
+// operands must not take the shared memory the copies in flight need.  Four
+// converter warps (8-11, a warpgroup of their own; thread r owns token row
+// r) turn each stage's codes into fp16: K row r goes to TMEM
+// lane r (the S MMA reads K from tensor memory), V row r into the same
+// shared-memory layout the bfloat16 pass reads (the V codes land in the
+// upper half of that buffer and each row's codes are read before they are
+// written over).  A stage then holds 16 KiB of K codes (where the softmax
+// later writes P) and 32 KiB of V, four stages in the ring against three.
+// Rows past the context become zeros.  E4M3 values convert to fp16 exactly,
+// Q is staged as fp16 (exact inside fp16's range), P is split into an fp16
+// high part and remainder, and the MMAs run on f16 operands; the K scale is
+// folded into the score scale and the V scale into the O readout.  K and V
+// copies complete on barriers of their own, and the S MMA waits only for
+// the K rows, the P.V MMA for the V rows.  Twelve warps leave 168 registers
+// a thread at launch; the converters then give some back and the softmax
+// and the producer / MMA warpgroups take them.
 //
 // Every mbarrier wait is bounded; a wait that gives up records
 // KV_DEV_WAIT_TIMEOUT and the role runs the rest of its loops without waiting
@@ -54,8 +78,39 @@
 
 namespace pkv {
 
-constexpr int kTcWarps = 7;
+// Instruction descriptor of kind::f16 with f16 A and B (format 0 in bits
+// 7-9 and 10-12; bf16 is 1, tc.cuh's idesc_bf16), the rest as there.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+constexpr int kTcWarps = 8;
 constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcCvtWarps = 4;  // FP8 converter warps (8-11)
+constexpr int kTcCvtWarp0 = 8;
+// FP8 register split per warpgroup: softmax, producers and MMA, converters,
+// against the 168 a thread that twelve warps are launched with (the launcher
+// checks that count)
+constexpr int kTcRegsLaunchF8 = 168;
+constexpr int kTcRegsSoftmax = 232, kTcRegsHelper = 176, kTcRegsCvt = 96;
+static_assert(128 * (kTcRegsSoftmax + kTcRegsHelper + kTcRegsCvt) <= kTcRegsLaunchF8 * 12 * 32,
+              "register split within the launch's registers");
+
+// A warpgroup's register count moved from the launch count to N: raised
+// (setmaxnreg.inc) or lowered (setmaxnreg.dec), never the other way round.
+template <int N>
+__device__ __forceinline__ void tc_regs_f8() {
+  if constexpr (N > kTcRegsLaunchF8)
+    reg_alloc<N>();
+  else if constexpr (N < kTcRegsLaunchF8)
+    reg_dealloc<N>();
+}
+
+template <bool F8>
+constexpr int tc_threads() {
+  return F8 ? (kTcCvtWarp0 + kTcCvtWarps) * 32 : kTcThreads;
+}
 
 struct TcCfg {
   static constexpr int D = 128;
@@ -70,13 +125,31 @@ struct TcCfg {
   static constexpr int TM_O = 64;           // O^T: high-part sums at 64, remainder at 96
   static constexpr int TM_COLS = 128;
   static constexpr float TAU = 8.f;
+  // FP8: four stages of K codes (16 KiB) and fp16 V (32 KiB); K tiles in
+  // TMEM after S and O, 64 columns (128 fp16) a stage
+  static constexpr int NST_F8 = 4;
+  static constexpr int TM_K = 128;
+  static constexpr int TM_COLS_F8 = 512;
+  static constexpr int NBARS = 40;          // mbarrier slots (the FP8 pass uses 32)
 };
+static_assert(TcCfg::TM_K + TcCfg::NST_F8 * 64 <= TcCfg::TM_COLS_F8, "TMEM columns");
 
+// Ring depth and shared-memory bytes of a stage's K buffer for each pass.
+template <bool F8>
+constexpr int tc_stages() {
+  return F8 ? TcCfg::NST_F8 : TcCfg::NST;
+}
+template <bool F8>
+constexpr int tc_k_stage_bytes() {
+  return F8 ? TcCfg::HALF : TcCfg::STAGE;
+}
+
+template <bool F8>
 constexpr int decode_tc_smem_bytes() {
-  return 2 * TcCfg::NST * TcCfg::STAGE  // K, V stages
+  return tc_stages<F8>() * (tc_k_stage_bytes<F8>() + TcCfg::STAGE)  // K, V stages
          + TcCfg::QBUF * TcCfg::QTILE   // Q tiles
          + 3 * 4 * 32 * 4               // column maxima, per-warp broadcast, l sums
-         + 20 * 8                       // mbarriers
+         + TcCfg::NBARS * 8             // mbarriers
          + 4 * 8 + 16                   // walk state, TMEM address
          + 2 * kTableCache * 4          // producer table caches
          + 128                          // start record
@@ -164,9 +237,10 @@ struct TcSoftmax {
   }
 
   // One piece with at least one stage; NCP = 8, 16 or 32 query columns.
-  template <int NCP>
+  template <int NCP, bool F8>
   __device__ void run(const Piece& p, int n_st) {
     using C = TcCfg;
+    constexpr int NST = tc_stages<F8>();
     const int t = threadIdx.x;  // token row of a stage / dimension of O^T
     const int warp = t >> 5, lane = t & 31;
     const uint32_t tl = static_cast<uint32_t>(warp * 32) << 16;
@@ -179,11 +253,11 @@ struct TcSoftmax {
     }
     const float qs = a->qscale;
     for (int i = 0; i < n_st; ++i, ++stage) {
-      const int slot = stage % C::NST;
+      const int slot = stage % NST;
       const int tok0 = p.b0 * B + i * C::TS;
       const int nvalid = p.tok_end - tok0 < C::TS ? p.tok_end - tok0 : C::TS;
       const bool valid = t < nvalid;
-      wait(&full[slot], (stage / C::NST) & 1);
+      if constexpr (!F8) wait(&full[slot], (stage / NST) & 1);  // (rows zeroed below)
       wait(&s_full[stage & 1], (stage >> 1) & 1);
       __syncwarp();
       tc_fence_after();
@@ -224,7 +298,7 @@ struct TcSoftmax {
           // rescale O^T once the previous stage's MMAs are done with it
           // (the stage's empty barrier completes with them; its phases are
           // NST stages apart, so the parity cannot alias)
-          wait(&empty[(stage - 1) % C::NST], ((stage - 1) / C::NST) & 1);
+          wait(&empty[(stage - 1) % NST], ((stage - 1) / NST) & 1);
           __syncwarp();
           tc_fence_after();
 #pragma unroll
@@ -237,9 +311,10 @@ struct TcSoftmax {
           }
         }
       }
-      // ---- weights: bf16 high part (chunks 0-3) and remainder (chunks 4-7)
-      // of row t of P (N-major, 128-byte swizzle: chunk c at c ^ (t & 7))
-      const uint32_t pb = smem_u32(k_st + slot * C::STAGE);
+      // ---- weights: bf16 (F8: fp16) high part (chunks 0-3) and remainder
+      // (chunks 4-7) of row t of P (N-major, 128-byte swizzle: chunk c at
+      // c ^ (t & 7))
+      const uint32_t pb = smem_u32(k_st + slot * tc_k_stage_bytes<F8>());
 #pragma unroll
       for (int c8 = 0; c8 < NCP / 8; ++c8) {
         uint32_t hi[4], lo[4];
@@ -250,16 +325,22 @@ struct TcSoftmax {
           const float p1 = valid ? exp2_approx(x[c + 1]) : 0.f;
           l_part[c] += p0;
           l_part[c + 1] += p1;
-          hi[k] = pack_bf16(p0, p1);
-          lo[k] = pack_bf16(p0 - __uint_as_float(hi[k] << 16),
-                            p1 - __uint_as_float(hi[k] & 0xffff0000u));
+          if constexpr (F8) {
+            hi[k] = pack_f16(p0, p1);
+            lo[k] = pack_f16(p0 - half_lo(hi[k]), p1 - half_hi(hi[k]));
+          } else {
+            hi[k] = pack_bf16(p0, p1);
+            lo[k] = pack_bf16(p0 - __uint_as_float(hi[k] << 16),
+                              p1 - __uint_as_float(hi[k] & 0xffff0000u));
+          }
         }
         sts128(pb + t * 128 + ((c8 ^ (t & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
         sts128(pb + t * 128 + (((4 + c8) ^ (t & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
       }
       // rows past the context inside the last 16-row MMA step: V must be
-      // finite there (unused slots may hold anything), so it is zeroed
-      if (!valid && t < ((nvalid + 15) & ~15)) {
+      // finite there (unused slots may hold anything), so it is zeroed (FP8:
+      // by the converters)
+      if (!F8 && !valid && t < ((nvalid + 15) & ~15)) {
         const uint32_t vb = smem_u32(v_st + slot * C::STAGE) + t * 128;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -269,12 +350,12 @@ struct TcSoftmax {
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[stage & 1]);
+      if (lane == 0) mbar_arrive(&p_full[stage % NST]);
     }
 
     // ---- end of the piece: O^T from TMEM once the last stage's MMAs are
     // done, l reduced over the 128 rows
-    wait(&empty[(stage - 1) % C::NST], ((stage - 1) / C::NST) & 1);
+    wait(&empty[(stage - 1) % NST], ((stage - 1) / NST) & 1);
     __syncwarp();
     tc_fence_after();
     const long long slot_id = (long long)blockIdx.x + p.seg;
@@ -285,9 +366,11 @@ struct TcSoftmax {
       tmem_ld8(tmem + C::TM_O + 32 + c0 + tl, ol);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        if (c0 + c < ncols)
-          a->ws_o[(slot_id * cstride + c0 + c) * C::D + t] =
-              __uint_as_float(oh[c]) + __uint_as_float(ol[c]);
+        if (c0 + c < ncols) {
+          float o = __uint_as_float(oh[c]) + __uint_as_float(ol[c]);
+          if constexpr (F8) o *= a->vscale;
+          a->ws_o[(slot_id * cstride + c0 + c) * C::D + t] = o;
+        }
     }
     tc_fence_before();
     __syncwarp();
@@ -308,17 +391,18 @@ struct TcSoftmax {
   }
 };
 
-template <bool PLAN>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <bool PLAN, bool F8 = false>
+__global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a) {
   using C = TcCfg;
-  constexpr int NST = C::NST;
+  constexpr int NST = tc_stages<F8>();
+  constexpr int KSTAGE = tc_k_stage_bytes<F8>();  // FP8: the K codes, later P
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_st = smem;
-  unsigned char* v_st = k_st + NST * C::STAGE;
+  unsigned char* v_st = k_st + NST * KSTAGE;
   unsigned char* q_s = v_st + NST * C::STAGE;  // QBUF Q tiles
   float* red = reinterpret_cast<float*>(q_s + C::QBUF * C::QTILE);
   float* cmx = red + 128;
@@ -326,12 +410,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(lsum + 128);
   uint64_t* empty = full + NST;
   uint64_t* s_full = empty + NST;  // [2]
-  uint64_t* p_full = s_full + 2;   // [2]
-  uint64_t* q_full = p_full + 2;           // [QBUF]
+  uint64_t* p_full = s_full + 2;   // [NST] by ring slot
+  uint64_t* q_full = p_full + NST;         // [QBUF]
   uint64_t* q_empty = q_full + C::QBUF;    // [QBUF]
   uint64_t* o_free = q_empty + C::QBUF;
   uint64_t* fin = o_free + 1;
-  long long* walk = reinterpret_cast<long long*>(full + 20);
+  uint64_t* full_v = fin + 1;     // [NST] F8: the V copies (full: the K copies)
+  uint64_t* cvt_k = full_v + NST;  // [NST] F8: K rows in TMEM
+  uint64_t* cvt_v = cvt_k + NST;   // [NST] F8: V rows converted in shared memory
+  long long* walk = reinterpret_cast<long long*>(full + C::NBARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(walk + 4);
   int32_t* tcache = reinterpret_cast<int32_t*>(tmem_slot + 4);
   PlanStart* rec_s = reinterpret_cast<PlanStart*>(tcache + 2 * kTableCache);
@@ -341,7 +428,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int B = a.block_size;
   const int H = a.n_kv_heads;
   const int G = a.n_q_heads / H;
-  const int UR = B < 64 ? B : 64;  // rows per TMA box (a multiple of 8 dividing B and 128)
+  // rows per TMA box (a multiple of 8 dividing B and 128); FP8: the code
+  // tensor map's box, one 128-byte row of codes wide
+  const int UR = F8 ? mma_box_rows(B, C::TS) : (B < 64 ? B : 64);
 
   // self-check: swizzled buffers must sit on 1 KiB boundaries
   if ((smem_u32(k_st) & 1023u) != 0u) {
@@ -350,23 +439,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 2);  // the K and the V producer
+      mbar_init(&full[i], F8 ? 1 : 2);  // the K and the V producer (F8: K only)
       mbar_init(&empty[i], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], 4);
-    mbar_init(&p_full[1], 4);
+    for (int i = 0; i < NST; ++i) mbar_init(&p_full[i], 4);
     for (int i = 0; i < C::QBUF; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
     mbar_init(o_free, 4);
-    mbar_init(fin, 1);
+    mbar_init(fin, 2);  // both MMA issuers
+    if constexpr (F8) {
+      for (int i = 0; i < NST; ++i) {
+        mbar_init(&full_v[i], 1);
+        mbar_init(&cvt_k[i], kTcCvtWarps);
+        mbar_init(&cvt_v[i], kTcCvtWarps);
+      }
+    }
     fence_barrier_init();
   }
+  constexpr uint32_t kTmCols = F8 ? C::TM_COLS_F8 : C::TM_COLS;
   if (warp == 0) {
-    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_alloc(tmem_slot, kTmCols);
     tmem_relinquish();
   }
   // The walk start and the producers' first block-table entries read only
@@ -498,6 +594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 4 || warp == 5) {
     // ----------------------------------------------- producers (K, V)
+    if constexpr (F8) tc_regs_f8<kTcRegsHelper>();
     const bool kp = warp == 4;  // K producer, also stages Q
     const CUtensorMap* tmap = kp ? &tmap_k : &tmap_v;
     unsigned char* dst_st = kp ? k_st : v_st;
@@ -559,8 +656,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int idx = k * 32 + lane;
           const int col = idx >> 4, cg = idx & 15;
           const int h = cg >> 3, c = cg & 7;
-          sts128(qs + h * C::QHALF + col * 128 + ((c ^ (col & 7)) << 4), qv[k].x, qv[k].y,
-                 qv[k].z, qv[k].w);
+          uint4 w = qv[k];
+          if constexpr (F8) {  // bf16 -> fp16 pairs
+            w.x = pack_f16(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+            w.y = pack_f16(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            w.z = pack_f16(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+            w.w = pack_f16(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+          }
+          sts128(qs + h * C::QHALF + col * 128 + ((c ^ (col & 7)) << 4), w.x, w.y, w.z, w.w);
         }
         fence_async_smem();
         __syncwarp();
@@ -600,10 +703,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int j = t / B;
             const int pid = from_rec ? rec_s->pid[j - rec_s->b0] : tc.ent[j - tc.base];
             if (pid >= 0 && pid < a.n_blocks)
-              write_new_row<C::D, false>(a, p.rep, p.head, pid, t - j * B, kp, !kp, lane);
+              write_new_row<C::D, F8>(a, p.rep, p.head, pid, t - j * B, kp, !kp, lane);
           }
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 1u * nunits * UR * C::D * 2);
+        uint64_t* landed = F8 && !kp ? &full_v[slot] : &full[slot];
+        if (lane == 0) mbar_arrive_expect_tx(landed, 1u * nunits * UR * C::D * (F8 ? 1 : 2));
         __syncwarp();
         for (int u = lane; u < nunits; u += 32) {
           const int tk = tok0 + u * UR;
@@ -615,11 +719,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pid = 0;  // stay in bounds; the result is flagged as invalid
           }
           const int y = (a.layer * a.n_blocks + pid) * B + row;
+          if constexpr (F8) {
+            // the codes of UR rows: K at the start of its 16 KiB buffer, V
+            // into the upper half of its fp16 buffer
+            tma_load_2d(dst_st + slot * (kp ? KSTAGE : C::STAGE) + (kp ? 0 : C::HALF) + u * UR * 128,
+                        tmap, p.head * C::D, y, landed);
+          } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int x = p.head * C::D + h * 64;
-            const int off = slot * C::STAGE + h * C::HALF + u * UR * 128;
-            tma_load_2d(dst_st + off, tmap, x, y, &full[slot]);
+            for (int h = 0; h < 2; ++h) {
+              const int x = p.head * C::D + h * 64;
+              const int off = slot * C::STAGE + h * C::HALF + u * UR * 128;
+              tma_load_2d(dst_st + off, tmap, x, y, &full[slot]);
+            }
           }
         }
         if (i == 0) {
@@ -636,16 +747,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // copies still in flight land before the CTA may exit
     const int first = stage > NST ? stage - NST : 0;
+    uint64_t* landed = F8 && !kp ? full_v : full;
     for (int k = first; k < stage && alive; ++k)
-      alive = mbar_wait_bounded(&full[k % NST], (k / NST) & 1, kWaitLimitNs);
-  } else if (warp == 6) {
-    // -------------------------------------------------------- MMA issuer
+      alive = mbar_wait_bounded(&landed[k % NST], (k / NST) & 1, kWaitLimitNs);
+  } else if (warp == 6 || warp == 7) {
+    // ------------------------------------- MMA issuers: 6 for S, 7 for P.V
+    if constexpr (F8) tc_regs_f8<kTcRegsHelper>();
     wait_previous_grid();
     if (lane == 0) {
       const uint32_t kb = smem_u32(k_st), vb = smem_u32(v_st), qb = smem_u32(q_s);
-      constexpr uint32_t idS16 = idesc_bf16(128, 16, false, false);
-      constexpr uint32_t idS32 = idesc_bf16(128, 32, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, 64, true, true);
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (alive && !mbar_wait_bounded(bar, parity, kWaitLimitNs)) {
@@ -654,72 +764,175 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         return alive;
       };
-      auto issue_s = [&](int st, uint32_t idS, uint32_t qbase) {
-        const uint32_t ks = kb + (st % NST) * C::STAGE;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
-          const uint32_t qoff = (k >> 2) * C::QHALF + (k & 3) * 32;
-          tc_mma(tmem + C::TM_S + (st & 1) * 32, smem_desc(ks + off, 16, 1024, kSwizzle128),
-                 smem_desc(qbase + qoff, 16, 1024, kSwizzle128), idS, k > 0);
-        }
-        tc_commit(&s_full[st & 1]);
-      };
       int stage = 0, npiece = 0;
       Piece p;
-      while (next_piece(p)) {
-        const int n_st = stages_of(p);
-        if (n_st == 0) continue;
-        const uint32_t idS = p.ncols <= 16 ? idS16 : idS32;
-        const int qbi = npiece % C::QBUF;
-        const uint32_t qbase = qb + qbi * C::QTILE;
-        wait(&q_full[qbi], (npiece / C::QBUF) & 1);
-        if (npiece > 0) wait(o_free, (npiece - 1) & 1);
-        int issued = 0;  // S issued for stages stage .. stage + issued - 1
-        // S of the next stage; blocking, or only when its data is already in
-        auto issue_next = [&](bool block) {
-          const int st = stage + issued;
-          const bool ok = block ? wait(&full[st % NST], (st / NST) & 1)
-                                : alive && mbar_test_wait(&full[st % NST], (st / NST) & 1);
-          if (!ok) return;
-          tc_fence_after();
-          issue_s(st, idS, qbase);
-          if (++issued == n_st) tc_commit(&q_empty[qbi]);  // Q tile free once these are done
-        };
-        issue_next(true);
-        for (int i = 0; i < n_st; ++i) {
-          const int cur = stage + i;
-          // the next stage's S goes first when its data is already in (its S
-          // buffer was released with P of the stage before); the wait for P
-          // suspends the thread rather than spinning, since this lane shares
-          // a scheduler with a softmax warp
-          if (issued == i + 1 && issued < n_st) issue_next(false);
-          wait(&p_full[cur & 1], (cur >> 1) & 1);
-          if (alive) {
+      if (warp == 6) {
+        // S^T of each stage as soon as its K is in and its TMEM buffer has
+        // been read (P of the stage two before is written)
+        constexpr uint32_t idS16 =
+            F8 ? idesc_f16(128, 16, false, false) : idesc_bf16(128, 16, false, false);
+        constexpr uint32_t idS32 =
+            F8 ? idesc_f16(128, 32, false, false) : idesc_bf16(128, 32, false, false);
+        uint64_t* ready = F8 ? cvt_k : full;  // a stage's K is in shared memory (F8: TMEM)
+        while (next_piece(p)) {
+          const int n_st = stages_of(p);
+          if (n_st == 0) continue;
+          const uint32_t idS = p.ncols <= 16 ? idS16 : idS32;
+          const int qbi = npiece % C::QBUF;
+          const uint32_t qbase = qb + qbi * C::QTILE;
+          wait(&q_full[qbi], (npiece / C::QBUF) & 1);
+          for (int i = 0; i < n_st; ++i) {
+            const int st = stage + i;
+            if (st >= 2) wait(&p_full[(st - 2) % NST], ((st - 2) / NST) & 1);
+            wait(&ready[st % NST], (st / NST) & 1);
+            if (!alive) continue;
+            tc_fence_after();
+            const uint32_t ks = kb + (st % NST) * KSTAGE;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (k >> 2) * C::HALF + (k & 3) * 32;
+              const uint32_t qoff = (k >> 2) * C::QHALF + (k & 3) * 32;
+              const uint64_t qd = smem_desc(qbase + qoff, 16, 1024, kSwizzle128);
+              if constexpr (F8)  // K rows in TMEM: 8 columns (16 fp16) a k-step
+                tc_mma_ts(tmem + C::TM_S + (st & 1) * 32, tmem + C::TM_K + (st % NST) * 64 + k * 8,
+                          qd, idS, k > 0);
+              else
+                tc_mma(tmem + C::TM_S + (st & 1) * 32, smem_desc(ks + off, 16, 1024, kSwizzle128),
+                       qd, idS, k > 0);
+            }
+            tc_commit(&s_full[st & 1]);
+          }
+          tc_commit(&q_empty[qbi]);  // the Q tile is free once these are done
+          stage += n_st;
+          ++npiece;
+        }
+      } else {
+        // O^T += V^T . [P_hi | P_lo]^T of each stage once P is written (F8:
+        // and its V rows converted); a piece's first stage starts O^T anew
+        // once the previous piece's O^T has been read out
+        constexpr uint32_t idPV =
+            F8 ? idesc_f16(128, 64, true, true) : idesc_bf16(128, 64, true, true);
+        while (next_piece(p)) {
+          const int n_st = stages_of(p);
+          if (n_st == 0) continue;
+          if (npiece > 0) wait(o_free, (npiece - 1) & 1);
+          for (int i = 0; i < n_st; ++i) {
+            const int cur = stage + i;
+            wait(&p_full[cur % NST], (cur / NST) & 1);
+            if constexpr (F8) wait(&cvt_v[cur % NST], (cur / NST) & 1);
+            if (!alive) continue;
             tc_fence_after();
             const int tok0 = p.b0 * B + i * C::TS;
             const int nvalid = p.tok_end - tok0 < C::TS ? p.tok_end - tok0 : C::TS;
             const int nk = (nvalid + 15) >> 4;
             const uint32_t vs = vb + (cur % NST) * C::STAGE;
-            const uint32_t ps = kb + (cur % NST) * C::STAGE;
+            const uint32_t ps = kb + (cur % NST) * KSTAGE;
             for (int k = 0; k < nk; ++k)
               tc_mma(tmem + C::TM_O, smem_desc(vs + k * 2048, C::HALF, 1024, kSwizzle128),
                      smem_desc(ps + k * 2048, C::HALF, 1024, kSwizzle128), idPV,
                      (i > 0 || k > 0) ? 1u : 0u);
             tc_commit(&empty[cur % NST]);
           }
-          if (issued == i + 1 && issued < n_st) issue_next(true);
+          stage += n_st;
+          ++npiece;
         }
-        stage += n_st;
-        ++npiece;
       }
-      // every MMA issued has completed before TMEM is released
+      // every MMA either thread issued has completed before TMEM is released
       tc_commit(fin);
       mbar_wait_bounded(fin, 0, kWaitLimitNs);
     }
     __syncwarp();
+  } else if (warp >= kTcCvtWarp0) {
+    // ------------------------------------------------ FP8 converters (8-11)
+    if constexpr (F8) {
+      tc_regs_f8<kTcRegsCvt>();
+      wait_previous_grid();
+      const int r = threadIdx.x - kTcCvtWarp0 * 32;  // token row of a stage
+      bool alive = true;
+      int stage = 0;
+      // row r of a stage's V: its 128 codes (upper half, 128-byte swizzle)
+      // read whole, then written as 128 fp16 values over both halves
+      auto convert_v = [&](unsigned char* st, bool valid) {
+        const uint32_t b = smem_u32(st);
+        uint32_t w[8][4];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          w[c][0] = w[c][1] = w[c][2] = w[c][3] = 0u;
+          if (valid)
+            lds128(b + C::HALF + r * 128 + ((c ^ (r & 7)) << 4), w[c][0], w[c][1], w[c][2],
+                   w[c][3]);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t h[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) e4m3x4_to_f16(w[c][k], h[2 * k], h[2 * k + 1]);
+          // codes 16c .. 16c + 15: half c / 4, 16-byte chunks 2 (c % 4) and + 1
+          const uint32_t row = b + (c >> 2) * C::HALF + r * 128;
+          const int cc = (c & 3) * 2;
+          sts128(row + ((cc ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+          sts128(row + (((cc + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+        }
+      };
+      // row r of a stage's K: its codes (128-byte swizzle) as 64 fp16 pairs
+      // into TMEM lane r, dimensions 2j and 2j + 1 in column j
+      const uint32_t tl = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      auto convert_k = [&](unsigned char* st, uint32_t tcol, bool valid) {
+        const uint32_t b = smem_u32(st);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t w[4][4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            w[c][0] = w[c][1] = w[c][2] = w[c][3] = 0u;
+            if (valid)
+              lds128(b + r * 128 + (((4 * hf + c) ^ (r & 7)) << 4), w[c][0], w[c][1], w[c][2],
+                     w[c][3]);
+          }
+          uint32_t h[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              e4m3x4_to_f16(w[c][k], h[8 * c + 2 * k], h[8 * c + 2 * k + 1]);
+          __syncwarp();
+          tmem_st32(tmem + tl + tcol + hf * 32, h);
+        }
+      };
+      Piece p;
+      while (next_piece(p)) {
+        const int n_st = stages_of(p);
+        for (int i = 0; i < n_st; ++i, ++stage) {
+          const int slot = stage % NST;
+          const uint32_t par = (stage / NST) & 1;
+          if (alive && !mbar_wait_bounded(&full[slot], par, kWaitLimitNs)) {
+            alive = false;
+            record_status(a.status, 8);
+          }
+          alive = __all_sync(0xffffffffu, alive);
+          if (!alive) continue;
+          const int tok0 = p.b0 * B + i * C::TS;
+          const bool valid = r < p.tok_end - tok0;
+          convert_k(k_st + slot * KSTAGE, C::TM_K + slot * 64, valid);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cvt_k[slot]);
+          if (alive && !mbar_wait_bounded(&full_v[slot], par, kWaitLimitNs)) {
+            alive = false;
+            record_status(a.status, 8);
+          }
+          alive = __all_sync(0xffffffffu, alive);
+          if (!alive) continue;
+          convert_v(v_st + slot * C::STAGE, valid);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cvt_v[slot]);
+        }
+      }
+    }
   } else {
     // ----------------------------------------------------- softmax warps
+    if constexpr (F8) tc_regs_f8<kTcRegsSoftmax>();
     wait_previous_grid();
     TcSoftmax sm;
     sm.a = &a;
@@ -753,11 +966,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         continue;
       }
       if (p.ncols <= 8)
-        sm.run<8>(p, n_st);
+        sm.template run<8, F8>(p, n_st);
       else if (p.ncols <= 16)
-        sm.run<16>(p, n_st);
+        sm.template run<16, F8>(p, n_st);
       else
-        sm.run<32>(p, n_st);
+        sm.template run<32, F8>(p, n_st);
     }
   }
 
@@ -765,8 +978,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TM_COLS);
+    tmem_dealloc(tmem, kTmCols);
   }
+}
+
+// Launch of the tcgen05 split pass, one CTA per SM (capped at max_grid) on
+// the first call for a pool (*grid_io <= 0), the same count afterwards.
+template <bool F8>
+cudaError_t launch_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a_in,
+                      int sm_count, int max_grid, int* grid_io, cudaStream_t st, bool pdl) {
+  constexpr int smem = decode_tc_smem_bytes<F8>();
+  auto k_plain = decode_tc_kernel<false, F8>;
+  auto k_plan = decode_tc_kernel<true, F8>;
+  // the dynamic shared-memory limit is a per-function, per-device attribute
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int v = a_in.segs ? 1 : 0;
+  if (!attr_set[v][dev]) {
+    e = cudaFuncSetAttribute(v ? k_plan : k_plain, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    if constexpr (F8) {
+      // the warpgroups' register split assumes this launch count
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, v ? k_plan : k_plain);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kTcRegsLaunchF8) return cudaErrorInvalidConfiguration;
+    }
+    attr_set[v][dev] = true;
+  }
+  if (*grid_io <= 0) *grid_io = sm_count < max_grid ? sm_count : max_grid;
+  DecodeArgs a = a_in;
+  a.grid = *grid_io;
+  return launch_kernel(pdl, v ? k_plan : k_plain, dim3(a.grid), dim3(tc_threads<F8>()), smem, st,
+                       tk, tv, a);
 }
 
 }  // namespace pkv

@@ -72,12 +72,12 @@ kvStatus encode_cache_map(kvPool* p, void* base, int inner, int rows, bool swizz
 
 // Split-pass kernel for a pool (after ensure_device) and its decode-path
 // option: CUDA cores, warp-level MMA (mma.sync), or tcgen05 with TMEM
-// accumulators (bfloat16, D_h = 128).
+// accumulators (bfloat16 or FP8, D_h = 128).
 enum DecodeKernel { kKernelCudaCores, kKernelMma, kKernelTc };
 
 DecodeKernel decode_kernel(const kvPool* p) {
   const bool mma = p->mma_ok;
-  const bool tc = p->mma_ok && pool_tc_shape(p);
+  const bool tc = p->mma_ok && pool_tc_decode_shape(p);
   switch (p->decode_path) {
     case 1: return kKernelCudaCores;
     case 2: return mma ? kKernelMma : kKernelCudaCores;
@@ -97,8 +97,9 @@ kvStatus ensure_device(kvPool* p) {
   if (p->dtype == KV_DTYPE_Q8_0 && (!p->k_sc || !p->v_sc))
     return KV_ERR_INVALID_ARG;  // a q8_0 pool needs its scale arrays
   if (pool_codes8(p)) {
-    // FP8 / q8_0 codes: only the warp-level MMA pass, one 128-byte swizzled
-    // box (128 codes, all of D_h = 128) by mma_box_rows(B, 128) rows
+    // FP8 / q8_0 codes: the tensor-core passes (q8_0: the warp-level one),
+    // one 128-byte swizzled box (128 codes, all of D_h = 128) by
+    // mma_box_rows(B, 128) rows
     if (!pool_tensor_core_shape(p)) return KV_ERR_UNSUPPORTED;
     const int rm = pkv::mma_box_rows(p->B, pkv::mma_stage_tokens(p->D, true));
     kvStatus s = encode_cache_map(p, p->k, 128, rm, true, reinterpret_cast<CUtensorMap*>(p->tmap[2]));
@@ -876,8 +877,14 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  if (pool_codes8(p)) {
-    if (kern != kKernelMma) return KV_ERR_UNSUPPORTED;  // codes: warp-level MMA pass only
+  if (pool_codes8(p) && kern == kKernelTc) {
+    const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
+    const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
+    e = pkv::launch_tc_fp8(tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io, as_stream(stream),
+                           p->pdl);
+    supported = true;
+  } else if (pool_codes8(p)) {
+    if (kern != kKernelMma) return KV_ERR_UNSUPPORTED;  // no CUDA-core pass over codes
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
     a.k_sc = p->k_sc;
@@ -1001,7 +1008,7 @@ kvStatus partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
   // option turns the planned pass off
   if (decode_kernel(p) == kKernelCudaCores || ilog2_small(G) < 0) return KV_ERR_UNSUPPORTED;
   const bool tc = hd.kernel == kPlanKernelTc;
-  if (tc && !pool_tc_shape(p)) return KV_ERR_UNSUPPORTED;
+  if (tc && !pool_tc_decode_shape(p)) return KV_ERR_UNSUPPORTED;
   const unsigned char* dp = reinterpret_cast<const unsigned char*>(d_plan);
   unsigned char* ws = reinterpret_cast<unsigned char*>(d_workspace);
   pkv::DecodeArgs a;
@@ -1046,8 +1053,11 @@ kvStatus partials_planned(kvPool* p, int layer, const void* d_q, int n_q_heads,
   const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
   bool supported = true;
   const cudaError_t e =
-      tc ? pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
-                               as_stream(stream), p->pdl)
+      tc ? (p->dtype == KV_DTYPE_FP8_E4M3
+                ? pkv::launch_tc_fp8(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
+                                     as_stream(stream), p->pdl)
+                : pkv::launch_tc_bf16(tk, tv, a, p->sm_count, kMaxDecodeCtas, &p->grid_tc,
+                                      as_stream(stream), p->pdl))
       : p->dtype == KV_DTYPE_Q8_0
           ? pkv::launch_mma_q8(p->D, G, tk, tv, a, p->sm_count, kMaxDecodeCtas,
                                &p->grid_by_g[ilog2_small(G)], as_stream(stream), p->pdl,

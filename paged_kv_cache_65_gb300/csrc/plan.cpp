@@ -399,7 +399,7 @@ kvStatus plan_build(const kvPool* p, const int32_t* seq_ids, int n_seq, int n_q_
   // cost little per byte at any width), else the warp-level MMA pass (which
   // streams narrow segments faster)
   int kernel = kPlanKernelMma;
-  if (pool_tc_shape(p)) {
+  if (pool_tc_decode_shape(p)) {
     if (p->decode_path == 3) {
       kernel = kPlanKernelTc;
     } else if (p->decode_path == 0) {

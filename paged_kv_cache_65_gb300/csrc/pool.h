@@ -115,6 +115,13 @@ inline bool pool_tc_shape(const kvPool* p) {
   return p->dtype == KV_DTYPE_BF16 && pool_tensor_core_shape(p) && p->D == 128;
 }
 
+// The tcgen05 decode pass: bfloat16 as above, or FP8 codes (converted to fp16
+// in shared memory) with D_h = 128.
+inline bool pool_tc_decode_shape(const kvPool* p) {
+  return (p->dtype == KV_DTYPE_BF16 || p->dtype == KV_DTYPE_FP8_E4M3) &&
+         pool_tensor_core_shape(p) && p->D == 128;
+}
+
 // Largest CTA count the split pass uses; sizes the decode workspace.
 constexpr int kMaxDecodeCtas = 1024;
 

@@ -46,6 +46,9 @@ bf16 rows and stored as codes of x / scale):
 * ``qwen_2k_q8``  -- ``qwen_2k`` with a q8_0 pool (one fp16 scale per 32
                    values, "第 8 章 推理优化" §8.4.2 Fig. 8-23).
 * ``prefill_4k_fp8`` -- ``prefill_4k`` over an FP8 pool (scales 1).
+* ``shared_8k_fp8``, ``gqa70b_32k_fp8`` -- ``shared_8k`` and ``gqa70b_32k``
+                   with FP8 pools (scales 1): shared prompts and narrower KV
+                   together.
 
 Context lengths named above are the lengths after the first decode step
 (the step writes its token first, then attends over every position up to
@@ -62,6 +65,7 @@ the workload::
 
 from __future__ import annotations
 
+import dataclasses
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -194,8 +198,6 @@ def _prefill_4k(seed: int = 7) -> Workload:
 
 
 def _prefill_4k_fp8(seed: int = 7) -> Workload:
-    import dataclasses
-
     return dataclasses.replace(_prefill_4k(seed), name="prefill_4k_fp8", dtype="fp8_e4m3")
 
 
@@ -282,6 +284,14 @@ def _gqa70b_32k(seed: int = 3, keep_parents: bool = True) -> Workload:
                     "12 parents x 4 branches, shared partial tail (3 of 16)")
 
 
+def _shared_8k_fp8(seed: int = 2) -> Workload:
+    return dataclasses.replace(_shared_8k(seed), name="shared_8k_fp8", dtype="fp8_e4m3")
+
+
+def _gqa70b_32k_fp8(seed: int = 3) -> Workload:
+    return dataclasses.replace(_gqa70b_32k(seed), name="gqa70b_32k_fp8", dtype="fp8_e4m3")
+
+
 def _pool36(seed: int = 4, block_size: int = 16, n_steps: int = 64) -> Workload:
     n_seq, n_share, prefix = 128, 32, 6144
     rng = np.random.Generator(np.random.PCG64(_seed_seq((seed, 4))))
@@ -310,6 +320,8 @@ WORKLOADS = {
     "qwen_2k": _qwen_2k,
     "shared_8k": _shared_8k,
     "gqa70b_32k": _gqa70b_32k,
+    "shared_8k_fp8": _shared_8k_fp8,
+    "gqa70b_32k_fp8": _gqa70b_32k_fp8,
     "pool36": _pool36,
     "prefill_tiny": _prefill_tiny,
     "prefill_4k": _prefill_4k,

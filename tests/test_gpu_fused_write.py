@@ -105,9 +105,17 @@ def test_fused_write_gqa70b_32k_with_copy_on_write(path):
     fused_steps(synth.workload("gqa70b_32k"), path, 2, expect_cow=[48, 0])
 
 
-def test_fused_write_fp8_pool():
-    # quantized on the way in, one copy-on-write in the first step
-    fused_steps(synth.workload("fp8_small"), 0, 3, expect_cow=[1, 0, 0])
+@pytest.mark.parametrize("path", [0, 3])
+def test_fused_write_fp8_pool(path):
+    # quantized on the way in, one copy-on-write in the first step; the
+    # warp-level pass (automatic) and tcgen05
+    fused_steps(synth.workload("fp8_small"), path, 3, expect_cow=[1, 0, 0])
+
+
+def test_fused_write_fp8_gqa70b_32k_with_copy_on_write():
+    # FP8 codes written by the tcgen05 producers (automatic choice) after 48
+    # copy-on-write copies of shared tails
+    fused_steps(synth.workload("gqa70b_32k_fp8"), 0, 2, expect_cow=[48, 0])
 
 
 @pytest.mark.parametrize("B,path", [(8, 2), (16, 3), (32, 2), (64, 3)])
