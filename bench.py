@@ -50,13 +50,15 @@ DEFAULT_WORKLOAD = "pool36"
 # launch (profiles/), valid only while the sources of that kernel family hash
 # to "sha" (kernel_sha(family)).
 TRAFFIC = {
-    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331465472 + 3789824, "sha": "bd159cc715a68af0"},
-    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170884864 + 3303680, "sha": "bd159cc715a68af0"},
-    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615901952 + 6168064, "sha": "bd159cc715a68af0"},
-    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169169664 + 3423744, "sha": "bd159cc715a68af0"},
-    ("qwen_2k_q8", 16, "decode_mma_kernel"): {"bytes": 179525120 + 3512064, "sha": "bd159cc715a68af0"},
-    # one layer of the pool36 pool (B = 16), the same per-layer launch as in the 36-layer step
-    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464344832 + 5829888, "sha": "bd159cc715a68af0"},
+    ("qwen_2k", 16, "decode_mma_kernel"): {"bytes": 331453952 + 3647232, "sha": "bbd095098e8316bd"},
+    ("shared_8k", 16, "decode_mma_kernel"): {"bytes": 170885888 + 3263744, "sha": "bbd095098e8316bd"},
+    ("gqa70b_32k", 16, "decode_tc_kernel"): {"bytes": 1615905024 + 6258432, "sha": "bbd095098e8316bd"},
+    ("qwen_2k_fp8", 16, "decode_mma_kernel"): {"bytes": 169168128 + 3468032, "sha": "bbd095098e8316bd"},
+    ("qwen_2k_q8", 16, "decode_mma_kernel"): {"bytes": 179549184 + 3918848, "sha": "bbd095098e8316bd"},
+    ("gqa70b_32k_fp8", 16, "decode_tc_kernel"): {"bytes": 809733376 + 6476032,
+                                                  "sha": "bbd095098e8316bd"},
+    # one layer's launch of the 36-layer pool, captured on a one-layer pool of the same recipe
+    ("pool36", 16, "decode_mma_kernel"): {"bytes": 3464012544 + 5924864, "sha": "bbd095098e8316bd"},
     ("prefill_4k", 16, "prefill_tc_kernel"): {"bytes": 164881920 + 33188864, "sha": "2d5b25821dda64ad"},
     # the attention launch over the bfloat16 copy of the FP8 pool's blocks
     ("prefill_4k_fp8", 16, "prefill_tc_kernel"): {"bytes": 166232832 + 34139136,
