@@ -14,8 +14,6 @@
 // merge reads is written by the split pass of the same call.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "pool.h"
 
 namespace {
@@ -25,24 +23,19 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
 // Device address of the array on the current device.  The host-side symbol
-// is only a stand-in, so the address comes from cudaGetSymbolAddress, once
-// per device, with that device current.
+// is only a stand-in, so the address comes from cudaGetSymbolAddress, with
+// that device current, on every call: the call allocates nothing and
+// enqueues no work, and an address kept from an earlier call could be stale
+// after the device's context was reset.
 kvStatus scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KV_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess || !p) return KV_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || !p) return KV_ERR_CUDA;
+  *out = p;
   return KV_OK;
 }
 
