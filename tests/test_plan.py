@@ -76,7 +76,8 @@ def check_plan(bm, plan, seqs, G, min_tokens):
 
 
 @pytest.mark.parametrize("path", [0, 3])
-@pytest.mark.parametrize("name", ["tiny", "qwen_2k", "shared_8k", "gqa70b_32k"])
+@pytest.mark.parametrize("name", ["tiny", "qwen_2k", "shared_8k", "gqa70b_32k", "qwen_2k_fp8",
+                                  "shared_8k_fp8", "gqa70b_32k_fp8", "qwen_2k_q8"])
 def test_plans_of_the_workloads(name, path):
     from paged_kv_cache_65_gb300 import _lib
 
@@ -88,22 +89,25 @@ def test_plans_of_the_workloads(name, path):
     buf, ws = c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)
     plan = parse_plan(buf)
     check_plan(bm, plan, wl.decode_seqs, G, 128)
-    # the tcgen05 kernel is only for bfloat16 pools with D_h = 128 and B a multiple of 8
-    tc_shape = wl.dtype == "bf16" and wl.head_dim == 128 and wl.block_size % 8 == 0
+    # the tcgen05 kernel is for bfloat16 and FP8 pools with D_h = 128 and B a
+    # multiple of 8 (q8_0 pools take the warp-level pass)
+    tc_shape = (wl.dtype in ("bf16", "fp8_e4m3") and wl.head_dim == 128
+                and wl.block_size % 8 == 0)
     # automatic: tcgen05 when segments wider than 16 columns hold half of the blocks
     wide = sum(int(s["b1"] - s["b0"]) for s in plan["segs"] if s["ncols"] > 16)
     total = sum(int(s["b1"] - s["b0"]) for s in plan["segs"])
     auto_tc = 2 * wide >= total
     assert plan["kernel"] == (3 if tc_shape and (path == 3 or auto_tc) else 2)
-    if name == "gqa70b_32k":
+    base = name.replace("_fp8", "").replace("_q8", "")
+    if base == "gqa70b_32k":
         assert auto_tc
     assert ws > 0
     shared = [s for s in plan["segs"] if s["ncols"] > G]
-    if name == "gqa70b_32k":
+    if base == "gqa70b_32k":
         # 12 parents x 4 branches: one shared segment per parent and K/V head
         assert len(shared) == 12 * 8 and all(s["ncols"] == 32 for s in shared)
         assert all(s["b1"] == 2048 for s in shared)
-    elif name == "shared_8k":
+    elif base == "shared_8k":
         # 16 sharers of 384 blocks at G = 4: two sub-groups of 8 per K/V head
         assert len(shared) == 2 * 8 and all(s["b1"] == 384 for s in shared)
     else:
