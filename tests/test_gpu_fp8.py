@@ -149,14 +149,15 @@ def test_fp8_qwen_2k_full():
     assert cache.kv_pool_device_status() == 0
 
 
-@pytest.mark.parametrize("pinned", [False, True])
-def test_fp8_host_buffer_step(pinned):
+@pytest.mark.parametrize("pinned,path", [(False, 0), (True, 0), (True, 3)])
+def test_fp8_host_buffer_step(pinned, path):
     # the whole-step C entry point with host buffers: bf16 q and new K/V in,
     # quantized on the device, float32 out; pageable buffers go through the
-    # staging area, page-locked ones are read and written in place
+    # staging area, page-locked ones are read and written in place; path 3:
+    # the step's planned pass on tcgen05
     wl = synth.workload("fp8_small")
     orc = OracleRun(wl)
-    cache, run = make(wl)
+    cache, run = make(wl, path=path)
     max_blocks = 32
     n = len(wl.decode_seqs)
     staging = torch.empty(cache.kv_decode_step_staging_bytes(n, wl.n_q_heads, max_blocks),
