@@ -653,7 +653,9 @@ def measure_decode(args, name, block_size, steps, dev, world, clocks, min_timed_
     return res
 
 
-PER_CONFIG = ("shared_8k", "gqa70b_32k", "qwen_2k")
+# the target configs and config 1, then the same steps over FP8 pools (the
+# warp-level pass on qwen_2k_fp8, the tcgen05 pass on gqa70b_32k_fp8)
+PER_CONFIG = ("shared_8k", "gqa70b_32k", "qwen_2k", "qwen_2k_fp8", "gqa70b_32k_fp8")
 
 
 def free_device():
