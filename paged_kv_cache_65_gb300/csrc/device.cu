@@ -877,7 +877,7 @@ kvStatus paged_decode_partials(kvPool* p, int layer, const void* d_q, int n_q_he
   int* grid_io = kern == kKernelTc ? &p->grid_tc : &p->grid_by_g[ilog2_small(G)];
   bool supported = false;
   cudaError_t e;
-  if (pool_codes8(p) && kern == kKernelTc) {
+  if (p->dtype == KV_DTYPE_FP8_E4M3 && kern == kKernelTc) {
     const CUtensorMap& tk = *reinterpret_cast<const CUtensorMap*>(p->tmap[2]);
     const CUtensorMap& tv = *reinterpret_cast<const CUtensorMap*>(p->tmap[3]);
     e = pkv::launch_tc_fp8(tk, tv, a, p->sm_count, kMaxDecodeCtas, grid_io, as_stream(stream),

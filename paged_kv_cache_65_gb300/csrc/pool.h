@@ -115,8 +115,9 @@ inline bool pool_tc_shape(const kvPool* p) {
   return p->dtype == KV_DTYPE_BF16 && pool_tensor_core_shape(p) && p->D == 128;
 }
 
-// The tcgen05 decode pass: bfloat16 as above, or FP8 codes (converted to fp16
-// in shared memory) with D_h = 128.
+// The tcgen05 decode pass: bfloat16 as above, or FP8 codes with D_h = 128
+// (converted to fp16 in the pass: K rows into tensor memory, V rows into
+// shared memory).
 inline bool pool_tc_decode_shape(const kvPool* p) {
   return (p->dtype == KV_DTYPE_BF16 || p->dtype == KV_DTYPE_FP8_E4M3) &&
          pool_tensor_core_shape(p) && p->D == 128;
