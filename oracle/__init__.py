@@ -30,6 +30,9 @@ follows, not to be fast:
 * ``q8`` -- q8_0 codes (one fp16 scale per group of 32 values), the
   plainest rounding rule the pages' byte layout supports; ``kv_store`` holds
   such pools.
+* ``q4`` -- q4_0 codes (4-bit, one fp16 scale per group of 32 values), the
+  q8_0 rule with 7 in place of 127 and a stated nibble order; a codec only
+  (no pool holds them).
 * ``prefill`` -- chunked-prefill attention over a paged history.
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against
