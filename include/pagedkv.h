@@ -386,12 +386,11 @@ kvStatus paged_decode_attention_planned(kvPool* pool, int layer, const void* d_q
  * 16 MiB array in the library's static device memory, one per GPU, held
  * until the process exits.  Requests whose paged_decode_workspace_bytes()
  * exceed 16 MiB (about 880 sequences at G = 4, D_h = 128, H_kv = 8) fail with
- * KV_ERR_SCRATCH_TOO_SMALL before any device work.  The first call on a
- * device looks up the array's device address and keeps it for the life of
- * the process.  The kept address is not valid after cudaDeviceReset (or any
- * teardown of the device's primary context): do not call this entry point
- * after one.  Calls on one GPU share the array: calls that overlap on the
- * GPU race.  The pages have no counterpart of this call. */
+ * KV_ERR_SCRATCH_TOO_SMALL before any device work.  Every call looks the
+ * array's device address up on the current device (no allocation, no device
+ * work), so no address is kept across a reset of the device's context.
+ * Calls on one GPU share the array: calls that overlap on the GPU race.  The
+ * pages have no counterpart of this call. */
 kvStatus paged_decode_attention_noalloc(kvPool* pool, int layer, const void* d_q, int n_q_heads,
                                         const int32_t* d_block_table, int max_blocks,
                                         const int32_t* d_context_lens, int n_seq, float scale,
