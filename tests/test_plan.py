@@ -251,3 +251,25 @@ def test_nested_forks_read_every_shared_block_once(levels, G):
         assert plan["n_shared_segs"] == n_nodes * H
     else:
         assert all(r > len(distinct) for r in read)  # the deepest runs are read per sharer
+
+
+@pytest.mark.parametrize("dtype,B,head_dim,expect", [
+    ("fp8_e4m3", 16, 128, 3), ("fp8_e4m3", 24, 128, 2), ("fp8_e4m3", 192, 128, 3),
+    ("bf16", 16, 64, 2), ("q8_0", 16, 128, 2), ("bf16", 32, 128, 3)])
+def test_forced_tcgen05_plans_only_where_the_pass_exists(dtype, B, head_dim, expect):
+    # KV_OPT_DECODE_PATH 3 asks for tcgen05; the plan takes it for bfloat16
+    # and FP8 pools with D_h = 128 and a block size whose rows fill whole
+    # TMA boxes, else the warp-level pass (q8_0 pools always)
+    from paged_kv_cache_65_gb300 import _lib
+
+    H, G = 2, 4
+    ops = [("append", 0, 5 * B + 3, 0), ("fork", 0, 1), ("append", 2, 3 * B, 2)]
+    wl = synth.Workload("forced", 1, 64, B, H * G, H, head_dim, dtype, 5,
+                        synth.permutation((5, 1), 64), ops, [0, 1, 2])
+    bm, c = build_both(wl)
+    c.kv_pool_set_option(_lib.KV_OPT_DECODE_PATH, 3)
+    mb = max(len(bm.tables[s]) for s in wl.decode_seqs)
+    buf, _ = c.paged_decode_plan(wl.decode_seqs, wl.n_q_heads, mb)
+    plan = parse_plan(buf)
+    assert plan["kernel"] == expect
+    check_plan(bm, plan, wl.decode_seqs, G, 128)
